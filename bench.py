@@ -1,0 +1,488 @@
+#!/usr/bin/env python
+"""Benchmark of the Flint-shaped 4-bit sparse MoE FFN layer on B300.
+
+Default workload: one Flint-shaped MoE layer decoding one token (d=2048,
+f=512, 256 routed experts, top-6, one shared expert, NVFP4 weights, T=1),
+with the L2 cache flushed between steps. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+A step is one pass of the layer (router, top-k, bucketing, expert gate/up,
+down projection, combine) over the workload's tokens. Per-step device time is
+taken with CUDA events on the launching stream around the forward only; the
+L2 flush (a memset of twice the L2 size) runs between steps, outside those
+events. With torchrun (N > 1) every rank runs an independent replica of the
+workload on its own GPU (the layer does not shard); the reported time is the
+maximum over ranks and the value counts the tokens of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_quantized_expert_softmax_b300 import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s"
+FALLBACK_HBM_GBS = 6400.0
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Maximum of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None) -> None:
+    if world <= 1:
+        return
+    import torch.distributed as dist
+    if device is not None and device.type == "cuda":
+        dist.barrier(device_ids=[device.index])
+    else:
+        dist.barrier()
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self) -> dict:
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for(device) -> str:
+    import torch
+    props = torch.cuda.get_device_properties(device)
+    uuid = getattr(props, "uuid", None)
+    if uuid is not None:
+        s = str(uuid)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    return str(device.index)
+
+
+def source_digest(*paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str, digest: str):
+    """DRAM bytes per launch of `kernel` from a committed ncu capture, if the
+    capture was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    rec = d.get(f"{kernel}@{workload}")
+    if not rec or rec.get("source_digest") != digest:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+
+
+def algorithmic_bytes(cfg, n_active_experts: int, T: int) -> dict:
+    """Bytes the layer must move once per step (weights of the experts it
+    uses, router, activations), and the share of the gate/up kernel."""
+    per_mat = cfg.codes_per_matrix + cfg.scales_per_matrix + (4 if cfg.wfmt == 0 else 0)
+    selected = n_active_experts * 3 * per_mat
+    router = cfg.router_bytes + cfg.n_experts * 4
+    acts = 2 * T * cfg.d * 2
+    P = T * (cfg.top_k + 1)
+    gateup = n_active_experts * 2 * per_mat + T * cfg.d * 2 + P * cfg.f * 4
+    return {"selected_expert_bytes": selected, "layer_bytes": selected + router + acts,
+            "gateup_kernel_bytes": gateup}
+
+
+def run_ours(args, cfg, world, rank, local):
+    import torch
+    from bit_quantized_expert_softmax_b300 import build
+    build.build()
+    from bit_quantized_expert_softmax_b300 import flint_moe as fm
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    T = cfg.tokens
+    n_layers = cfg.n_layers
+    m = fm.MoE(cfg, max_tokens=T, n_layers=n_layers, device=local)
+    for i in range(n_layers):          # one layer in host memory at a time
+        m.load(i, synth.make_layer(cfg, layer=i))
+    bits = synth.make_hidden(cfg)
+    x = fm.hidden_to_device(bits, local)
+    out = torch.empty_like(x)
+    stream = torch.cuda.current_stream(device)
+
+    # routing of the workload (for the byte count): experts used + shared
+    idx = torch.empty((T, cfg.top_k), dtype=torch.int32, device=device)
+    fm.flint_moe_router(m.h, 0, x, T, None, idx, None)
+    torch.cuda.synchronize()
+    n_active = int(np.unique(idx.cpu().numpy()).size) + 1
+    nbytes = algorithmic_bytes(cfg, n_active, T)
+    if n_layers > 1:
+        nbytes = {k: v * n_layers for k, v in nbytes.items()}   # per-layer routing differs; T=1 -> 7 each
+
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
+
+    if n_layers > 1:
+        xs = x.clone()
+
+        def step():
+            fm.flint_moe_forward_stack(m.h, 0, n_layers, xs, T, stream)
+        # one CUDA graph per token for the whole stack
+        g = torch.cuda.CUDAGraph()
+        s2 = torch.cuda.Stream(device)
+        s2.wait_stream(stream)
+        with torch.cuda.stream(s2):
+            fm.flint_moe_forward_stack(m.h, 0, n_layers, xs, T, s2)   # warm
+        stream.wait_stream(s2)
+        torch.cuda.synchronize()
+        launches_per_step = None
+        before = fm.flint_moe_launch_count(m.h)
+        with torch.cuda.graph(g):
+            fm.flint_moe_forward_stack(m.h, 0, n_layers, xs, T, torch.cuda.current_stream())
+        launches_per_step = fm.flint_moe_launch_count(m.h) - before
+
+        def step():   # noqa: F811
+            g.replay()
+    else:
+        launches_per_step = None
+
+        def step():
+            fm.flint_moe_forward(m.h, 0, x, T, out, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert fm.flint_moe_status(m.h) == fm.FLINT_OK
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    profile = n_layers == 1
+    barrier(world, device)
+    torch.cuda.synchronize()
+    launches0 = fm.flint_moe_launch_count(m.h)
+    with ClockSampler(gpu_id_for(device)) as clk:
+        if profile:
+            fm.flint_moe_profile_begin(m.h, K)
+        t0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        if profile:
+            phase_ms, n_prof = fm.flint_moe_profile_end(m.h)
+    barrier(world, device)
+    launches = fm.flint_moe_launch_count(m.h) - launches0
+    if launches_per_step is not None:
+        launches = launches_per_step * K
+    assert fm.flint_moe_status(m.h) == fm.FLINT_OK
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(ms, world, device)
+    value = world * T / (ms_max / 1e3)
+
+    # end to end through the public API: pinned host in -> forward -> pinned host out
+    xh = fm.hidden_to_host(x).copy()
+    x_pin = torch.from_numpy(xh.view(np.int16)).pin_memory()
+    o_pin = torch.empty_like(x_pin).pin_memory()
+    x_dev = torch.empty((T, cfg.d), dtype=torch.int16, device=device)
+    o_dev = torch.empty_like(x_dev)
+    Ke = min(K, 2000)
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    for i in range(Ke + 3):
+        flush.zero_()
+        j = i - 3
+        if j >= 0:
+            es[j].record(stream)
+        x_dev.copy_(x_pin, non_blocking=True)
+        if n_layers > 1:
+            fm.flint_moe_forward_stack(m.h, 0, n_layers, x_dev.view(torch.bfloat16), T, stream)
+            o_pin.copy_(x_dev, non_blocking=True)
+        else:
+            fm.flint_moe_forward(m.h, 0, x_dev.view(torch.bfloat16), T, o_dev.view(torch.bfloat16), stream)
+            o_pin.copy_(o_dev, non_blocking=True)
+        if j >= 0:
+            ee[j].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(es, ee)), world, device)
+
+    peaks = measured_peaks()
+    res = {
+        "step_ms": step_ms, "ms": ms_max, "value": value, "wall_s": wall, "launches": launches,
+        "clocks": clk.summary(), "bytes": nbytes, "n_active": n_active,
+        "e2e_value": world * T / (e2e_ms / 1e3), "e2e_ms": e2e_ms, "peaks": peaks,
+    }
+    if profile:
+        res["phase_us"] = [p / n_prof * 1e3 for p in phase_ms]
+    m.close()
+    return res
+
+
+def cpu_baseline(cfg, seconds: float) -> dict:
+    """The CPU oracle (test infrastructure), timed as it stands on the host
+    cores, on a bounded sample of the workload."""
+    import oracle
+    T = cfg.tokens
+    if cfg.n_layers > 1:
+        # bounded sample of the stack: whole layers of it, one at a time
+        el, n = 0.0, 0
+        bits = synth.make_hidden(cfg, tokens=T, stream=1)
+        while el < seconds and n < cfg.n_layers:
+            L = synth.make_layer(cfg, layer=n)
+            t0 = time.perf_counter()
+            r = oracle.moe.moe_layer(bits, L)
+            bits = oracle.formats.bf16_bits(oracle.formats.bf16_round(
+                oracle.formats.bf16_array(bits) + r.out_bf16))
+            el += time.perf_counter() - t0
+            n += 1
+        per_token = el / n * cfg.n_layers
+        return {"value": T / per_token, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                "sample": f"{n} of the {cfg.n_layers} layers (T={T}) through the float64 numpy oracle in "
+                          f"{el:.1f} s, scaled to the whole stack"}
+    L = synth.make_layer(cfg)
+    done = 0
+    steps = 0
+    t0 = time.perf_counter()
+    while True:
+        bits = synth.make_hidden(cfg, tokens=T, stream=1 + steps)
+        oracle.moe.moe_layer(bits, L)
+        done += T
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": done / el, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{steps} full steps of the workload ({done} tokens) through the float64 numpy "
+                      f"oracle in {el:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default per workload: about 1-5 s of device time)")
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--config", type=int, default=2, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    cfg = synth.CONFIGS[args.config]
+    if args.steps is None:
+        args.steps = {1: 20000, 2: 20000, 3: 10000, 4: 5000, 5: 40}[args.config]
+    world, rank, local = dist_env()
+    if world != args.gpus and world > 1:
+        print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
+
+    workload = {"workload": f"{cfg.name}: {cfg.n_layers} MoE layer(s), d={cfg.d}, f={cfg.f}, "
+                            f"{cfg.n_experts} routed experts top-{cfg.top_k} + 1 shared, "
+                            f"{'NVFP4' if cfg.wfmt == 0 else 'q4_1'} weights, T={cfg.tokens}"
+                            + (", Zipf(1.1) router bias" if cfg.bias == "zipf" else ""),
+                "tokens_per_step": cfg.tokens,
+                "l2": "flushed between steps (memset of 2x L2, outside the per-step events)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps = []
+        budget = 120.0
+        t_all = time.perf_counter()
+        import oracle
+        n_keep = min(cfg.n_layers, 4)     # a stack step is timed on its first layers and scaled
+        layers = [synth.make_layer(cfg, layer=i) for i in range(n_keep)]
+        for i in range(args.warmup + args.steps):
+            bits = synth.make_hidden(cfg, stream=1 + i)
+            t0 = time.perf_counter()
+            for L in layers:
+                oracle.moe.moe_layer(bits, L)
+            dt = (time.perf_counter() - t0) * cfg.n_layers / n_keep
+            if i >= args.warmup:
+                steps.append(dt)
+            if time.perf_counter() - t_all > budget and len(steps) >= 3:
+                break
+        ms = statistics.mean(steps) * 1e3
+        value = cfg.tokens / (ms / 1e3)
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": len(steps), "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": workload,
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle",
+                                 "cores": blas_threads(),
+                                 "sample": f"{len(steps)} steps of the workload, one oracle call each "
+                                           f"(run capped at {budget:.0f} s)"},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    res = run_ours(args, cfg, world, rank, local)
+    if rank == 0:
+        peaks = res["peaks"]
+        hbm = peaks["hbm_gbs"]
+        nb = res["bytes"]
+        line = {
+            "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16", "data": "synthetic", "config": workload,
+        }
+        layer_gbs = nb["layer_bytes"] / (res["ms"] * 1e-3) / 1e9
+        if "phase_us" in res:
+            gu_us = res["phase_us"][1]
+            achieved = nb["gateup_kernel_bytes"] / (gu_us * 1e-6) / 1e9
+            digest = source_digest("bit_quantized_expert_softmax_b300/csrc/experts.cu",
+                                   "bit_quantized_expert_softmax_b300/csrc/common.cuh")
+            line["roofline"] = {
+                "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": recorded_traffic("gateup_kernel", cfg.name, digest),
+                "kernel": "gateup_kernel (expert gate/up, SwiGLU)",
+                "algorithmic_bytes_per_launch": nb["gateup_kernel_bytes"], "avg_launch_us": gu_us,
+                "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
+                else "fallback 6.4 TB/s",
+            }
+            line["phases_us"] = {"router_topk_bucket": res["phase_us"][0], "gateup": res["phase_us"][1],
+                                 "down_combine": res["phase_us"][2]}
+        line["layer_hbm"] = {"bytes_per_step": nb["layer_bytes"],
+                             "selected_expert_bytes_per_step": nb["selected_expert_bytes"],
+                             "achieved_gbs": layer_gbs, "frac_of_measured": layer_gbs / hbm,
+                             "selected_frac_of_measured": nb["selected_expert_bytes"] / (res["ms"] * 1e-3) / 1e9 / hbm,
+                             "experts_read": res["n_active"]}
+        line["e2e"] = {"value": res["e2e_value"], "unit": "tokens/s",
+                       "h2d_bytes_per_step": cfg.tokens * cfg.d * 2,
+                       "d2h_bytes_per_step": cfg.tokens * cfg.d * 2}
+        line["gpu_launches"] = int(res["launches"])
+        line["clocks"] = res["clocks"]
+        step_ms = np.array(res["step_ms"])
+        line["step_ms_p10_p50_p90"] = [float(np.percentile(step_ms, q)) for q in (10, 50, 90)]
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,470 @@
+// C ABI of the layer: handle, weight loading, forward orchestration.
+#include <math.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "../../include/flint_moe.h"
+#include "kernels.cuh"
+
+using flint::LayerDev;
+using flint::Shape;
+using flint::Workspace;
+
+struct flint_moe {
+    Shape s;
+    int n_layers = 0;
+    int device = 0;
+    std::vector<LayerDev> layers;
+    Workspace ws{};
+    void* ws_base = nullptr;
+    size_t ws_bytes = 0;
+    size_t weight_bytes = 0;
+    cudaStream_t load_stream = nullptr;
+    uint64_t launches = 0;
+    // phase events of profiled forwards: 4 per forward
+    std::vector<cudaEvent_t> prof_events;
+    int prof_max = 0, prof_n = 0;
+};
+
+namespace {
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        ok = (cudaSetDevice(dev) == cudaSuccess);
+    }
+    ~DeviceGuard() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+flint_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return FLINT_OK;
+    if (e == cudaErrorMemoryAllocation) return FLINT_ENOMEM;
+    return FLINT_ECUDA;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+void free_layer(LayerDev& L) {
+    cudaFree(L.router);
+    cudaFree(L.bias);
+    cudaFree(L.codes);
+    cudaFree(L.scales);
+    cudaFree(L.tscale);
+    L = LayerDev{};
+}
+
+flint_status validate_config(const flint_moe_config* c) {
+    if (c == nullptr) return FLINT_EINVAL;
+    if (c->d < 128 || c->d > 4096 || c->d % 128 != 0) return FLINT_EINVAL;
+    if (c->f < 128 || c->f > 4096 || c->f % 128 != 0) return FLINT_EINVAL;
+    if (c->n_experts < 32 || c->n_experts > 256 || c->n_experts % 32 != 0) return FLINT_EINVAL;
+    if (c->top_k < 1 || c->top_k > 8 || c->top_k > c->n_experts) return FLINT_EINVAL;
+    if (c->n_shared != 0 && c->n_shared != 1) return FLINT_EINVAL;
+    if (c->wfmt != FLINT_W_NVFP4 && c->wfmt != FLINT_W_Q4_1) return FLINT_EINVAL;
+    if (c->max_tokens < 1 || c->max_tokens > 65536) return FLINT_EINVAL;
+    if (c->n_layers < 1 || c->n_layers > 4096) return FLINT_EINVAL;
+    if (c->device < 0) return FLINT_EINVAL;
+    return FLINT_OK;
+}
+
+// Carve the workspace out of one allocation.
+struct Carver {
+    char* base;
+    size_t off = 0;
+    template <class T>
+    T* take(size_t count) {
+        off = align_up(off, 256);
+        T* p = reinterpret_cast<T*>(base ? base + off : nullptr);
+        off += count * sizeof(T);
+        return p;
+    }
+};
+
+Workspace carve(const Shape& s, char* base, size_t* total) {
+    Carver cv{base};
+    Workspace w{};
+    const size_t Tm = s.max_tokens;
+    const size_t P = (size_t)s.positions(s.max_tokens);
+    const size_t n_chunks = (Tm * s.k + flint::kBucketChunk - 1) / flint::kBucketChunk;
+    w.logits = cv.take<float>(Tm * s.E);
+    w.idx = cv.take<int>(Tm * s.k);
+    w.w = cv.take<float>(Tm * s.k);
+    w.perm = cv.take<int>(Tm * s.k);
+    w.inv = cv.take<int>(Tm * s.k);
+    w.offsets = cv.take<int>(s.E + 1);
+    w.slot_expert = cv.take<int>(s.E + 1);
+    w.slot_off = cv.take<int>(s.E + 1);
+    w.slot_cnt = cv.take<int>(s.E + 1);
+    w.meta = cv.take<int>(8);
+    w.x16 = cv.take<__half>(Tm * s.d);
+    w.xinv = cv.take<float>(Tm);
+    w.hf = cv.take<float>(P * s.f);
+    w.hamax = cv.take<uint32_t>(P);
+    w.yw = cv.take<float>(P * s.d);
+    w.chunk_hist = cv.take<int>(n_chunks * s.E);
+    w.counters = cv.take<uint32_t>(flint::kCounters);
+    w.status = cv.take<uint32_t>(1);
+    *total = align_up(cv.off, 256);
+    return w;
+}
+
+bool finite_f32(const float* p, size_t n) {
+    for (size_t i = 0; i < n; ++i)
+        if (!isfinite(p[i])) return false;
+    return true;
+}
+
+flint_status check_forward_args(flint_moe* h, int layer, const void* a, const void* b, int T) {
+    if (h == nullptr) return FLINT_EINVAL;
+    if (layer < 0 || layer >= h->n_layers) return FLINT_EINVAL;
+    if (T < 0 || T > h->s.max_tokens) return FLINT_EINVAL;
+    if (T > 0) {
+        if (a == nullptr || !aligned16(a)) return FLINT_EINVAL;
+        if (b != nullptr && !aligned16(b)) return FLINT_EINVAL;
+    }
+    if (!h->layers[layer].loaded) return FLINT_ESTATE;
+    return FLINT_OK;
+}
+
+void prof_free(flint_moe* h) {
+    for (cudaEvent_t ev : h->prof_events) cudaEventDestroy(ev);
+    h->prof_events.clear();
+    h->prof_max = h->prof_n = 0;
+}
+
+void prof_record(flint_moe* h, int phase, cudaStream_t st) {
+    if (h->prof_n < h->prof_max) cudaEventRecord(h->prof_events[(size_t)h->prof_n * 4 + phase], st);
+}
+
+cudaError_t run_layer(flint_moe* h, int layer, const __nv_bfloat16* x, int T, __nv_bfloat16* out,
+                      const __nv_bfloat16* residual, cudaStream_t st) {
+    const LayerDev& L = h->layers[layer];
+    int n = 0;
+    prof_record(h, 0, st);
+    cudaError_t e = flint::launch_router(h->s, L, x, T, h->ws, st, &n);
+    prof_record(h, 1, st);
+    if (e == cudaSuccess) e = flint::launch_gateup(h->s, L, T, h->ws, st, &n);
+    prof_record(h, 2, st);
+    if (e == cudaSuccess) e = flint::launch_down(h->s, L, T, h->ws, out, residual, st, &n);
+    prof_record(h, 3, st);
+    if (h->prof_n < h->prof_max) ++h->prof_n;
+    h->launches += n;
+    return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* flint_moe_status_string(flint_status s) {
+    switch (s) {
+        case FLINT_OK: return "ok";
+        case FLINT_EINVAL: return "invalid argument";
+        case FLINT_ENOMEM: return "out of device memory";
+        case FLINT_ECUDA: return "CUDA error";
+        case FLINT_ESTATE: return "layer weights not loaded";
+        case FLINT_ETIMEOUT: return "device wait timed out";
+        case FLINT_ENOTIMPL: return "not implemented";
+        case FLINT_EDEVICE: return "device reported a data fault";
+    }
+    return "unknown status";
+}
+
+flint_status flint_moe_create(const flint_moe_config* cfg, flint_moe** out) {
+    if (out == nullptr) return FLINT_EINVAL;
+    *out = nullptr;
+    flint_status st = validate_config(cfg);
+    if (st != FLINT_OK) return st;
+    int n_dev = 0;
+    if (cudaGetDeviceCount(&n_dev) != cudaSuccess || cfg->device >= n_dev) return FLINT_EINVAL;
+    DeviceGuard guard(cfg->device);
+    if (!guard.ok) return FLINT_ECUDA;
+    flint_moe* h = new (std::nothrow) flint_moe();
+    if (h == nullptr) return FLINT_ENOMEM;
+    h->s = Shape{cfg->d, cfg->f, cfg->n_experts, cfg->top_k, cfg->n_shared, cfg->wfmt, cfg->max_tokens};
+    h->n_layers = cfg->n_layers;
+    h->device = cfg->device;
+    h->layers.resize(cfg->n_layers);
+    size_t total = 0;
+    carve(h->s, nullptr, &total);
+    cudaError_t e = cudaMalloc(&h->ws_base, total);
+    if (e != cudaSuccess) {
+        delete h;
+        return cuda_status(e);
+    }
+    h->ws_bytes = total;
+    h->ws = carve(h->s, static_cast<char*>(h->ws_base), &total);
+    e = cudaMemset(h->ws_base, 0, total);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->load_stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cudaFree(h->ws_base);
+        delete h;
+        return cuda_status(e);
+    }
+    *out = h;
+    return FLINT_OK;
+}
+
+flint_status flint_moe_load_weights(flint_moe* h, int layer, const flint_moe_weights* w) {
+    if (h == nullptr || w == nullptr) return FLINT_EINVAL;
+    if (layer < 0 || layer >= h->n_layers) return FLINT_EINVAL;
+    if (w->router == nullptr || w->codes == nullptr || w->scales == nullptr) return FLINT_EINVAL;
+    const Shape& s = h->s;
+    if (s.wfmt == FLINT_W_NVFP4 && w->tensor_scale == nullptr) return FLINT_EINVAL;
+    const int n_slots = s.n_slots();
+    const size_t cpm = s.codes_per_matrix(), spm = s.scales_per_matrix();
+    const size_t n_codes = (size_t)n_slots * 3 * cpm, n_scales = (size_t)n_slots * 3 * spm;
+    // host-side validation
+    if (!finite_f32(w->router, (size_t)s.E * s.d)) return FLINT_EINVAL;
+    if (w->router_bias && !finite_f32(w->router_bias, s.E)) return FLINT_EINVAL;
+    if (s.wfmt == FLINT_W_NVFP4) {
+        if (!finite_f32(w->tensor_scale, (size_t)n_slots * 3)) return FLINT_EINVAL;
+        for (size_t i = 0; i < n_scales; ++i)
+            if (w->scales[i] > 0x7E) return FLINT_EINVAL;   // sign bit set, or NaN
+    } else {
+        for (size_t i = 0; i < n_scales; i += 2) {
+            const uint16_t v = (uint16_t)(w->scales[i] | (w->scales[i + 1] << 8));
+            if (((v >> 10) & 0x1f) == 0x1f) return FLINT_EINVAL;   // inf or NaN
+        }
+    }
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return FLINT_ECUDA;
+    LayerDev& L = h->layers[layer];
+    cudaError_t e = cudaSuccess;
+    if (L.codes == nullptr) {
+        e = cudaMalloc(&L.router, (size_t)s.E * s.d * sizeof(float));
+        if (e == cudaSuccess) e = cudaMalloc(&L.bias, (size_t)s.E * sizeof(float));
+        if (e == cudaSuccess) e = cudaMalloc(&L.codes, n_codes);
+        if (e == cudaSuccess) e = cudaMalloc(&L.scales, n_scales);
+        if (e == cudaSuccess) e = cudaMalloc(&L.tscale, (size_t)n_slots * 3 * sizeof(float));
+        if (e != cudaSuccess) {
+            free_layer(L);
+            return cuda_status(e);
+        }
+        h->weight_bytes += (size_t)s.E * s.d * 4 + (size_t)s.E * 4 + n_codes + n_scales + (size_t)n_slots * 12;
+    }
+    L.loaded = false;
+    uint8_t* stage = nullptr;
+    e = cudaMalloc(&stage, n_codes + n_scales);
+    if (e != cudaSuccess) return cuda_status(e);
+    cudaStream_t st = h->load_stream;
+    e = cudaMemcpyAsync(L.router, w->router, (size_t)s.E * s.d * sizeof(float), cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) {
+        if (w->router_bias)
+            e = cudaMemcpyAsync(L.bias, w->router_bias, (size_t)s.E * sizeof(float), cudaMemcpyHostToDevice, st);
+        else
+            e = cudaMemsetAsync(L.bias, 0, (size_t)s.E * sizeof(float), st);
+    }
+    if (e == cudaSuccess) {
+        if (s.wfmt == FLINT_W_NVFP4) {
+            e = cudaMemcpyAsync(L.tscale, w->tensor_scale, (size_t)n_slots * 3 * sizeof(float),
+                                cudaMemcpyHostToDevice, st);
+        } else {
+            std::vector<float> ones((size_t)n_slots * 3, 1.0f);
+            e = cudaMemcpyAsync(L.tscale, ones.data(), ones.size() * sizeof(float), cudaMemcpyHostToDevice, st);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        }
+    }
+    if (e == cudaSuccess) e = cudaMemcpyAsync(stage, w->codes, n_codes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(stage + n_codes, w->scales, n_scales, cudaMemcpyHostToDevice, st);
+    for (int sl = 0; sl < n_slots && e == cudaSuccess; ++sl) {
+        for (int m = 0; m < 3 && e == cudaSuccess; ++m) {
+            const int R = m < 2 ? s.f : s.d, K = m < 2 ? s.d : s.f;
+            const size_t mi = (size_t)sl * 3 + m;
+            e = flint::launch_repack_matrix(stage + mi * cpm, stage + n_codes + mi * spm, L.codes + mi * cpm,
+                                            L.scales + mi * spm, R, K, s.wfmt, st);
+        }
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    cudaFree(stage);
+    if (e != cudaSuccess) return cuda_status(e);
+    L.loaded = true;
+    return FLINT_OK;
+}
+
+flint_status flint_moe_forward(flint_moe* h, int layer, const void* hidden_dev, int T, void* out_dev,
+                               void* stream) {
+    flint_status st = check_forward_args(h, layer, hidden_dev, out_dev, T);
+    if (st != FLINT_OK) return st;
+    if (T > 0 && out_dev == nullptr) return FLINT_EINVAL;
+    if (T == 0) return FLINT_OK;
+    const char* x0 = static_cast<const char*>(hidden_dev);
+    const char* o0 = static_cast<const char*>(out_dev);
+    const size_t bytes = (size_t)T * h->s.d * 2;
+    if (x0 < o0 + bytes && o0 < x0 + bytes) return FLINT_EINVAL;   // overlap
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return FLINT_ECUDA;
+    cudaError_t e = run_layer(h, layer, static_cast<const __nv_bfloat16*>(hidden_dev), T,
+                              static_cast<__nv_bfloat16*>(out_dev), nullptr, (cudaStream_t)stream);
+    return cuda_status(e);
+}
+
+flint_status flint_moe_forward_stack(flint_moe* h, int layer0, int n_layers, void* hidden_dev, int T,
+                                     void* stream) {
+    if (h == nullptr || n_layers < 0) return FLINT_EINVAL;
+    if (layer0 < 0 || layer0 + n_layers > h->n_layers) return FLINT_EINVAL;
+    for (int l = layer0; l < layer0 + n_layers; ++l) {
+        flint_status st = check_forward_args(h, l, hidden_dev, nullptr, T);
+        if (st != FLINT_OK) return st;
+    }
+    if (T == 0 || n_layers == 0) return FLINT_OK;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return FLINT_ECUDA;
+    __nv_bfloat16* x = static_cast<__nv_bfloat16*>(hidden_dev);
+    for (int l = layer0; l < layer0 + n_layers; ++l) {
+        cudaError_t e = run_layer(h, l, x, T, x, x, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return FLINT_OK;
+}
+
+void flint_moe_destroy(flint_moe* h) {
+    if (h == nullptr) return;
+    {
+        DeviceGuard guard(h->device);
+        cudaDeviceSynchronize();
+        for (auto& L : h->layers) free_layer(L);
+        prof_free(h);
+        cudaFree(h->ws_base);
+        if (h->load_stream) cudaStreamDestroy(h->load_stream);
+    }
+    delete h;
+}
+
+flint_status flint_moe_status(flint_moe* h) {
+    if (h == nullptr) return FLINT_EINVAL;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return FLINT_ECUDA;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return FLINT_ECUDA;
+    uint32_t v = 0;
+    e = cudaMemcpy(&v, h->ws.status, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(h->ws.status, 0, sizeof(v));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return FLINT_ECUDA;
+    if (v & flint::kStatusTimeout) return FLINT_ETIMEOUT;
+    if (v != 0) return FLINT_EDEVICE;
+    return FLINT_OK;
+}
+
+flint_status flint_moe_router(flint_moe* h, int layer, const void* hidden_dev, int T, float* logits_dev,
+                              int32_t* idx_dev, float* w_dev, void* stream) {
+    flint_status st = check_forward_args(h, layer, hidden_dev, nullptr, T);
+    if (st != FLINT_OK) return st;
+    if (T == 0) return FLINT_OK;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return FLINT_ECUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const LayerDev& L = h->layers[layer];
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(hidden_dev);
+    int n = 0;
+    cudaError_t e = flint::launch_router(h->s, L, x, T, h->ws, s, &n);
+    h->launches += n;
+    if (e == cudaSuccess && logits_dev)
+        e = cudaMemcpyAsync(logits_dev, h->ws.logits, (size_t)T * h->s.E * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess && idx_dev)
+        e = cudaMemcpyAsync(idx_dev, h->ws.idx, (size_t)T * h->s.k * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess && w_dev)
+        e = cudaMemcpyAsync(w_dev, h->ws.w, (size_t)T * h->s.k * 4, cudaMemcpyDeviceToDevice, s);
+    return cuda_status(e);
+}
+
+flint_status flint_moe_topk(const float* logits_dev, int T, int E, int k, int32_t* idx_dev, float* w_dev,
+                            void* stream) {
+    if (T < 0 || E < 32 || E > 256 || E % 32 != 0 || k < 1 || k > 8 || k > E) return FLINT_EINVAL;
+    if (T == 0) return FLINT_OK;
+    if (logits_dev == nullptr || idx_dev == nullptr) return FLINT_EINVAL;
+    return cuda_status(flint::launch_topk(logits_dev, T, E, k, idx_dev, w_dev, (cudaStream_t)stream));
+}
+
+flint_status flint_moe_bucket(flint_moe* h, const int32_t* idx_dev, int T, int32_t* offsets_dev,
+                              int32_t* perm_dev, void* stream) {
+    if (h == nullptr || T < 0 || T > h->s.max_tokens) return FLINT_EINVAL;
+    if (T == 0) return FLINT_OK;
+    if (idx_dev == nullptr || offsets_dev == nullptr || perm_dev == nullptr) return FLINT_EINVAL;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return FLINT_ECUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    int n = 0;
+    cudaError_t e = flint::launch_bucket(h->s, idx_dev, T, h->ws, s, &n);
+    h->launches += n;
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(offsets_dev, h->ws.offsets, (size_t)(h->s.E + 1) * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(perm_dev, h->ws.perm, (size_t)T * h->s.k * 4, cudaMemcpyDeviceToDevice, s);
+    return cuda_status(e);
+}
+
+flint_status flint_moe_dequant(flint_moe* h, int layer, int expert, int mat, float* out_dev, void* stream) {
+    if (h == nullptr || out_dev == nullptr) return FLINT_EINVAL;
+    if (layer < 0 || layer >= h->n_layers) return FLINT_EINVAL;
+    if (expert < 0 || expert >= h->s.n_slots() || mat < 0 || mat > 2) return FLINT_EINVAL;
+    if (!h->layers[layer].loaded) return FLINT_ESTATE;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return FLINT_ECUDA;
+    const Shape& s = h->s;
+    const LayerDev& L = h->layers[layer];
+    const int R = mat < 2 ? s.f : s.d, K = mat < 2 ? s.d : s.f;
+    const size_t mi = (size_t)expert * 3 + mat;
+    cudaError_t e = flint::launch_dequant_matrix(L.codes + mi * s.codes_per_matrix(),
+                                                 L.scales + mi * s.scales_per_matrix(), 1.0f,
+                                                 s.wfmt == FLINT_W_NVFP4 ? L.tscale + mi : nullptr, R, K,
+                                                 s.wfmt, out_dev, (cudaStream_t)stream);
+    return cuda_status(e);
+}
+
+size_t flint_moe_device_bytes(const flint_moe* h) {
+    if (h == nullptr) return 0;
+    return h->ws_bytes + h->weight_bytes;
+}
+
+uint64_t flint_moe_launch_count(const flint_moe* h) { return h ? h->launches : 0; }
+
+flint_status flint_moe_profile_begin(flint_moe* h, int max_forwards) {
+    if (h == nullptr || max_forwards < 1 || max_forwards > (1 << 22)) return FLINT_EINVAL;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return FLINT_ECUDA;
+    prof_free(h);
+    h->prof_events.resize((size_t)max_forwards * 4);
+    for (size_t i = 0; i < h->prof_events.size(); ++i) {
+        if (cudaEventCreate(&h->prof_events[i]) != cudaSuccess) {
+            h->prof_events.resize(i);
+            prof_free(h);
+            return FLINT_ECUDA;
+        }
+    }
+    h->prof_max = max_forwards;
+    h->prof_n = 0;
+    return FLINT_OK;
+}
+
+flint_status flint_moe_profile_end(flint_moe* h, float* phase_ms, int* n_forwards) {
+    if (h == nullptr || phase_ms == nullptr || n_forwards == nullptr) return FLINT_EINVAL;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return FLINT_ECUDA;
+    double acc[3] = {0, 0, 0};
+    cudaError_t e = cudaSuccess;
+    for (int f = 0; f < h->prof_n && e == cudaSuccess; ++f) {
+        e = cudaEventSynchronize(h->prof_events[(size_t)f * 4 + 3]);
+        for (int p = 0; p < 3 && e == cudaSuccess; ++p) {
+            float ms = 0.f;
+            e = cudaEventElapsedTime(&ms, h->prof_events[(size_t)f * 4 + p], h->prof_events[(size_t)f * 4 + p + 1]);
+            acc[p] += ms;
+        }
+    }
+    for (int p = 0; p < 3; ++p) phase_ms[p] = (float)acc[p];
+    *n_forwards = h->prof_n;
+    prof_free(h);
+    return cuda_status(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,151 @@
+// Device helpers shared by the layer's kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace flint {
+
+constexpr int kWarp = 32;
+constexpr int kKTile = 128;   // K elements per weight tile (8 mma k16 steps)
+constexpr int kRowTile = 8;   // rows per weight tile
+
+// Device status word bits.
+constexpr uint32_t kStatusNonFiniteLogit = 1u;
+constexpr uint32_t kStatusBadIndex = 2u;
+constexpr uint32_t kStatusTimeout = 4u;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// Fragment permutation inside a 128-element K tile.
+//
+// mma.m16n8k16 gives lane (g = lane/4, c = lane%4) the K positions
+// {2c, 2c+1, 2c+8, 2c+9} of every 16-wide step. Activations are stored so that
+// one lane's four values of all 8 steps of a tile are contiguous:
+//   position p = c*32 + s*4 + j  holds  K index 16*s + {2c, 2c+1, 2c+8, 2c+9}[j]
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ int kperm_pos(int k /* 0..127 */) {
+    int s = k >> 4, r = k & 15;
+    int c = (r & 7) >> 1;
+    int j = (r & 1) | ((r >> 3) << 1);
+    return c * 32 + s * 4 + j;
+}
+
+// ---------------------------------------------------------------------------
+// 4-bit and 8-bit float conversions (hardware cvt, exact)
+// ---------------------------------------------------------------------------
+
+// Four bytes of packed E2M1 pairs -> four f16x2 (byte i -> r[i]; the low
+// nibble goes to the low half).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& r0, uint32_t& r1,
+                                                uint32_t& r2, uint32_t& r3) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+        : "r"(w));
+}
+
+// Two E4M3 bytes (low 16 bits of w) -> f16x2 (low byte -> low half).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+    uint32_t r;
+    uint16_t v = (uint16_t)(w & 0xffffu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// broadcast the low / high f16 of x to both halves
+__device__ __forceinline__ uint32_t bcast_lo(uint32_t x) { return __byte_perm(x, 0, 0x1010); }
+__device__ __forceinline__ uint32_t bcast_hi(uint32_t x) { return __byte_perm(x, 0, 0x3232); }
+
+// q4_1: byte (two 4-bit q) -> f16x2 {q_lo, q_hi} exactly, via 1024 + q.
+__device__ __forceinline__ uint32_t q4x2_to_f16x2(uint32_t byte) {
+    uint32_t v = 0x64006400u | (byte & 0xfu) | ((byte & 0xf0u) << 12);
+    return hsub2_u(v, 0x64006400u);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------------------
+// mma.sync m16n8k16, f16 inputs, f32 accumulate (D = A B + D)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------------------
+// loads
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(r.x), "=r"(r.y)
+                 : "l"(p));
+    return r;
+}
+
+// 2^e as float for e in [-126, 127]
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// Power-of-two multiplier that brings a positive amax into [2^14, 2^15):
+// values scaled by it fit fp16 with full precision. 1 for amax 0 or non-finite.
+__device__ __forceinline__ float f16_range_mult(float amax) {
+    uint32_t b = __float_as_uint(amax);
+    int ef = (int)((b >> 23) & 0xff);
+    if (amax <= 0.0f || ef == 0xff) return 1.0f;
+    int e = (ef == 0) ? -126 : ef - 127;   // floor(log2(amax)) for normals
+    int m = 14 - e;
+    m = m > 126 ? 126 : (m < -126 ? -126 : m);
+    return exp2i(m);
+}
+
+}  // namespace flint

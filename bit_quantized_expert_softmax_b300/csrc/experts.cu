@@ -1,0 +1,476 @@
+// Expert projections for small and medium token counts: SwiGLU gate/up,
+// down projection and the weighted combine with the shared expert.
+//
+// The Flint blog ("Recursive Flint 40B-A2.5B", section "The architecture is
+// an argument about memory bandwidth") frames decode as moving the selected
+// experts' weights from memory to the arithmetic units; these kernels stream
+// only the selected experts' packed 4-bit tiles, once, with one 16-byte load
+// per lane per 8x128 tile, and decode them in registers.
+//
+// Arithmetic: weights are decoded to fp16 (NVFP4: E2M1 x E4M3 is exact in
+// fp16; q4_1: d*q + m rounded once to fp16 by an fma), activations are fp16
+// scaled per token (or per position) by a power of two that brings their
+// maximum into [2^14, 2^15), and mma.sync m16n8k16 accumulates in fp32. The
+// fp32 tensor scale and the inverse activation scale are applied to the
+// accumulator.
+#include "kernels.cuh"
+
+namespace flint {
+
+namespace {
+
+constexpr int kThreads = 128;   // 4 warps
+constexpr int kNB = 4;          // n-tiles (8 tokens each) per pass
+
+struct ExpertArgs {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    const float* tscale;
+    size_t codes_per_mat, scales_per_mat;
+    int d, f, E, k, n_shared, T;
+    Workspace ws;
+    __nv_bfloat16* out;
+    const __nv_bfloat16* residual;
+    int fuse_combine;
+};
+
+__device__ __forceinline__ int token_of(const ExpertArgs& a, int pos) {
+    const int routed = a.T * a.k;
+    return pos < routed ? __ldg(a.ws.perm + pos) / a.k : pos - routed;
+}
+
+// Decode one 8-row x 128-K tile pair (rows g and g+8 of a 16-row A tile) into
+// A fragments of the 8 k16 steps. wg/wh: the lane's 16 code bytes of the two
+// 8-row tiles; sg/sh: scale data of rows g and g+8.
+template <int WFMT>
+struct TileScales;
+
+template <>
+struct TileScales<0> {   // NVFP4: 8 E4M3 bytes per row (one per step)
+    uint2 g, h;
+};
+template <>
+struct TileScales<1> {   // q4_1: 4 blocks x (fp16 d, fp16 m) per row
+    uint4 g, h;
+};
+
+template <int WFMT>
+__device__ __forceinline__ TileScales<WFMT> load_scales(const uint8_t* base_g, const uint8_t* base_h,
+                                                        int g);
+
+template <>
+__device__ __forceinline__ TileScales<0> load_scales<0>(const uint8_t* base_g, const uint8_t* base_h,
+                                                        int g) {
+    TileScales<0> s;
+    s.g = ldg_nc_v2(base_g + g * 8);
+    s.h = ldg_nc_v2(base_h + g * 8);
+    return s;
+}
+
+template <>
+__device__ __forceinline__ TileScales<1> load_scales<1>(const uint8_t* base_g, const uint8_t* base_h,
+                                                        int g) {
+    TileScales<1> s;
+    s.g = ldg_nc_v4(base_g + g * 16);
+    s.h = ldg_nc_v4(base_h + g * 16);
+    return s;
+}
+
+__device__ __forceinline__ uint32_t u4_get(const uint4& v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+__device__ __forceinline__ uint32_t u2_get(const uint2& v, int i) { return i == 0 ? v.x : v.y; }
+
+// a[s][0..3] = A fragment registers of step s
+template <int WFMT>
+__device__ __forceinline__ void decode_tile(const uint4& wg, const uint4& wh, const TileScales<WFMT>& sc,
+                                            uint32_t (&a)[8][4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {   // word j holds steps 2j, 2j+1
+        const uint32_t xg = u4_get(wg, j), xh = u4_get(wh, j);
+        if constexpr (WFMT == 0) {
+            uint32_t g0, g1, g2, g3, h0, h1, h2, h3;
+            e2m1x8_to_f16x2(xg, g0, g1, g2, g3);
+            e2m1x8_to_f16x2(xh, h0, h1, h2, h3);
+            // scale bytes of steps 2j, 2j+1: bytes 2j, 2j+1 of the row's 8 bytes
+            const uint32_t sgw = u2_get(sc.g, j >> 1) >> ((j & 1) * 16);
+            const uint32_t shw = u2_get(sc.h, j >> 1) >> ((j & 1) * 16);
+            const uint32_t sg2 = e4m3x2_to_f16x2(sgw), sh2 = e4m3x2_to_f16x2(shw);
+            const uint32_t sg_a = bcast_lo(sg2), sg_b = bcast_hi(sg2);
+            const uint32_t sh_a = bcast_lo(sh2), sh_b = bcast_hi(sh2);
+            a[2 * j][0] = hmul2_u(g0, sg_a);
+            a[2 * j][1] = hmul2_u(h0, sh_a);
+            a[2 * j][2] = hmul2_u(g1, sg_a);
+            a[2 * j][3] = hmul2_u(h1, sh_a);
+            a[2 * j + 1][0] = hmul2_u(g2, sg_b);
+            a[2 * j + 1][1] = hmul2_u(h2, sh_b);
+            a[2 * j + 1][2] = hmul2_u(g3, sg_b);
+            a[2 * j + 1][3] = hmul2_u(h3, sh_b);
+        } else {
+            // steps 2j, 2j+1 form 32-element block j: (d, m) word of block j
+            const uint32_t dmg = u4_get(sc.g, j), dmh = u4_get(sc.h, j);
+            const uint32_t dg = bcast_lo(dmg), mg = bcast_hi(dmg);
+            const uint32_t dh = bcast_lo(dmh), mh = bcast_hi(dmh);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const uint32_t qg = q4x2_to_f16x2((xg >> (8 * b)) & 0xffu);
+                const uint32_t qh = q4x2_to_f16x2((xh >> (8 * b)) & 0xffu);
+                const int s = 2 * j + (b >> 1);
+                const int lo = (b & 1) * 2;   // byte 0/2 -> k 2c.., byte 1/3 -> k 2c+8..
+                a[s][lo + 0] = hfma2_u(qg, dg, mg);
+                a[s][lo + 1] = hfma2_u(qh, dh, mh);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// a5 + a7 (gate/up part): h = silu(W_gate x) * (W_up x) for one 16-row tile of
+// f for every position of one active expert slot.
+// ---------------------------------------------------------------------------
+template <int WFMT>
+__global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertArgs a) {
+    __shared__ float red[4][2][kNB][32][4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int KT = a.d >> 7;
+    const int tiles = a.f >> 4;
+    const int n_tasks = a.ws.meta[0] * tiles;
+    const size_t tile_bytes_s = (WFMT == 0) ? 64 : 128;
+    for (int task = blockIdx.x; task < n_tasks; task += gridDim.x) {
+        const int slot = task / tiles, r16 = task - slot * tiles;
+        const int e = a.ws.slot_expert[slot];
+        const int p0 = a.ws.slot_off[slot], cnt = a.ws.slot_cnt[slot];
+        const uint8_t* cbase = a.codes + (size_t)e * 3 * a.codes_per_mat;
+        const uint8_t* sbase = a.scales + (size_t)e * 3 * a.scales_per_mat;
+        const float tsg = a.tscale[e * 3 + 0], tsu = a.tscale[e * 3 + 1];
+        const size_t rtg = (size_t)(2 * r16) * KT, rth = (size_t)(2 * r16 + 1) * KT;
+        for (int n0 = 0; n0 < cnt; n0 += 8 * kNB) {
+            const int nb = min(kNB, (cnt - n0 + 7) >> 3);
+            float accg[kNB][4], accu[kNB][4];
+#pragma unroll
+            for (int i = 0; i < kNB; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) accg[i][j] = accu[i][j] = 0.f;
+            int tok[kNB];
+#pragma unroll
+            for (int nt = 0; nt < kNB; ++nt) {
+                const int n = n0 + nt * 8 + g;
+                tok[nt] = (nt < nb && n < cnt) ? token_of(a, p0 + n) : -1;
+            }
+            for (int kt = warp; kt < KT; kt += 4) {
+                const uint8_t* cg = cbase;                       // gate
+                const uint8_t* cu = cbase + a.codes_per_mat;     // up
+                const uint4 wgg = ldg_nc_v4(cg + (rtg + kt) * 512 + lane * 16);
+                const uint4 wgh = ldg_nc_v4(cg + (rth + kt) * 512 + lane * 16);
+                const uint4 wug = ldg_nc_v4(cu + (rtg + kt) * 512 + lane * 16);
+                const uint4 wuh = ldg_nc_v4(cu + (rth + kt) * 512 + lane * 16);
+                const uint8_t* sg = sbase;
+                const uint8_t* su = sbase + a.scales_per_mat;
+                const TileScales<WFMT> scg = load_scales<WFMT>(sg + (rtg + kt) * tile_bytes_s,
+                                                               sg + (rth + kt) * tile_bytes_s, g);
+                const TileScales<WFMT> scu = load_scales<WFMT>(su + (rtg + kt) * tile_bytes_s,
+                                                               su + (rth + kt) * tile_bytes_s, g);
+                uint32_t fa[8][4], fu[8][4];
+                decode_tile<WFMT>(wgg, wgh, scg, fa);
+                decode_tile<WFMT>(wug, wuh, scu, fu);
+#pragma unroll
+                for (int nt = 0; nt < kNB; ++nt) {
+                    if (nt >= nb) break;
+                    uint32_t b[16];
+                    if (tok[nt] >= 0) {
+                        const uint4* xp = reinterpret_cast<const uint4*>(
+                            a.ws.x16 + (size_t)tok[nt] * a.d + kt * 128 + c * 32);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 v = __ldg(xp + q);
+                            b[4 * q + 0] = v.x;
+                            b[4 * q + 1] = v.y;
+                            b[4 * q + 2] = v.z;
+                            b[4 * q + 3] = v.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) b[q] = 0u;
+                    }
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        mma_16816(accg[nt], fa[s][0], fa[s][1], fa[s][2], fa[s][3], b[2 * s], b[2 * s + 1]);
+                        mma_16816(accu[nt], fu[s][0], fu[s][1], fu[s][2], fu[s][3], b[2 * s], b[2 * s + 1]);
+                    }
+                }
+            }
+            // reduce the four K-partials
+#pragma unroll
+            for (int nt = 0; nt < kNB; ++nt)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    red[warp][0][nt][lane][j] = accg[nt][j];
+                    red[warp][1][nt][lane][j] = accu[nt][j];
+                }
+            __syncthreads();
+            const int nt = warp;
+            if (nt < nb) {
+                float hv[4];
+                int posv[2] = {-1, -1};
+                float xinv[2] = {0.f, 0.f};
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int n = n0 + nt * 8 + 2 * c + q;
+                    if (n < cnt) {
+                        posv[q] = p0 + n;
+                        xinv[q] = a.ws.xinv[token_of(a, p0 + n)];
+                    }
+                }
+                float hmax[2] = {0.f, 0.f};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float sg = ((red[0][0][nt][lane][j] + red[1][0][nt][lane][j]) +
+                                      red[2][0][nt][lane][j]) + red[3][0][nt][lane][j];
+                    const float su = ((red[0][1][nt][lane][j] + red[1][1][nt][lane][j]) +
+                                      red[2][1][nt][lane][j]) + red[3][1][nt][lane][j];
+                    const int q = j & 1;
+                    const float gv = sg * tsg * xinv[q];
+                    const float uv = su * tsu * xinv[q];
+                    hv[j] = gv / (1.0f + expf(-gv)) * uv;
+                    if (posv[q] >= 0) hmax[q] = fmaxf(hmax[q], fabsf(hv[j]));
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int q = j & 1;
+                    if (posv[q] < 0) continue;
+                    const int row = r16 * 16 + g + ((j >> 1) << 3);
+                    a.ws.hf[(size_t)posv[q] * a.f + (row & ~127) + kperm_pos(row & 127)] = hv[j];
+                }
+                // max over the 8 row groups sharing these positions
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+#pragma unroll
+                    for (int o = 4; o < 32; o <<= 1)
+                        hmax[q] = fmaxf(hmax[q], __shfl_xor_sync(0xffffffffu, hmax[q], o));
+                }
+                if (g == 0) {
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+                        if (posv[q] >= 0) atomicMax(a.ws.hamax + posv[q], __float_as_uint(hmax[q]));
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// a6 + a7 + a8: y = W_down h for 64 output rows of one active slot, weighted
+// by the routing weight (1 for the shared expert) into yw; with fuse_combine,
+// the last slot to finish a row block sums the block's outputs in slot order
+// and writes bf16.
+// ---------------------------------------------------------------------------
+__device__ void combine_rows(const ExpertArgs& a, int row0, int nrows) {
+    const int T = a.T;
+    for (int i = threadIdx.x; i < T * nrows; i += blockDim.x) {
+        const int t = i / nrows, row = row0 + i % nrows;
+        float v = 0.f;
+        if (a.n_shared) v = __ldcg(a.ws.yw + (size_t)(T * a.k + t) * a.d + row);
+        for (int j = 0; j < a.k; ++j) {
+            const int pos = __ldcg(a.ws.inv + t * a.k + j);
+            v += __ldcg(a.ws.yw + (size_t)pos * a.d + row);
+        }
+        __nv_bfloat16 o = __float2bfloat16_rn(v);
+        if (a.residual != nullptr) {
+            const float r = __bfloat162float(a.residual[(size_t)t * a.d + row]);
+            o = __float2bfloat16_rn(r + __bfloat162float(o));
+        }
+        a.out[(size_t)t * a.d + row] = o;
+    }
+}
+
+template <int WFMT>
+__global__ void __launch_bounds__(kThreads) down_kernel(ExpertArgs a) {
+    __shared__ int s_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int KT = a.f >> 7;
+    const int blocks = a.d >> 6;
+    const int n_slots = a.ws.meta[0];
+    const int n_tasks = n_slots * blocks;
+    const size_t tile_bytes_s = (WFMT == 0) ? 64 : 128;
+    for (int task = blockIdx.x; task < n_tasks; task += gridDim.x) {
+        const int blk = task % blocks, slot = task / blocks;
+        const int e = a.ws.slot_expert[slot];
+        const int p0 = a.ws.slot_off[slot], cnt = a.ws.slot_cnt[slot];
+        const bool shared = (e == a.E);
+        const uint8_t* cd = a.codes + ((size_t)e * 3 + 2) * a.codes_per_mat;
+        const uint8_t* sd = a.scales + ((size_t)e * 3 + 2) * a.scales_per_mat;
+        const float tsd = a.tscale[e * 3 + 2];
+        const int r16 = blk * 4 + warp;
+        const size_t rtg = (size_t)(2 * r16) * KT, rth = (size_t)(2 * r16 + 1) * KT;
+        for (int n0 = 0; n0 < cnt; n0 += 8 * kNB) {
+            const int nb = min(kNB, (cnt - n0 + 7) >> 3);
+            float acc[kNB][4];
+#pragma unroll
+            for (int i = 0; i < kNB; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+            int posb[kNB];
+            float multb[kNB];
+#pragma unroll
+            for (int nt = 0; nt < kNB; ++nt) {
+                const int n = n0 + nt * 8 + g;
+                posb[nt] = (nt < nb && n < cnt) ? p0 + n : -1;
+                multb[nt] = posb[nt] >= 0 ? f16_range_mult(__uint_as_float(a.ws.hamax[posb[nt]])) : 1.f;
+            }
+            for (int kt = 0; kt < KT; ++kt) {
+                const uint4 wg = ldg_nc_v4(cd + (rtg + kt) * 512 + lane * 16);
+                const uint4 wh = ldg_nc_v4(cd + (rth + kt) * 512 + lane * 16);
+                const TileScales<WFMT> sc = load_scales<WFMT>(sd + (rtg + kt) * tile_bytes_s,
+                                                              sd + (rth + kt) * tile_bytes_s, g);
+                uint32_t fa[8][4];
+                decode_tile<WFMT>(wg, wh, sc, fa);
+#pragma unroll
+                for (int nt = 0; nt < kNB; ++nt) {
+                    if (nt >= nb) break;
+                    uint32_t b[16];
+                    if (posb[nt] >= 0) {
+                        const float4* hp = reinterpret_cast<const float4*>(
+                            a.ws.hf + (size_t)posb[nt] * a.f + kt * 128 + c * 32);
+                        const float m = multb[nt];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            float4 v = __ldcg(hp + q);
+                            b[2 * q + 0] = pack_half2(v.x * m, v.y * m);
+                            b[2 * q + 1] = pack_half2(v.z * m, v.w * m);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) b[q] = 0u;
+                    }
+#pragma unroll
+                    for (int s = 0; s < 8; ++s)
+                        mma_16816(acc[nt], fa[s][0], fa[s][1], fa[s][2], fa[s][3], b[2 * s], b[2 * s + 1]);
+                }
+            }
+            // epilogue: rows g, g+8 of this warp's tile; positions 2c, 2c+1 of each n-tile
+#pragma unroll
+            for (int nt = 0; nt < kNB; ++nt) {
+                if (nt >= nb) break;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int n = n0 + nt * 8 + 2 * c + q;
+                    if (n >= cnt) continue;
+                    const int pos = p0 + n;
+                    const float wr = shared ? 1.0f : a.ws.w[__ldg(a.ws.perm + pos)];
+                    const float mult = f16_range_mult(__uint_as_float(a.ws.hamax[pos]));
+                    const float sc = tsd / mult * wr;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int row = r16 * 16 + g + hh * 8;
+                        a.ws.yw[(size_t)pos * a.d + row] = acc[nt][hh * 2 + q] * sc;
+                    }
+                }
+            }
+        }
+        if (a.fuse_combine) {
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                const uint32_t prev = atomicAdd(a.ws.counters + 1 + blk, 1u);
+                s_last = (prev == (uint32_t)n_slots - 1u);
+            }
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                combine_rows(a, blk * 64, 64);
+                if (threadIdx.x == 0) a.ws.counters[1 + blk] = 0u;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
+    const int rows_per_cta = 256;
+    const int nblk = (a.d + rows_per_cta - 1) / rows_per_cta;
+    const int t = blockIdx.x / nblk;
+    const int row0 = (blockIdx.x % nblk) * rows_per_cta;
+    const int row = row0 + threadIdx.x;
+    if (t >= a.T || row >= a.d) return;
+    float v = 0.f;
+    if (a.n_shared) v = a.ws.yw[(size_t)(a.T * a.k + t) * a.d + row];
+    for (int j = 0; j < a.k; ++j) {
+        const int pos = a.ws.inv[t * a.k + j];
+        v += a.ws.yw[(size_t)pos * a.d + row];
+    }
+    __nv_bfloat16 o = __float2bfloat16_rn(v);
+    if (a.residual != nullptr) {
+        const float r = __bfloat162float(a.residual[(size_t)t * a.d + row]);
+        o = __float2bfloat16_rn(r + __bfloat162float(o));
+    }
+    a.out[(size_t)t * a.d + row] = o;
+}
+
+}  // namespace
+
+namespace {
+
+ExpertArgs make_args(const Shape& s, const LayerDev& L, int T, const Workspace& ws) {
+    ExpertArgs a;
+    a.codes = L.codes;
+    a.scales = L.scales;
+    a.tscale = L.tscale;
+    a.codes_per_mat = s.codes_per_matrix();
+    a.scales_per_mat = s.scales_per_matrix();
+    a.d = s.d;
+    a.f = s.f;
+    a.E = s.E;
+    a.k = s.k;
+    a.n_shared = s.n_shared;
+    a.T = T;
+    a.ws = ws;
+    a.out = nullptr;
+    a.residual = nullptr;
+    a.fuse_combine = (T <= kSmallT) ? 1 : 0;
+    return a;
+}
+
+int grid_for(int tasks) {
+    const int cap = 148 * 8;
+    return tasks < cap ? tasks : cap;
+}
+
+}  // namespace
+
+cudaError_t launch_gateup(const Shape& s, const LayerDev& L, int T, const Workspace& ws,
+                          cudaStream_t st, int* n_launch) {
+    ExpertArgs a = make_args(s, L, T, ws);
+    const int max_slots = min(s.E, T * s.k) + s.n_shared;
+    const int grid = grid_for(max_slots * (s.f / 16));
+    if (s.wfmt == 0)
+        gateup_kernel<0><<<grid, kThreads, 0, st>>>(a);
+    else
+        gateup_kernel<1><<<grid, kThreads, 0, st>>>(a);
+    *n_launch += 1;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_down(const Shape& s, const LayerDev& L, int T, const Workspace& ws,
+                        __nv_bfloat16* out, const __nv_bfloat16* residual, cudaStream_t st,
+                        int* n_launch) {
+    ExpertArgs a = make_args(s, L, T, ws);
+    a.out = out;
+    a.residual = residual;
+    const int max_slots = min(s.E, T * s.k) + s.n_shared;
+    const int grid = grid_for(max_slots * (s.d / 64));
+    if (s.wfmt == 0)
+        down_kernel<0><<<grid, kThreads, 0, st>>>(a);
+    else
+        down_kernel<1><<<grid, kThreads, 0, st>>>(a);
+    *n_launch += 1;
+    if (!a.fuse_combine) {
+        const int nblk = (s.d + 255) / 256;
+        combine_kernel<<<T * nblk, 256, 0, st>>>(a);
+        *n_launch += 1;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace flint

@@ -1,0 +1,92 @@
+// Internal interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace flint {
+
+// Device-resident weights of one layer, in the kernels' tiled layout.
+//
+// Codes of a matrix [R x K] are stored as tiles of 8 rows x 128 K, tile
+// (rt, kt) at byte offset (rt*(K/128) + kt)*512. Inside a tile, lane
+// l = 4g + c owns 16 bytes at offset l*16; byte 2s (s = 0..7) is canonical
+// byte kt*64 + 8s + c of row rt*8 + g (K elements 16s+2c, 16s+2c+1 of the
+// tile) and byte 2s+1 is canonical byte kt*64 + 8s + c + 4 (K elements
+// 16s+2c+8, 16s+2c+9). This is the A-fragment order of mma.m16n8k16, so one
+// 16-byte load per lane and tile feeds 8 mma steps.
+//
+// NVFP4 block scales: per tile 64 bytes, [g][s] = scale of row rt*8+g for the
+// 16 K elements of step s. q4_1: per tile 128 bytes, [g][b] = 4 bytes
+// (fp16 d, fp16 m) of row rt*8+g for K block kt*4+b (32 elements).
+struct LayerDev {
+    float* router = nullptr;        // [E][d]
+    float* bias = nullptr;          // [E] (zeros when absent)
+    uint8_t* codes = nullptr;       // [n_slots][3][f*d/2] tiled
+    uint8_t* scales = nullptr;      // [n_slots][3][scale bytes] tiled
+    float* tscale = nullptr;        // [n_slots][3]
+    bool loaded = false;
+};
+
+struct Shape {
+    int d, f, E, k, n_shared, wfmt, max_tokens;
+    int n_slots() const { return E + n_shared; }
+    size_t codes_per_matrix() const { return (size_t)f * d / 2; }
+    size_t scales_per_matrix() const {
+        return wfmt == 0 ? (size_t)f * d / 16 : (size_t)f * d / 32 * 4;
+    }
+    int positions(int T) const { return T * (k + n_shared); }
+};
+
+// Per-handle scratch for one forward (sized for max_tokens).
+struct Workspace {
+    float* logits;        // [Tm][E]
+    int* idx;             // [Tm][k]
+    float* w;             // [Tm][k]
+    int* perm;            // [Tm*k]  sorted position -> assignment t*k+j
+    int* inv;             // [Tm*k]  assignment -> sorted position
+    int* offsets;         // [E+1]
+    int* slot_expert;     // [E+1]  active slot -> expert (E = shared)
+    int* slot_off;        // [E+1]  first position of the slot
+    int* slot_cnt;        // [E+1]  positions of the slot
+    int* meta;            // [8]    0: number of active slots
+    __half* x16;          // [Tm][d]  fp16 hidden, scaled per token, fragment-permuted
+    float* xinv;          // [Tm]     inverse of the per-token fp16 scale
+    float* hf;            // [P][f]   expert intermediate h (fp32, fragment-permuted)
+    uint32_t* hamax;      // [P]      max |h| per position (float bits)
+    float* yw;            // [P][d]   weighted expert outputs
+    int* chunk_hist;      // [n_chunks][E]
+    uint32_t* counters;   // [kCounters] arrival counters (self-resetting)
+    uint32_t* status;     // device status word
+};
+
+constexpr int kCounters = 1024;
+constexpr int kBucketChunk = 2048;      // assignments per bucketing CTA
+constexpr int kSmallT = 64;             // fused decode path up to this many tokens
+
+// router.cu
+cudaError_t launch_router(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
+                          const Workspace& ws, cudaStream_t st, int* n_launch);
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int* idx, float* w,
+                        cudaStream_t st);
+cudaError_t launch_bucket(const Shape& s, const int* idx, int T, const Workspace& ws,
+                          cudaStream_t st, int* n_launch);
+
+// experts.cu: gate/up (one launch), then down + combine (one or two launches)
+cudaError_t launch_gateup(const Shape& s, const LayerDev& L, int T, const Workspace& ws,
+                          cudaStream_t st, int* n_launch);
+cudaError_t launch_down(const Shape& s, const LayerDev& L, int T, const Workspace& ws,
+                        __nv_bfloat16* out, const __nv_bfloat16* residual, cudaStream_t st,
+                        int* n_launch);
+
+// repack.cu
+cudaError_t launch_repack_matrix(const uint8_t* codes_src, const uint8_t* scales_src,
+                                 uint8_t* codes_dst, uint8_t* scales_dst, int R, int K, int wfmt,
+                                 cudaStream_t st);
+cudaError_t launch_dequant_matrix(const uint8_t* codes, const uint8_t* scales, float tscale_host,
+                                  const float* tscale_dev, int R, int K, int wfmt, float* out,
+                                  cudaStream_t st);
+
+}  // namespace flint

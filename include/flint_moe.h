@@ -1,0 +1,205 @@
+/*
+ * flint_moe.h -- C ABI of the B300 (sm_103a) sparse 4-bit MoE FFN layer.
+ *
+ * The layer is the conditional FFN of a Flint-shaped model ("Recursive Flint
+ * 40B-A2.5B: a coding model designed speed-first", orcarouter.ai blog,
+ * section "The architecture is an argument about memory bandwidth", Sparsity
+ * bullet): per MoE layer 256 routed experts with 6 chosen per token plus one
+ * always-on shared expert; 47 of the model's 49 layers are MoE layers. The
+ * experts carry 4-bit weights, NVFP4 or q4_1 (section "What actually
+ * shipped"). For one layer and tokens x[t] (bfloat16, width d):
+ *
+ *   L[t,e]  = sum_i x[t,i] W_r[e,i] + b[e]                  fp32 router logits
+ *   S_t     = 6 largest logits (ties: lower expert index), descending
+ *   w[t,j]  = softmax(L[t,:])[S_t[j]] / sum_{e in S_t} softmax(L[t,:])[e]
+ *   y_e(x)  = W_down_e ( silu(W_gate_e x) * (W_up_e x) ),  silu(z) = z/(1+e^-z)
+ *   out[t]  = bf16( y_shared(x[t]) + sum_j w[t,j] y_{S_t[j]}(x[t]) )
+ *
+ * Weight formats (canonical host layout accepted by flint_moe_load_weights):
+ *   NVFP4: w = E2M1(code) * E4M3(block scale) * fp32 tensor scale; one E4M3
+ *          block scale per 16 consecutive elements of a row, one fp32 tensor
+ *          scale per matrix. Two codes per byte, element 2i in the low nibble.
+ *   q4_1 : w = d*q + m, q in 0..15; per 32 consecutive elements of a row one
+ *          fp16 d followed by one fp16 m (little endian, 4 bytes). Codes as
+ *          for NVFP4.
+ * Matrices per expert: 0 = gate [f x d], 1 = up [f x d], 2 = down [d x f],
+ * each row-major with the contraction axis (K) contiguous.
+ *
+ * Conventions shared by every call:
+ *   - Pointers named *_dev are CUDA device pointers on the handle's device;
+ *     all others are host pointers. The caller owns every buffer it passes.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls that
+ *     take a stream only enqueue work and return; results are ready once the
+ *     stream reaches that point.
+ *   - Errors are returned, never thrown. FLINT_EINVAL / FLINT_ESTATE mean
+ *     nothing was enqueued. Faults detected on the device (non-finite router
+ *     logits, out-of-range indices) set a status word that flint_moe_status
+ *     reports and clears.
+ *   - A handle is not safe for concurrent use from several host threads, and
+ *     two forwards on one handle must not overlap on the GPU (they share one
+ *     workspace).
+ */
+#ifndef FLINT_MOE_H
+#define FLINT_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FLINT_API __attribute__((visibility("default")))
+#else
+#define FLINT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct flint_moe flint_moe;
+
+typedef enum {
+    FLINT_OK = 0,
+    FLINT_EINVAL = 1,    /* bad argument: NULL, size, alignment, range */
+    FLINT_ENOMEM = 2,    /* device allocation failed */
+    FLINT_ECUDA = 3,     /* a CUDA runtime call or launch failed */
+    FLINT_ESTATE = 4,    /* handle not ready (weights of the layer not loaded) */
+    FLINT_ETIMEOUT = 5,  /* a bounded device-side wait gave up */
+    FLINT_ENOTIMPL = 6,  /* configuration not supported by this build */
+    FLINT_EDEVICE = 7    /* the device reported a data fault (see flint_moe_status) */
+} flint_status;
+
+typedef enum { FLINT_W_NVFP4 = 0, FLINT_W_Q4_1 = 1 } flint_wfmt;
+
+/* Shape of the layers held by one handle. Constraints: d and f multiples of
+ * 128; 32 <= n_experts <= 256 and a multiple of 32; 1 <= top_k <= 8 and
+ * top_k <= n_experts; n_shared 0 or 1; 1 <= max_tokens <= 65536;
+ * n_layers >= 1. The Flint shape is d=2048, f=512, n_experts=256, top_k=6,
+ * n_shared=1, n_layers=47. */
+typedef struct {
+    int d;
+    int f;
+    int n_experts;
+    int top_k;
+    int n_shared;
+    int wfmt;        /* flint_wfmt */
+    int max_tokens;  /* largest T any forward on this handle will pass */
+    int n_layers;
+    int device;      /* CUDA device ordinal */
+} flint_moe_config;
+
+/* One layer's weights, canonical host layout (see the format notes above).
+ * n = n_experts + n_shared expert slots; the shared expert is slot n_experts.
+ *   router        float  [n_experts][d]          one row per expert
+ *   router_bias   float  [n_experts] or NULL (all zero)
+ *   codes         uint8  [n][3][f*d/2]
+ *   scales        uint8  [n][3][f*d/16]   (NVFP4: E4M3 bytes)
+ *                        [n][3][f*d/32*4] (q4_1: fp16 d, fp16 m per block)
+ *   tensor_scale  float  [n][3] (NVFP4); ignored for q4_1 (may be NULL)
+ * E4M3 block scales must be non-negative and not NaN (bytes 0x00..0x7E); fp16
+ * d and m, the router, its bias and the tensor scales must be finite. */
+typedef struct {
+    const float* router;
+    const float* router_bias;
+    const uint8_t* codes;
+    const uint8_t* scales;
+    const float* tensor_scale;
+} flint_moe_weights;
+
+/* Create a handle on cfg->device: validates cfg and allocates the per-token
+ * workspace for cfg->max_tokens (no weights yet). *out is NULL on failure.
+ * Errors: FLINT_EINVAL (cfg), FLINT_ENOTIMPL, FLINT_ENOMEM, FLINT_ECUDA. */
+FLINT_API flint_status flint_moe_create(const flint_moe_config* cfg, flint_moe** out);
+
+/* Copy layer `layer`'s weights from host memory into device memory owned by
+ * the handle and repack them into the kernels' tiled layout. Synchronous: the
+ * host buffers may be freed on return. Loading a layer again replaces it.
+ * Errors: FLINT_EINVAL (NULL pointer, layer out of range, NaN/negative E4M3
+ * scale, non-finite fp16 or fp32 value), FLINT_ENOMEM, FLINT_ECUDA. */
+FLINT_API flint_status flint_moe_load_weights(flint_moe* h, int layer, const flint_moe_weights* w);
+
+/* One MoE layer: out_dev[T][d] = MoE_layer(hidden_dev[T][d]), both bfloat16,
+ * 16-byte aligned, not overlapping. T == 0 is a no-op returning FLINT_OK.
+ * Errors: FLINT_EINVAL (NULL, misaligned, T < 0 or T > max_tokens, layer out
+ * of range), FLINT_ESTATE (layer not loaded), FLINT_ECUDA (launch). */
+FLINT_API flint_status flint_moe_forward(flint_moe* h, int layer, const void* hidden_dev, int T,
+                               void* out_dev, void* stream);
+
+/* Decode stack with residual: for l = layer0 .. layer0+n_layers-1,
+ *   x <- bf16( x + MoE_layer_l(x) )   (the sum taken in fp32 of the bf16 values)
+ * applied in place to hidden_dev[T][d] (bfloat16, 16-byte aligned). Same
+ * errors as flint_moe_forward. Enqueues only kernels, so the whole call can be
+ * captured into a CUDA graph. */
+FLINT_API flint_status flint_moe_forward_stack(flint_moe* h, int layer0, int n_layers, void* hidden_dev,
+                                     int T, void* stream);
+
+/* Release the handle and all device memory it owns. NULL-safe. Synchronises
+ * the device first. */
+FLINT_API void flint_moe_destroy(flint_moe* h);
+
+/* Wait for the device, then read and clear the handle's device status word.
+ * FLINT_OK if no fault was recorded; FLINT_EDEVICE if a kernel recorded a
+ * data fault (non-finite router logit); FLINT_ETIMEOUT if a bounded wait gave
+ * up; FLINT_ECUDA if the device reports a CUDA error. */
+FLINT_API flint_status flint_moe_status(flint_moe* h);
+
+/* Static description of a status code. */
+FLINT_API const char* flint_moe_status_string(flint_status s);
+
+/* ---- per-step entry points (the same kernels the forward runs) ---------- */
+
+/* Router of one layer (steps a1-a2): logits_dev[T][n_experts] fp32,
+ * idx_dev[T][top_k] int32 (descending logit, ties to the lower index),
+ * w_dev[T][top_k] fp32 renormalised softmax weights. Any output pointer may
+ * be NULL. Errors as flint_moe_forward. */
+FLINT_API flint_status flint_moe_router(flint_moe* h, int layer, const void* hidden_dev, int T,
+                              float* logits_dev, int32_t* idx_dev, float* w_dev, void* stream);
+
+/* Top-k selection and renormalised softmax weights on given fp32 logits
+ * (step a2). logits_dev [T][E]; idx_dev [T][k]; w_dev [T][k] (may be NULL).
+ * Needs no handle. Constraints: E multiple of 32 in 32..256, 1 <= k <= 8,
+ * T >= 0. Non-finite logits rank below every finite one; they are not
+ * reported here. */
+FLINT_API flint_status flint_moe_topk(const float* logits_dev, int T, int E, int k, int32_t* idx_dev,
+                            float* w_dev, void* stream);
+
+/* Token -> expert bucketing (step a3) of idx_dev[T][k] (values in 0..E-1):
+ * offsets_dev[E+1] exclusive prefix sum of the per-expert counts,
+ * perm_dev[T*k] the flat assignments a = t*k + j ordered by (expert, a).
+ * Uses the handle's workspace (T <= max_tokens, k == top_k, E == n_experts).
+ * Out-of-range expert indices set the device status word (FLINT_EDEVICE) and
+ * are dropped. */
+FLINT_API flint_status flint_moe_bucket(flint_moe* h, const int32_t* idx_dev, int T, int32_t* offsets_dev,
+                              int32_t* perm_dev, void* stream);
+
+/* Dequantise one matrix of one expert of a loaded layer from the device
+ * layout back to fp32 in canonical order: out_dev[R][K] with [R, K] =
+ * [f, d] (mat 0 gate, 1 up) or [d, f] (mat 2 down); expert == n_experts is the
+ * shared expert. NVFP4 values are fp32(E2M1 * E4M3 * tensor scale), q4_1
+ * values fp32(d*q + m), each rounded once. Errors as flint_moe_forward. */
+FLINT_API flint_status flint_moe_dequant(flint_moe* h, int layer, int expert, int mat, float* out_dev,
+                               void* stream);
+
+/* Bytes of device memory the handle holds (weights + workspace). */
+FLINT_API size_t flint_moe_device_bytes(const flint_moe* h);
+
+/* ---- measurement hooks ---------------------------------------------------- */
+
+/* Number of kernels this handle has launched so far (all entry points). */
+FLINT_API uint64_t flint_moe_launch_count(const flint_moe* h);
+
+/* Start recording CUDA events on the caller's stream around the three phases
+ * of the next max_forwards single-layer forwards (phase 0: router, top-k and
+ * bucketing; 1: expert gate/up; 2: expert down projection and combine).
+ * Allocates the events; FLINT_EINVAL if max_forwards < 1. */
+FLINT_API flint_status flint_moe_profile_begin(flint_moe* h, int max_forwards);
+
+/* Wait for the recorded forwards, write the summed duration of each phase in
+ * milliseconds to phase_ms[0..2] and the number of recorded forwards to
+ * *n_forwards, then free the events and stop recording. */
+FLINT_API flint_status flint_moe_profile_end(flint_moe* h, float* phase_ms, int* n_forwards);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLINT_MOE_H */

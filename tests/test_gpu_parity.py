@@ -1,0 +1,336 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact: dequantised weights, top-k indices on given logits, bucketing.
+Tolerances: router logits 1e-4 relative; layer outputs relative L2 <= 5e-3
+and max abs <= 3e-2 x RMS of the oracle output.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+from bit_quantized_expert_softmax_b300 import synth
+from oracle import formats as F
+from oracle import moe as M
+from tests.gpu_util import assert_logits_close, assert_out_close, compare_routing
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def fm():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from bit_quantized_expert_softmax_b300 import build
+    build.build()
+    from bit_quantized_expert_softmax_b300 import flint_moe
+    flint_moe.lib()
+    return flint_moe
+
+
+def _cfg(n, **kw):
+    return dataclasses.replace(synth.CONFIGS[n], **kw)
+
+
+def _moe(fm, cfg, layers, max_tokens):
+    m = fm.MoE(cfg, max_tokens=max_tokens, n_layers=len(layers))
+    for i, L in enumerate(layers):
+        m.load(i, L)
+    return m
+
+
+def _forward(fm, m, bits, layer=0):
+    x = fm.hidden_to_device(bits)
+    out = m.forward(x, layer)
+    torch.cuda.synchronize()
+    assert fm.flint_moe_status(m.h) == fm.FLINT_OK
+    return fm.hidden_to_host(out)
+
+
+# ---------------------------------------------------------------------------
+# a4: dequantisation, bit for bit
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("wfmt", [synth.WFMT_NVFP4, synth.WFMT_Q4_1])
+def test_dequant_bit_exact(fm, wfmt):
+    cfg = _cfg(1, wfmt=wfmt)
+    L = synth.make_layer(cfg)
+    if wfmt == synth.WFMT_NVFP4:
+        # edge scale bytes: zero, smallest subnormal, smallest normal, largest
+        L.scales[3, 0, :4] = [0x00, 0x01, 0x08, 0x7E]
+        L.codes[3, 0, :8] = [0x88, 0x80, 0x08, 0xF7, 0x7F, 0x12, 0x9A, 0xFF]   # incl. -0 codes
+    m = _moe(fm, cfg, [L], 4)
+    for e in [0, 3, 131, cfg.n_experts - 1, cfg.n_experts]:
+        for mat in range(3):
+            R, K = (cfg.f, cfg.d) if mat < 2 else (cfg.d, cfg.f)
+            out = torch.empty((R, K), dtype=torch.float32, device="cuda")
+            fm.flint_moe_dequant(m.h, 0, e, mat, out)
+            torch.cuda.synchronize()
+            got = out.cpu().numpy()
+            ref = M.dequant_matrix(L, e, mat).astype(np.float32)
+            assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), (e, mat)
+    m.close()
+
+
+def test_dequant_bit_exact_flint_shape(fm):
+    cfg = _cfg(2)
+    L = synth.make_layer(cfg)
+    m = _moe(fm, cfg, [L], 1)
+    for e, mat in [(0, 0), (100, 1), (255, 2), (256, 2)]:
+        R, K = (cfg.f, cfg.d) if mat < 2 else (cfg.d, cfg.f)
+        out = torch.empty((R, K), dtype=torch.float32, device="cuda")
+        fm.flint_moe_dequant(m.h, 0, e, mat, out)
+        torch.cuda.synchronize()
+        ref = M.dequant_matrix(L, e, mat).astype(np.float32)
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32)), (e, mat)
+    m.close()
+
+
+# ---------------------------------------------------------------------------
+# a2: top-k on given logits, a3: bucketing
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 256, 6), (300, 256, 6), (33, 32, 8), (7, 64, 1)])
+def test_topk_bit_exact_on_given_logits(fm, T, E, k):
+    rng = np.random.default_rng(T * 1000 + E + k)
+    L = rng.standard_normal((T, E)).astype(np.float32)
+    if T >= 3:
+        L[0, [5, 9, 30]] = 4.0                 # tie at the top
+        L[1, :] = 0.25                         # all equal -> lowest indices
+        L[2, [E - 1, E - 2]] = L[2].max() + 1  # tie between the last two experts
+    lg = torch.from_numpy(L).cuda()
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    fm.flint_moe_topk(lg, T, E, k, idx, w)
+    torch.cuda.synchronize()
+    ref = M.select_topk(L, k)
+    assert np.array_equal(idx.cpu().numpy(), ref)
+    wref = M.route_weights(L.astype(np.float64), ref)
+    assert np.max(np.abs(w.cpu().numpy() - wref)) <= 2e-6
+
+
+@pytest.mark.parametrize("T", [1, 5, 64, 65, 683, 8192])
+def test_bucket_bit_exact(fm, T):
+    cfg = _cfg(5)
+    rng = np.random.default_rng(T)
+    # Zipf-like skew over experts, k distinct experts per token
+    p = 1.0 / np.arange(1, cfg.n_experts + 1) ** 1.1
+    p /= p.sum()
+    sel = np.stack([rng.choice(cfg.n_experts, size=cfg.top_k, replace=False, p=p) for _ in range(T)])
+    sel = sel.astype(np.int32)
+    L = synth.make_layer(_cfg(1))   # any loaded layer; bucketing uses only the workspace
+    m = fm.MoE(dataclasses.replace(_cfg(1), tokens=T), max_tokens=T)
+    m.load(0, L)
+    idx = torch.from_numpy(sel).cuda()
+    offs = torch.empty(cfg.n_experts + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * cfg.top_k, dtype=torch.int32, device="cuda")
+    fm.flint_moe_bucket(m.h, idx, T, offs, perm)
+    torch.cuda.synchronize()
+    ref = M.bucket(sel, cfg.n_experts)
+    assert np.array_equal(offs.cpu().numpy(), ref.offsets)
+    assert np.array_equal(perm.cpu().numpy(), ref.perm)
+    m.close()
+
+
+# ---------------------------------------------------------------------------
+# a1-a2: router of a loaded layer (small-T fused path and large-T path)
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("n,T", [(1, 4), (1, 64), (1, 200), (3, 64), (5, 8192)])
+def test_router_parity(fm, n, T):
+    cfg = _cfg(n, tokens=T)
+    L = synth.make_layer(cfg)
+    bits = synth.make_hidden(cfg)
+    m = _moe(fm, cfg, [L], T)
+    x = fm.hidden_to_device(bits)
+    logits = torch.empty((T, cfg.n_experts), dtype=torch.float32, device="cuda")
+    idx = torch.empty((T, cfg.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, cfg.top_k), dtype=torch.float32, device="cuda")
+    fm.flint_moe_router(m.h, 0, x, T, logits, idx, w)
+    torch.cuda.synchronize()
+    assert fm.flint_moe_status(m.h) == fm.FLINT_OK
+    ref_L = M.router_logits(F.bf16_array(bits), L.router, L.router_bias)
+    assert_logits_close(logits.cpu().numpy(), ref_L)
+    ref_sel = M.select_topk(ref_L.astype(np.float32), cfg.top_k)
+    got_idx = idx.cpu().numpy()
+    same = compare_routing(got_idx, ref_sel, ref_L, cfg.top_k)
+    wref = M.route_weights(ref_L, ref_sel)
+    assert np.max(np.abs(w.cpu().numpy()[same] - wref[same])) <= 1e-5
+    m.close()
+
+
+# ---------------------------------------------------------------------------
+# the layer
+# ---------------------------------------------------------------------------
+
+
+def _layer_parity(fm, cfg, T, sample=None, mutate=None):
+    L = synth.make_layer(cfg)
+    if mutate:
+        mutate(L)
+    bits = synth.make_hidden(cfg, tokens=T)
+    m = _moe(fm, cfg, [L], T)
+    got = _forward(fm, m, bits)
+    idx = torch.empty((T, cfg.top_k), dtype=torch.int32, device="cuda")
+    fm.flint_moe_router(m.h, 0, fm.hidden_to_device(bits), T, None, idx, None)
+    torch.cuda.synchronize()
+    m.close()
+    rows = np.arange(T) if sample is None else np.asarray(sample)
+    ref = M.moe_layer(bits[rows], L)
+    # the GPU's routing must agree with the oracle's (near ties excepted);
+    # tokens routed differently at a near tie are left out of the comparison
+    same = compare_routing(idx.cpu().numpy()[rows], ref.sel, ref.logits, cfg.top_k)
+    assert same.mean() >= 0.95
+    ref.out = ref.out[same]
+    return got[rows][same], ref
+
+
+@pytest.mark.parametrize("T", [1, 3, 4, 17, 64, 65, 130])
+def test_layer_tiny_nvfp4(fm, T):
+    cfg = _cfg(1)
+    got, ref = _layer_parity(fm, cfg, T)
+    assert_out_close(got, ref.out, f"tiny nvfp4 T={T}")
+
+
+@pytest.mark.parametrize("T", [1, 5, 64, 70])
+def test_layer_tiny_q4_1(fm, T):
+    cfg = _cfg(1, wfmt=synth.WFMT_Q4_1, bias="zipf")
+    got, ref = _layer_parity(fm, cfg, T)
+    assert_out_close(got, ref.out, f"tiny q4_1 T={T}")
+
+
+def test_layer_flint_decode_T1(fm):
+    cfg = _cfg(2)
+    got, ref = _layer_parity(fm, cfg, 1)
+    assert_out_close(got, ref.out, "decode T=1")
+
+
+def test_layer_flint_batched_q4_1_T64(fm):
+    cfg = _cfg(3)
+    got, ref = _layer_parity(fm, cfg, 64)
+    assert_out_close(got, ref.out, "batched decode T=64 q4_1")
+
+
+def test_layer_flint_prefill_T8192_sampled(fm):
+    cfg = _cfg(5)
+    rng = np.random.default_rng(0)
+    sample = np.unique(np.concatenate([[0, 1, 8191], rng.choice(8192, 61, replace=False)]))
+    got, ref = _layer_parity(fm, cfg, 8192, sample=sample)
+    assert_out_close(got, ref.out, "prefill T=8192 (sampled tokens)")
+
+
+def test_stack_47_layers_T1(fm):
+    cfg = _cfg(4)
+    bits = synth.make_hidden(cfg)
+    m = fm.MoE(cfg, max_tokens=1, n_layers=cfg.n_layers)
+    ref_bits = bits.copy()
+    min_gap = np.inf
+    for i in range(cfg.n_layers):          # one layer in host memory at a time
+        L = synth.make_layer(cfg, layer=i)
+        m.load(i, L)
+        r = M.moe_layer(ref_bits, L)
+        s = np.sort(r.logits[0])[::-1]
+        min_gap = min(min_gap, (s[cfg.top_k - 1] - s[cfg.top_k]) / np.sqrt(np.mean(r.logits ** 2)))
+        ref_bits = F.bf16_bits(F.bf16_round(F.bf16_array(ref_bits) + r.out_bf16))
+    x = fm.hidden_to_device(bits)
+    m.forward_stack(x, 0, cfg.n_layers)
+    torch.cuda.synchronize()
+    assert fm.flint_moe_status(m.h) == fm.FLINT_OK
+    got = fm.hidden_to_host(x)
+    m.close()
+    # a routing near tie in any layer would make the two stacks diverge legitimately
+    assert min_gap > 1e-3, f"seed has a routing near tie (relative gap {min_gap:.2e})"
+    assert_out_close(got, F.bf16_array(ref_bits), "47-layer stack")
+
+
+# ---------------------------------------------------------------------------
+# edge cases and properties
+# ---------------------------------------------------------------------------
+
+
+def test_zero_routed_experts_give_shared_expert(fm):
+    cfg = _cfg(1)
+
+    def zero(L):
+        L.codes[: cfg.n_experts] = 0
+
+    got, ref = _layer_parity(fm, cfg, 4, mutate=zero)
+    assert_out_close(got, ref.out, "shared only")
+
+
+def test_forward_is_deterministic_and_stack_matches_forwards(fm):
+    cfg = _cfg(1, n_layers=2)
+    layers = [synth.make_layer(cfg, layer=i) for i in range(2)]
+    bits = synth.make_hidden(cfg, tokens=5)
+    m = _moe(fm, cfg, layers, 5)
+    x = fm.hidden_to_device(bits)
+    o1 = m.forward(x, 0).clone()
+    o2 = m.forward(x, 0).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    x1 = (x.float() + o1.float()).to(torch.bfloat16)
+    o3 = m.forward(x1, 1)
+    x2 = (x1.float() + o3.float()).to(torch.bfloat16)
+    xs = x.clone()
+    m.forward_stack(xs, 0, 2)
+    torch.cuda.synchronize()
+    assert torch.equal(xs.view(torch.int16), x2.view(torch.int16))
+    m.close()
+
+
+def test_boundary_errors(fm):
+    cfg = _cfg(1)
+    m = fm.MoE(cfg, max_tokens=8, n_layers=2)
+    x = torch.zeros((8, cfg.d), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(x)
+    with pytest.raises(fm.FlintError) as ei:          # layer not loaded
+        fm.flint_moe_forward(m.h, 0, x, 8, out)
+    assert ei.value.code == fm.FLINT_ESTATE
+    L = synth.make_layer(cfg)
+    m.load(0, L)
+    fm.flint_moe_forward(m.h, 0, x, 0, out)           # T == 0: no-op
+    for T in (-1, 9):
+        with pytest.raises(fm.FlintError) as ei:
+            fm.flint_moe_forward(m.h, 0, x, T, out)
+        assert ei.value.code == fm.FLINT_EINVAL
+    with pytest.raises(fm.FlintError) as ei:          # layer out of range
+        fm.flint_moe_forward(m.h, 2, x, 1, out)
+    assert ei.value.code == fm.FLINT_EINVAL
+    flat = torch.zeros(8 * cfg.d + 8, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fm.FlintError) as ei:          # misaligned hidden
+        fm.flint_moe_forward(m.h, 0, flat[1:], 1, out)
+    assert ei.value.code == fm.FLINT_EINVAL
+    with pytest.raises(fm.FlintError) as ei:          # in and out overlap
+        fm.flint_moe_forward(m.h, 0, x, 2, x[1:])
+    assert ei.value.code == fm.FLINT_EINVAL
+    bad = synth.make_layer(cfg)
+    bad.scales[0, 0, 5] = 0x7F                         # NaN block scale
+    with pytest.raises(fm.FlintError) as ei:
+        m.load(1, bad)
+    assert ei.value.code == fm.FLINT_EINVAL
+    bad.scales[0, 0, 5] = 0xB8                         # negative block scale
+    with pytest.raises(fm.FlintError) as ei:
+        m.load(1, bad)
+    assert ei.value.code == fm.FLINT_EINVAL
+    assert fm.flint_moe_status(m.h) == fm.FLINT_OK
+    m.close()
+
+
+def test_non_finite_hidden_sets_status(fm):
+    cfg = _cfg(1)
+    L = synth.make_layer(cfg)
+    m = _moe(fm, cfg, [L], 4)
+    bits = synth.make_hidden(cfg, tokens=4)
+    bits[2, 7] = 0x7FC0                              # bf16 NaN
+    x = fm.hidden_to_device(bits)
+    m.forward(x, 0)
+    assert fm.flint_moe_status(m.h) == fm.FLINT_EDEVICE
+    assert fm.flint_moe_status(m.h) == fm.FLINT_OK   # read clears
+    got = _forward(fm, m, synth.make_hidden(cfg, tokens=4))   # handle still usable
+    assert np.all(np.isfinite(F.bf16_array(got)))
+    m.close()
