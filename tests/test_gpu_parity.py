@@ -243,9 +243,14 @@ def test_stack_47_layers_T1(fm):
     assert fm.flint_moe_status(m.h) == fm.FLINT_OK
     got = fm.hidden_to_host(x)
     m.close()
-    # a routing near tie in any layer would make the two stacks diverge legitimately
-    assert min_gap > 1e-3, f"seed has a routing near tie (relative gap {min_gap:.2e})"
-    assert_out_close(got, F.bf16_array(ref_bits), "47-layer stack")
+    # The smallest gap between the 6th and 7th logit over all layers (relative
+    # to the logit RMS) is reported with any mismatch: one-ulp bf16 differences
+    # in the residual stream move logits by ~1e-4, so a routing near tie below
+    # that would make the two stacks diverge legitimately.
+    try:
+        assert_out_close(got, F.bf16_array(ref_bits), "47-layer stack")
+    except AssertionError as e:
+        raise AssertionError(f"{e} (smallest relative routing gap over the stack {min_gap:.2e})")
 
 
 # ---------------------------------------------------------------------------
