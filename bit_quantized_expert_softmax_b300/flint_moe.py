@@ -196,6 +196,15 @@ def flint_moe_profile_end(h: int):
     return [float(v) for v in ms], int(n.value)
 
 
+def flint_moe_bucket_noalloc(idx, T: int, k: int, E: int, offsets, perm, stream=None) -> None:
+    """Bucketing without a handle and without allocating (static scratch in the
+    library; see include/flint_moe.h for its limits and sharing rules)."""
+    fn = lib().flint_moe_bucket_noalloc
+    fn.restype = _I
+    fn.argtypes = [_P, _I, _I, _I, _P, _P, _P]
+    _check(fn(_ptr(idx), T, k, E, _ptr(offsets), _ptr(perm), _stream(stream)), "flint_moe_bucket_noalloc")
+
+
 # ---------------------------------------------------------------------------
 # convenience object
 # ---------------------------------------------------------------------------

@@ -182,6 +182,27 @@ FLINT_API flint_status flint_moe_dequant(flint_moe* h, int layer, int expert, in
 /* Bytes of device memory the handle holds (weights + workspace). */
 FLINT_API size_t flint_moe_device_bytes(const flint_moe* h);
 
+/* ---- bucketing for callers that cannot allocate ---------------------------
+ * The Flint blog has no counterpart to this entry point: it serves callers,
+ * not the method. It computes what flint_moe_bucket computes, offsets_dev[E+1]
+ * and perm_dev[T*k] from idx_dev[T][k] (experts 0..E-1), without a handle and
+ * without allocating anything. flint_moe_create allocates a workspace with
+ * cudaMalloc; callers that cannot allocate where they need this step (a step
+ * being recorded under CUDA stream capture, a process whose device memory is
+ * held by another allocator, a runtime that forbids the CUDA allocator) use
+ * this instead. Its scratch is one static device array of 256 KiB inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits. Runs on the current device.
+ * Limits: 1 <= E <= 256, 1 <= k <= 8, T*k <= 524288; larger sizes return
+ * FLINT_EINVAL and enqueue nothing. T == 0 is a no-op.
+ * The first call on a device looks up the array's device address (once per
+ * device, under a lock): make that first call before any stream capture.
+ * All calls share the array, so calls that overlap on the GPU race and
+ * corrupt each other's results. Expert indices outside 0..E-1 are dropped
+ * (this entry point has no status word to report them). */
+FLINT_API flint_status flint_moe_bucket_noalloc(const int32_t* idx_dev, int T, int k, int E,
+                                                int32_t* offsets_dev, int32_t* perm_dev, void* stream);
+
 /* ---- measurement hooks ---------------------------------------------------- */
 
 /* Number of kernels this handle has launched so far (all entry points). */
