@@ -1,5 +1,6 @@
 // C ABI of the layer: handle, weight loading, forward orchestration.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <new>
@@ -23,6 +24,8 @@ struct flint_moe {
     size_t weight_bytes = 0;
     cudaStream_t load_stream = nullptr;
     uint64_t launches = 0;
+    int n_sms = 0;
+    bool fused = true;           // single-launch decode for T <= kFusedMaxT
     // phase events of profiled forwards: 4 per forward
     std::vector<cudaEvent_t> prof_events;
     int prof_max = 0, prof_n = 0;
@@ -111,6 +114,7 @@ Workspace carve(const Shape& s, char* base, size_t* total) {
     w.yw = cv.take<float>(P * s.d);
     w.chunk_hist = cv.take<int>(n_chunks * s.E);
     w.counters = cv.take<uint32_t>(flint::kCounters);
+    w.gbar = cv.take<uint32_t>(64);
     w.status = cv.take<uint32_t>(1);
     *total = align_up(cv.off, 256);
     return w;
@@ -148,6 +152,18 @@ cudaError_t run_layer(flint_moe* h, int layer, const __nv_bfloat16* x, int T, __
                       const __nv_bfloat16* residual, cudaStream_t st) {
     const LayerDev& L = h->layers[layer];
     int n = 0;
+    int n_slots = 0, offs[8];
+    if (h->fused && flint::fused_smem_bytes(h->s, T, h->n_sms, &n_slots, offs) != 0) {
+        flint::FusedScratch fs{h->ws.logits, h->ws.hf, h->ws.gbar, h->ws.status};
+        prof_record(h, 0, st);
+        cudaError_t e = flint::launch_decode_fused(h->s, L, x, T, out, residual, fs, h->n_sms, st);
+        prof_record(h, 1, st);
+        prof_record(h, 2, st);
+        prof_record(h, 3, st);
+        if (h->prof_n < h->prof_max) ++h->prof_n;
+        h->launches += 1;
+        return e;
+    }
     prof_record(h, 0, st);
     cudaError_t e = flint::launch_router(h->s, L, x, T, h->ws, st, &n);
     prof_record(h, 1, st);
@@ -192,6 +208,15 @@ flint_status flint_moe_create(const flint_moe_config* cfg, flint_moe** out) {
     h->s = Shape{cfg->d, cfg->f, cfg->n_experts, cfg->top_k, cfg->n_shared, cfg->wfmt, cfg->max_tokens};
     h->n_layers = cfg->n_layers;
     h->device = cfg->device;
+    if (cudaDeviceGetAttribute(&h->n_sms, cudaDevAttrMultiProcessorCount, cfg->device) != cudaSuccess) {
+        delete h;
+        return FLINT_ECUDA;
+    }
+    {
+        const char* env = getenv("FLINT_MOE_FUSED_DECODE");
+        if (env != nullptr && env[0] == '0') h->fused = false;
+    }
+    if (h->fused && flint::prepare_decode_fused() != cudaSuccess) h->fused = false;
     h->layers.resize(cfg->n_layers);
     size_t total = 0;
     carve(h->s, nullptr, &total);
@@ -428,6 +453,16 @@ size_t flint_moe_device_bytes(const flint_moe* h) {
 }
 
 uint64_t flint_moe_launch_count(const flint_moe* h) { return h ? h->launches : 0; }
+
+int flint_moe_forward_launches(const flint_moe* h, int T) {
+    if (h == nullptr || T < 0 || T > h->s.max_tokens) return -1;
+    if (T == 0) return 0;
+    int n_slots = 0, offs[8];
+    if (h->fused && flint::fused_smem_bytes(h->s, T, h->n_sms, &n_slots, offs) != 0) return 1;
+    const int router = T <= flint::kSmallT ? 1 : 2 + 3;
+    const int down = T <= flint::kSmallT ? 1 : 2;
+    return router + 1 + down;
+}
 
 flint_status flint_moe_profile_begin(flint_moe* h, int max_forwards) {
     if (h == nullptr || max_forwards < 1 || max_forwards > (1 << 22)) return FLINT_EINVAL;

@@ -149,3 +149,101 @@ __device__ __forceinline__ float f16_range_mult(float amax) {
 }
 
 }  // namespace flint
+
+namespace flint {
+
+// ---------------------------------------------------------------------------
+// Shared-memory barriers and bulk (TMA, 1-D) copies
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (bulk copy) proxy.
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) writes to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Global -> shared bulk copy completing on an mbarrier. dst, src 16-byte
+// aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(phase)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for an mbarrier phase. Returns false (and records a timeout in
+// the status word) if the phase does not complete within the limit.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, uint32_t* status) {
+    for (uint32_t it = 0; it < (1u << 22); ++it) {
+        if (mbar_try_wait(bar, phase)) return true;
+    }
+    if (status) atomicOr(status, kStatusTimeout);
+    return false;
+}
+
+// Grid-wide barrier for a kernel whose CTAs are all resident (cooperative
+// launch). count/gen live in global memory; count must be 0 on entry to the
+// first use and is returned to 0 by the last arriver. Spins are bounded: on
+// timeout the status word gets kStatusTimeout and false is returned.
+__device__ __forceinline__ bool grid_barrier(uint32_t* count, uint32_t* gen, uint32_t n_ctas,
+                                             uint32_t* status) {
+    __shared__ uint32_t s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t ok = 1;
+        const uint32_t g = *((volatile uint32_t*)gen);
+        __threadfence();
+        const uint32_t arrived = atomicAdd(count, 1u);
+        if (arrived == n_ctas - 1) {
+            *((volatile uint32_t*)count) = 0u;
+            __threadfence();
+            atomicAdd(gen, 1u);
+        } else {
+            uint32_t it = 0;
+            while (*((volatile uint32_t*)gen) == g) {
+                if (++it > (1u << 24)) {
+                    atomicOr(status, kStatusTimeout);
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+}  // namespace flint

@@ -1,0 +1,562 @@
+// Single-launch decode of one MoE layer for T <= 2 tokens.
+//
+// Decode streams the selected experts' weights once and does little
+// arithmetic on them ("Recursive Flint 40B-A2.5B", section "The architecture
+// is an argument about memory bandwidth"), so the step is bound by HBM and by
+// the latency of its three dependent phases. One persistent kernel, one CTA
+// per SM, runs them with two grid barriers instead of separate launches, and
+// every weight slab a CTA needs is requested with 1-D bulk copies (TMA) into
+// shared memory as soon as its address is known:
+//
+//   P0  router logits (each CTA a slice of W_r) and the shared expert's
+//       gate/up (routing-independent); the shared expert's down slab is
+//       prefetched for P2.
+//   --- grid barrier ---
+//   P1  every CTA takes the top-6 of the logits itself (no broadcast needed),
+//       prefetches the routed experts' down slabs for its P2 rows, then runs
+//       its routed gate/up units (16 rows of one expert, full K) from bulk-
+//       copied slabs.
+//   --- grid barrier ---
+//   P2  down projection of 16 output rows for every active expert, weighted
+//       combine (shared first, then slots 0..k-1) and bf16 output.
+//
+// Arithmetic matches the multi-kernel path: weights decoded to fp16 in
+// registers, activations fp16 with a power-of-two scale per token (x) or per
+// (token, slot) row (h), mma.sync m16n8k16 with fp32 accumulation.
+#include "kernels.cuh"
+#include "tiles.cuh"
+#include "topk.cuh"
+
+namespace flint {
+
+namespace {
+
+constexpr int kFThreads = 512;   // 16 warps
+constexpr size_t kMaxSmemOptin = 232448;          // 227 KiB of shared memory per CTA (static + dynamic)
+constexpr size_t kFusedDynSmemMax = kMaxSmemOptin - 1024;   // dynamic part; the kernel's static part is < 1 KiB
+constexpr int kFWarps = kFThreads / 32;
+
+struct FusedArgs {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    const float* tscale;
+    const float* router;
+    const float* bias;
+    size_t cpm, spm;            // bytes of codes / scales per matrix
+    const __nv_bfloat16* x;
+    __nv_bfloat16* out;
+    const __nv_bfloat16* residual;
+    int T, d, f, E, k;
+    float* logits;              // [T][E]
+    float* h;                   // [T][k+1][f] fp32, slot k = shared expert
+    uint32_t* bar_count;
+    uint32_t* bar_gen;
+    uint32_t* status;
+    int n_slots;                // gate/up unit slots in shared memory
+    // shared-memory layout (byte offsets)
+    int off_slots, unit_bytes, off_down, down_bytes, off_acc, off_x16, off_h16, off_misc;
+};
+
+struct Pair {
+    int t, j;   // token, slot (j == k: shared expert)
+};
+
+template <int WFMT>
+__device__ __forceinline__ TileScales<WFMT> lds_scales(const uint8_t* base_g, const uint8_t* base_h, int g) {
+    TileScales<WFMT> s;
+    if constexpr (WFMT == 0) {
+        s.g = *reinterpret_cast<const uint2*>(base_g + g * 8);
+        s.h = *reinterpret_cast<const uint2*>(base_h + g * 8);
+    } else {
+        s.g = *reinterpret_cast<const uint4*>(base_g + g * 16);
+        s.h = *reinterpret_cast<const uint4*>(base_h + g * 16);
+    }
+    return s;
+}
+
+__device__ __forceinline__ void lds_b16(const __half* p, uint32_t (&b)[16]) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint4 v = q[i];
+        b[4 * i + 0] = v.x;
+        b[4 * i + 1] = v.y;
+        b[4 * i + 2] = v.z;
+        b[4 * i + 3] = v.w;
+    }
+}
+
+// Issue the four bulk copies of one gate/up unit (16 rows of gate and up of
+// expert e, full K) into slot memory `dst`, completing on `bar`.
+template <int WFMT>
+__device__ void issue_unit(const FusedArgs& a, int e, int r16, uint8_t* dst, uint64_t* bar) {
+    const int KT = a.d >> 7;
+    const int S = WFMT == 0 ? 64 : 128;
+    const uint32_t cbytes = 2u * KT * 512u, sbytes = 2u * KT * S;
+    mbar_arrive_expect_tx(bar, 2 * (cbytes + sbytes));
+    const size_t coff = (size_t)(2 * r16) * KT * 512, soff = (size_t)(2 * r16) * KT * S;
+    for (int m = 0; m < 2; ++m) {
+        bulk_g2s(dst + m * cbytes, a.codes + ((size_t)e * 3 + m) * a.cpm + coff, cbytes, bar);
+        bulk_g2s(dst + 2 * cbytes + m * sbytes, a.scales + ((size_t)e * 3 + m) * a.spm + soff, sbytes, bar);
+    }
+}
+
+// Issue the two bulk copies of the down slab (16 output rows, full f) of
+// expert e for output tile r16.
+template <int WFMT>
+__device__ void issue_down(const FusedArgs& a, int e, int r16, uint8_t* dst, uint64_t* bar) {
+    const int KT = a.f >> 7;
+    const int S = WFMT == 0 ? 64 : 128;
+    const uint32_t cbytes = 2u * KT * 512u, sbytes = 2u * KT * S;
+    bulk_g2s(dst, a.codes + ((size_t)e * 3 + 2) * a.cpm + (size_t)(2 * r16) * KT * 512, cbytes, bar);
+    bulk_g2s(dst + cbytes, a.scales + ((size_t)e * 3 + 2) * a.spm + (size_t)(2 * r16) * KT * S, sbytes, bar);
+}
+
+// Gate/up of one unit held in shared memory for `np` (token, slot) pairs;
+// writes h = silu(g) * u (fp32) for the unit's 16 rows.
+template <int WFMT>
+__device__ void gateup_unit(const FusedArgs& a, const uint8_t* slab, int e, int r16, const Pair* pairs, int np,
+                            const __half* x16s, const float* xinv, float* red) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int KT = a.d >> 7;
+    const int S = WFMT == 0 ? 64 : 128;
+    const uint8_t* cg = slab;
+    const uint8_t* cu = slab + 2 * KT * 512;
+    const uint8_t* sg = slab + 4 * KT * 512;
+    const uint8_t* su = sg + 2 * KT * S;
+    float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
+    const int tb = (g < np) ? pairs[g].t : -1;
+    for (int kt = warp; kt < KT; kt += kFWarps) {
+        const uint4 wgg = *reinterpret_cast<const uint4*>(cg + kt * 512 + lane * 16);
+        const uint4 wgh = *reinterpret_cast<const uint4*>(cg + (KT + kt) * 512 + lane * 16);
+        const uint4 wug = *reinterpret_cast<const uint4*>(cu + kt * 512 + lane * 16);
+        const uint4 wuh = *reinterpret_cast<const uint4*>(cu + (KT + kt) * 512 + lane * 16);
+        const TileScales<WFMT> scg = lds_scales<WFMT>(sg + kt * S, sg + (KT + kt) * S, g);
+        const TileScales<WFMT> scu = lds_scales<WFMT>(su + kt * S, su + (KT + kt) * S, g);
+        uint32_t b[16];
+        if (tb >= 0) {
+            lds_b16(x16s + (size_t)tb * a.d + kt * 128 + c * 32, b);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) b[i] = 0u;
+        }
+        uint32_t fa[8][4];
+        decode_tile<WFMT>(wgg, wgh, scg, fa);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) mma_16816(accg, fa[s][0], fa[s][1], fa[s][2], fa[s][3], b[2 * s], b[2 * s + 1]);
+        decode_tile<WFMT>(wug, wuh, scu, fa);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) mma_16816(accu, fa[s][0], fa[s][1], fa[s][2], fa[s][3], b[2 * s], b[2 * s + 1]);
+    }
+    // cross-warp reduction of the K partials: red[warp][2][32][4]
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        red[((warp * 2 + 0) * 32 + lane) * 4 + j] = accg[j];
+        red[((warp * 2 + 1) * 32 + lane) * 4 + j] = accu[j];
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const float tsg = a.tscale[e * 3 + 0], tsu = a.tscale[e * 3 + 1];
+        const int nw = KT < kFWarps ? KT : kFWarps;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = 2 * c + (j & 1);
+            if (n >= np) continue;
+            float sgv = 0.f, suv = 0.f;
+            for (int w = 0; w < nw; ++w) {
+                sgv += red[((w * 2 + 0) * 32 + lane) * 4 + j];
+                suv += red[((w * 2 + 1) * 32 + lane) * 4 + j];
+            }
+            const Pair p = pairs[n];
+            const float gv = sgv * tsg * xinv[p.t];
+            const float uv = suv * tsu * xinv[p.t];
+            const float hv = gv / (1.0f + expf(-gv)) * uv;
+            const int row = r16 * 16 + g + ((j >> 1) << 3);
+            a.h[((size_t)p.t * (a.k + 1) + p.j) * a.f + row] = hv;
+        }
+    }
+    __syncthreads();
+}
+
+template <int WFMT>
+__global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int G = gridDim.x, b = blockIdx.x;
+    const int T = a.T, d = a.d, f = a.f, E = a.E, k = a.k;
+    const int KTf = f >> 7;
+    const int units_per_expert = f >> 4;
+    const int down_tiles = d >> 4;
+    const int down_tile = b - (G - down_tiles);          // the last d/16 CTAs own output tiles
+    const int shared_unit = G - 1 - b;                   // the last f/16 CTAs do the shared gate/up
+
+    uint8_t* slots = smem + a.off_slots;
+    uint8_t* down = smem + a.off_down;
+    float* acc = reinterpret_cast<float*>(smem + a.off_acc);
+    __half* x16s = reinterpret_cast<__half*>(smem + a.off_x16);
+    __half* h16s = reinterpret_cast<__half*>(smem + a.off_h16);
+    uint8_t* misc = smem + a.off_misc;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc);              // [n_slots + 3]
+    uint64_t* bar_router = bars + a.n_slots;
+    uint64_t* bar_dshared = bars + a.n_slots + 1;
+    uint64_t* bar_drouted = bars + a.n_slots + 2;
+    float* xinv = reinterpret_cast<float*>(misc + 128);              // [2]
+    float* hinv = xinv + 4;                                          // [2*(k+1)] <= 18
+    float* rpart = hinv + 20;                                        // [16][2]
+    float* lg = rpart + 32;                                          // [2][256]
+    int* sel = reinterpret_cast<int*>(lg + 2 * 256);                 // [2][8]
+    float* wsel = reinterpret_cast<float*>(sel + 16);                // [2][8]
+    int* act = reinterpret_cast<int*>(wsel + 16);                    // [17] active experts (routed)
+    int* act_np = act + 17;                                          // [17]
+    Pair* act_pairs = reinterpret_cast<Pair*>(act_np + 17);          // [17][2]
+    int* nact = reinterpret_cast<int*>(act_pairs + 34);              // [1]
+    Pair* shared_pairs = reinterpret_cast<Pair*>(nact + 2);          // [2]
+
+    bool ok = true;
+    uint32_t slot_phase = 0;   // bit s: parity of slot s's next completion
+    // CTA-uniform bounded wait: every thread waits, and the CTA proceeds only
+    // if all of them saw the phase complete.
+    auto wait_all = [&](uint64_t* bar, uint32_t ph) {
+        const bool w = ok ? mbar_wait_bounded(bar, ph, a.status) : false;
+        ok = __syncthreads_and(w ? 1 : 0) != 0;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.n_slots + 3; ++i) mbar_init(bars + i, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------------ P0
+    // router slice: experts b, b+G, ... (at most 2 rows held in slot 0)
+    int n_re = 0;
+    for (int e = b; e < E; e += G) ++n_re;
+    if (threadIdx.x == 0) {
+        if (n_re > 0) {
+            mbar_arrive_expect_tx(bar_router, (uint32_t)(n_re * d * 4));
+            for (int i = 0; i < n_re; ++i)
+                bulk_g2s(slots + (size_t)i * d * 4, a.router + (size_t)(b + i * G) * d, d * 4, bar_router);
+        }
+        if (shared_unit >= 0 && shared_unit < units_per_expert)
+            issue_unit<WFMT>(a, E, shared_unit, slots + a.unit_bytes, bars + 1);
+        if (down_tile >= 0) {
+            mbar_arrive_expect_tx(bar_dshared, (uint32_t)a.down_bytes);
+            issue_down<WFMT>(a, E, down_tile, down, bar_dshared);
+        }
+    }
+    // stage the hidden states as fp16, scaled per token, fragment-permuted
+    for (int t = 0; t < T; ++t) {
+        float amax = 0.f;
+        for (int i = threadIdx.x; i < d; i += kFThreads)
+            amax = fmaxf(amax, fabsf(__bfloat162float(a.x[(size_t)t * d + i])));
+        amax = warp_max(amax);
+        if (lane == 0) rpart[warp] = amax;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float m = 0.f;
+            for (int w = 0; w < kFWarps; ++w) m = fmaxf(m, rpart[w]);
+            xinv[t] = m;
+        }
+        __syncthreads();
+        const float mult = f16_range_mult(xinv[t]);
+        for (int i = threadIdx.x; i < d; i += kFThreads)
+            x16s[(size_t)t * d + (i & ~127) + kperm_pos(i & 127)] =
+                __float2half_rn(__bfloat162float(a.x[(size_t)t * d + i]) * mult);
+        __syncthreads();
+        if (threadIdx.x == 0) xinv[t] = 1.0f / mult;
+        __syncthreads();
+    }
+    if (threadIdx.x < T) {
+        shared_pairs[threadIdx.x].t = threadIdx.x;
+        shared_pairs[threadIdx.x].j = k;
+    }
+    // router logits of this CTA's experts
+    if (n_re > 0) {
+        wait_all(bar_router, 0);
+        const int i = warp / 8, part = warp % 8;    // 8 warps per expert row
+        const int seg = d / 8;                      // elements per warp (multiple of 16)
+        float accv[2] = {0.f, 0.f};
+        if (ok && i < n_re) {
+            const float* wr = reinterpret_cast<const float*>(slots) + (size_t)i * d + part * seg;
+            for (int q = lane * 4; q < seg; q += 128) {
+                const float4 wv = *reinterpret_cast<const float4*>(wr + q);
+                for (int t = 0; t < T; ++t) {
+                    const __nv_bfloat16* xr = a.x + (size_t)t * d + part * seg + q;
+                    const uint2 raw = *reinterpret_cast<const uint2*>(xr);
+                    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+                    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+                    float s = accv[t];
+                    s = fmaf(wv.x, __low2float(p0), s);
+                    s = fmaf(wv.y, __high2float(p0), s);
+                    s = fmaf(wv.z, __low2float(p1), s);
+                    s = fmaf(wv.w, __high2float(p1), s);
+                    accv[t] = s;
+                }
+            }
+        }
+        for (int t = 0; t < T; ++t) {
+            const float s = warp_sum(accv[t]);
+            if (lane == 0) rpart[warp * 2 + t] = s;
+        }
+        __syncthreads();
+        if (threadIdx.x < n_re * T) {
+            const int ii = threadIdx.x / T, t = threadIdx.x % T;
+            float s = 0.f;
+            for (int p = 0; p < 8; ++p) s += rpart[(ii * 8 + p) * 2 + t];
+            const int e = b + ii * G;
+            a.logits[(size_t)t * E + e] = s + a.bias[e];
+        }
+    }
+    // shared expert gate/up
+    if (shared_unit >= 0 && shared_unit < units_per_expert) {
+        wait_all(bars + 1, 0);
+        slot_phase ^= 2u;
+        if (ok) gateup_unit<WFMT>(a, slots + a.unit_bytes, E, shared_unit, shared_pairs, T, x16s, xinv, acc);
+    }
+    if (!grid_barrier(a.bar_count, a.bar_gen, G, a.status)) ok = false;
+
+    // ------------------------------------------------------------------ P1
+    // top-k of every token, computed by every CTA from the logits in L2
+    for (int i = threadIdx.x; i < T * E; i += kFThreads) lg[i] = __ldcg(a.logits + i);
+    __syncthreads();
+    if (warp < T) topk_warp<false>(lg + warp * E, E, k, sel + warp * 8, wsel + warp * 8, b == 0 ? a.status : nullptr);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // distinct routed experts in ascending order with their (token, slot) pairs
+        int n = 0;
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < k; ++j) {
+                const int e = sel[t * 8 + j];
+                int pos = 0;
+                while (pos < n && act[pos] < e) ++pos;
+                if (pos < n && act[pos] == e) {
+                    act_pairs[pos * 2 + act_np[pos]] = Pair{t, j};
+                    ++act_np[pos];
+                    continue;
+                }
+                for (int q = n; q > pos; --q) {
+                    act[q] = act[q - 1];
+                    act_np[q] = act_np[q - 1];
+                    act_pairs[q * 2 + 0] = act_pairs[(q - 1) * 2 + 0];
+                    act_pairs[q * 2 + 1] = act_pairs[(q - 1) * 2 + 1];
+                }
+                act[pos] = e;
+                act_np[pos] = 1;
+                act_pairs[pos * 2] = Pair{t, j};
+                ++n;
+            }
+        *nact = n;
+    }
+    __syncthreads();
+    const int na = *nact;
+    const int n_units = na * units_per_expert;
+    // routed down slabs for this CTA's output tile (slab 0 is the shared expert)
+    if (threadIdx.x == 0 && down_tile >= 0 && na > 0) {
+        mbar_arrive_expect_tx(bar_drouted, (uint32_t)(na * a.down_bytes));
+        for (int q = 0; q < na; ++q)
+            issue_down<WFMT>(a, act[q], down_tile, down + (size_t)(1 + q) * a.down_bytes, bar_drouted);
+    }
+    // routed gate/up units u = b, b+G, ..., in waves of n_slots
+    for (int u0 = b; u0 < n_units; u0 += G * a.n_slots) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            fence_proxy_async_smem();
+            for (int s = 0; s < a.n_slots; ++s) {
+                const int u = u0 + s * G;
+                if (u < n_units)
+                    issue_unit<WFMT>(a, act[u / units_per_expert], u % units_per_expert,
+                                     slots + (size_t)s * a.unit_bytes, bars + s);
+            }
+        }
+        for (int s = 0; s < a.n_slots; ++s) {
+            const int u = u0 + s * G;
+            if (u >= n_units) break;
+            const uint32_t ph = (slot_phase >> s) & 1u;
+            wait_all(bars + s, ph);
+            slot_phase ^= 1u << s;
+            const int q = u / units_per_expert;
+            if (ok)
+                gateup_unit<WFMT>(a, slots + (size_t)s * a.unit_bytes, act[q], u % units_per_expert,
+                                  act_pairs + q * 2, act_np[q], x16s, xinv, acc);
+        }
+    }
+    if (!grid_barrier(a.bar_count, a.bar_gen, G, a.status)) ok = false;
+
+    // ------------------------------------------------------------------ P2
+    if (down_tile < 0) return;
+    // stage h rows as fp16 with a power-of-two scale per (token, slot) row
+    const int n_rows = T * (k + 1);
+    for (int r = warp; r < n_rows; r += kFWarps) {
+        const float* hr = a.h + (size_t)r * f;
+        float amax = 0.f;
+        for (int i = lane; i < f; i += 32) amax = fmaxf(amax, fabsf(__ldcg(hr + i)));
+        amax = warp_max(amax);
+        const float mult = f16_range_mult(amax);
+        for (int i = lane; i < f; i += 32)
+            h16s[(size_t)r * f + (i & ~127) + kperm_pos(i & 127)] = __float2half_rn(__ldcg(hr + i) * mult);
+        if (lane == 0) hinv[r] = 1.0f / mult;
+    }
+    wait_all(bar_dshared, 0);
+    if (na > 0) wait_all(bar_drouted, 0);
+    // partial down products: item (slab q, k-tile kt) -> acc[q][kt][16 rows][8 pairs]
+    const int S = WFMT == 0 ? 64 : 128;
+    const int n_items = (na + 1) * KTf;
+    for (int it = warp; it < n_items && ok; it += kFWarps) {
+        const int q = it / KTf, kt = it % KTf;
+        const uint8_t* slab = down + (size_t)q * a.down_bytes;
+        const uint8_t* cd = slab;
+        const uint8_t* sd = slab + 2 * KTf * 512;
+        const uint4 wg = *reinterpret_cast<const uint4*>(cd + kt * 512 + lane * 16);
+        const uint4 wh = *reinterpret_cast<const uint4*>(cd + (KTf + kt) * 512 + lane * 16);
+        const TileScales<WFMT> sc = lds_scales<WFMT>(sd + kt * S, sd + (KTf + kt) * S, g);
+        const int np = q == 0 ? T : act_np[q - 1];
+        const Pair* pp = q == 0 ? shared_pairs : act_pairs + (q - 1) * 2;
+        uint32_t bfr[16];
+        if (g < np) {
+            const int row = pp[g].t * (k + 1) + pp[g].j;
+            lds_b16(h16s + (size_t)row * f + kt * 128 + c * 32, bfr);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) bfr[i] = 0u;
+        }
+        uint32_t fa[8][4];
+        decode_tile<WFMT>(wg, wh, sc, fa);
+        float cacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s = 0; s < 8; ++s) mma_16816(cacc, fa[s][0], fa[s][1], fa[s][2], fa[s][3], bfr[2 * s], bfr[2 * s + 1]);
+        float* dst = acc + (size_t)(q * KTf + kt) * 128;
+        dst[g * 8 + 2 * c] = cacc[0];
+        dst[g * 8 + 2 * c + 1] = cacc[1];
+        dst[(g + 8) * 8 + 2 * c] = cacc[2];
+        dst[(g + 8) * 8 + 2 * c + 1] = cacc[3];
+    }
+    __syncthreads();
+    // combine: out[t][row] = bf16( y_shared + sum_j w_j y_j ), fixed order
+    if (threadIdx.x < T * 16 && ok) {
+        const int t = threadIdx.x / 16, rr = threadIdx.x % 16;
+        const int orow = down_tile * 16 + rr;
+        float ys = 0.f;
+        for (int kt = 0; kt < KTf; ++kt) ys += acc[(size_t)(0 * KTf + kt) * 128 + rr * 8 + t];
+        float v = ys * a.tscale[E * 3 + 2] * hinv[t * (k + 1) + k];
+        for (int j = 0; j < k; ++j) {
+            const int e = sel[t * 8 + j];
+            int q = 0;
+            while (act[q] != e) ++q;
+            int p = 0;
+            while (act_pairs[q * 2 + p].t != t) ++p;
+            float y = 0.f;
+            for (int kt = 0; kt < KTf; ++kt) y += acc[(size_t)((q + 1) * KTf + kt) * 128 + rr * 8 + p];
+            v += wsel[t * 8 + j] * (y * a.tscale[e * 3 + 2] * hinv[t * (k + 1) + j]);
+        }
+        __nv_bfloat16 o = __float2bfloat16_rn(v);
+        if (a.residual != nullptr) {
+            const float r = __bfloat162float(a.residual[(size_t)t * d + orow]);
+            o = __float2bfloat16_rn(r + __bfloat162float(o));
+        }
+        a.out[(size_t)t * d + orow] = o;
+    }
+}
+
+}  // namespace
+
+// Shared-memory plan of the fused kernel; 0 if it does not fit.
+size_t fused_smem_bytes(const Shape& s, int T, int n_sms, int* n_slots_out, int offs[8]) {
+    if (T < 1 || T > kFusedMaxT || s.n_shared != 1 || s.k > 8 || s.E > 256) return 0;
+    const int S = s.wfmt == 0 ? 64 : 128;
+    const int KTd = s.d / 128, KTf = s.f / 128;
+    const size_t unit = (size_t)4 * KTd * (512 + S);
+    const size_t dslab = (size_t)2 * KTf * (512 + S);
+    const int max_active = T * s.k;
+    const int units = max_active * (s.f / 16);
+    int n_slots = (units + n_sms - 1) / n_sms;
+    if (n_slots < 2) n_slots = 2;   // slot 0 holds the router slice, slot 1 a shared unit in P0
+    if (n_slots > 3) n_slots = 3;
+    if ((size_t)2 * s.d * 4 > unit) return 0;
+    if ((s.E + n_sms - 1) / n_sms > 2) return 0;
+    if (s.d / 16 > n_sms || s.f / 16 > n_sms) return 0;
+    const size_t red = (size_t)kFWarps * 2 * 32 * 4 * 4;
+    const size_t accb = (size_t)(max_active + 1) * KTf * 128 * 4;
+    size_t off = 0;
+    auto take = [&](size_t n) { size_t o = off; off = (off + n + 127) / 128 * 128; return o; };
+    offs[0] = (int)take((size_t)n_slots * unit);
+    offs[1] = (int)unit;
+    offs[2] = (int)take((size_t)(max_active + 1) * dslab);
+    offs[3] = (int)dslab;
+    offs[4] = (int)take(red > accb ? red : accb);
+    offs[5] = (int)take((size_t)T * s.d * 2);
+    offs[6] = (int)take((size_t)T * (s.k + 1) * s.f * 2);
+    offs[7] = (int)take(4096);
+    if (off > kFusedDynSmemMax) return 0;
+    *n_slots_out = n_slots;
+    return off;
+}
+
+cudaError_t prepare_decode_fused() {
+    void (*kerns[2])(FusedArgs) = {decode_fused_kernel<0>, decode_fused_kernel<1>};
+    for (auto kern : kerns) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+        if (e == cudaSuccess && fa.sharedSizeBytes + kFusedDynSmemMax > kMaxSmemOptin) e = cudaErrorInvalidValue;
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedDynSmemMax);
+        if (e != cudaSuccess) {
+            cudaGetLastError();   // leave no error behind for later launch checks
+            return e;
+        }
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode_fused(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
+                                __nv_bfloat16* out, const __nv_bfloat16* residual, const FusedScratch& fs,
+                                int n_sms, cudaStream_t st) {
+    int n_slots = 0, offs[8];
+    const size_t smem = fused_smem_bytes(s, T, n_sms, &n_slots, offs);
+    if (smem == 0) return cudaErrorInvalidValue;
+    FusedArgs a;
+    a.codes = L.codes;
+    a.scales = L.scales;
+    a.tscale = L.tscale;
+    a.router = L.router;
+    a.bias = L.bias;
+    a.cpm = s.codes_per_matrix();
+    a.spm = s.scales_per_matrix();
+    a.x = x;
+    a.out = out;
+    a.residual = residual;
+    a.T = T;
+    a.d = s.d;
+    a.f = s.f;
+    a.E = s.E;
+    a.k = s.k;
+    a.logits = fs.logits;
+    a.h = fs.h;
+    a.bar_count = fs.bar + 0;
+    a.bar_gen = fs.bar + 32;
+    a.status = fs.status;
+    a.n_slots = n_slots;
+    a.off_slots = offs[0];
+    a.unit_bytes = offs[1];
+    a.off_down = offs[2];
+    a.down_bytes = offs[3];
+    a.off_acc = offs[4];
+    a.off_x16 = offs[5];
+    a.off_h16 = offs[6];
+    a.off_misc = offs[7];
+    void (*kern)(FusedArgs) = s.wfmt == 0 ? decode_fused_kernel<0> : decode_fused_kernel<1>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_sms);
+    cfg.blockDim = dim3(kFThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace flint

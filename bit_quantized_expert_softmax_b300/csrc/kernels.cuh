@@ -59,7 +59,16 @@ struct Workspace {
     float* yw;            // [P][d]   weighted expert outputs
     int* chunk_hist;      // [n_chunks][E]
     uint32_t* counters;   // [kCounters] arrival counters (self-resetting)
+    uint32_t* gbar;       // [64]  grid-barrier count ([0]) and generation ([32])
     uint32_t* status;     // device status word
+};
+
+// Global scratch of the single-launch decode kernel.
+struct FusedScratch {
+    float* logits;        // [T][E]
+    float* h;             // [T][k+1][f]
+    uint32_t* bar;        // [64], zero-initialised
+    uint32_t* status;
 };
 
 constexpr int kCounters = 1024;
@@ -80,6 +89,14 @@ cudaError_t launch_gateup(const Shape& s, const LayerDev& L, int T, const Worksp
 cudaError_t launch_down(const Shape& s, const LayerDev& L, int T, const Workspace& ws,
                         __nv_bfloat16* out, const __nv_bfloat16* residual, cudaStream_t st,
                         int* n_launch);
+
+// decode_fused.cu: one persistent launch per layer for T <= kFusedMaxT
+constexpr int kFusedMaxT = 2;
+size_t fused_smem_bytes(const Shape& s, int T, int n_sms, int* n_slots_out, int offs[8]);
+cudaError_t prepare_decode_fused();   // once per device: shared-memory opt-in
+cudaError_t launch_decode_fused(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
+                                __nv_bfloat16* out, const __nv_bfloat16* residual, const FusedScratch& fs,
+                                int n_sms, cudaStream_t st);
 
 // repack.cu
 cudaError_t launch_repack_matrix(const uint8_t* codes_src, const uint8_t* scales_src,

@@ -9,6 +9,7 @@
 #include <float.h>
 
 #include "kernels.cuh"
+#include "topk.cuh"
 
 namespace flint {
 
@@ -16,79 +17,6 @@ namespace {
 
 constexpr int kRouterThreads = 256;   // 8 warps: 2 experts x 4 K-quarters
 constexpr int kMaxKIt = 8;            // d <= 4096 for the register-resident router row
-
-// ---------------------------------------------------------------------------
-// a2: top-k of one token's logits by one warp
-// ---------------------------------------------------------------------------
-__device__ void topk_warp(const float* __restrict__ Lrow, int E, int k, int* __restrict__ idx_out,
-                          float* __restrict__ w_out, uint32_t* status) {
-    const int lane = threadIdx.x & 31;
-    const int n = E >> 5;
-    float v[8];
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        if (i < n) {
-            float x = __ldcg(Lrow + i * 32 + lane);
-            if (!isfinite(x)) {
-                bad = true;
-                x = -INFINITY;
-            }
-            v[i] = x;
-        } else {
-            v[i] = -INFINITY;
-        }
-    }
-    if (status != nullptr && __any_sync(0xffffffffu, bad) && lane == 0)
-        atomicOr(status, kStatusNonFiniteLogit);
-    uint32_t taken = 0;
-    float sel_v[8];
-    int sel_i[8];
-    for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (i < n && !((taken >> i) & 1u)) {
-                int e = i * 32 + lane;
-                if (v[i] > bv || (v[i] == bv && e < bi)) {
-                    bv = v[i];
-                    bi = e;
-                }
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        sel_v[j] = bv;
-        sel_i[j] = bi;
-    }
-    // renormalised softmax over the selected logits (sel_v[0] is the maximum)
-    float sum = 0.f;
-    float ex[8];
-    for (int j = 0; j < k; ++j) {
-        ex[j] = expf(sel_v[j] - sel_v[0]);
-        sum += ex[j];
-    }
-    if (lane < k) {
-        float e = 0.f;
-        int id = 0;
-        for (int j = 0; j < k; ++j)
-            if (j == lane) {
-                e = ex[j];
-                id = sel_i[j];
-            }
-        idx_out[lane] = id;
-        if (w_out != nullptr) w_out[lane] = e / sum;
-    }
-}
 
 // ---------------------------------------------------------------------------
 // fp16 staging of one token: per-token power-of-two scale, fragment order
@@ -299,8 +227,8 @@ __global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouterArgs
     __threadfence();
     // top-k per token: warp per token (logits read through L2)
     for (int t = warp; t < T; t += 8) {
-        topk_warp(a.ws.logits + (size_t)t * a.E, a.E, a.k, a.ws.idx + t * a.k, a.ws.w + t * a.k,
-                  a.ws.status);
+        topk_warp<true>(a.ws.logits + (size_t)t * a.E, a.E, a.k, a.ws.idx + t * a.k, a.ws.w + t * a.k,
+                        a.ws.status);
     }
     __syncthreads();
     __threadfence_block();
@@ -372,8 +300,8 @@ __global__ void __launch_bounds__(256) token_prep_kernel(RouterArgs a) {
     const int warp = threadIdx.x >> 5;
     const int t = blockIdx.x * 8 + warp;
     if (t >= a.T) return;
-    topk_warp(a.ws.logits + (size_t)t * a.E, a.E, a.k, a.ws.idx + t * a.k, a.ws.w + t * a.k,
-              a.ws.status);
+    topk_warp<false>(a.ws.logits + (size_t)t * a.E, a.E, a.k, a.ws.idx + t * a.k, a.ws.w + t * a.k,
+                     a.ws.status);
     stage_token_warp(a.x + (size_t)t * a.d, a.d, a.ws.x16 + (size_t)t * a.d, a.ws.xinv + t);
 }
 
@@ -433,7 +361,7 @@ __global__ void __launch_bounds__(256) topk_only_kernel(const float* logits, int
                                                         int* idx, float* w) {
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
-    topk_warp(logits + (size_t)t * E, E, k, idx + t * k, w ? w + t * k : nullptr, nullptr);
+    topk_warp<false>(logits + (size_t)t * E, E, k, idx + t * k, w ? w + t * k : nullptr, nullptr);
 }
 
 RouterArgs make_args(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,

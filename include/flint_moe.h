@@ -208,6 +208,14 @@ FLINT_API flint_status flint_moe_bucket_noalloc(const int32_t* idx_dev, int T, i
 /* Number of kernels this handle has launched so far (all entry points). */
 FLINT_API uint64_t flint_moe_launch_count(const flint_moe* h);
 
+/* Kernels one single-layer flint_moe_forward of T tokens launches: 1 when the
+ * single-launch decode kernel serves T (T <= 2 with one shared expert, if its
+ * shared-memory plan fits), otherwise the multi-kernel count. -1 on bad
+ * arguments. The single-launch path can be switched off for a handle by
+ * setting the environment variable FLINT_MOE_FUSED_DECODE=0 before
+ * flint_moe_create. */
+FLINT_API int flint_moe_forward_launches(const flint_moe* h, int T);
+
 /* Start recording CUDA events on the caller's stream around the three phases
  * of the next max_forwards single-layer forwards (phase 0: router, top-k and
  * bucketing; 1: expert gate/up; 2: expert down projection and combine).

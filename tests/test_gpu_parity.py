@@ -190,24 +190,42 @@ def _layer_parity(fm, cfg, T, sample=None, mutate=None):
     return got[rows][same], ref
 
 
-@pytest.mark.parametrize("T", [1, 3, 4, 17, 64, 65, 130])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 17, 64, 65, 130])
 def test_layer_tiny_nvfp4(fm, T):
     cfg = _cfg(1)
     got, ref = _layer_parity(fm, cfg, T)
     assert_out_close(got, ref.out, f"tiny nvfp4 T={T}")
 
 
-@pytest.mark.parametrize("T", [1, 5, 64, 70])
+@pytest.mark.parametrize("T", [1, 2, 5, 64, 70])
 def test_layer_tiny_q4_1(fm, T):
     cfg = _cfg(1, wfmt=synth.WFMT_Q4_1, bias="zipf")
     got, ref = _layer_parity(fm, cfg, T)
     assert_out_close(got, ref.out, f"tiny q4_1 T={T}")
 
 
-def test_layer_flint_decode_T1(fm):
+@pytest.mark.parametrize("T", [1, 2])
+def test_layer_flint_decode_nvfp4(fm, T):
     cfg = _cfg(2)
-    got, ref = _layer_parity(fm, cfg, 1)
-    assert_out_close(got, ref.out, "decode T=1")
+    got, ref = _layer_parity(fm, cfg, T)
+    assert_out_close(got, ref.out, f"decode T={T}")
+
+
+@pytest.mark.parametrize("T", [1, 2])
+def test_layer_flint_decode_q4_1(fm, T):
+    cfg = _cfg(3)
+    got, ref = _layer_parity(fm, cfg, T)
+    assert_out_close(got, ref.out, f"q4_1 decode T={T}")
+
+
+@pytest.mark.parametrize("wfmt,T", [(synth.WFMT_NVFP4, 1), (synth.WFMT_NVFP4, 2), (synth.WFMT_Q4_1, 1)])
+def test_multikernel_decode_path(fm, monkeypatch, wfmt, T):
+    """The single-launch decode kernel serves T <= 2 by default; the
+    multi-kernel path must give the same layer when it is selected instead."""
+    monkeypatch.setenv("FLINT_MOE_FUSED_DECODE", "0")
+    cfg = _cfg(2, wfmt=wfmt)
+    got, ref = _layer_parity(fm, cfg, T)
+    assert_out_close(got, ref.out, f"multi-kernel decode T={T}")
 
 
 def test_layer_flint_batched_q4_1_T64(fm):
@@ -225,32 +243,46 @@ def test_layer_flint_prefill_T8192_sampled(fm):
 
 
 def test_stack_47_layers_T1(fm):
+    """47-layer decode stack. Every layer is checked against the oracle on the
+    oracle's own input x_l (full size, per-layer weights); the GPU stack must
+    equal the GPU chain of single-layer forwards bit for bit; and the end to
+    end drift from the oracle is bounded. One-ulp bf16 differences in the
+    residual stream move later logits by ~1e-4 and can flip a near-tie routing
+    decision, after which the two 47-layer trajectories legitimately part, so
+    the end-to-end bound (5e-2) is looser than the per-layer one (5e-3)."""
     cfg = _cfg(4)
     bits = synth.make_hidden(cfg)
     m = fm.MoE(cfg, max_tokens=1, n_layers=cfg.n_layers)
     ref_bits = bits.copy()
-    min_gap = np.inf
+    idx = torch.empty((1, cfg.top_k), dtype=torch.int32, device="cuda")
     for i in range(cfg.n_layers):          # one layer in host memory at a time
         L = synth.make_layer(cfg, layer=i)
         m.load(i, L)
         r = M.moe_layer(ref_bits, L)
-        s = np.sort(r.logits[0])[::-1]
-        min_gap = min(min_gap, (s[cfg.top_k - 1] - s[cfg.top_k]) / np.sqrt(np.mean(r.logits ** 2)))
+        xi = fm.hidden_to_device(ref_bits)
+        got = fm.hidden_to_host(m.forward(xi, i))
+        fm.flint_moe_router(m.h, i, xi, 1, None, idx, None)
+        torch.cuda.synchronize()
+        same = compare_routing(idx.cpu().numpy(), r.sel, r.logits, cfg.top_k)
+        if same.all():
+            assert_out_close(got, r.out, f"stack layer {i}")
         ref_bits = F.bf16_bits(F.bf16_round(F.bf16_array(ref_bits) + r.out_bf16))
+    assert fm.flint_moe_status(m.h) == fm.FLINT_OK
     x = fm.hidden_to_device(bits)
-    m.forward_stack(x, 0, cfg.n_layers)
+    xs = x.clone()
+    m.forward_stack(xs, 0, cfg.n_layers)
+    y = x.clone()
+    for i in range(cfg.n_layers):
+        o = m.forward(y, i)
+        y = (y.float() + o.float()).to(torch.bfloat16)
     torch.cuda.synchronize()
     assert fm.flint_moe_status(m.h) == fm.FLINT_OK
-    got = fm.hidden_to_host(x)
+    assert torch.equal(xs.view(torch.int16), y.view(torch.int16))
+    got = F.bf16_array(fm.hidden_to_host(xs))
+    ref = F.bf16_array(ref_bits)
+    drift = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
     m.close()
-    # The smallest gap between the 6th and 7th logit over all layers (relative
-    # to the logit RMS) is reported with any mismatch: one-ulp bf16 differences
-    # in the residual stream move logits by ~1e-4, so a routing near tie below
-    # that would make the two stacks diverge legitimately.
-    try:
-        assert_out_close(got, F.bf16_array(ref_bits), "47-layer stack")
-    except AssertionError as e:
-        raise AssertionError(f"{e} (smallest relative routing gap over the stack {min_gap:.2e})")
+    assert drift <= 5e-2, f"47-layer drift {drift:.3e}"
 
 
 # ---------------------------------------------------------------------------
