@@ -152,7 +152,7 @@ cudaError_t run_layer(flint_moe* h, int layer, const __nv_bfloat16* x, int T, __
                       const __nv_bfloat16* residual, cudaStream_t st) {
     const LayerDev& L = h->layers[layer];
     int n = 0;
-    int n_slots = 0, offs[8];
+    int n_slots = 0, offs[10];
     if (h->fused && flint::fused_smem_bytes(h->s, T, h->n_sms, &n_slots, offs) != 0) {
         flint::FusedScratch fs{h->ws.logits, h->ws.hf, h->ws.gbar, h->ws.status};
         prof_record(h, 0, st);
@@ -270,7 +270,8 @@ flint_status flint_moe_load_weights(flint_moe* h, int layer, const flint_moe_wei
         if (e == cudaSuccess) e = cudaMalloc(&L.bias, (size_t)s.E * sizeof(float));
         if (e == cudaSuccess) e = cudaMalloc(&L.codes, n_codes);
         if (e == cudaSuccess) e = cudaMalloc(&L.scales, n_scales);
-        if (e == cudaSuccess) e = cudaMalloc(&L.tscale, (size_t)n_slots * 3 * sizeof(float));
+        if (e == cudaSuccess) e = cudaMalloc(&L.tscale, flint::tscale_bytes(s));
+        if (e == cudaSuccess) e = cudaMemset(L.tscale, 0, flint::tscale_bytes(s));
         if (e != cudaSuccess) {
             free_layer(L);
             return cuda_status(e);
@@ -457,7 +458,7 @@ uint64_t flint_moe_launch_count(const flint_moe* h) { return h ? h->launches : 0
 int flint_moe_forward_launches(const flint_moe* h, int T) {
     if (h == nullptr || T < 0 || T > h->s.max_tokens) return -1;
     if (T == 0) return 0;
-    int n_slots = 0, offs[8];
+    int n_slots = 0, offs[10];
     if (h->fused && flint::fused_smem_bytes(h->s, T, h->n_sms, &n_slots, offs) != 0) return 1;
     const int router = T <= flint::kSmallT ? 1 : 2 + 3;
     const int down = T <= flint::kSmallT ? 1 : 2;

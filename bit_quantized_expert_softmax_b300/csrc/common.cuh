@@ -212,34 +212,83 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase,
 }
 
 // Grid-wide barrier for a kernel whose CTAs are all resident (cooperative
-// launch). count/gen live in global memory; count must be 0 on entry to the
-// first use and is returned to 0 by the last arriver. Spins are bounded: on
-// timeout the status word gets kStatusTimeout and false is returned.
-__device__ __forceinline__ bool grid_barrier(uint32_t* count, uint32_t* gen, uint32_t n_ctas,
-                                             uint32_t* status) {
+// launch). count/gen live in global memory; count is 0 between barriers (the
+// last arriver resets it before releasing the others). Arrival is a release
+// (publishes the CTA's earlier writes, ordered by the preceding
+// __syncthreads), the wait an acquire. Spins are bounded: on timeout the
+// status word gets kStatusTimeout and false is returned.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Grid barrier on a monotonically increasing 64-bit arrival counter, for a
+// kernel whose CTAs are all resident (cooperative launch). Every CTA adds 1
+// (a release, publishing the CTA's writes ordered by the __syncthreads) and
+// waits (acquire) until the counter reaches `target`, the base read at kernel
+// start plus n_ctas per barrier passed. The counter is a multiple of n_ctas
+// between kernels. Spins are bounded: on timeout the status word gets
+// kStatusTimeout and false is returned.
+struct GridSync {
+    unsigned long long* count;
+    unsigned long long base;
+    uint32_t n;
+    uint32_t passed;
+};
+
+// Call by every thread at kernel start, before this CTA's first arrival.
+__device__ __forceinline__ GridSync grid_sync_init(unsigned long long* count, uint32_t n_ctas) {
+    __shared__ unsigned long long s_base;
+    if (threadIdx.x == 0) {
+        const unsigned long long c = ld_acquire_gpu_u64(count);
+        s_base = c - c % n_ctas;   // fewer than n_ctas arrivals can precede ours
+    }
+    __syncthreads();
+    return GridSync{count, s_base, n_ctas, 0u};
+}
+
+__device__ __forceinline__ bool grid_sync(GridSync& gs, uint32_t* status) {
     __shared__ uint32_t s_ok;
     __syncthreads();
+    gs.passed += 1;
     if (threadIdx.x == 0) {
         uint32_t ok = 1;
-        const uint32_t g = *((volatile uint32_t*)gen);
-        __threadfence();
-        const uint32_t arrived = atomicAdd(count, 1u);
-        if (arrived == n_ctas - 1) {
-            *((volatile uint32_t*)count) = 0u;
-            __threadfence();
-            atomicAdd(gen, 1u);
-        } else {
-            uint32_t it = 0;
-            while (*((volatile uint32_t*)gen) == g) {
-                if (++it > (1u << 24)) {
-                    atomicOr(status, kStatusTimeout);
-                    ok = 0;
-                    break;
-                }
-                __nanosleep(64);
+        const unsigned long long target = gs.base + (unsigned long long)gs.n * gs.passed;
+        red_release_gpu_add_u64(gs.count, 1ull);
+        uint32_t it = 0;
+        while (ld_acquire_gpu_u64(gs.count) < target) {
+            if (++it > (1u << 26)) {
+                atomicOr(status, kStatusTimeout);
+                ok = 0;
+                break;
             }
+            if (it > 256) __nanosleep(32);
         }
-        __threadfence();
         s_ok = ok;
     }
     __syncthreads();

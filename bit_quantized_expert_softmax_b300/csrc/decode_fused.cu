@@ -49,12 +49,12 @@ struct FusedArgs {
     int T, d, f, E, k;
     float* logits;              // [T][E]
     float* h;                   // [T][k+1][f] fp32, slot k = shared expert
-    uint32_t* bar_count;
-    uint32_t* bar_gen;
+    unsigned long long* bar_count;   // grid-barrier arrival counter
     uint32_t* status;
     int n_slots;                // gate/up unit slots in shared memory
     // shared-memory layout (byte offsets)
-    int off_slots, unit_bytes, off_down, down_bytes, off_acc, off_x16, off_h16, off_misc;
+    int off_slots, unit_bytes, off_down, down_bytes, off_acc, off_x16, off_h16, off_misc, off_xbf, off_ts;
+    int ts_bytes;               // bytes of the tensor-scale array copied to shared memory
 };
 
 struct Pair {
@@ -116,7 +116,7 @@ __device__ void issue_down(const FusedArgs& a, int e, int r16, uint8_t* dst, uin
 // writes h = silu(g) * u (fp32) for the unit's 16 rows.
 template <int WFMT>
 __device__ void gateup_unit(const FusedArgs& a, const uint8_t* slab, int e, int r16, const Pair* pairs, int np,
-                            const __half* x16s, const float* xinv, float* red) {
+                            const __half* x16s, const float* xinv, const float* tss, float* red) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const int KT = a.d >> 7;
@@ -149,30 +149,35 @@ __device__ void gateup_unit(const FusedArgs& a, const uint8_t* slab, int e, int 
 #pragma unroll
         for (int s = 0; s < 8; ++s) mma_16816(accu, fa[s][0], fa[s][1], fa[s][2], fa[s][3], b[2 * s], b[2 * s + 1]);
     }
-    // cross-warp reduction of the K partials: red[warp][2][32][4]
+    // cross-warp reduction of the K partials: red[warp][gate/up][128]
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        red[((warp * 2 + 0) * 32 + lane) * 4 + j] = accg[j];
-        red[((warp * 2 + 1) * 32 + lane) * 4 + j] = accu[j];
+        red[(warp * 2 + 0) * 128 + lane * 4 + j] = accg[j];
+        red[(warp * 2 + 1) * 128 + lane * 4 + j] = accu[j];
     }
     __syncthreads();
-    if (warp == 0) {
-        const float tsg = a.tscale[e * 3 + 0], tsu = a.tscale[e * 3 + 1];
-        const int nw = KT < kFWarps ? KT : kFWarps;
+    if (threadIdx.x < 128) {
+        // thread i owns fragment element i = lane' * 4 + j' of the 16 x 8 tile
+        const int i = threadIdx.x, ln = i >> 2, j = i & 3;
+        const int n = 2 * (ln & 3) + (j & 1);
+        if (n < np) {
+            float sgv[kFWarps], suv[kFWarps];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int n = 2 * c + (j & 1);
-            if (n >= np) continue;
-            float sgv = 0.f, suv = 0.f;
-            for (int w = 0; w < nw; ++w) {
-                sgv += red[((w * 2 + 0) * 32 + lane) * 4 + j];
-                suv += red[((w * 2 + 1) * 32 + lane) * 4 + j];
+            for (int w = 0; w < kFWarps; ++w) {
+                sgv[w] = red[(w * 2 + 0) * 128 + i];
+                suv[w] = red[(w * 2 + 1) * 128 + i];
+            }
+            float sg_ = 0.f, su_ = 0.f;
+#pragma unroll
+            for (int w = 0; w < kFWarps; ++w) {
+                sg_ += sgv[w];
+                su_ += suv[w];
             }
             const Pair p = pairs[n];
-            const float gv = sgv * tsg * xinv[p.t];
-            const float uv = suv * tsu * xinv[p.t];
+            const float gv = sg_ * tss[e * 3 + 0] * xinv[p.t];
+            const float uv = su_ * tss[e * 3 + 1] * xinv[p.t];
             const float hv = gv / (1.0f + expf(-gv)) * uv;
-            const int row = r16 * 16 + g + ((j >> 1) << 3);
+            const int row = r16 * 16 + (ln >> 2) + ((j >> 1) << 3);
             a.h[((size_t)p.t * (a.k + 1) + p.j) * a.f + row] = hv;
         }
     }
@@ -198,10 +203,13 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     __half* x16s = reinterpret_cast<__half*>(smem + a.off_x16);
     __half* h16s = reinterpret_cast<__half*>(smem + a.off_h16);
     uint8_t* misc = smem + a.off_misc;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(misc);              // [n_slots + 3]
+    const __nv_bfloat16* xbf = reinterpret_cast<const __nv_bfloat16*>(smem + a.off_xbf);
+    const float* tss = reinterpret_cast<const float*>(smem + a.off_ts);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc);              // [n_slots + 4]
     uint64_t* bar_router = bars + a.n_slots;
     uint64_t* bar_dshared = bars + a.n_slots + 1;
     uint64_t* bar_drouted = bars + a.n_slots + 2;
+    uint64_t* bar_x = bars + a.n_slots + 3;
     float* xinv = reinterpret_cast<float*>(misc + 128);              // [2]
     float* hinv = xinv + 4;                                          // [2*(k+1)] <= 18
     float* rpart = hinv + 20;                                        // [16][2]
@@ -213,6 +221,8 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     Pair* act_pairs = reinterpret_cast<Pair*>(act_np + 17);          // [17][2]
     int* nact = reinterpret_cast<int*>(act_pairs + 34);              // [1]
     Pair* shared_pairs = reinterpret_cast<Pair*>(nact + 2);          // [2]
+    float* bias_s = reinterpret_cast<float*>(shared_pairs + 2);      // [2]
+    int* cmap = reinterpret_cast<int*>(bias_s + 2);                  // [2][8]
 
     bool ok = true;
     uint32_t slot_phase = 0;   // bit s: parity of slot s's next completion
@@ -224,47 +234,59 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     };
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < a.n_slots + 3; ++i) mbar_init(bars + i, 1);
+        for (int i = 0; i < a.n_slots + 4; ++i) mbar_init(bars + i, 1);
         mbar_fence_init();
     }
     __syncthreads();
 
     // ------------------------------------------------------------------ P0
-    // router slice: experts b, b+G, ... (at most 2 rows held in slot 0)
+    // router slice: experts b, b+G, ... (at most 2 rows held in slot 0); the
+    // shared expert's gate/up unit (slot n_slots-1) and down slab are
+    // prefetched now and used in P1 / P2.
     int n_re = 0;
     for (int e = b; e < E; e += G) ++n_re;
+    const int shared_slot = a.n_slots - 1;
+    const bool has_shared = shared_unit >= 0 && shared_unit < units_per_expert;
     if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(bar_x, (uint32_t)(T * d * 2 + a.ts_bytes));
+        bulk_g2s(smem + a.off_xbf, a.x, (uint32_t)(T * d * 2), bar_x);
+        bulk_g2s(smem + a.off_ts, a.tscale, (uint32_t)a.ts_bytes, bar_x);
         if (n_re > 0) {
             mbar_arrive_expect_tx(bar_router, (uint32_t)(n_re * d * 4));
             for (int i = 0; i < n_re; ++i)
                 bulk_g2s(slots + (size_t)i * d * 4, a.router + (size_t)(b + i * G) * d, d * 4, bar_router);
         }
-        if (shared_unit >= 0 && shared_unit < units_per_expert)
-            issue_unit<WFMT>(a, E, shared_unit, slots + a.unit_bytes, bars + 1);
+        if (has_shared) issue_unit<WFMT>(a, E, shared_unit, slots + (size_t)shared_slot * a.unit_bytes, bars + shared_slot);
         if (down_tile >= 0) {
             mbar_arrive_expect_tx(bar_dshared, (uint32_t)a.down_bytes);
             issue_down<WFMT>(a, E, down_tile, down, bar_dshared);
         }
     }
+    if (threadIdx.x >= 32 && threadIdx.x < 32 + n_re) bias_s[threadIdx.x - 32] = __ldg(a.bias + b + (threadIdx.x - 32) * G);
+    GridSync gsync = grid_sync_init(a.bar_count, (uint32_t)G);   // includes a __syncthreads
     // stage the hidden states as fp16, scaled per token, fragment-permuted
+    wait_all(bar_x, 0);
     for (int t = 0; t < T; ++t) {
+        float xv[8];
         float amax = 0.f;
-        for (int i = threadIdx.x; i < d; i += kFThreads)
-            amax = fmaxf(amax, fabsf(__bfloat162float(a.x[(size_t)t * d + i])));
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = threadIdx.x + q * kFThreads;
+            xv[q] = i < d ? __bfloat162float(xbf[(size_t)t * d + i]) : 0.f;
+            amax = fmaxf(amax, fabsf(xv[q]));
+        }
         amax = warp_max(amax);
         if (lane == 0) rpart[warp] = amax;
         __syncthreads();
-        if (threadIdx.x == 0) {
-            float m = 0.f;
-            for (int w = 0; w < kFWarps; ++w) m = fmaxf(m, rpart[w]);
-            xinv[t] = m;
+        float m = 0.f;
+#pragma unroll
+        for (int w = 0; w < kFWarps; ++w) m = fmaxf(m, rpart[w]);
+        const float mult = f16_range_mult(m);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = threadIdx.x + q * kFThreads;
+            if (i < d) x16s[(size_t)t * d + (i & ~127) + kperm_pos(i & 127)] = __float2half_rn(xv[q] * mult);
         }
-        __syncthreads();
-        const float mult = f16_range_mult(xinv[t]);
-        for (int i = threadIdx.x; i < d; i += kFThreads)
-            x16s[(size_t)t * d + (i & ~127) + kperm_pos(i & 127)] =
-                __float2half_rn(__bfloat162float(a.x[(size_t)t * d + i]) * mult);
-        __syncthreads();
         if (threadIdx.x == 0) xinv[t] = 1.0f / mult;
         __syncthreads();
     }
@@ -283,7 +305,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
             for (int q = lane * 4; q < seg; q += 128) {
                 const float4 wv = *reinterpret_cast<const float4*>(wr + q);
                 for (int t = 0; t < T; ++t) {
-                    const __nv_bfloat16* xr = a.x + (size_t)t * d + part * seg + q;
+                    const __nv_bfloat16* xr = xbf + (size_t)t * d + part * seg + q;
                     const uint2 raw = *reinterpret_cast<const uint2*>(xr);
                     const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
                     const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
@@ -306,16 +328,10 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
             float s = 0.f;
             for (int p = 0; p < 8; ++p) s += rpart[(ii * 8 + p) * 2 + t];
             const int e = b + ii * G;
-            a.logits[(size_t)t * E + e] = s + a.bias[e];
+            a.logits[(size_t)t * E + e] = s + bias_s[ii];
         }
     }
-    // shared expert gate/up
-    if (shared_unit >= 0 && shared_unit < units_per_expert) {
-        wait_all(bars + 1, 0);
-        slot_phase ^= 2u;
-        if (ok) gateup_unit<WFMT>(a, slots + a.unit_bytes, E, shared_unit, shared_pairs, T, x16s, xinv, acc);
-    }
-    if (!grid_barrier(a.bar_count, a.bar_gen, G, a.status)) ok = false;
+    if (!grid_sync(gsync, a.status)) ok = false;
 
     // ------------------------------------------------------------------ P1
     // top-k of every token, computed by every CTA from the logits in L2
@@ -323,66 +339,78 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     __syncthreads();
     if (warp < T) topk_warp<false>(lg + warp * E, E, k, sel + warp * 8, wsel + warp * 8, b == 0 ? a.status : nullptr);
     __syncthreads();
-    if (threadIdx.x == 0) {
-        // distinct routed experts in ascending order with their (token, slot) pairs
-        int n = 0;
-        for (int t = 0; t < T; ++t)
-            for (int j = 0; j < k; ++j) {
-                const int e = sel[t * 8 + j];
-                int pos = 0;
-                while (pos < n && act[pos] < e) ++pos;
-                if (pos < n && act[pos] == e) {
-                    act_pairs[pos * 2 + act_np[pos]] = Pair{t, j};
-                    ++act_np[pos];
-                    continue;
-                }
-                for (int q = n; q > pos; --q) {
-                    act[q] = act[q - 1];
-                    act_np[q] = act_np[q - 1];
-                    act_pairs[q * 2 + 0] = act_pairs[(q - 1) * 2 + 0];
-                    act_pairs[q * 2 + 1] = act_pairs[(q - 1) * 2 + 1];
-                }
-                act[pos] = e;
-                act_np[pos] = 1;
-                act_pairs[pos * 2] = Pair{t, j};
-                ++n;
+    if (warp == 0) {
+        // distinct routed experts and their (token, slot) pairs, by one warp:
+        // entry i = t*k + j; an entry is the first of its expert if no earlier
+        // entry has the same expert; experts are numbered in first-occurrence
+        // order (the order does not change any result).
+        const int n = T * k;
+        const int t = lane / k, j = lane - (lane / k) * k;
+        const int e = lane < n ? sel[t * 8 + j] : -1 - lane;
+        int first = lane, p = 0;
+        for (int i = 0; i < n; ++i) {
+            const int ei = __shfl_sync(0xffffffffu, e, i);
+            if (i < lane && ei == e) {
+                if (first == lane) first = i;
+                ++p;
             }
-        *nact = n;
+        }
+        const uint32_t firsts = __ballot_sync(0xffffffffu, lane < n && first == lane);
+        const int q = __popc(firsts & ((1u << first) - 1u));   // dense index of this entry's expert
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        if (lane < n) {
+            if (first == lane) {
+                act[q] = e;
+                act_np[q] = __popc(same);
+            }
+            act_pairs[q * 2 + p] = Pair{t, j};
+            cmap[t * 8 + j] = (q + 1) * 4 + p;
+        }
+        if (lane == 0) *nact = __popc(firsts);
     }
     __syncthreads();
     const int na = *nact;
     const int n_units = na * units_per_expert;
-    // routed down slabs for this CTA's output tile (slab 0 is the shared expert)
+    // routed gate/up units u = b, b+G, ..., in waves of n_slots-1 slots
+    const int n_rs = a.n_slots - 1;
+    for (int u0 = b; u0 < n_units; u0 += G * n_rs) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            fence_proxy_async_smem();
+            for (int s2 = 0; s2 < n_rs; ++s2) {
+                const int u = u0 + s2 * G;
+                if (u < n_units)
+                    issue_unit<WFMT>(a, act[u / units_per_expert], u % units_per_expert,
+                                     slots + (size_t)s2 * a.unit_bytes, bars + s2);
+            }
+        }
+        for (int s2 = 0; s2 < n_rs; ++s2) {
+            const int u = u0 + s2 * G;
+            if (u >= n_units) break;
+            const uint32_t ph = (slot_phase >> s2) & 1u;
+            wait_all(bars + s2, ph);
+            slot_phase ^= 1u << s2;
+            const int q = u / units_per_expert;
+            if (ok)
+                gateup_unit<WFMT>(a, slots + (size_t)s2 * a.unit_bytes, act[q], u % units_per_expert,
+                                  act_pairs + q * 2, act_np[q], x16s, xinv, tss, acc);
+        }
+    }
+    // routed down slabs for this CTA's output tile (slab 0 is the shared
+    // expert), requested once the gate/up slabs have landed so that they do
+    // not compete with them; they are needed only after the next barrier
     if (threadIdx.x == 0 && down_tile >= 0 && na > 0) {
         mbar_arrive_expect_tx(bar_drouted, (uint32_t)(na * a.down_bytes));
         for (int q = 0; q < na; ++q)
             issue_down<WFMT>(a, act[q], down_tile, down + (size_t)(1 + q) * a.down_bytes, bar_drouted);
     }
-    // routed gate/up units u = b, b+G, ..., in waves of n_slots
-    for (int u0 = b; u0 < n_units; u0 += G * a.n_slots) {
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            fence_proxy_async_smem();
-            for (int s = 0; s < a.n_slots; ++s) {
-                const int u = u0 + s * G;
-                if (u < n_units)
-                    issue_unit<WFMT>(a, act[u / units_per_expert], u % units_per_expert,
-                                     slots + (size_t)s * a.unit_bytes, bars + s);
-            }
-        }
-        for (int s = 0; s < a.n_slots; ++s) {
-            const int u = u0 + s * G;
-            if (u >= n_units) break;
-            const uint32_t ph = (slot_phase >> s) & 1u;
-            wait_all(bars + s, ph);
-            slot_phase ^= 1u << s;
-            const int q = u / units_per_expert;
-            if (ok)
-                gateup_unit<WFMT>(a, slots + (size_t)s * a.unit_bytes, act[q], u % units_per_expert,
-                                  act_pairs + q * 2, act_np[q], x16s, xinv, acc);
-        }
+    // the shared expert's unit, prefetched in P0
+    if (has_shared) {
+        wait_all(bars + shared_slot, 0);
+        if (ok) gateup_unit<WFMT>(a, slots + (size_t)shared_slot * a.unit_bytes, E, shared_unit, shared_pairs, T,
+                                  x16s, xinv, tss, acc);
     }
-    if (!grid_barrier(a.bar_count, a.bar_gen, G, a.status)) ok = false;
+    if (!grid_sync(gsync, a.status)) ok = false;
 
     // ------------------------------------------------------------------ P2
     if (down_tile < 0) return;
@@ -390,43 +418,57 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     const int n_rows = T * (k + 1);
     for (int r = warp; r < n_rows; r += kFWarps) {
         const float* hr = a.h + (size_t)r * f;
+        float hv[32];
         float amax = 0.f;
-        for (int i = lane; i < f; i += 32) amax = fmaxf(amax, fabsf(__ldcg(hr + i)));
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+            const int i = lane + 32 * q;
+            hv[q] = i < f ? __ldcg(hr + i) : 0.f;
+            amax = fmaxf(amax, fabsf(hv[q]));
+        }
         amax = warp_max(amax);
         const float mult = f16_range_mult(amax);
-        for (int i = lane; i < f; i += 32)
-            h16s[(size_t)r * f + (i & ~127) + kperm_pos(i & 127)] = __float2half_rn(__ldcg(hr + i) * mult);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+            const int i = lane + 32 * q;
+            if (i < f) h16s[(size_t)r * f + (i & ~127) + kperm_pos(i & 127)] = __float2half_rn(hv[q] * mult);
+        }
         if (lane == 0) hinv[r] = 1.0f / mult;
     }
     wait_all(bar_dshared, 0);
     if (na > 0) wait_all(bar_drouted, 0);
-    // partial down products: item (slab q, k-tile kt) -> acc[q][kt][16 rows][8 pairs]
+    // down products: warps 2q and 2q+1 (slab q = shared, then routed) run the
+    // two halves of the k-tiles -> acc[q][half][16 rows][8 pairs]
     const int S = WFMT == 0 ? 64 : 128;
-    const int n_items = (na + 1) * KTf;
-    for (int it = warp; it < n_items && ok; it += kFWarps) {
-        const int q = it / KTf, kt = it % KTf;
+    const int kt_half = (KTf + 1) / 2;
+    for (int it = warp; it < 2 * (na + 1) && ok; it += kFWarps) {
+        const int q = it >> 1, hf = it & 1;
         const uint8_t* slab = down + (size_t)q * a.down_bytes;
         const uint8_t* cd = slab;
         const uint8_t* sd = slab + 2 * KTf * 512;
-        const uint4 wg = *reinterpret_cast<const uint4*>(cd + kt * 512 + lane * 16);
-        const uint4 wh = *reinterpret_cast<const uint4*>(cd + (KTf + kt) * 512 + lane * 16);
-        const TileScales<WFMT> sc = lds_scales<WFMT>(sd + kt * S, sd + (KTf + kt) * S, g);
         const int np = q == 0 ? T : act_np[q - 1];
         const Pair* pp = q == 0 ? shared_pairs : act_pairs + (q - 1) * 2;
-        uint32_t bfr[16];
-        if (g < np) {
-            const int row = pp[g].t * (k + 1) + pp[g].j;
-            lds_b16(h16s + (size_t)row * f + kt * 128 + c * 32, bfr);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) bfr[i] = 0u;
-        }
-        uint32_t fa[8][4];
-        decode_tile<WFMT>(wg, wh, sc, fa);
+        const int hrow = g < np ? pp[g].t * (k + 1) + pp[g].j : -1;
         float cacc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int kt1 = min(KTf, (hf + 1) * kt_half);
+        for (int kt = hf * kt_half; kt < kt1; ++kt) {
+            const uint4 wg = *reinterpret_cast<const uint4*>(cd + kt * 512 + lane * 16);
+            const uint4 wh = *reinterpret_cast<const uint4*>(cd + (KTf + kt) * 512 + lane * 16);
+            const TileScales<WFMT> sc = lds_scales<WFMT>(sd + kt * S, sd + (KTf + kt) * S, g);
+            uint32_t bfr[16];
+            if (hrow >= 0) {
+                lds_b16(h16s + (size_t)hrow * f + kt * 128 + c * 32, bfr);
+            } else {
 #pragma unroll
-        for (int s = 0; s < 8; ++s) mma_16816(cacc, fa[s][0], fa[s][1], fa[s][2], fa[s][3], bfr[2 * s], bfr[2 * s + 1]);
-        float* dst = acc + (size_t)(q * KTf + kt) * 128;
+                for (int i = 0; i < 16; ++i) bfr[i] = 0u;
+            }
+            uint32_t fa[8][4];
+            decode_tile<WFMT>(wg, wh, sc, fa);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                mma_16816(cacc, fa[s][0], fa[s][1], fa[s][2], fa[s][3], bfr[2 * s], bfr[2 * s + 1]);
+        }
+        float* dst = acc + (size_t)it * 128;
         dst[g * 8 + 2 * c] = cacc[0];
         dst[g * 8 + 2 * c + 1] = cacc[1];
         dst[(g + 8) * 8 + 2 * c] = cacc[2];
@@ -437,18 +479,13 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     if (threadIdx.x < T * 16 && ok) {
         const int t = threadIdx.x / 16, rr = threadIdx.x % 16;
         const int orow = down_tile * 16 + rr;
-        float ys = 0.f;
-        for (int kt = 0; kt < KTf; ++kt) ys += acc[(size_t)(0 * KTf + kt) * 128 + rr * 8 + t];
-        float v = ys * a.tscale[E * 3 + 2] * hinv[t * (k + 1) + k];
+        float v = (acc[rr * 8 + t] + acc[128 + rr * 8 + t]) * tss[E * 3 + 2] * hinv[t * (k + 1) + k];
         for (int j = 0; j < k; ++j) {
             const int e = sel[t * 8 + j];
-            int q = 0;
-            while (act[q] != e) ++q;
-            int p = 0;
-            while (act_pairs[q * 2 + p].t != t) ++p;
-            float y = 0.f;
-            for (int kt = 0; kt < KTf; ++kt) y += acc[(size_t)((q + 1) * KTf + kt) * 128 + rr * 8 + p];
-            v += wsel[t * 8 + j] * (y * a.tscale[e * 3 + 2] * hinv[t * (k + 1) + j]);
+            const int qp = cmap[t * 8 + j];
+            const float* aq = acc + (size_t)(qp >> 2) * 256 + rr * 8 + (qp & 3);
+            const float y = aq[0] + aq[128];
+            v += wsel[t * 8 + j] * (y * tss[e * 3 + 2] * hinv[t * (k + 1) + j]);
         }
         __nv_bfloat16 o = __float2bfloat16_rn(v);
         if (a.residual != nullptr) {
@@ -462,34 +499,40 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
 }  // namespace
 
 // Shared-memory plan of the fused kernel; 0 if it does not fit.
-size_t fused_smem_bytes(const Shape& s, int T, int n_sms, int* n_slots_out, int offs[8]) {
+size_t fused_smem_bytes(const Shape& s, int T, int n_sms, int* n_slots_out, int offs[10]) {
     if (T < 1 || T > kFusedMaxT || s.n_shared != 1 || s.k > 8 || s.E > 256) return 0;
+    if (s.d > 8 * kFThreads || s.f > 32 * 32) return 0;   // register staging of x and h rows
     const int S = s.wfmt == 0 ? 64 : 128;
     const int KTd = s.d / 128, KTf = s.f / 128;
     const size_t unit = (size_t)4 * KTd * (512 + S);
     const size_t dslab = (size_t)2 * KTf * (512 + S);
     const int max_active = T * s.k;
     const int units = max_active * (s.f / 16);
-    int n_slots = (units + n_sms - 1) / n_sms;
-    if (n_slots < 2) n_slots = 2;   // slot 0 holds the router slice, slot 1 a shared unit in P0
-    if (n_slots > 3) n_slots = 3;
     if ((size_t)2 * s.d * 4 > unit) return 0;
     if ((s.E + n_sms - 1) / n_sms > 2) return 0;
     if (s.d / 16 > n_sms || s.f / 16 > n_sms) return 0;
-    const size_t red = (size_t)kFWarps * 2 * 32 * 4 * 4;
-    const size_t accb = (size_t)(max_active + 1) * KTf * 128 * 4;
+    const size_t red = (size_t)kFWarps * 2 * 128 * 4;
+    const size_t accb = (size_t)(max_active + 1) * 2 * 128 * 4;
+    int n_rs = (units + n_sms - 1) / n_sms;                 // routed slots for one wave
+    if (n_rs > 3) n_rs = 3;
     size_t off = 0;
     auto take = [&](size_t n) { size_t o = off; off = (off + n + 127) / 128 * 128; return o; };
-    offs[0] = (int)take((size_t)n_slots * unit);
-    offs[1] = (int)unit;
-    offs[2] = (int)take((size_t)(max_active + 1) * dslab);
-    offs[3] = (int)dslab;
-    offs[4] = (int)take(red > accb ? red : accb);
-    offs[5] = (int)take((size_t)T * s.d * 2);
-    offs[6] = (int)take((size_t)T * (s.k + 1) * s.f * 2);
-    offs[7] = (int)take(4096);
-    if (off > kFusedDynSmemMax) return 0;
-    *n_slots_out = n_slots;
+    for (;; --n_rs) {
+        if (n_rs < 1) return 0;
+        off = 0;
+        offs[0] = (int)take((size_t)(n_rs + 1) * unit);     // + the shared expert's unit
+        offs[1] = (int)unit;
+        offs[2] = (int)take((size_t)(max_active + 1) * dslab);
+        offs[3] = (int)dslab;
+        offs[4] = (int)take(red > accb ? red : accb);
+        offs[5] = (int)take((size_t)T * s.d * 2);
+        offs[6] = (int)take((size_t)T * (s.k + 1) * s.f * 2);
+        offs[7] = (int)take(4096);
+        offs[8] = (int)take((size_t)T * s.d * 2);
+        offs[9] = (int)take(tscale_bytes(s));
+        if (off <= kFusedDynSmemMax) break;
+    }
+    *n_slots_out = n_rs + 1;
     return off;
 }
 
@@ -512,7 +555,7 @@ cudaError_t prepare_decode_fused() {
 cudaError_t launch_decode_fused(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
                                 __nv_bfloat16* out, const __nv_bfloat16* residual, const FusedScratch& fs,
                                 int n_sms, cudaStream_t st) {
-    int n_slots = 0, offs[8];
+    int n_slots = 0, offs[10];
     const size_t smem = fused_smem_bytes(s, T, n_sms, &n_slots, offs);
     if (smem == 0) return cudaErrorInvalidValue;
     FusedArgs a;
@@ -533,8 +576,7 @@ cudaError_t launch_decode_fused(const Shape& s, const LayerDev& L, const __nv_bf
     a.k = s.k;
     a.logits = fs.logits;
     a.h = fs.h;
-    a.bar_count = fs.bar + 0;
-    a.bar_gen = fs.bar + 32;
+    a.bar_count = reinterpret_cast<unsigned long long*>(fs.bar);
     a.status = fs.status;
     a.n_slots = n_slots;
     a.off_slots = offs[0];
@@ -545,6 +587,9 @@ cudaError_t launch_decode_fused(const Shape& s, const LayerDev& L, const __nv_bf
     a.off_x16 = offs[5];
     a.off_h16 = offs[6];
     a.off_misc = offs[7];
+    a.off_xbf = offs[8];
+    a.off_ts = offs[9];
+    a.ts_bytes = (int)tscale_bytes(s);
     void (*kern)(FusedArgs) = s.wfmt == 0 ? decode_fused_kernel<0> : decode_fused_kernel<1>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(n_sms);

@@ -40,6 +40,10 @@ struct Shape {
     int positions(int T) const { return T * (k + n_shared); }
 };
 
+// Device bytes of a layer's tensor-scale array ([n_slots][3] fp32), padded to
+// 256 bytes so that it can be bulk-copied whole.
+inline size_t tscale_bytes(const Shape& s) { return ((size_t)s.n_slots() * 12 + 255) / 256 * 256; }
+
 // Per-handle scratch for one forward (sized for max_tokens).
 struct Workspace {
     float* logits;        // [Tm][E]
@@ -92,7 +96,7 @@ cudaError_t launch_down(const Shape& s, const LayerDev& L, int T, const Workspac
 
 // decode_fused.cu: one persistent launch per layer for T <= kFusedMaxT
 constexpr int kFusedMaxT = 2;
-size_t fused_smem_bytes(const Shape& s, int T, int n_sms, int* n_slots_out, int offs[8]);
+size_t fused_smem_bytes(const Shape& s, int T, int n_sms, int* n_slots_out, int offs[10]);
 cudaError_t prepare_decode_fused();   // once per device: shared-memory opt-in
 cudaError_t launch_decode_fused(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
                                 __nv_bfloat16* out, const __nv_bfloat16* residual, const FusedScratch& fs,

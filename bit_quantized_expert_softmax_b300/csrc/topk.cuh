@@ -32,34 +32,34 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ Lrow, int E,
     }
     if (status != nullptr && __any_sync(0xffffffffu, bad) && lane == 0)
         atomicOr(status, kStatusNonFiniteLogit);
+    // Order-preserving unsigned key of a float (-0.0 folded onto +0.0 so that
+    // equal values compare equal); the warp max of keys picks the value, the
+    // warp min of indices among lanes holding it picks the lower expert.
+    uint32_t key[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t b = __float_as_uint(v[i] + 0.0f);
+        key[i] = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    }
     uint32_t taken = 0;
     float sel_v[8];
     int sel_i[8];
     for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
+        uint32_t bk = 0u;
         int bi = 0x7fffffff;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            if (i < n && !((taken >> i) & 1u)) {
-                int e = i * 32 + lane;
-                if (v[i] > bv || (v[i] == bv && e < bi)) {
-                    bv = v[i];
-                    bi = e;
-                }
+            if (i < n && !((taken >> i) & 1u) && (key[i] > bk || bi == 0x7fffffff)) {
+                bk = key[i];
+                bi = i * 32 + lane;
             }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        sel_v[j] = bv;
-        sel_i[j] = bi;
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        const int wi = (int)__reduce_min_sync(0xffffffffu, (bk == mk && bi != 0x7fffffff) ? (uint32_t)bi : 0xffffffffu);
+        if ((wi & 31) == lane) taken |= 1u << (wi >> 5);
+        const uint32_t wb = (mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk;
+        sel_v[j] = __uint_as_float(wb);
+        sel_i[j] = wi;
     }
     // renormalised softmax over the selected logits (sel_v[0] is the maximum)
     float sum = 0.f;
