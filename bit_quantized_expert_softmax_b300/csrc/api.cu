@@ -217,6 +217,10 @@ flint_status flint_moe_create(const flint_moe_config* cfg, flint_moe** out) {
         if (env != nullptr && env[0] == '0') h->fused = false;
     }
     if (h->fused && flint::prepare_decode_fused() != cudaSuccess) h->fused = false;
+    if (flint::prepare_router() != cudaSuccess) {
+        delete h;
+        return FLINT_ECUDA;
+    }
     h->layers.resize(cfg->n_layers);
     size_t total = 0;
     carve(h->s, nullptr, &total);
@@ -460,8 +464,8 @@ int flint_moe_forward_launches(const flint_moe* h, int T) {
     if (T == 0) return 0;
     int n_slots = 0, offs[10];
     if (h->fused && flint::fused_smem_bytes(h->s, T, h->n_sms, &n_slots, offs) != 0) return 1;
-    const int router = T <= flint::kSmallT ? 1 : 2 + 3;
-    const int down = T <= flint::kSmallT ? 1 : 2;
+    const int router = (T <= flint::kSmallT && h->s.d <= 2560) ? 1 : 2 + 3;
+    const int down = T <= flint::kFuseCombineT ? 1 : 2;
     return router + 1 + down;
 }
 

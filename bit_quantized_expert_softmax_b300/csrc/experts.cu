@@ -344,7 +344,7 @@ ExpertArgs make_args(const Shape& s, const LayerDev& L, int T, const Workspace& 
     a.ws = ws;
     a.out = nullptr;
     a.residual = nullptr;
-    a.fuse_combine = (T <= kSmallT) ? 1 : 0;
+    a.fuse_combine = (T <= kFuseCombineT) ? 1 : 0;
     return a;
 }
 

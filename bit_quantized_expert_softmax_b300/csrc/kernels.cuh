@@ -77,9 +77,11 @@ struct FusedScratch {
 
 constexpr int kCounters = 1024;
 constexpr int kBucketChunk = 2048;      // assignments per bucketing CTA
-constexpr int kSmallT = 64;             // fused decode path up to this many tokens
+constexpr int kSmallT = 64;             // fused router (logits + top-k + bucketing) up to this many tokens
+constexpr int kFuseCombineT = 8;        // combine in the down kernel's last CTA up to this many tokens
 
 // router.cu
+cudaError_t prepare_router();   // once per device: shared-memory opt-in of the fused router
 cudaError_t launch_router(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
                           const Workspace& ws, cudaStream_t st, int* n_launch);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int* idx, float* w,

@@ -16,7 +16,6 @@ namespace flint {
 namespace {
 
 constexpr int kRouterThreads = 256;   // 8 warps: 2 experts x 4 K-quarters
-constexpr int kMaxKIt = 8;            // d <= 4096 for the register-resident router row
 
 // ---------------------------------------------------------------------------
 // fp16 staging of one token: per-token power-of-two scale, fragment order
@@ -115,24 +114,62 @@ __device__ void bucket_count_block(const int* __restrict__ sel, int a0, int a1, 
     }
 }
 
-// Offsets, active-slot list and metadata from total counts (one CTA).
+// Exclusive prefix sum of one int per thread over a block of 256 threads;
+// *total receives the sum of all. wsum: shared scratch of 8 ints.
+__device__ __forceinline__ int block_exclusive_scan_256(int v, int* wsum, int* total) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < 8 ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < 8) wsum[lane] = w;
+    }
+    __syncthreads();
+    const int base = warp > 0 ? wsum[warp - 1] : 0;
+    *total = wsum[7];
+    __syncthreads();
+    return base + x - v;
+}
+
+// Offsets, active-slot list and metadata from total counts, by one CTA of 256
+// threads (thread e owns expert e): one block scan over (count | nonempty<<20)
+// gives both the offset and the active-slot index of every expert.
 __device__ void bucket_finish_block(const int* cnt /* smem [E] */, int E, int T, int k, int n_shared,
                                     int* offs_smem /* smem [E+1] */, int* __restrict__ offsets,
                                     int* __restrict__ slot_expert, int* __restrict__ slot_off,
                                     int* __restrict__ slot_cnt, int* __restrict__ meta) {
-    if (threadIdx.x == 0) {
-        int run = 0, ns = 0;
-        for (int e = 0; e < E; ++e) {
-            offs_smem[e] = run;
-            if (cnt[e] > 0) {
-                slot_expert[ns] = e;
-                slot_off[ns] = run;
-                slot_cnt[ns] = cnt[e];
-                ++ns;
-            }
-            run += cnt[e];
+    __shared__ int wsum[8];
+    const int e = threadIdx.x;
+    const int c = e < E ? cnt[e] : 0;
+    const int packed = c | ((c > 0 ? 1 : 0) << 20);
+    int total = 0;
+    const int excl = block_exclusive_scan_256(packed, wsum, &total);
+    const int off = excl & 0xfffff, slot = excl >> 20;
+    if (e < E) {
+        offs_smem[e] = off;
+        offsets[e] = off;
+        if (c > 0) {
+            slot_expert[slot] = e;
+            slot_off[slot] = off;
+            slot_cnt[slot] = c;
         }
-        offs_smem[E] = run;
+    }
+    if (threadIdx.x == 0) {
+        const int n_assign = total & 0xfffff;
+        int ns = total >> 20;
+        offs_smem[E] = n_assign;
+        offsets[E] = n_assign;
         if (n_shared) {
             slot_expert[ns] = E;
             slot_off[ns] = T * k;
@@ -143,7 +180,6 @@ __device__ void bucket_finish_block(const int* cnt /* smem [E] */, int E, int T,
         meta[1] = T;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = offs_smem[e];
 }
 
 struct RouterArgs {
@@ -160,67 +196,76 @@ struct RouterArgs {
 // grid = E/2 CTAs; warp w computes a quarter of the dot products of expert
 // 2*blockIdx + w/4.
 // ---------------------------------------------------------------------------
+constexpr int kTokGroup = 8;   // tokens per CTA (one warp per token)
+
+// grid = (E/2 expert pairs, ceil(T/8) token groups). Each CTA bulk-copies its
+// two router rows and its (up to) 8 hidden rows into shared memory; warp w
+// computes both experts' dot products for token w of the group over the full
+// K, with 4 consecutive elements per lane per 128-element chunk.
 __global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouterArgs a) {
-    __shared__ float part[8][kSmallT];
+    extern __shared__ __align__(128) uint8_t rsm[];   // [2][d] fp32 router rows, then [8][d] bf16 hidden rows
+    __shared__ uint64_t rbar;
     __shared__ float red[32];
     __shared__ int s_cnt[256];
     __shared__ int s_offs[257];
     __shared__ int s_wcnt[8 * 256];
     __shared__ int s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * 2 + (warp >> 2);
-    const int q = warp & 3;
     const int T = a.T, d = a.d;
-    const int n_it = d >> 7;   // 128-element chunks of the row
-
-    // router row chunks it = q, q+4, ... of expert e, 4 floats per lane
-    float4 wv[kMaxKIt / 4 * 4 / 4 > 0 ? kMaxKIt : 1];
-    int cnt_it = 0;
-#pragma unroll
-    for (int j = 0; j < kMaxKIt; ++j) {
-        int it = q + 4 * j;
-        if (it < n_it) {
-            wv[j] = *reinterpret_cast<const float4*>(a.wr + (size_t)e * d + it * 128 + lane * 4);
-            ++cnt_it;
-        }
+    const int e0 = blockIdx.x * 2;
+    const int t0 = blockIdx.y * kTokGroup;
+    const int nt = min(kTokGroup, T - t0);
+    const float* wsm = reinterpret_cast<const float*>(rsm);
+    const __nv_bfloat16* xsm = reinterpret_cast<const __nv_bfloat16*>(rsm + (size_t)2 * d * 4);
+    if (threadIdx.x == 0) {
+        mbar_init(&rbar, 1);
+        mbar_fence_init();
+        mbar_arrive_expect_tx(&rbar, (uint32_t)(2 * d * 4 + nt * d * 2));
+        bulk_g2s(rsm, a.wr + (size_t)e0 * d, (uint32_t)(2 * d * 4), &rbar);
+        bulk_g2s(rsm + (size_t)2 * d * 4, a.x + (size_t)t0 * d, (uint32_t)(nt * d * 2), &rbar);
     }
-    for (int t = 0; t < T; ++t) {
-        float acc = 0.f;
-        const __nv_bfloat16* xr = a.x + (size_t)t * d;
-#pragma unroll
-        for (int j = 0; j < kMaxKIt; ++j) {
-            if (j < cnt_it) {
-                int it = q + 4 * j;
-                uint2 raw = *reinterpret_cast<const uint2*>(xr + it * 128 + lane * 4);
-                __nv_bfloat162 p0 = *reinterpret_cast<__nv_bfloat162*>(&raw.x);
-                __nv_bfloat162 p1 = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
-                acc = fmaf(wv[j].x, __low2float(p0), acc);
-                acc = fmaf(wv[j].y, __high2float(p0), acc);
-                acc = fmaf(wv[j].z, __low2float(p1), acc);
-                acc = fmaf(wv[j].w, __high2float(p1), acc);
-            }
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) part[warp][t] = acc;
-    }
+    const float b0 = a.bias[e0], b1 = a.bias[e0 + 1];
     __syncthreads();
-    for (int i = threadIdx.x; i < 2 * T; i += blockDim.x) {
-        int ee = i / T, t = i % T;
-        int ex = blockIdx.x * 2 + ee;
-        float l = ((part[ee * 4 + 0][t] + part[ee * 4 + 1][t]) + part[ee * 4 + 2][t]) + part[ee * 4 + 3][t];
-        l += a.bias[ex];
-        a.ws.logits[(size_t)t * a.E + ex] = l;
+    const bool w_ok = mbar_wait_bounded(&rbar, 0, a.ws.status);
+    const bool ok = __syncthreads_and(w_ok ? 1 : 0) != 0;
+    if (ok && warp < nt) {
+        const __nv_bfloat16* xr = xsm + (size_t)warp * d;
+        float s0 = 0.f, s1 = 0.f;
+        for (int i = lane * 4; i < d; i += 128) {
+            const float4 w0 = *reinterpret_cast<const float4*>(wsm + i);
+            const float4 w1 = *reinterpret_cast<const float4*>(wsm + d + i);
+            const uint2 raw = *reinterpret_cast<const uint2*>(xr + i);
+            const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+            const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+            const float x0 = __low2float(p0), x1 = __high2float(p0), x2 = __low2float(p1), x3 = __high2float(p1);
+            s0 = fmaf(w0.x, x0, s0);
+            s0 = fmaf(w0.y, x1, s0);
+            s0 = fmaf(w0.z, x2, s0);
+            s0 = fmaf(w0.w, x3, s0);
+            s1 = fmaf(w1.x, x0, s1);
+            s1 = fmaf(w1.y, x1, s1);
+            s1 = fmaf(w1.z, x2, s1);
+            s1 = fmaf(w1.w, x3, s1);
+        }
+        s0 = warp_sum(s0);
+        s1 = warp_sum(s1);
+        if (lane == 0) {
+            a.ws.logits[(size_t)(t0 + warp) * a.E + e0] = s0 + b0;
+            a.ws.logits[(size_t)(t0 + warp) * a.E + e0 + 1] = s1 + b1;
+        }
     }
-    // fp16 staging of token rows owned by this CTA
-    for (int t = blockIdx.x; t < T; t += gridDim.x)
+    // fp16 staging: CTA (p, g) with p < 8 stages token 8g + p
+    if (blockIdx.x < kTokGroup && (int)blockIdx.x < nt) {
+        const int t = t0 + blockIdx.x;
         stage_token_block(a.x + (size_t)t * d, d, a.ws.x16 + (size_t)t * d, a.ws.xinv + t, red);
+    }
 
     // last CTA to arrive finishes the routing
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
         uint32_t prev = atomicAdd(&a.ws.counters[0], 1u);
-        s_last = (prev == gridDim.x - 1);
+        s_last = (prev == gridDim.x * gridDim.y - 1);
     }
     __syncthreads();
     if (!s_last) return;
@@ -399,11 +444,22 @@ cudaError_t launch_bucket(const Shape& s, const int* idx, int T, const Workspace
     return cudaGetLastError();
 }
 
+// Dynamic shared memory the fused router may use (set once per device).
+constexpr size_t kRouterDynSmemMax = 160 * 1024;
+
+cudaError_t prepare_router() {
+    const cudaError_t e = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kRouterDynSmemMax);
+    if (e != cudaSuccess) cudaGetLastError();
+    return e;
+}
+
 cudaError_t launch_router(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
                           const Workspace& ws, cudaStream_t st, int* n_launch) {
     RouterArgs a = make_args(s, L, x, T, ws);
-    if (T <= kSmallT) {
-        router_small_kernel<<<s.E / 2, kRouterThreads, 0, st>>>(a);
+    const size_t smem = (size_t)2 * s.d * 4 + (size_t)kTokGroup * s.d * 2;
+    if (T <= kSmallT && smem <= kRouterDynSmemMax) {
+        router_small_kernel<<<dim3(s.E / 2, (T + kTokGroup - 1) / kTokGroup), kRouterThreads, smem, st>>>(a);
         *n_launch += 1;
         return cudaGetLastError();
     }

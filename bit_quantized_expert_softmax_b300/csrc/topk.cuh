@@ -42,42 +42,39 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ Lrow, int E,
         key[i] = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
     }
     uint32_t taken = 0;
-    float sel_v[8];
-    int sel_i[8];
-    for (int j = 0; j < k; ++j) {
-        uint32_t bk = 0u;
-        int bi = 0x7fffffff;
+    float my_v = 0.f;   // lane j < k ends with selection j
+    int my_i = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (i < n && !((taken >> i) & 1u) && (key[i] > bk || bi == 0x7fffffff)) {
-                bk = key[i];
-                bi = i * 32 + lane;
+    for (int j = 0; j < 8; ++j) {
+        if (j < k) {
+            uint32_t bk = 0u;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i < n && !((taken >> i) & 1u) && (key[i] > bk || bi == 0x7fffffff)) {
+                    bk = key[i];
+                    bi = i * 32 + lane;
+                }
+            }
+            const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+            const int wi =
+                (int)__reduce_min_sync(0xffffffffu, (bk == mk && bi != 0x7fffffff) ? (uint32_t)bi : 0xffffffffu);
+            if ((wi & 31) == lane) taken |= 1u << (wi >> 5);
+            if (lane == j) {
+                my_v = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk);
+                my_i = wi;
             }
         }
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-        const int wi = (int)__reduce_min_sync(0xffffffffu, (bk == mk && bi != 0x7fffffff) ? (uint32_t)bi : 0xffffffffu);
-        if ((wi & 31) == lane) taken |= 1u << (wi >> 5);
-        const uint32_t wb = (mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk;
-        sel_v[j] = __uint_as_float(wb);
-        sel_i[j] = wi;
     }
-    // renormalised softmax over the selected logits (sel_v[0] is the maximum)
-    float sum = 0.f;
-    float ex[8];
-    for (int j = 0; j < k; ++j) {
-        ex[j] = expf(sel_v[j] - sel_v[0]);
-        sum += ex[j];
-    }
+    // renormalised softmax over the selected logits (selection 0 is the maximum)
+    const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
+    const float ex = lane < k ? expf(my_v - v0) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     if (lane < k) {
-        float e = 0.f;
-        int id = 0;
-        for (int j = 0; j < k; ++j)
-            if (j == lane) {
-                e = ex[j];
-                id = sel_i[j];
-            }
-        idx_out[lane] = id;
-        if (w_out != nullptr) w_out[lane] = e / sum;
+        idx_out[lane] = my_i;
+        if (w_out != nullptr) w_out[lane] = ex / sum;
     }
 }
 
