@@ -26,6 +26,7 @@ struct flint_moe {
     uint64_t launches = 0;
     int n_sms = 0;
     bool fused = true;           // single-launch decode for T <= kFusedMaxT
+    bool prefill = true;         // tensor-core (tcgen05) kernels for large T
     // phase events of profiled forwards: 4 per forward
     std::vector<cudaEvent_t> prof_events;
     int prof_max = 0, prof_n = 0;
@@ -56,6 +57,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 void free_layer(LayerDev& L) {
+    cudaFree(L.router_hi);
+    cudaFree(L.router_lo);
     cudaFree(L.router);
     cudaFree(L.bias);
     cudaFree(L.codes);
@@ -217,6 +220,11 @@ flint_status flint_moe_create(const flint_moe_config* cfg, flint_moe** out) {
         if (env != nullptr && env[0] == '0') h->fused = false;
     }
     if (h->fused && flint::prepare_decode_fused() != cudaSuccess) h->fused = false;
+    {
+        const char* env = getenv("FLINT_MOE_TCGEN05_PREFILL");
+        if (env != nullptr && env[0] == '0') h->prefill = false;
+    }
+    if (h->prefill && flint::prepare_prefill() != cudaSuccess) h->prefill = false;
     if (flint::prepare_router() != cudaSuccess) {
         delete h;
         return FLINT_ECUDA;
@@ -274,13 +282,15 @@ flint_status flint_moe_load_weights(flint_moe* h, int layer, const flint_moe_wei
         if (e == cudaSuccess) e = cudaMalloc(&L.bias, (size_t)s.E * sizeof(float));
         if (e == cudaSuccess) e = cudaMalloc(&L.codes, n_codes);
         if (e == cudaSuccess) e = cudaMalloc(&L.scales, n_scales);
+        if (e == cudaSuccess) e = cudaMalloc(&L.router_hi, (size_t)s.E * s.d * 2);
+        if (e == cudaSuccess) e = cudaMalloc(&L.router_lo, (size_t)s.E * s.d * 2);
         if (e == cudaSuccess) e = cudaMalloc(&L.tscale, flint::tscale_bytes(s));
         if (e == cudaSuccess) e = cudaMemset(L.tscale, 0, flint::tscale_bytes(s));
         if (e != cudaSuccess) {
             free_layer(L);
             return cuda_status(e);
         }
-        h->weight_bytes += (size_t)s.E * s.d * 4 + (size_t)s.E * 4 + n_codes + n_scales + (size_t)n_slots * 12;
+        h->weight_bytes += (size_t)s.E * s.d * 8 + (size_t)s.E * 4 + n_codes + n_scales + flint::tscale_bytes(s);
     }
     L.loaded = false;
     uint8_t* stage = nullptr;
@@ -314,9 +324,13 @@ flint_status flint_moe_load_weights(flint_moe* h, int layer, const flint_moe_wei
                                             L.scales + mi * spm, R, K, s.wfmt, st);
         }
     }
+    if (e == cudaSuccess) e = flint::split_router(L.router, L.router_hi, L.router_lo, (size_t)s.E * s.d, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     cudaFree(stage);
     if (e != cudaSuccess) return cuda_status(e);
+    L.umma_router = h->prefill && flint::router_umma_supported(s) &&
+                    flint::make_tmap_bf16(&L.tmap_router_hi, L.router_hi, s.E, s.d) &&
+                    flint::make_tmap_bf16(&L.tmap_router_lo, L.router_lo, s.E, s.d);
     L.loaded = true;
     return FLINT_OK;
 }
@@ -458,6 +472,14 @@ size_t flint_moe_device_bytes(const flint_moe* h) {
 }
 
 uint64_t flint_moe_launch_count(const flint_moe* h) { return h ? h->launches : 0; }
+
+int flint_moe_tensor_core_plan(const flint_moe* h, int layer, int T) {
+    if (h == nullptr || layer < 0 || layer >= h->n_layers || T < 0 || T > h->s.max_tokens) return -1;
+    const LayerDev& L = h->layers[layer];
+    int plan = 0;
+    if (T > flint::kSmallT && L.loaded && L.umma_router) plan |= 1;
+    return plan;
+}
 
 int flint_moe_forward_launches(const flint_moe* h, int T) {
     if (h == nullptr || T < 0 || T > h->s.max_tokens) return -1;

@@ -1,6 +1,7 @@
 // Internal interface between the C ABI (api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -27,6 +28,10 @@ struct LayerDev {
     uint8_t* codes = nullptr;       // [n_slots][3][f*d/2] tiled
     uint8_t* scales = nullptr;      // [n_slots][3][scale bytes] tiled
     float* tscale = nullptr;        // [n_slots][3]
+    __nv_bfloat16* router_hi = nullptr;   // [E][d] bf16(W_r)
+    __nv_bfloat16* router_lo = nullptr;   // [E][d] bf16(W_r - bf16(W_r))
+    CUtensorMap tmap_router_hi, tmap_router_lo;   // 128x64 swizzled boxes of the two
+    bool umma_router = false;
     bool loaded = false;
 };
 
@@ -103,6 +108,14 @@ cudaError_t prepare_decode_fused();   // once per device: shared-memory opt-in
 cudaError_t launch_decode_fused(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
                                 __nv_bfloat16* out, const __nv_bfloat16* residual, const FusedScratch& fs,
                                 int n_sms, cudaStream_t st);
+
+// prefill_fp4.cu: tensor-core kernels for large T
+cudaError_t prepare_prefill();   // once per device: shared-memory opt-in
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rows, int cols);
+bool router_umma_supported(const Shape& s);
+cudaError_t split_router(const float* w, __nv_bfloat16* hi, __nv_bfloat16* lo, size_t n, cudaStream_t st);
+cudaError_t launch_router_umma(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T, float* logits,
+                               uint32_t* status, cudaStream_t st);
 
 // repack.cu
 cudaError_t launch_repack_matrix(const uint8_t* codes_src, const uint8_t* scales_src,

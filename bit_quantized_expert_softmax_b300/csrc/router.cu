@@ -463,8 +463,13 @@ cudaError_t launch_router(const Shape& s, const LayerDev& L, const __nv_bfloat16
         *n_launch += 1;
         return cudaGetLastError();
     }
-    dim3 g1((T + kLTok - 1) / kLTok, (s.E + kLExp - 1) / kLExp);
-    router_logits_tiled<<<g1, 256, 0, st>>>(a);
+    if (L.umma_router) {
+        const cudaError_t e = launch_router_umma(s, L, x, T, ws.logits, ws.status, st);
+        if (e != cudaSuccess) return e;
+    } else {
+        dim3 g1((T + kLTok - 1) / kLTok, (s.E + kLExp - 1) / kLExp);
+        router_logits_tiled<<<g1, 256, 0, st>>>(a);
+    }
     token_prep_kernel<<<(T + 7) / 8, 256, 0, st>>>(a);
     *n_launch += 2;
     return launch_bucket(s, ws.idx, T, ws, st, n_launch);

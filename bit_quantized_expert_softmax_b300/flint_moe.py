@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
             "flint_moe_device_bytes": (ctypes.c_size_t, [_P]),
             "flint_moe_launch_count": (ctypes.c_uint64, [_P]),
             "flint_moe_forward_launches": (_I, [_P, _I]),
+            "flint_moe_tensor_core_plan": (_I, [_P, _I, _I]),
             "flint_moe_profile_begin": (_I, [_P, _I]),
             "flint_moe_profile_end": (_I, [_P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_I)]),
         }
@@ -187,6 +188,10 @@ def flint_moe_launch_count(h: int) -> int:
 
 def flint_moe_forward_launches(h: int, T: int) -> int:
     return int(lib().flint_moe_forward_launches(h, T))
+
+
+def flint_moe_tensor_core_plan(h: int, layer: int, T: int) -> int:
+    return int(lib().flint_moe_tensor_core_plan(h, layer, T))
 
 
 def flint_moe_profile_begin(h: int, max_forwards: int) -> None:

@@ -182,6 +182,13 @@ FLINT_API flint_status flint_moe_dequant(flint_moe* h, int layer, int expert, in
 /* Bytes of device memory the handle holds (weights + workspace). */
 FLINT_API size_t flint_moe_device_bytes(const flint_moe* h);
 
+/* Which 5th-generation tensor-core (tcgen05) kernels a single-layer forward
+ * of T tokens on this loaded layer uses: bit 0 = router logits GEMM, bit 1 =
+ * block-scaled FP4 expert GEMMs. 0 when neither; -1 on bad arguments.
+ * Setting FLINT_MOE_TCGEN05_PREFILL=0 before flint_moe_create turns these
+ * kernels off for the handle (the mma.sync and CUDA-core paths remain). */
+FLINT_API int flint_moe_tensor_core_plan(const flint_moe* h, int layer, int T);
+
 /* ---- bucketing for callers that cannot allocate ---------------------------
  * The Flint blog has no counterpart to this entry point: it serves callers,
  * not the method. It computes what flint_moe_bucket computes, offsets_dev[E+1]

@@ -154,6 +154,8 @@ def test_router_parity(fm, n, T):
     fm.flint_moe_router(m.h, 0, x, T, logits, idx, w)
     torch.cuda.synchronize()
     assert fm.flint_moe_status(m.h) == fm.FLINT_OK
+    if T > 64:   # large T: the logits come from the tcgen05 (bf16 hi + lo) GEMM
+        assert fm.flint_moe_tensor_core_plan(m.h, 0, T) & 1
     ref_L = M.router_logits(F.bf16_array(bits), L.router, L.router_bias)
     assert_logits_close(logits.cpu().numpy(), ref_L)
     ref_sel = M.select_topk(ref_L.astype(np.float32), cfg.top_k)
