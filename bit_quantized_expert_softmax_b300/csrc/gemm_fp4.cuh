@@ -1,0 +1,208 @@
+// Persistent block-scaled FP4 GEMM on the 5th-generation tensor cores
+// (tcgen05.mma kind::mxf4nvf4, scale_vec::4X): D[128 x 128] (fp32, TMEM)
+// += A[128 x K] . B[128 x K]^T with A and B packed E2M1 and one UE4M3 scale
+// per 16 elements along K.
+//
+// Operands are stored in global memory already in the shared-memory image the
+// MMA reads ("swizzled tiles"): a tile is 128 rows x 256 K-elements, 128 bytes
+// per row, rows 128 bytes apart, the 16-byte chunk c of row r stored at chunk
+// c ^ (r % 8) (the 128-byte swizzle). Its scale factors are 128 rows x 16
+// bytes, row-major. One 1-D bulk copy per tile moves it into shared memory.
+//
+// Warp roles of a CTA (320 threads, one CTA per SM):
+//   warp 0      producer: bulk-copies A, B and their scales into a 4-stage ring
+//   warp 1      allocates tensor memory; one thread issues the MMAs
+//               (M=128, N=128, K=64 each; 4 per stage) into one of two
+//               accumulators
+//   warps 2..5  scale writers: shared memory -> tensor memory (tcgen05.st),
+//               one row (lane) per thread
+//   warps 6..9  epilogue: tensor memory -> registers -> the problem's store
+// Tensor memory columns: accumulators [0,128) and [128,256); per stage s the
+// A scales at 256+32s..+15 and the B scales at 256+32s+16..+31.
+//
+// Scale layout in tensor memory (per MMA of K = 64, 4 columns): lane m0 of
+// every 32-lane quadrant, column m1 (0..3) holds the four UE4M3 scales (one
+// per 16 K-elements, lowest K first) of tile row m0 + 32*m1; the four lane
+// quadrants hold the same data. The MMA is given the first of its 4 columns.
+#pragma once
+
+#include "umma.cuh"
+
+namespace flint {
+
+constexpr int kGM = 128, kGN = 128, kGK = 256;
+constexpr int kGTile = kGM * kGK / 2;          // 16 KiB of packed E2M1
+constexpr int kGSf = kGM * kGK / 16;           // 2 KiB of UE4M3 scales
+constexpr int kGStage = 2 * kGTile + 2 * kGSf; // A, B, scales of A, scales of B
+constexpr int kGStages = 4;
+constexpr int kGSmem = kGStages * kGStage + 1024;
+constexpr int kGThreads = 320;
+
+// One output tile of a problem.
+struct Fp4Item {
+    const uint8_t* a;    // first k-tile of A (k-tiles of one row tile are contiguous)
+    const uint8_t* asf;
+    const uint8_t* b;
+    const uint8_t* bsf;
+    int kt;              // number of k-tiles
+    int m, n, aux;       // problem-defined (row tile, column tile, group)
+};
+
+// Byte offset of element pair byte `j` (0..127) of row `r` (0..127) inside a
+// swizzled tile.
+__host__ __device__ __forceinline__ int swz_offset(int r, int j) {
+    return r * 128 + ((((j >> 4) ^ (r & 7)) & 7) << 4) + (j & 15);
+}
+
+template <class P>
+__global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, uint32_t* status) {
+    extern __shared__ uint8_t graw[];
+    __shared__ __align__(8) uint64_t full[kGStages], sfready[kGStages], empty[kGStages], accfull[2], accempty[2];
+    __shared__ uint32_t tmem_base;
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(graw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&sfready[s], 4);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accfull[b], 1);
+            mbar_init(&accempty[b], 4);
+        }
+        mbar_fence_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    const int n_items = prob.n_items();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t kcount = 0;
+            bool ok = true;
+            for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+                Fp4Item w;
+                if (!prob.item(i, w)) continue;
+                for (int kt = 0; kt < w.kt; ++kt, ++kcount) {
+                    const int s = kcount % kGStages;
+                    const uint32_t use = kcount / kGStages;
+                    if (use > 0 && !mbar_wait_bounded(&empty[s], (use - 1) & 1, status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = sm + s * kGStage;
+                    mbar_arrive_expect_tx(&full[s], kGStage);
+                    bulk_g2s(st, w.a + (size_t)kt * kGTile, kGTile, &full[s]);
+                    bulk_g2s(st + kGTile, w.b + (size_t)kt * kGTile, kGTile, &full[s]);
+                    bulk_g2s(st + 2 * kGTile, w.asf + (size_t)kt * kGSf, kGSf, &full[s]);
+                    bulk_g2s(st + 2 * kGTile + kGSf, w.bsf + (size_t)kt * kGSf, kGSf, &full[s]);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_nvfp4_f32(kGM, kGN);
+            uint32_t kcount = 0, n_done = 0;
+            bool ok = true;
+            for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+                Fp4Item w;
+                if (!prob.item(i, w)) continue;
+                const uint32_t buf = n_done & 1;
+                if (n_done >= 2 && !mbar_wait_bounded(&accempty[buf], ((n_done >> 1) - 1) & 1, status)) break;
+                tc_fence_after();
+                const uint32_t acc = tmem + buf * kGN;
+                for (int kt = 0; kt < w.kt; ++kt, ++kcount) {
+                    const int s = kcount % kGStages;
+                    const uint32_t use = kcount / kGStages;
+                    if (!mbar_wait_bounded(&sfready[s], use & 1, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t* st = sm + s * kGStage;
+                    const uint64_t da = sdesc_kmajor_sw128(st);
+                    const uint64_t db = sdesc_kmajor_sw128(st + kGTile);
+                    const uint32_t sfa = tmem + 256 + 32 * s, sfb = sfa + 16;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)   // 64 E2M1 = 32 bytes = 2 descriptor units per MMA
+                        umma_nvfp4(acc, da + 2 * j, db + 2 * j, idesc, sfa + 4 * j, sfb + 4 * j, (kt | j) != 0);
+                    umma_commit(&empty[s]);
+                }
+                umma_commit(&accfull[buf]);
+                ++n_done;
+            }
+        }
+    } else if (warp < 6) {
+        // scale writers: every quadrant writes the same 32 x 16-byte image:
+        // thread (quadrant, lane m0) stores rows m0, m0+32, m0+64, m0+96
+        const int quad = warp & 3;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        uint32_t kcount = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+            Fp4Item w;
+            if (!prob.item(i, w)) continue;
+            for (int kt = 0; kt < w.kt; ++kt, ++kcount) {
+                const int s = kcount % kGStages;
+                const uint32_t use = kcount / kGStages;
+                const bool got = mbar_wait_bounded(&full[s], use & 1, status);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* st = sm + s * kGStage;
+#pragma unroll
+                for (int op = 0; op < 2; ++op) {
+                    const uint8_t* sf = st + 2 * kGTile + op * kGSf;
+                    uint4 r[4];
+#pragma unroll
+                    for (int m1 = 0; m1 < 4; ++m1) r[m1] = *reinterpret_cast<const uint4*>(sf + (lane + 32 * m1) * 16);
+                    const uint32_t col = tmem + lane_base + 256 + 32 * s + 16 * op;
+                    // MMA j (K elements 64j..64j+63) reads word j of each row
+                    tmem_st4(col + 0, r[0].x, r[1].x, r[2].x, r[3].x);
+                    tmem_st4(col + 4, r[0].y, r[1].y, r[2].y, r[3].y);
+                    tmem_st4(col + 8, r[0].z, r[1].z, r[2].z, r[3].z);
+                    tmem_st4(col + 12, r[0].w, r[1].w, r[2].w, r[3].w);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sfready[s]);
+            }
+        }
+    } else {
+        // epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        uint32_t n_done = 0;
+        for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+            Fp4Item w;
+            if (!prob.item(i, w)) continue;
+            const uint32_t buf = n_done & 1;
+            const bool got = mbar_wait_bounded(&accfull[buf], (n_done >> 1) & 1, status);
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc_fence_after();
+            prob.epilogue(w, tmem + lane_base + buf * kGN, row);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&accempty[buf]);
+            ++n_done;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace flint

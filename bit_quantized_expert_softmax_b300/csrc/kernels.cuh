@@ -117,6 +117,11 @@ cudaError_t split_router(const float* w, __nv_bfloat16* hi, __nv_bfloat16* lo, s
 cudaError_t launch_router_umma(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T, float* logits,
                                uint32_t* status, cudaStream_t st);
 
+// gemm_fp4.cu: swizzled-tile packing for the block-scaled FP4 GEMM
+cudaError_t pack_fp4_tiles(const uint8_t* codes, const uint8_t* scales, uint8_t* tiles, uint8_t* sf, int R, int K,
+                           cudaStream_t st);
+cudaError_t prepare_gemm_fp4();
+
 // repack.cu
 cudaError_t launch_repack_matrix(const uint8_t* codes_src, const uint8_t* scales_src,
                                  uint8_t* codes_dst, uint8_t* scales_dst, int R, int K, int wfmt,

@@ -73,9 +73,38 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
+// Instruction descriptor of the block-scaled FP4 MMA (kind::mxf4nvf4 with
+// scale_vec::4X): A and B packed E2M1, K-major, one UE4M3 scale per 16
+// elements along K, fp32 accumulator, K = 64 per instruction.
+__host__ __device__ constexpr uint32_t idesc_nvfp4_f32(int M, int N) {
+    return (1u << 7)                      // A format: E2M1
+           | (1u << 10)                   // B format: E2M1
+           | ((uint32_t)(N >> 3) << 17)   // N / 8
+           | (0u << 23)                   // scale format: UE4M3
+           | ((uint32_t)(M >> 7) << 27);  // M / 128
+}
+
+// 32 lanes x 32 bits, 4 consecutive columns: each thread stores its lane's 4 words.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
+                 "r"(v2), "r"(v3)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // MMA issue and completion
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void umma_nvfp4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+            "r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
     asm volatile(

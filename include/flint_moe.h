@@ -189,6 +189,18 @@ FLINT_API size_t flint_moe_device_bytes(const flint_moe* h);
  * kernels off for the handle (the mma.sync and CUDA-core paths remain). */
 FLINT_API int flint_moe_tensor_core_plan(const flint_moe* h, int layer, int T);
 
+/* Block-scaled FP4 matrix product on the 5th-generation tensor cores, through
+ * the same kernel the large-T expert projections use: d_dev[M][N] (fp32) =
+ * A . B^T with A [M][K] and B [N][K] in canonical NVFP4 layout (codes
+ * [rows][K/2], element 2i in the low nibble; E4M3 scales [rows][K/16]; no
+ * tensor scale), all device pointers, 16-byte aligned. M and N multiples of
+ * 128, K a multiple of 256. Synchronous; allocates and frees temporary device
+ * memory for the packed tiles. Errors: FLINT_EINVAL (sizes, NULL),
+ * FLINT_ENOMEM, FLINT_ECUDA, FLINT_ETIMEOUT (a bounded device wait gave up). */
+FLINT_API flint_status flint_moe_debug_fp4_gemm(const uint8_t* a_codes_dev, const uint8_t* a_scales_dev,
+                                                const uint8_t* b_codes_dev, const uint8_t* b_scales_dev, int M,
+                                                int N, int K, float* d_dev, void* stream);
+
 /* ---- bucketing for callers that cannot allocate ---------------------------
  * The Flint blog has no counterpart to this entry point: it serves callers,
  * not the method. It computes what flint_moe_bucket computes, offsets_dev[E+1]
