@@ -328,6 +328,35 @@ def test_act_quant_error_is_within_half_a_grid_step():
     assert np.all(err[small] <= 0.25 * S[small] * (1 + 1e-6) + 1e-12)
 
 
+def test_w4a4_expert_by_brute_force():
+    """The quantised-activation expert against a scalar evaluation on a tiny
+    case: exact sums (math.fsum) of the quantised operands, silu through
+    math.exp, and the bfloat16 rounding of h done by torch's float32 ->
+    bfloat16 conversion rather than the oracle's own rounding routine."""
+    import math
+
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(10)
+    f, d = 32, 48
+    wg = rng.standard_normal((f, d)) * 0.2
+    wu = rng.standard_normal((f, d)) * 0.2
+    wd = rng.standard_normal((d, f)) * 0.2
+    x = rng.standard_normal((3, d)).astype(np.float32)
+    got = M.expert_forward_w4a4(wg, wu, wd, x)
+    xq = M.quant_act_nvfp4(x)[3]
+    for t in range(3):
+        h = np.zeros(f, dtype=np.float32)
+        for i in range(f):
+            g = math.fsum(xq[t, j] * wg[i, j] for j in range(d))
+            u = math.fsum(xq[t, j] * wu[i, j] for j in range(d))
+            h[i] = np.float32(g / (1.0 + math.exp(-g)) * u)
+        hb = torch.from_numpy(h).to(torch.bfloat16).to(torch.float32).numpy()
+        hq = M.quant_act_nvfp4(hb[None, :])[3][0]
+        for o in range(d):
+            want = math.fsum(hq[i] * wd[o, i] for i in range(f))
+            assert abs(got[t, o] - want) <= 1e-12 * max(1.0, abs(want)), (t, o)
+
+
 # ---------------------------------------------------------------------------
 # the Flint shape against the numbers the blog prints
 # ---------------------------------------------------------------------------
