@@ -27,6 +27,9 @@ struct flint_moe {
     int n_sms = 0;
     bool fused = true;           // single-launch decode for T <= kFusedMaxT
     bool prefill = true;         // tensor-core (tcgen05) kernels for large T
+    bool fp4_experts = false;    // block-scaled FP4 expert GEMMs for T > kSmallT
+    void* pws = nullptr;         // their workspace (swizzled activation tiles, h, fp32 sums)
+    size_t pws_bytes = 0;
     // phase events of profiled forwards: 4 per forward
     std::vector<cudaEvent_t> prof_events;
     int prof_max = 0, prof_n = 0;
@@ -64,6 +67,7 @@ void free_layer(LayerDev& L) {
     cudaFree(L.codes);
     cudaFree(L.scales);
     cudaFree(L.tscale);
+    cudaFree(L.prefill);
     L = LayerDev{};
 }
 
@@ -167,6 +171,19 @@ cudaError_t run_layer(flint_moe* h, int layer, const __nv_bfloat16* x, int T, __
         h->launches += 1;
         return e;
     }
+    if (T > flint::kSmallT && h->fp4_experts && L.prefill != nullptr) {
+        prof_record(h, 0, st);
+        cudaError_t e = flint::launch_router(h->s, L, x, T, h->ws, st, &n, false);
+        prof_record(h, 1, st);
+        prof_record(h, 2, st);
+        if (e == cudaSuccess)
+            e = flint::launch_prefill_experts(h->s, L, x, T, h->ws, static_cast<uint8_t*>(h->pws), h->s.max_tokens,
+                                              out, residual, st, &n);
+        prof_record(h, 3, st);
+        if (h->prof_n < h->prof_max) ++h->prof_n;
+        h->launches += n;
+        return e;
+    }
     prof_record(h, 0, st);
     cudaError_t e = flint::launch_router(h->s, L, x, T, h->ws, st, &n);
     prof_record(h, 1, st);
@@ -225,6 +242,11 @@ flint_status flint_moe_create(const flint_moe_config* cfg, flint_moe** out) {
         if (env != nullptr && env[0] == '0') h->prefill = false;
     }
     if (h->prefill && flint::prepare_prefill() != cudaSuccess) h->prefill = false;
+    {
+        const char* env = getenv("FLINT_MOE_FP4_EXPERTS");
+        h->fp4_experts = h->prefill && !(env != nullptr && env[0] == '0') && cfg->max_tokens > flint::kSmallT &&
+                         flint::prefill_fp4_supported(h->s) && flint::prepare_prefill_fp4() == cudaSuccess;
+    }
     if (flint::prepare_router() != cudaSuccess) {
         delete h;
         return FLINT_ECUDA;
@@ -239,6 +261,17 @@ flint_status flint_moe_create(const flint_moe_config* cfg, flint_moe** out) {
     }
     h->ws_bytes = total;
     h->ws = carve(h->s, static_cast<char*>(h->ws_base), &total);
+    if (h->fp4_experts) {
+        h->pws_bytes = flint::prefill_workspace_bytes(h->s, cfg->max_tokens);
+        e = cudaMalloc(&h->pws, h->pws_bytes);
+        if (e == cudaSuccess) e = cudaMemset(h->pws, 0, h->pws_bytes);
+        if (e != cudaSuccess) {
+            cudaFree(h->pws);
+            cudaFree(h->ws_base);
+            delete h;
+            return cuda_status(e);
+        }
+    }
     e = cudaMemset(h->ws_base, 0, total);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->load_stream, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -286,11 +319,13 @@ flint_status flint_moe_load_weights(flint_moe* h, int layer, const flint_moe_wei
         if (e == cudaSuccess) e = cudaMalloc(&L.router_lo, (size_t)s.E * s.d * 2);
         if (e == cudaSuccess) e = cudaMalloc(&L.tscale, flint::tscale_bytes(s));
         if (e == cudaSuccess) e = cudaMemset(L.tscale, 0, flint::tscale_bytes(s));
+        if (e == cudaSuccess && h->fp4_experts) e = cudaMalloc(&L.prefill, flint::prefill_weight_bytes(s));
         if (e != cudaSuccess) {
             free_layer(L);
             return cuda_status(e);
         }
         h->weight_bytes += (size_t)s.E * s.d * 8 + (size_t)s.E * 4 + n_codes + n_scales + flint::tscale_bytes(s);
+        if (L.prefill != nullptr) h->weight_bytes += flint::prefill_weight_bytes(s);
     }
     L.loaded = false;
     uint8_t* stage = nullptr;
@@ -324,6 +359,8 @@ flint_status flint_moe_load_weights(flint_moe* h, int layer, const flint_moe_wei
                                             L.scales + mi * spm, R, K, s.wfmt, st);
         }
     }
+    if (e == cudaSuccess && L.prefill != nullptr)
+        e = flint::pack_prefill_weights(s, stage, stage + n_codes, L.prefill, st);
     if (e == cudaSuccess) e = flint::split_router(L.router, L.router_hi, L.router_lo, (size_t)s.E * s.d, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     cudaFree(stage);
@@ -379,6 +416,7 @@ void flint_moe_destroy(flint_moe* h) {
         for (auto& L : h->layers) free_layer(L);
         prof_free(h);
         cudaFree(h->ws_base);
+        cudaFree(h->pws);
         if (h->load_stream) cudaStreamDestroy(h->load_stream);
     }
     delete h;
@@ -468,7 +506,7 @@ flint_status flint_moe_dequant(flint_moe* h, int layer, int expert, int mat, flo
 
 size_t flint_moe_device_bytes(const flint_moe* h) {
     if (h == nullptr) return 0;
-    return h->ws_bytes + h->weight_bytes;
+    return h->ws_bytes + h->pws_bytes + h->weight_bytes;
 }
 
 uint64_t flint_moe_launch_count(const flint_moe* h) { return h ? h->launches : 0; }
@@ -478,6 +516,7 @@ int flint_moe_tensor_core_plan(const flint_moe* h, int layer, int T) {
     const LayerDev& L = h->layers[layer];
     int plan = 0;
     if (T > flint::kSmallT && L.loaded && L.umma_router) plan |= 1;
+    if (T > flint::kSmallT && L.loaded && h->fp4_experts && L.prefill != nullptr) plan |= 2;
     return plan;
 }
 
@@ -487,6 +526,7 @@ int flint_moe_forward_launches(const flint_moe* h, int T) {
     int n_slots = 0, offs[10];
     if (h->fused && flint::fused_smem_bytes(h->s, T, h->n_sms, &n_slots, offs) != 0) return 1;
     const int router = (T <= flint::kSmallT && h->s.d <= 2560) ? 1 : 2 + 3;
+    if (T > flint::kSmallT && h->fp4_experts) return router + 8;
     const int down = T <= flint::kFuseCombineT ? 1 : 2;
     return router + 1 + down;
 }

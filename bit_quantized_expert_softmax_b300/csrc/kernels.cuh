@@ -32,6 +32,7 @@ struct LayerDev {
     __nv_bfloat16* router_lo = nullptr;   // [E][d] bf16(W_r - bf16(W_r))
     CUtensorMap tmap_router_hi, tmap_router_lo;   // 128x64 swizzled boxes of the two
     bool umma_router = false;
+    uint8_t* prefill = nullptr;     // swizzled FP4 tiles of all experts (large-T path), or null
     bool loaded = false;
 };
 
@@ -88,7 +89,7 @@ constexpr int kFuseCombineT = 8;        // combine in the down kernel's last CTA
 // router.cu
 cudaError_t prepare_router();   // once per device: shared-memory opt-in of the fused router
 cudaError_t launch_router(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
-                          const Workspace& ws, cudaStream_t st, int* n_launch);
+                          const Workspace& ws, cudaStream_t st, int* n_launch, bool stage_x16 = true);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int* idx, float* w,
                         cudaStream_t st);
 cudaError_t launch_bucket(const Shape& s, const int* idx, int T, const Workspace& ws,
@@ -116,6 +117,19 @@ bool router_umma_supported(const Shape& s);
 cudaError_t split_router(const float* w, __nv_bfloat16* hi, __nv_bfloat16* lo, size_t n, cudaStream_t st);
 cudaError_t launch_router_umma(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T, float* logits,
                                uint32_t* status, cudaStream_t st);
+
+// moe_prefill.cu: block-scaled FP4 expert projections for large T
+bool prefill_fp4_supported(const Shape& s);
+size_t prefill_weight_bytes(const Shape& s);
+size_t prefill_workspace_bytes(const Shape& s, int Tm);
+cudaError_t prepare_prefill_fp4();
+cudaError_t pack_prefill_weights(const Shape& s, const uint8_t* codes, const uint8_t* scales, uint8_t* dst,
+                                 cudaStream_t st);
+cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
+                                   const Workspace& ws, uint8_t* pw, int Tm, __nv_bfloat16* out,
+                                   const __nv_bfloat16* residual, cudaStream_t st, int* n_launch);
+cudaError_t launch_act_quant(const __nv_bfloat16* x, int T, int K, uint8_t* codes, uint8_t* scales, float* rowscale,
+                             cudaStream_t st);
 
 // gemm_fp4.cu: swizzled-tile packing for the block-scaled FP4 GEMM
 cudaError_t pack_fp4_tiles(const uint8_t* codes, const uint8_t* scales, uint8_t* tiles, uint8_t* sf, int R, int K,

@@ -187,6 +187,7 @@ struct RouterArgs {
     const float* wr;
     const float* bias;
     int T, d, E, k, n_shared;
+    int stage_x16;   // large-T path: also stage fp16 hidden states for the mma.sync experts
     Workspace ws;
 };
 
@@ -347,7 +348,7 @@ __global__ void __launch_bounds__(256) token_prep_kernel(RouterArgs a) {
     if (t >= a.T) return;
     topk_warp<false>(a.ws.logits + (size_t)t * a.E, a.E, a.k, a.ws.idx + t * a.k, a.ws.w + t * a.k,
                      a.ws.status);
-    stage_token_warp(a.x + (size_t)t * a.d, a.d, a.ws.x16 + (size_t)t * a.d, a.ws.xinv + t);
+    if (a.stage_x16) stage_token_warp(a.x + (size_t)t * a.d, a.d, a.ws.x16 + (size_t)t * a.d, a.ws.xinv + t);
 }
 
 struct BucketArgs {
@@ -420,6 +421,7 @@ RouterArgs make_args(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, 
     a.E = s.E;
     a.k = s.k;
     a.n_shared = s.n_shared;
+    a.stage_x16 = 1;
     a.ws = ws;
     return a;
 }
@@ -455,8 +457,9 @@ cudaError_t prepare_router() {
 }
 
 cudaError_t launch_router(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
-                          const Workspace& ws, cudaStream_t st, int* n_launch) {
+                          const Workspace& ws, cudaStream_t st, int* n_launch, bool stage_x16) {
     RouterArgs a = make_args(s, L, x, T, ws);
+    a.stage_x16 = stage_x16 ? 1 : 0;
     const size_t smem = (size_t)2 * s.d * 4 + (size_t)kTokGroup * s.d * 2;
     if (T <= kSmallT && smem <= kRouterDynSmemMax) {
         router_small_kernel<<<dim3(s.E / 2, (T + kTokGroup - 1) / kTokGroup), kRouterThreads, smem, st>>>(a);

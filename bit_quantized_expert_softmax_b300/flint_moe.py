@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
             "flint_moe_forward_launches": (_I, [_P, _I]),
             "flint_moe_tensor_core_plan": (_I, [_P, _I, _I]),
             "flint_moe_debug_fp4_gemm": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
+            "flint_moe_debug_act_quant": (_I, [_P, _I, _I, _P, _P, _P, _P]),
             "flint_moe_profile_begin": (_I, [_P, _I]),
             "flint_moe_profile_end": (_I, [_P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_I)]),
         }
@@ -189,6 +190,11 @@ def flint_moe_launch_count(h: int) -> int:
 
 def flint_moe_forward_launches(h: int, T: int) -> int:
     return int(lib().flint_moe_forward_launches(h, T))
+
+
+def flint_moe_debug_act_quant(x, T: int, K: int, codes, scales, rowscale, stream=None) -> None:
+    _check(lib().flint_moe_debug_act_quant(_ptr(x), T, K, _ptr(codes), _ptr(scales), _ptr(rowscale), _stream(stream)),
+           "flint_moe_debug_act_quant")
 
 
 def flint_moe_debug_fp4_gemm(a_codes, a_scales, b_codes, b_scales, M: int, N: int, K: int, d, stream=None) -> None:

@@ -185,8 +185,14 @@ FLINT_API size_t flint_moe_device_bytes(const flint_moe* h);
 /* Which 5th-generation tensor-core (tcgen05) kernels a single-layer forward
  * of T tokens on this loaded layer uses: bit 0 = router logits GEMM, bit 1 =
  * block-scaled FP4 expert GEMMs. 0 when neither; -1 on bad arguments.
- * Setting FLINT_MOE_TCGEN05_PREFILL=0 before flint_moe_create turns these
- * kernels off for the handle (the mma.sync and CUDA-core paths remain). */
+ * Bit 1 is set for T > 64 on NVFP4 weights with d = 2048, f = 512 and one
+ * shared expert when max_tokens > 64; that path quantises the activations
+ * entering each expert projection to NVFP4 (flint_moe_debug_act_quant; h is
+ * rounded to bf16 first), so its result is the W4A4 product, not the W4A16
+ * one the other paths compute. Setting FLINT_MOE_TCGEN05_PREFILL=0 before
+ * flint_moe_create turns all these kernels off for the handle (the mma.sync
+ * and CUDA-core paths remain); FLINT_MOE_FP4_EXPERTS=0 turns off only the
+ * FP4 expert GEMMs. */
 FLINT_API int flint_moe_tensor_core_plan(const flint_moe* h, int layer, int T);
 
 /* Block-scaled FP4 matrix product on the 5th-generation tensor cores, through
@@ -200,6 +206,21 @@ FLINT_API int flint_moe_tensor_core_plan(const flint_moe* h, int layer, int T);
 FLINT_API flint_status flint_moe_debug_fp4_gemm(const uint8_t* a_codes_dev, const uint8_t* a_scales_dev,
                                                 const uint8_t* b_codes_dev, const uint8_t* b_scales_dev, int M,
                                                 int N, int K, float* d_dev, void* stream);
+
+/* NVFP4 quantisation of bf16 activations exactly as the large-T expert path
+ * applies it before its block-scaled FP4 GEMMs (T > 64, NVFP4 weights):
+ * per row an fp32 scale s = amax/2688 (rowscale_dev[T]); per 16 elements an
+ * E4M3 scale byte sb = E4M3_rne((amax_16/6)/s) (scales_dev[T][K/16]); codes
+ * E2M1_rne(v * (1/(E4M3(sb)*s))) in fp32 (codes_dev[T][K/2], element 2i in
+ * the low nibble). A zero row gives s = 0, zero scales and zero codes. The
+ * pages fix only the weights' NVFP4 format ("Flint", the repository list of
+ * the NVFP4 GGUF build); using it for the activations, with one fp32 scale per
+ * token, is this library's reading, forced by the FP4 x FP4 tensor-core MMA
+ * that NVFP4 weights take. K must be 2048 or 512; x_dev and codes_dev
+ * 16-byte aligned, scales_dev 4-byte aligned. Asynchronous on `stream`.
+ * Errors: FLINT_EINVAL (K, T < 0, NULL, misaligned), FLINT_ECUDA. */
+FLINT_API flint_status flint_moe_debug_act_quant(const void* x_dev, int T, int K, uint8_t* codes_dev,
+                                                 uint8_t* scales_dev, float* rowscale_dev, void* stream);
 
 /* ---- bucketing for callers that cannot allocate ---------------------------
  * The Flint blog has no counterpart to this entry point: it serves callers,

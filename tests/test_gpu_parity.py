@@ -236,7 +236,10 @@ def test_layer_flint_batched_q4_1_T64(fm):
     assert_out_close(got, ref.out, "batched decode T=64 q4_1")
 
 
-def test_layer_flint_prefill_T8192_sampled(fm):
+def test_layer_flint_prefill_T8192_sampled_mma_path(fm, monkeypatch):
+    """The 16-bit-activation expert kernels at the full prefill size (the FP4
+    tensor-core expert path is switched off for this handle)."""
+    monkeypatch.setenv("FLINT_MOE_FP4_EXPERTS", "0")
     cfg = _cfg(5)
     rng = np.random.default_rng(0)
     sample = np.unique(np.concatenate([[0, 1, 8191], rng.choice(8192, 61, replace=False)]))
