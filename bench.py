@@ -37,6 +37,7 @@ from bit_quantized_expert_softmax_b300 import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s"
 FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
 
 
 # ---------------------------------------------------------------------------
@@ -49,8 +50,9 @@ def measured_peaks() -> dict:
     if os.path.exists(p):
         with open(p) as fh:
             d = json.load(fh)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)),
+                "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS, "source": "fallback"}
 
 
 def dist_env():
@@ -184,17 +186,30 @@ def blas_threads() -> int:
 # ---------------------------------------------------------------------------
 
 
+def fp4_expert_path(cfg) -> bool:
+    """Whether the library runs this workload's experts as block-scaled FP4
+    GEMMs (NVFP4 weights, d=2048, f=512, more than 64 tokens); the bench
+    checks this against the handle's own plan."""
+    return cfg.wfmt == 0 and cfg.d == 2048 and cfg.f == 512 and cfg.tokens > 64
+
+
 def algorithmic_bytes(cfg, n_active_experts: int, T: int) -> dict:
     """Bytes the layer must move once per step (weights of the experts it
-    uses, router, activations), and the share of the gate/up kernel."""
+    uses, router, activations), and those of its expert kernels: the 16-bit
+    activation gate/up kernel, and the FP4 path's gate/up and down GEMMs
+    (weights of the experts used, their NVFP4 activation rows in, h or the
+    fp32 sum out), with the GEMMs' algorithmic FLOPs."""
     per_mat = cfg.codes_per_matrix + cfg.scales_per_matrix + (4 if cfg.wfmt == 0 else 0)
     selected = n_active_experts * 3 * per_mat
     router = cfg.router_bytes + cfg.n_experts * 4
     acts = 2 * T * cfg.d * 2
     P = T * (cfg.top_k + 1)
     gateup = n_active_experts * 2 * per_mat + T * cfg.d * 2 + P * cfg.f * 4
+    fp4_gemm1 = n_active_experts * 2 * per_mat + P * (cfg.d // 2 + cfg.d // 16 + 4) + P * cfg.f * 2
+    fp4_gemm2 = n_active_experts * per_mat + P * (cfg.f // 2 + cfg.f // 16 + 4) + T * cfg.d * 4
     return {"selected_expert_bytes": selected, "layer_bytes": selected + router + acts,
-            "gateup_kernel_bytes": gateup}
+            "gateup_kernel_bytes": gateup, "fp4_gemm1_bytes": fp4_gemm1, "fp4_gemm2_bytes": fp4_gemm2,
+            "fp4_gemm1_flops": 2 * P * cfg.d * 2 * cfg.f, "fp4_gemm2_flops": 2 * P * cfg.f * cfg.d}
 
 
 def run_ours(args, cfg, world, rank, local):
@@ -228,6 +243,8 @@ def run_ours(args, cfg, world, rank, local):
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
 
     launches_per_forward = fm.flint_moe_forward_launches(m.h, T)
+    plan = fm.flint_moe_tensor_core_plan(m.h, 0, T)
+    assert bool(plan & 2) == fp4_expert_path(cfg), f"tensor-core plan {plan} for {cfg.name}"
     graph = None
     if n_layers > 1:
         xs = x.clone()
@@ -312,7 +329,7 @@ def run_ours(args, cfg, world, rank, local):
         # per-kernel split of the multi-kernel path (a separate pass: the
         # extra events would otherwise sit inside the timed steps)
         _, (phase_ms, n_prof) = timed(min(K, 2000), profile=True)
-        phase_us = [p_ / n_prof * 1e3 for p_ in phase_ms]
+        phase_us = {k: p_ / n_prof * 1e3 for k, p_ in zip(fm.PROFILE_PHASES, phase_ms)}
 
     # end to end through the public API: pinned host in -> forward -> pinned host out
     xh = fm.hidden_to_host(x).copy()
@@ -346,14 +363,16 @@ def run_ours(args, cfg, world, rank, local):
         "clocks": clk.summary(), "bytes": nbytes, "n_active": n_active,
         "e2e_value": world * T / (e2e_ms / 1e3), "e2e_ms": e2e_ms, "peaks": peaks,
         "launches_per_forward": launches_per_forward, "phase_us": phase_us, "graph": graph is not None,
+        "plan": plan,
     }
     m.close()
     return res
 
 
-def cpu_baseline(cfg, seconds: float) -> dict:
+def cpu_baseline(cfg, seconds: float, act_quant: bool = False) -> dict:
     """The CPU oracle (test infrastructure), timed as it stands on the host
-    cores, on a bounded sample of the workload."""
+    cores, on a bounded sample of the workload (with the NVFP4 activation
+    quantisation where the GPU path applies it)."""
     import oracle
     T = cfg.tokens
     if cfg.n_layers > 1:
@@ -378,7 +397,7 @@ def cpu_baseline(cfg, seconds: float) -> dict:
     t0 = time.perf_counter()
     while True:
         bits = synth.make_hidden(cfg, tokens=T, stream=1 + steps)
-        oracle.moe.moe_layer(bits, L)
+        oracle.moe.moe_layer(bits, L, act_quant=act_quant)
         done += T
         steps += 1
         el = time.perf_counter() - t0
@@ -434,7 +453,7 @@ def main():
             bits = synth.make_hidden(cfg, stream=1 + i)
             t0 = time.perf_counter()
             for L in layers:
-                oracle.moe.moe_layer(bits, L)
+                oracle.moe.moe_layer(bits, L, act_quant=fp4_expert_path(cfg))
             dt = (time.perf_counter() - t0) * cfg.n_layers / n_keep
             if i >= args.warmup:
                 steps.append(dt)
@@ -445,6 +464,7 @@ def main():
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
                 "n_gpus": args.gpus, "steps": len(steps), "warmup": args.warmup, "ms_per_step": ms,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "oracle_mode": "quantised activations (NVFP4)" if fp4_expert_path(cfg) else "16-bit activations",
                 "data": "synthetic", "config": workload,
                 "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle",
                                  "cores": blas_threads(),
@@ -469,7 +489,7 @@ def main():
             "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f16", "data": "synthetic", "config": workload,
+            "dtype": "nvfp4" if res["plan"] & 2 else "f16", "data": "synthetic", "config": workload,
         }
         layer_gbs = nb["layer_bytes"] / (res["ms"] * 1e-3) / 1e9
         if res["launches_per_forward"] == 1 and cfg.n_layers == 1:
@@ -481,16 +501,37 @@ def main():
                     "bit_quantized_expert_softmax_b300/csrc/tiles.cuh",
                     "bit_quantized_expert_softmax_b300/csrc/common.cuh")
             kkey = "decode_fused_kernel"
+        elif res["phase_us"] is not None and res["plan"] & 2:
+            # FP4 path: the gate/up GEMM (largest phase), bound by HBM: its
+            # algorithmic bytes take longer at the measured copy bandwidth
+            # than its FLOPs at the FP4 tensor peak
+            k_us = res["phase_us"]["gateup"]
+            k_bytes = nb["fp4_gemm1_bytes"]
+            kname = "fp4_gemm_kernel<Gemm1> (expert gate/up, block-scaled FP4, SwiGLU epilogue)"
+            srcs = ("bit_quantized_expert_softmax_b300/csrc/moe_prefill.cu",
+                    "bit_quantized_expert_softmax_b300/csrc/gemm_fp4.cuh",
+                    "bit_quantized_expert_softmax_b300/csrc/umma.cuh",
+                    "bit_quantized_expert_softmax_b300/csrc/common.cuh")
+            kkey = "fp4_gemm_kernel<Gemm1>"
+            line["phases_us"] = res["phase_us"]
+            fp4_peak = peaks["bf16_tflops"] * 6.0      # nominal dense FP4 : bf16 = 13.5 : 2.25
+            line["tensor"] = {
+                "gateup_tflops": nb["fp4_gemm1_flops"] / (k_us * 1e-6) / 1e12,
+                "down_tflops": nb["fp4_gemm2_flops"] / (res["phase_us"]["down_combine"] * 1e-6) / 1e12,
+                "fp4_peak_tflops": fp4_peak,
+                "peak_source": "measured bf16 (MEASURED_PEAKS.json bf16_tflops) x 6, the nominal FP4:bf16 ratio",
+                "down_hbm_frac": nb["fp4_gemm2_bytes"] / (res["phase_us"]["down_combine"] * 1e-6) / 1e9 / hbm,
+            }
         elif res["phase_us"] is not None:
-            k_us = res["phase_us"][1]
+            k_us = res["phase_us"]["gateup"]
             k_bytes = nb["gateup_kernel_bytes"]
             kname = "gateup_kernel (expert gate/up, SwiGLU)"
             srcs = ("bit_quantized_expert_softmax_b300/csrc/experts.cu",
                     "bit_quantized_expert_softmax_b300/csrc/tiles.cuh",
                     "bit_quantized_expert_softmax_b300/csrc/common.cuh")
             kkey = "gateup_kernel"
-            line["phases_us"] = {"router_topk_bucket": res["phase_us"][0], "gateup": res["phase_us"][1],
-                                 "down_combine": res["phase_us"][2]}
+            line["phases_us"] = {k: v for k, v in res["phase_us"].items() if k in ("router_topk_bucket", "gateup",
+                                                                                    "down_combine")}
         else:
             # the stack: one graph of n_layers single-launch layers per step
             k_us = res["ms"] * 1e3 / cfg.n_layers
@@ -521,7 +562,7 @@ def main():
         step_ms = np.array(res["step_ms"])
         line["step_ms_p10_p50_p90"] = [float(np.percentile(step_ms, q)) for q in (10, 50, 90)]
         if not args.no_cpu_baseline and world == 1:
-            line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+            line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds, act_quant=bool(res["plan"] & 2))
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

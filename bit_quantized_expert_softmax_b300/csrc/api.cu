@@ -30,7 +30,7 @@ struct flint_moe {
     bool fp4_experts = false;    // block-scaled FP4 expert GEMMs for T > kSmallT
     void* pws = nullptr;         // their workspace (swizzled activation tiles, h, fp32 sums)
     size_t pws_bytes = 0;
-    // phase events of profiled forwards: 4 per forward
+    // events of profiled forwards: kProfMarks per forward (see prof_record)
     std::vector<cudaEvent_t> prof_events;
     int prof_max = 0, prof_n = 0;
 };
@@ -151,8 +151,20 @@ void prof_free(flint_moe* h) {
     h->prof_max = h->prof_n = 0;
 }
 
-void prof_record(flint_moe* h, int phase, cudaStream_t st) {
-    if (h->prof_n < h->prof_max) cudaEventRecord(h->prof_events[(size_t)h->prof_n * 4 + phase], st);
+// Marks of one profiled forward: 0 start, 1 routing done, 2 activations
+// quantised, 3 gate/up done, 4 h quantised, 5 down projection done, 6 output
+// written. A path without a step records its two marks back to back.
+// Phases: router 1-0, gate/up 3-2, down 5-4, quantisation (2-1)+(4-3), cast 6-5.
+constexpr int kProfMarks = 7;
+
+cudaEvent_t* prof_marks(flint_moe* h) {
+    return h->prof_n < h->prof_max ? &h->prof_events[(size_t)h->prof_n * kProfMarks] : nullptr;
+}
+void prof_record(flint_moe* h, int mark, cudaStream_t st) {
+    if (h->prof_n < h->prof_max) cudaEventRecord(h->prof_events[(size_t)h->prof_n * kProfMarks + mark], st);
+}
+void prof_next(flint_moe* h) {
+    if (h->prof_n < h->prof_max) ++h->prof_n;
 }
 
 cudaError_t run_layer(flint_moe* h, int layer, const __nv_bfloat16* x, int T, __nv_bfloat16* out,
@@ -164,10 +176,8 @@ cudaError_t run_layer(flint_moe* h, int layer, const __nv_bfloat16* x, int T, __
         flint::FusedScratch fs{h->ws.logits, h->ws.hf, h->ws.gbar, h->ws.status};
         prof_record(h, 0, st);
         cudaError_t e = flint::launch_decode_fused(h->s, L, x, T, out, residual, fs, h->n_sms, st);
-        prof_record(h, 1, st);
-        prof_record(h, 2, st);
-        prof_record(h, 3, st);
-        if (h->prof_n < h->prof_max) ++h->prof_n;
+        for (int k = 1; k < kProfMarks; ++k) prof_record(h, k, st);
+        prof_next(h);
         h->launches += 1;
         return e;
     }
@@ -175,23 +185,24 @@ cudaError_t run_layer(flint_moe* h, int layer, const __nv_bfloat16* x, int T, __
         prof_record(h, 0, st);
         cudaError_t e = flint::launch_router(h->s, L, x, T, h->ws, st, &n, false);
         prof_record(h, 1, st);
-        prof_record(h, 2, st);
         if (e == cudaSuccess)
             e = flint::launch_prefill_experts(h->s, L, x, T, h->ws, static_cast<uint8_t*>(h->pws), h->s.max_tokens,
-                                              out, residual, st, &n);
-        prof_record(h, 3, st);
-        if (h->prof_n < h->prof_max) ++h->prof_n;
+                                              out, residual, st, &n, prof_marks(h) ? prof_marks(h) + 1 : nullptr);
+        prof_next(h);
         h->launches += n;
         return e;
     }
     prof_record(h, 0, st);
     cudaError_t e = flint::launch_router(h->s, L, x, T, h->ws, st, &n);
     prof_record(h, 1, st);
-    if (e == cudaSuccess) e = flint::launch_gateup(h->s, L, T, h->ws, st, &n);
     prof_record(h, 2, st);
-    if (e == cudaSuccess) e = flint::launch_down(h->s, L, T, h->ws, out, residual, st, &n);
+    if (e == cudaSuccess) e = flint::launch_gateup(h->s, L, T, h->ws, st, &n);
     prof_record(h, 3, st);
-    if (h->prof_n < h->prof_max) ++h->prof_n;
+    prof_record(h, 4, st);
+    if (e == cudaSuccess) e = flint::launch_down(h->s, L, T, h->ws, out, residual, st, &n);
+    prof_record(h, 5, st);
+    prof_record(h, 6, st);
+    prof_next(h);
     h->launches += n;
     return e;
 }
@@ -526,7 +537,7 @@ int flint_moe_forward_launches(const flint_moe* h, int T) {
     int n_slots = 0, offs[10];
     if (h->fused && flint::fused_smem_bytes(h->s, T, h->n_sms, &n_slots, offs) != 0) return 1;
     const int router = (T <= flint::kSmallT && h->s.d <= 2560) ? 1 : 2 + 3;
-    if (T > flint::kSmallT && h->fp4_experts) return router + 8;
+    if (T > flint::kSmallT && h->fp4_experts) return router + 6;
     const int down = T <= flint::kFuseCombineT ? 1 : 2;
     return router + 1 + down;
 }
@@ -536,7 +547,7 @@ flint_status flint_moe_profile_begin(flint_moe* h, int max_forwards) {
     DeviceGuard guard(h->device);
     if (!guard.ok) return FLINT_ECUDA;
     prof_free(h);
-    h->prof_events.resize((size_t)max_forwards * 4);
+    h->prof_events.resize((size_t)max_forwards * kProfMarks);
     for (size_t i = 0; i < h->prof_events.size(); ++i) {
         if (cudaEventCreate(&h->prof_events[i]) != cudaSuccess) {
             h->prof_events.resize(i);
@@ -553,17 +564,20 @@ flint_status flint_moe_profile_end(flint_moe* h, float* phase_ms, int* n_forward
     if (h == nullptr || phase_ms == nullptr || n_forwards == nullptr) return FLINT_EINVAL;
     DeviceGuard guard(h->device);
     if (!guard.ok) return FLINT_ECUDA;
-    double acc[3] = {0, 0, 0};
+    // interval i = marks (i, i+1) -> phase
+    static const int kPhaseOf[kProfMarks - 1] = {0, 3, 1, 3, 2, 4};
+    double acc[FLINT_PROFILE_PHASES] = {0, 0, 0, 0, 0};
     cudaError_t e = cudaSuccess;
     for (int f = 0; f < h->prof_n && e == cudaSuccess; ++f) {
-        e = cudaEventSynchronize(h->prof_events[(size_t)f * 4 + 3]);
-        for (int p = 0; p < 3 && e == cudaSuccess; ++p) {
+        const cudaEvent_t* ev = &h->prof_events[(size_t)f * kProfMarks];
+        e = cudaEventSynchronize(ev[kProfMarks - 1]);
+        for (int i = 0; i + 1 < kProfMarks && e == cudaSuccess; ++i) {
             float ms = 0.f;
-            e = cudaEventElapsedTime(&ms, h->prof_events[(size_t)f * 4 + p], h->prof_events[(size_t)f * 4 + p + 1]);
-            acc[p] += ms;
+            e = cudaEventElapsedTime(&ms, ev[i], ev[i + 1]);
+            acc[kPhaseOf[i]] += ms;
         }
     }
-    for (int p = 0; p < 3; ++p) phase_ms[p] = (float)acc[p];
+    for (int p = 0; p < FLINT_PROFILE_PHASES; ++p) phase_ms[p] = (float)acc[p];
     *n_forwards = h->prof_n;
     prof_free(h);
     return cuda_status(e);

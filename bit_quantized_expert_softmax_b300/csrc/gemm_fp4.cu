@@ -41,7 +41,9 @@ struct DebugGemm {
     float* d;
     int mt, nt, kt, N;
     __device__ int n_items() const { return mt * nt; }
-    __device__ bool item(int i, Fp4Item& w) const {
+    struct Pre {};
+    __device__ Pre pre(const Fp4Item&, int, int) const { return {}; }
+    __device__ void item(int i, Fp4Item& w) const {
         const int m = i / nt, n = i % nt;
         w.a = a + (size_t)m * kt * kGTile;
         w.asf = asf + (size_t)m * kt * kGSf;
@@ -51,12 +53,14 @@ struct DebugGemm {
         w.m = m;
         w.n = n;
         w.aux = 0;
-        return true;
     }
-    __device__ void epilogue(const Fp4Item& w, uint32_t taddr, int row) const {
+    static constexpr int kStages = 4;
+    static constexpr int kEpiSmemPerWarp = 0;
+    __device__ void epilogue_finish() const {}
+    __device__ void epilogue(const Fp4Item& w, Pre, uint32_t taddr, int row, int half, uint8_t*) const {
         float* dst = d + (size_t)(w.m * kGM + row) * N + w.n * kGN;
 #pragma unroll 1
-        for (int c = 0; c < kGN / 16; ++c) {
+        for (int c = 4 * half; c < 4 * half + 4; ++c) {
             uint32_t r[16];
             tmem_ld16(taddr + c * 16, r);
             tmem_ld_wait();
@@ -81,7 +85,7 @@ cudaError_t pack_fp4_tiles(const uint8_t* codes, const uint8_t* scales, uint8_t*
 
 cudaError_t prepare_gemm_fp4() {
     cudaError_t e = cudaFuncSetAttribute(fp4_gemm_kernel<DebugGemm>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kGSmem);
+                                         fp4_gemm_smem<DebugGemm>());
     if (e != cudaSuccess) cudaGetLastError();
     return e;
 }
@@ -110,7 +114,7 @@ extern "C" flint_status flint_moe_debug_fp4_gemm(const uint8_t* a_codes, const u
     if (e == cudaSuccess) {
         DebugGemm p{buf, buf + at, buf + at + asf, buf + at + asf + bt, d, M / kGM, N / kGN, KT, N};
         const int items = (M / kGM) * (N / kGN);
-        fp4_gemm_kernel<DebugGemm><<<items < 148 ? items : 148, kGThreads, kGSmem, st>>>(p, status);
+        fp4_gemm_kernel<DebugGemm><<<items < 148 ? items : 148, kGThreads, fp4_gemm_smem<DebugGemm>(), st>>>(p, status);
         e = cudaGetLastError();
     }
     uint32_t hs = 0;

@@ -9,16 +9,19 @@
 // c ^ (r % 8) (the 128-byte swizzle). Its scale factors are 128 rows x 16
 // bytes, row-major. One 1-D bulk copy per tile moves it into shared memory.
 //
-// Warp roles of a CTA (320 threads, one CTA per SM):
-//   warp 0      producer: bulk-copies A, B and their scales into a 4-stage ring
+// Warp roles of a CTA (448 threads, one CTA per SM):
+//   warp 0      producer: bulk-copies A, B and their scales into a ring of
+//               P::kStages stages
 //   warp 1      allocates tensor memory; one thread issues the MMAs
 //               (M=128, N=128, K=64 each; 4 per stage) into one of two
 //               accumulators
 //   warps 2..5  scale writers: shared memory -> tensor memory (tcgen05.st),
 //               one row (lane) per thread
-//   warps 6..9  epilogue: tensor memory -> registers -> the problem's store
+//   warps 6..13 epilogue: tensor memory -> registers -> the problem's store;
+//               two warps per lane quadrant, each taking half of the 128
+//               accumulator columns
 // Tensor memory columns: accumulators [0,128) and [128,256); per stage s the
-// A scales at 256+32s..+15 and the B scales at 256+32s+16..+31.
+// A scales at 256+32s..+15 and the B scales at 256+32s+16..+31 (s < 8).
 //
 // Scale layout in tensor memory (per MMA of K = 64, 4 columns): lane m0 of
 // every 32-lane quadrant, column m1 (0..3) holds the four UE4M3 scales (one
@@ -34,9 +37,9 @@ constexpr int kGM = 128, kGN = 128, kGK = 256;
 constexpr int kGTile = kGM * kGK / 2;          // 16 KiB of packed E2M1
 constexpr int kGSf = kGM * kGK / 16;           // 2 KiB of UE4M3 scales
 constexpr int kGStage = 2 * kGTile + 2 * kGSf; // A, B, scales of A, scales of B
-constexpr int kGStages = 4;
-constexpr int kGSmem = kGStages * kGStage + 1024;
-constexpr int kGThreads = 320;
+constexpr int kGMaxStages = 8;
+constexpr int kGThreads = 448;
+constexpr int kGEpiWarps = 8;
 
 // One output tile of a problem.
 struct Fp4Item {
@@ -54,9 +57,26 @@ __host__ __device__ __forceinline__ int swz_offset(int r, int j) {
     return r * 128 + ((((j >> 4) ^ (r & 7)) & 7) << 4) + (j & 15);
 }
 
+// Dynamic shared memory of the kernel for problem P (1024 bytes of slack for
+// the 1024-byte alignment of the stage ring).
+template <class P>
+constexpr int fp4_gemm_smem() {
+    static_assert(P::kStages >= 2 && P::kStages <= kGMaxStages, "stage count");
+    return P::kStages * kGStage + kGEpiWarps * P::kEpiSmemPerWarp + 1024;
+}
+
+// A problem P provides kStages, kEpiSmemPerWarp, n_items(), item(i, w), a
+// per-thread prologue pre(w, row, half) -> P::Pre (its loads are issued one
+// item ahead, while the previous accumulator is being stored), the epilogue
+// epilogue(w, pre, taddr, row, half, epi) of one accumulator (row = tile row
+// of this thread, half = which 64 of the 128 columns, epi = kEpiSmemPerWarp
+// bytes of shared memory owned by the warp) and epilogue_finish(), run once
+// by every epilogue thread after its last item. Every role fetches the
+// description of its next item before it waits on the current one.
 template <class P>
 __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, uint32_t* status) {
     extern __shared__ uint8_t graw[];
+    constexpr int kGStages = P::kStages;
     __shared__ __align__(8) uint64_t full[kGStages], sfready[kGStages], empty[kGStages], accfull[2], accempty[2];
     __shared__ uint32_t tmem_base;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(graw) + 1023) & ~uintptr_t(1023));
@@ -69,7 +89,7 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accfull[b], 1);
-            mbar_init(&accempty[b], 4);
+            mbar_init(&accempty[b], kGEpiWarps);
         }
         mbar_fence_init();
     }
@@ -87,9 +107,11 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
         if (lane == 0) {
             uint32_t kcount = 0;
             bool ok = true;
+            Fp4Item nxt;
+            if ((int)blockIdx.x < n_items) prob.item(blockIdx.x, nxt);
             for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-                Fp4Item w;
-                if (!prob.item(i, w)) continue;
+                const Fp4Item w = nxt;
+                if (i + (int)gridDim.x < n_items) prob.item(i + gridDim.x, nxt);
                 for (int kt = 0; kt < w.kt; ++kt, ++kcount) {
                     const int s = kcount % kGStages;
                     const uint32_t use = kcount / kGStages;
@@ -111,9 +133,11 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
             const uint32_t idesc = idesc_nvfp4_f32(kGM, kGN);
             uint32_t kcount = 0, n_done = 0;
             bool ok = true;
+            Fp4Item nxt;
+            if ((int)blockIdx.x < n_items) prob.item(blockIdx.x, nxt);
             for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-                Fp4Item w;
-                if (!prob.item(i, w)) continue;
+                const Fp4Item w = nxt;
+                if (i + (int)gridDim.x < n_items) prob.item(i + gridDim.x, nxt);
                 const uint32_t buf = n_done & 1;
                 if (n_done >= 2 && !mbar_wait_bounded(&accempty[buf], ((n_done >> 1) - 1) & 1, status)) break;
                 tc_fence_after();
@@ -146,9 +170,11 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         uint32_t kcount = 0;
         bool ok = true;
+        Fp4Item nxt;
+        if ((int)blockIdx.x < n_items) prob.item(blockIdx.x, nxt);
         for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-            Fp4Item w;
-            if (!prob.item(i, w)) continue;
+            const Fp4Item w = nxt;
+            if (i + (int)gridDim.x < n_items) prob.item(i + gridDim.x, nxt);
             for (int kt = 0; kt < w.kt; ++kt, ++kcount) {
                 const int s = kcount % kGStages;
                 const uint32_t use = kcount / kGStages;
@@ -178,24 +204,38 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
             }
         }
     } else {
-        // epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31
+        // epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31 and the
+        // columns [64*half, 64*half + 64) of the accumulator
         const int quad = warp & 3;
+        const int half = (warp - 6) >> 2;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        uint8_t* epi = sm + kGStages * kGStage + (warp - 6) * P::kEpiSmemPerWarp;
         uint32_t n_done = 0;
+        Fp4Item nxt;
+        typename P::Pre pnxt{};
+        if ((int)blockIdx.x < n_items) {
+            prob.item(blockIdx.x, nxt);
+            pnxt = prob.pre(nxt, row, half);
+        }
         for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
-            Fp4Item w;
-            if (!prob.item(i, w)) continue;
+            const Fp4Item w = nxt;
+            const typename P::Pre pw = pnxt;
+            if (i + (int)gridDim.x < n_items) {
+                prob.item(i + gridDim.x, nxt);
+                pnxt = prob.pre(nxt, row, half);
+            }
             const uint32_t buf = n_done & 1;
             const bool got = mbar_wait_bounded(&accfull[buf], (n_done >> 1) & 1, status);
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
-            prob.epilogue(w, tmem + lane_base + buf * kGN, row);
+            prob.epilogue(w, pw, tmem + lane_base + buf * kGN, row, half, epi);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&accempty[buf]);
             ++n_done;
         }
+        prob.epilogue_finish();
     }
     tc_fence_before();
     __syncthreads();

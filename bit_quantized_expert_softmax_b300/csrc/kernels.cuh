@@ -127,7 +127,8 @@ cudaError_t pack_prefill_weights(const Shape& s, const uint8_t* codes, const uin
                                  cudaStream_t st);
 cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
                                    const Workspace& ws, uint8_t* pw, int Tm, __nv_bfloat16* out,
-                                   const __nv_bfloat16* residual, cudaStream_t st, int* n_launch);
+                                   const __nv_bfloat16* residual, cudaStream_t st, int* n_launch,
+                                   const cudaEvent_t* marks);
 cudaError_t launch_act_quant(const __nv_bfloat16* x, int T, int K, uint8_t* codes, uint8_t* scales, float* rowscale,
                              cudaStream_t st);
 

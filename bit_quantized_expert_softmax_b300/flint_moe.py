@@ -210,9 +210,12 @@ def flint_moe_profile_begin(h: int, max_forwards: int) -> None:
     _check(lib().flint_moe_profile_begin(h, max_forwards), "flint_moe_profile_begin")
 
 
+PROFILE_PHASES = ("router_topk_bucket", "gateup", "down_combine", "act_quant", "cast_out")
+
+
 def flint_moe_profile_end(h: int):
-    """-> (per-phase summed milliseconds [router, gate/up, down+combine], forwards)."""
-    ms = (ctypes.c_float * 3)()
+    """-> (per-phase summed milliseconds in PROFILE_PHASES order, forwards)."""
+    ms = (ctypes.c_float * len(PROFILE_PHASES))()
     n = _I()
     _check(lib().flint_moe_profile_end(h, ms, ctypes.byref(n)), "flint_moe_profile_end")
     return [float(v) for v in ms], int(n.value)

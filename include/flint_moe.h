@@ -256,15 +256,22 @@ FLINT_API uint64_t flint_moe_launch_count(const flint_moe* h);
  * flint_moe_create. */
 FLINT_API int flint_moe_forward_launches(const flint_moe* h, int T);
 
-/* Start recording CUDA events on the caller's stream around the three phases
- * of the next max_forwards single-layer forwards (phase 0: router, top-k and
- * bucketing; 1: expert gate/up; 2: expert down projection and combine).
- * Allocates the events; FLINT_EINVAL if max_forwards < 1. */
+/* Number of phases flint_moe_profile_end reports. */
+#define FLINT_PROFILE_PHASES 5
+
+/* Start recording CUDA events on the caller's stream between the kernels of
+ * the next max_forwards single-layer forwards. Phases: 0 router, top-k and
+ * bucketing; 1 expert gate/up; 2 expert down projection (and, on the
+ * 16-bit-activation path, the combine); 3 activation quantisation (FP4 path:
+ * plan, x and h quantisers); 4 output cast and clear of the fp32 sum (FP4
+ * path). The single-launch decode kernel counts entirely as phase 0. Phases a
+ * path does not have read 0. Allocates the events; FLINT_EINVAL if
+ * max_forwards < 1. */
 FLINT_API flint_status flint_moe_profile_begin(flint_moe* h, int max_forwards);
 
 /* Wait for the recorded forwards, write the summed duration of each phase in
- * milliseconds to phase_ms[0..2] and the number of recorded forwards to
- * *n_forwards, then free the events and stop recording. */
+ * milliseconds to phase_ms[0 .. FLINT_PROFILE_PHASES-1] and the number of
+ * recorded forwards to *n_forwards, then free the events and stop recording. */
 FLINT_API flint_status flint_moe_profile_end(flint_moe* h, float* phase_ms, int* n_forwards);
 
 #ifdef __cplusplus
