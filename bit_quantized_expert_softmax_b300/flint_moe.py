@@ -210,7 +210,7 @@ def flint_moe_profile_begin(h: int, max_forwards: int) -> None:
     _check(lib().flint_moe_profile_begin(h, max_forwards), "flint_moe_profile_begin")
 
 
-PROFILE_PHASES = ("router_topk_bucket", "gateup", "down_combine", "act_quant", "cast_out")
+PROFILE_PHASES = ("router_topk_bucket", "gateup", "down_combine", "act_quant", "combine_out")
 
 
 def flint_moe_profile_end(h: int):
