@@ -272,6 +272,35 @@ __device__ __forceinline__ GridSync grid_sync_init(unsigned long long* count, ui
     return GridSync{count, s_base, n_ctas, 0u};
 }
 
+// Split barrier: grid_arrive publishes this CTA's writes and counts it in;
+// grid_wait (later, after independent work) waits for all CTAs of the same
+// pass. grid_sync = grid_arrive + grid_wait.
+__device__ __forceinline__ void grid_arrive(GridSync& gs) {
+    __syncthreads();
+    gs.passed += 1;
+    if (threadIdx.x == 0) red_release_gpu_add_u64(gs.count, 1ull);
+}
+
+__device__ __forceinline__ bool grid_wait(GridSync& gs, uint32_t* status) {
+    __shared__ uint32_t s_okw;
+    if (threadIdx.x == 0) {
+        uint32_t ok = 1;
+        const unsigned long long target = gs.base + (unsigned long long)gs.n * gs.passed;
+        uint32_t it = 0;
+        while (ld_acquire_gpu_u64(gs.count) < target) {
+            if (++it > (1u << 26)) {
+                atomicOr(status, kStatusTimeout);
+                ok = 0;
+                break;
+            }
+            if (it > 256) __nanosleep(32);
+        }
+        s_okw = ok;
+    }
+    __syncthreads();
+    return s_okw != 0;
+}
+
 __device__ __forceinline__ bool grid_sync(GridSync& gs, uint32_t* status) {
     __shared__ uint32_t s_ok;
     __syncthreads();

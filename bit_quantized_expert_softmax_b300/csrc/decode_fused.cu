@@ -8,9 +8,10 @@
 // every weight slab a CTA needs is requested with 1-D bulk copies (TMA) into
 // shared memory as soon as its address is known:
 //
-//   P0  router logits (each CTA a slice of W_r) and the shared expert's
-//       gate/up (routing-independent); the shared expert's down slab is
-//       prefetched for P2.
+//   P0  router logits (each CTA a slice of W_r) -> arrive at the barrier;
+//       while it completes, stage x as fp16 and run the shared expert's
+//       gate/up (routing-independent, its slab requested at kernel start);
+//       the shared expert's down slab is prefetched for P2.
 //   --- grid barrier ---
 //   P1  every CTA takes the top-6 of the logits itself (no broadcast needed),
 //       prefetches the routed experts' down slabs for its P2 rows, then runs
@@ -86,18 +87,19 @@ __device__ __forceinline__ void lds_b16(const __half* p, uint32_t (&b)[16]) {
     }
 }
 
-// Issue the four bulk copies of one gate/up unit (16 rows of gate and up of
-// expert e, full K) into slot memory `dst`, completing on `bar`.
+// Issue the four bulk copies of one gate/up half-unit (8-row group g8 of gate
+// and of up of expert e, full K) into slot memory `dst`: gate codes, up codes
+// (KT tiles of 512 B each), gate scales, up scales; completing on `bar`.
 template <int WFMT>
-__device__ void issue_unit(const FusedArgs& a, int e, int r16, uint8_t* dst, uint64_t* bar) {
+__device__ void issue_half(const FusedArgs& a, int e, int g8, uint8_t* dst, uint64_t* bar) {
     const int KT = a.d >> 7;
     const int S = WFMT == 0 ? 64 : 128;
-    const uint32_t cbytes = 2u * KT * 512u, sbytes = 2u * KT * S;
+    const uint32_t cbytes = (uint32_t)KT * 512u, sbytes = (uint32_t)KT * S;
     mbar_arrive_expect_tx(bar, 2 * (cbytes + sbytes));
-    const size_t coff = (size_t)(2 * r16) * KT * 512, soff = (size_t)(2 * r16) * KT * S;
     for (int m = 0; m < 2; ++m) {
-        bulk_g2s(dst + m * cbytes, a.codes + ((size_t)e * 3 + m) * a.cpm + coff, cbytes, bar);
-        bulk_g2s(dst + 2 * cbytes + m * sbytes, a.scales + ((size_t)e * 3 + m) * a.spm + soff, sbytes, bar);
+        bulk_g2s(dst + m * cbytes, a.codes + ((size_t)e * 3 + m) * a.cpm + (size_t)g8 * cbytes, cbytes, bar);
+        bulk_g2s(dst + 2 * cbytes + m * sbytes, a.scales + ((size_t)e * 3 + m) * a.spm + (size_t)g8 * sbytes, sbytes,
+                 bar);
     }
 }
 
@@ -112,76 +114,92 @@ __device__ void issue_down(const FusedArgs& a, int e, int r16, uint8_t* dst, uin
     bulk_g2s(dst + cbytes, a.scales + ((size_t)e * 3 + 2) * a.spm + (size_t)(2 * r16) * KT * S, sbytes, bar);
 }
 
-// Gate/up of one unit held in shared memory for `np` (token, slot) pairs;
-// writes h = silu(g) * u (fp32) for the unit's 16 rows.
+constexpr int kMaxWaveUnits = 3;   // gate/up half-units computed together (one wave of slots)
+
+// One gate/up half-unit held in shared memory: slab, expert, 8-row group, and
+// its (token, slot) pairs.
+struct UnitRef {
+    const uint8_t* slab;
+    int e, g8;
+    const Pair* pairs;
+    int np;
+};
+
+// Gate/up of up to kMaxWaveUnits half-units at once. The MMA's 16 A rows are
+// the half-unit's 8 gate rows (rows 0-7) and the same 8 up rows (rows 8-15),
+// so one m16n8k16 chain yields both projections. Warp w takes k-tile w of
+// every half-unit, then the CTA reduces the 16 warp partials in warp order
+// and writes h = silu(g) * u (fp32) for the 8 rows.
 template <int WFMT>
-__device__ void gateup_unit(const FusedArgs& a, const uint8_t* slab, int e, int r16, const Pair* pairs, int np,
-                            const __half* x16s, const float* xinv, const float* tss, float* red) {
+__device__ void gateup_units(const FusedArgs& a, const UnitRef* units, int n_units, const __half* x16s,
+                             const float* xinv, const float* tss, float* red) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const int KT = a.d >> 7;
     const int S = WFMT == 0 ? 64 : 128;
-    const uint8_t* cg = slab;
-    const uint8_t* cu = slab + 2 * KT * 512;
-    const uint8_t* sg = slab + 4 * KT * 512;
-    const uint8_t* su = sg + 2 * KT * S;
-    float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
-    const int tb = (g < np) ? pairs[g].t : -1;
+    float acc[kMaxWaveUnits][4];
+#pragma unroll
+    for (int v = 0; v < kMaxWaveUnits; ++v)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[v][j] = 0.f;
     for (int kt = warp; kt < KT; kt += kFWarps) {
-        const uint4 wgg = *reinterpret_cast<const uint4*>(cg + kt * 512 + lane * 16);
-        const uint4 wgh = *reinterpret_cast<const uint4*>(cg + (KT + kt) * 512 + lane * 16);
-        const uint4 wug = *reinterpret_cast<const uint4*>(cu + kt * 512 + lane * 16);
-        const uint4 wuh = *reinterpret_cast<const uint4*>(cu + (KT + kt) * 512 + lane * 16);
-        const TileScales<WFMT> scg = lds_scales<WFMT>(sg + kt * S, sg + (KT + kt) * S, g);
-        const TileScales<WFMT> scu = lds_scales<WFMT>(su + kt * S, su + (KT + kt) * S, g);
-        uint32_t b[16];
-        if (tb >= 0) {
-            lds_b16(x16s + (size_t)tb * a.d + kt * 128 + c * 32, b);
-        } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) b[i] = 0u;
-        }
-        uint32_t fa[8][4];
-        decode_tile<WFMT>(wgg, wgh, scg, fa);
+        for (int v = 0; v < kMaxWaveUnits; ++v) {
+            if (v >= n_units) break;
+            const UnitRef& un = units[v];
+            const uint8_t* cg = un.slab;
+            const uint8_t* cu = un.slab + KT * 512;
+            const uint8_t* sg = un.slab + 2 * KT * 512;
+            const uint8_t* su = sg + KT * S;
+            const uint4 wg = *reinterpret_cast<const uint4*>(cg + kt * 512 + lane * 16);
+            const uint4 wu = *reinterpret_cast<const uint4*>(cu + kt * 512 + lane * 16);
+            const TileScales<WFMT> sc = lds_scales<WFMT>(sg + kt * S, su + kt * S, g);
+            const int tb = (g < un.np) ? un.pairs[g].t : -1;
+            uint32_t b[16];
+            if (tb >= 0) {
+                lds_b16(x16s + (size_t)tb * a.d + kt * 128 + c * 32, b);
+            } else {
 #pragma unroll
-        for (int s = 0; s < 8; ++s) mma_16816(accg, fa[s][0], fa[s][1], fa[s][2], fa[s][3], b[2 * s], b[2 * s + 1]);
-        decode_tile<WFMT>(wug, wuh, scu, fa);
-#pragma unroll
-        for (int s = 0; s < 8; ++s) mma_16816(accu, fa[s][0], fa[s][1], fa[s][2], fa[s][3], b[2 * s], b[2 * s + 1]);
-    }
-    // cross-warp reduction of the K partials: red[warp][gate/up][128]
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        red[(warp * 2 + 0) * 128 + lane * 4 + j] = accg[j];
-        red[(warp * 2 + 1) * 128 + lane * 4 + j] = accu[j];
-    }
-    __syncthreads();
-    if (threadIdx.x < 128) {
-        // thread i owns fragment element i = lane' * 4 + j' of the 16 x 8 tile
-        const int i = threadIdx.x, ln = i >> 2, j = i & 3;
-        const int n = 2 * (ln & 3) + (j & 1);
-        if (n < np) {
-            float sgv[kFWarps], suv[kFWarps];
-#pragma unroll
-            for (int w = 0; w < kFWarps; ++w) {
-                sgv[w] = red[(w * 2 + 0) * 128 + i];
-                suv[w] = red[(w * 2 + 1) * 128 + i];
+                for (int i = 0; i < 16; ++i) b[i] = 0u;
             }
-            float sg_ = 0.f, su_ = 0.f;
+            uint32_t fa[8][4];
+            decode_tile<WFMT>(wg, wu, sc, fa);
 #pragma unroll
-            for (int w = 0; w < kFWarps; ++w) {
-                sg_ += sgv[w];
-                su_ += suv[w];
-            }
-            const Pair p = pairs[n];
-            const float gv = sg_ * tss[e * 3 + 0] * xinv[p.t];
-            const float uv = su_ * tss[e * 3 + 1] * xinv[p.t];
-            const float hv = gv / (1.0f + expf(-gv)) * uv;
-            const int row = r16 * 16 + (ln >> 2) + ((j >> 1) << 3);
-            a.h[((size_t)p.t * (a.k + 1) + p.j) * a.f + row] = hv;
+            for (int st = 0; st < 8; ++st)
+                mma_16816(acc[v], fa[st][0], fa[st][1], fa[st][2], fa[st][3], b[2 * st], b[2 * st + 1]);
         }
     }
-    __syncthreads();
+#pragma unroll
+    for (int v = 0; v < kMaxWaveUnits; ++v) {
+        if (v >= n_units) break;
+        // cross-warp reduction of the K partials: red[warp][128]
+#pragma unroll
+        for (int j = 0; j < 4; ++j) red[warp * 128 + lane * 4 + j] = acc[v][j];
+        __syncthreads();
+        if (threadIdx.x < 64) {
+            // thread i: fragment lane ln = i/2, column 2*(ln%4) + i%2, row ln/4;
+            // its gate sum is element ln*4 + (i%2), its up sum element + 2
+            const UnitRef& un = units[v];
+            const int ln = threadIdx.x >> 1, jj = threadIdx.x & 1;
+            const int n = 2 * (ln & 3) + jj;
+            if (n < un.np) {
+                const int eg = ln * 4 + jj;
+                float sg_ = 0.f, su_ = 0.f;
+#pragma unroll
+                for (int w = 0; w < kFWarps; ++w) {
+                    sg_ += red[w * 128 + eg];
+                    su_ += red[w * 128 + eg + 2];
+                }
+                const Pair p = un.pairs[n];
+                const float gv = sg_ * tss[un.e * 3 + 0] * xinv[p.t];
+                const float uv = su_ * tss[un.e * 3 + 1] * xinv[p.t];
+                const float hv = gv / (1.0f + expf(-gv)) * uv;
+                const int row = un.g8 * 8 + (ln >> 2);
+                a.h[((size_t)p.t * (a.k + 1) + p.j) * a.f + row] = hv;
+            }
+        }
+        __syncthreads();
+    }
 }
 
 template <int WFMT>
@@ -192,10 +210,10 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     const int G = gridDim.x, b = blockIdx.x;
     const int T = a.T, d = a.d, f = a.f, E = a.E, k = a.k;
     const int KTf = f >> 7;
-    const int units_per_expert = f >> 4;
+    const int units_per_expert = f >> 3;                 // 8-row half-units
     const int down_tiles = d >> 4;
     const int down_tile = b - (G - down_tiles);          // the last d/16 CTAs own output tiles
-    const int shared_unit = G - 1 - b;                   // the last f/16 CTAs do the shared gate/up
+    const int shared_unit = G - 1 - b;                   // the last f/8 CTAs do the shared gate/up
 
     uint8_t* slots = smem + a.off_slots;
     uint8_t* down = smem + a.off_down;
@@ -256,7 +274,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
             for (int i = 0; i < n_re; ++i)
                 bulk_g2s(slots + (size_t)i * d * 4, a.router + (size_t)(b + i * G) * d, d * 4, bar_router);
         }
-        if (has_shared) issue_unit<WFMT>(a, E, shared_unit, slots + (size_t)shared_slot * a.unit_bytes, bars + shared_slot);
+        if (has_shared) issue_half<WFMT>(a, E, shared_unit, slots + (size_t)shared_slot * a.unit_bytes, bars + shared_slot);
         if (down_tile >= 0) {
             mbar_arrive_expect_tx(bar_dshared, (uint32_t)a.down_bytes);
             issue_down<WFMT>(a, E, down_tile, down, bar_dshared);
@@ -264,32 +282,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     }
     if (threadIdx.x >= 32 && threadIdx.x < 32 + n_re) bias_s[threadIdx.x - 32] = __ldg(a.bias + b + (threadIdx.x - 32) * G);
     GridSync gsync = grid_sync_init(a.bar_count, (uint32_t)G);   // includes a __syncthreads
-    // stage the hidden states as fp16, scaled per token, fragment-permuted
     wait_all(bar_x, 0);
-    for (int t = 0; t < T; ++t) {
-        float xv[8];
-        float amax = 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int i = threadIdx.x + q * kFThreads;
-            xv[q] = i < d ? __bfloat162float(xbf[(size_t)t * d + i]) : 0.f;
-            amax = fmaxf(amax, fabsf(xv[q]));
-        }
-        amax = warp_max(amax);
-        if (lane == 0) rpart[warp] = amax;
-        __syncthreads();
-        float m = 0.f;
-#pragma unroll
-        for (int w = 0; w < kFWarps; ++w) m = fmaxf(m, rpart[w]);
-        const float mult = f16_range_mult(m);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int i = threadIdx.x + q * kFThreads;
-            if (i < d) x16s[(size_t)t * d + (i & ~127) + kperm_pos(i & 127)] = __float2half_rn(xv[q] * mult);
-        }
-        if (threadIdx.x == 0) xinv[t] = 1.0f / mult;
-        __syncthreads();
-    }
     if (threadIdx.x < T) {
         shared_pairs[threadIdx.x].t = threadIdx.x;
         shared_pairs[threadIdx.x].j = k;
@@ -331,7 +324,34 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
             a.logits[(size_t)t * E + e] = s + bias_s[ii];
         }
     }
-    if (!grid_sync(gsync, a.status)) ok = false;
+    grid_arrive(gsync);
+    // while the barrier completes: stage the hidden states as fp16, scaled
+    // per token, fragment-permuted
+    for (int t = 0; t < T; ++t) {
+        float xv[8];
+        float amax = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = threadIdx.x + q * kFThreads;
+            xv[q] = i < d ? __bfloat162float(xbf[(size_t)t * d + i]) : 0.f;
+            amax = fmaxf(amax, fabsf(xv[q]));
+        }
+        amax = warp_max(amax);
+        if (lane == 0) rpart[warp] = amax;
+        __syncthreads();
+        float m = 0.f;
+#pragma unroll
+        for (int w = 0; w < kFWarps; ++w) m = fmaxf(m, rpart[w]);
+        const float mult = f16_range_mult(m);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = threadIdx.x + q * kFThreads;
+            if (i < d) x16s[(size_t)t * d + (i & ~127) + kperm_pos(i & 127)] = __float2half_rn(xv[q] * mult);
+        }
+        if (threadIdx.x == 0) xinv[t] = 1.0f / mult;
+        __syncthreads();
+    }
+    if (!grid_wait(gsync, a.status)) ok = false;
 
     // ------------------------------------------------------------------ P1
     // top-k of every token, computed by every CTA from the logits in L2
@@ -339,7 +359,17 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     __syncthreads();
     if (warp < T) topk_warp<false>(lg + warp * E, E, k, sel + warp * 8, wsel + warp * 8, b == 0 ? a.status : nullptr);
     __syncthreads();
-    if (warp == 0) {
+    if (T == 1) {
+        // one token: its k experts are distinct, one pair each
+        if (threadIdx.x < k) {
+            const int j = threadIdx.x;
+            act[j] = sel[j];
+            act_np[j] = 1;
+            act_pairs[j * 2] = Pair{0, j};
+            cmap[j] = (j + 1) * 4;
+            if (j == 0) *nact = k;
+        }
+    } else if (warp == 0) {
         // distinct routed experts and their (token, slot) pairs, by one warp:
         // entry i = t*k + j; an entry is the first of its expert if no earlier
         // entry has the same expert; experts are numbered in first-occurrence
@@ -371,19 +401,30 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     __syncthreads();
     const int na = *nact;
     const int n_units = na * units_per_expert;
-    // routed gate/up units u = b, b+G, ..., in waves of n_slots-1 slots
+    // routed gate/up units u = b, b+G, ..., in waves of n_slots-1 slots; the
+    // shared expert's unit (its slab landed in P0) is computed while the
+    // first wave's slabs are in flight
     const int n_rs = a.n_slots - 1;
-    for (int u0 = b; u0 < n_units; u0 += G * n_rs) {
+    bool shared_done = !has_shared;
+    for (int u0 = b; u0 < n_units || !shared_done; u0 += G * n_rs) {
         __syncthreads();
-        if (threadIdx.x == 0) {
+        if (threadIdx.x == 0 && u0 < n_units) {
             fence_proxy_async_smem();
             for (int s2 = 0; s2 < n_rs; ++s2) {
                 const int u = u0 + s2 * G;
                 if (u < n_units)
-                    issue_unit<WFMT>(a, act[u / units_per_expert], u % units_per_expert,
+                    issue_half<WFMT>(a, act[u / units_per_expert], u % units_per_expert,
                                      slots + (size_t)s2 * a.unit_bytes, bars + s2);
             }
         }
+        if (!shared_done) {
+            wait_all(bars + shared_slot, 0);
+            UnitRef su{slots + (size_t)shared_slot * a.unit_bytes, E, shared_unit, shared_pairs, T};
+            if (ok) gateup_units<WFMT>(a, &su, 1, x16s, xinv, tss, acc);
+            shared_done = true;
+        }
+        UnitRef wave[kMaxWaveUnits];
+        int nw = 0;
         for (int s2 = 0; s2 < n_rs; ++s2) {
             const int u = u0 + s2 * G;
             if (u >= n_units) break;
@@ -391,10 +432,10 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
             wait_all(bars + s2, ph);
             slot_phase ^= 1u << s2;
             const int q = u / units_per_expert;
-            if (ok)
-                gateup_unit<WFMT>(a, slots + (size_t)s2 * a.unit_bytes, act[q], u % units_per_expert,
-                                  act_pairs + q * 2, act_np[q], x16s, xinv, tss, acc);
+            wave[nw++] = UnitRef{slots + (size_t)s2 * a.unit_bytes, act[q], u % units_per_expert, act_pairs + q * 2,
+                                 act_np[q]};
         }
+        if (ok && nw > 0) gateup_units<WFMT>(a, wave, nw, x16s, xinv, tss, acc);
     }
     // routed down slabs for this CTA's output tile (slab 0 is the shared
     // expert), requested once the gate/up slabs have landed so that they do
@@ -403,12 +444,6 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
         mbar_arrive_expect_tx(bar_drouted, (uint32_t)(na * a.down_bytes));
         for (int q = 0; q < na; ++q)
             issue_down<WFMT>(a, act[q], down_tile, down + (size_t)(1 + q) * a.down_bytes, bar_drouted);
-    }
-    // the shared expert's unit, prefetched in P0
-    if (has_shared) {
-        wait_all(bars + shared_slot, 0);
-        if (ok) gateup_unit<WFMT>(a, slots + (size_t)shared_slot * a.unit_bytes, E, shared_unit, shared_pairs, T,
-                                  x16s, xinv, tss, acc);
     }
     if (!grid_sync(gsync, a.status)) ok = false;
 
@@ -504,13 +539,13 @@ size_t fused_smem_bytes(const Shape& s, int T, int n_sms, int* n_slots_out, int 
     if (s.d > 8 * kFThreads || s.f > 32 * 32) return 0;   // register staging of x and h rows
     const int S = s.wfmt == 0 ? 64 : 128;
     const int KTd = s.d / 128, KTf = s.f / 128;
-    const size_t unit = (size_t)4 * KTd * (512 + S);
+    const size_t unit = (size_t)2 * KTd * (512 + S);   // one 8-row half-unit of gate and up
     const size_t dslab = (size_t)2 * KTf * (512 + S);
     const int max_active = T * s.k;
-    const int units = max_active * (s.f / 16);
+    const int units = max_active * (s.f / 8);
     if ((size_t)2 * s.d * 4 > unit) return 0;
     if ((s.E + n_sms - 1) / n_sms > 2) return 0;
-    if (s.d / 16 > n_sms || s.f / 16 > n_sms) return 0;
+    if (s.d / 16 > n_sms || s.f / 8 > n_sms) return 0;
     const size_t red = (size_t)kFWarps * 2 * 128 * 4;
     const size_t accb = (size_t)(max_active + 1) * 2 * 128 * 4;
     int n_rs = (units + n_sms - 1) / n_sms;                 // routed slots for one wave
