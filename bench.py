@@ -198,7 +198,7 @@ def algorithmic_bytes(cfg, n_active_experts: int, T: int) -> dict:
     uses, router, activations), and those of its expert kernels: the 16-bit
     activation gate/up kernel, and the FP4 path's gate/up and down GEMMs
     (weights of the experts used, their NVFP4 activation rows in, h or the
-    fp32 sum out), with the GEMMs' algorithmic FLOPs."""
+    bf16 per-assignment contributions out), with the GEMMs' algorithmic FLOPs."""
     per_mat = cfg.codes_per_matrix + cfg.scales_per_matrix + (4 if cfg.wfmt == 0 else 0)
     selected = n_active_experts * 3 * per_mat
     router = cfg.router_bytes + cfg.n_experts * 4
@@ -206,7 +206,7 @@ def algorithmic_bytes(cfg, n_active_experts: int, T: int) -> dict:
     P = T * (cfg.top_k + 1)
     gateup = n_active_experts * 2 * per_mat + T * cfg.d * 2 + P * cfg.f * 4
     fp4_gemm1 = n_active_experts * 2 * per_mat + P * (cfg.d // 2 + cfg.d // 16 + 4) + P * cfg.f * 2
-    fp4_gemm2 = n_active_experts * per_mat + P * (cfg.f // 2 + cfg.f // 16 + 4) + T * cfg.d * 4
+    fp4_gemm2 = n_active_experts * per_mat + P * (cfg.f // 2 + cfg.f // 16 + 4) + P * cfg.d * 2
     return {"selected_expert_bytes": selected, "layer_bytes": selected + router + acts,
             "gateup_kernel_bytes": gateup, "fp4_gemm1_bytes": fp4_gemm1, "fp4_gemm2_bytes": fp4_gemm2,
             "fp4_gemm1_flops": 2 * P * cfg.d * 2 * cfg.f, "fp4_gemm2_flops": 2 * P * cfg.f * cfg.d}
