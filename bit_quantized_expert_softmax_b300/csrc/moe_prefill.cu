@@ -54,22 +54,41 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
     return __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
 }
 
-// Quantise the warp's row: v[EPL] per lane. Outputs per lane: EPL/2 code
-// bytes (codes[], little-endian words) and EPL/16 scale bytes (packed into
-// sbytes); returns the row scale.
+// Quantise the warp's row, held as packed bf16 (lane l: EPL consecutive
+// elements, EPL/8 uint4). Outputs per lane: EPL/2 code bytes (codes[],
+// little-endian words) and EPL/16 scale bytes (packed into sbytes); returns
+// the row scale. Values are converted to fp32 on the fly (exactly), so the
+// packed row costs EPL/2 registers instead of EPL.
+__device__ __forceinline__ void unpack8(const uint4& r, float* v) {
+    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        v[2 * u] = __low2float(p2[u]);
+        v[2 * u + 1] = __high2float(p2[u]);
+    }
+}
+
 template <int EPL>
-__device__ __forceinline__ float quant_row(const float (&v)[EPL], uint32_t (&codes)[EPL / 8], uint32_t& sbytes) {
+__device__ __forceinline__ float quant_row(const uint4 (&raw)[EPL / 8], uint32_t (&codes)[EPL / 8], uint32_t& sbytes) {
     float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    for (int i = 0; i < EPL / 8; ++i) {
+        float v[8];
+        unpack8(raw[i], v);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) amax = fmaxf(amax, fabsf(v[u]));
+    }
     const float amax_t = warp_max(amax);
     const float s_t = amax_t / 2688.0f;
     sbytes = 0u;
 #pragma unroll
     for (int b = 0; b < EPL / 16; ++b) {
+        float v[16];
+        unpack8(raw[2 * b], v);
+        unpack8(raw[2 * b + 1], v + 8);
         float ab = 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(v[16 * b + i]));
+        for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(v[i]));
         const float ratio = s_t > 0.f ? (ab / 6.0f) / s_t : 0.0f;
         const uint32_t sb = f32_to_e4m3(ratio);
         const float S = e4m3_to_f32(sb) * s_t;
@@ -78,7 +97,7 @@ __device__ __forceinline__ float quant_row(const float (&v)[EPL], uint32_t (&cod
             const float inv = 1.0f / S;
             float q[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) q[i] = v[16 * b + i] * inv;
+            for (int i = 0; i < 16; ++i) q[i] = v[i] * inv;
             codes[2 * b] = f32x8_to_e2m1(q);
             codes[2 * b + 1] = f32x8_to_e2m1(q + 8);
         } else {
@@ -215,34 +234,29 @@ __global__ void __launch_bounds__(256) plan_kernel(PrefillCtx c, int* meta_rw) {
 // slot). Padding rows of the tiles are never written: their products are
 // discarded by the epilogues.
 template <int EPL>
-__global__ void __launch_bounds__(256) quant_x_kernel(PrefillCtx c) {
+__global__ void __launch_bounds__(256, 4) quant_x_kernel(PrefillCtx c) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KT = c.d / kGK;
     const int shared_slot = c.meta[0] - 1;
     for (int t = blockIdx.x * 8 + warp; t < c.T; t += gridDim.x * 8) {
-        const __nv_bfloat16* xr = c.x + (size_t)t * c.d + lane * EPL;
-        float v[EPL];
-#pragma unroll
-        for (int i = 0; i < EPL; i += 8) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(xr + i);
-            const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                v[i + 2 * u] = __low2float(p2[u]);
-                v[i + 2 * u + 1] = __high2float(p2[u]);
-            }
+        // destination rows, lane j <= k: issued before the row is loaded so
+        // that their dependent lookups overlap the load and the quantisation
+        int my_rp = 0;
+        if (lane < c.k) {
+            const int slot = c.slot_of[__ldg(c.idx + t * c.k + lane)];
+            my_rp = c.poff[slot] + (__ldg(c.inv + t * c.k + lane) - c.slot_off[slot]);
+        } else if (lane == c.k) {
+            my_rp = c.poff[shared_slot] + t;
         }
+        const __nv_bfloat16* xr = c.x + (size_t)t * c.d + lane * EPL;
+        uint4 raw[EPL / 8];
+#pragma unroll
+        for (int i = 0; i < EPL / 8; ++i) raw[i] = *reinterpret_cast<const uint4*>(xr + 8 * i);
         uint32_t codes[EPL / 8];
         uint32_t sb = 0;
-        const float s_t = quant_row<EPL>(v, codes, sb);
+        const float s_t = quant_row<EPL>(raw, codes, sb);
         for (int j = 0; j <= c.k; ++j) {
-            int rp;
-            if (j < c.k) {
-                const int slot = c.slot_of[__ldg(c.idx + t * c.k + j)];
-                rp = c.poff[slot] + (__ldg(c.inv + t * c.k + j) - c.slot_off[slot]);
-            } else {
-                rp = c.poff[shared_slot] + t;
-            }
+            const int rp = __shfl_sync(0xffffffffu, my_rp, j);
             const int rt = rp / kGM, r = rp % kGM;
             store_row_swizzled<EPL>(c.a1 + (size_t)rt * KT * kGTile, c.a1sf + (size_t)rt * KT * kGSf, r, lane, codes,
                                     sb);
@@ -251,46 +265,44 @@ __global__ void __launch_bounds__(256) quant_x_kernel(PrefillCtx c) {
     }
 }
 
-// Quantise each h row (bf16, f elements) into the down GEMM's A tiles.
+// Quantise each h row (bf16, f elements) into the down GEMM's A tiles and
+// write the down GEMM's per-row epilogue data. One warp per padded row (the
+// grid covers the largest possible row count; warps past the actual rows
+// return); the row's lookups are issued before its h is loaded.
 template <int EPL>
 __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_rows = c.meta[2] * kGM;
     const int KT = c.f / kGK;
-    for (int row = blockIdx.x * 8 + warp; row < n_rows; row += gridDim.x * 8) {
-        const int mt = row / kGM, r = row % kGM;
-        const int slot = c.mt_slot[mt], m = c.mt_m[mt];
-        const int q = m * kGM + r;
-        const int rt = mt;
-        uint8_t* tiles = c.a2 + (size_t)rt * KT * kGTile;
-        uint8_t* sf = c.a2sf + (size_t)rt * KT * kGSf;
-        if (q >= c.slot_cnt[slot]) {           // padding row: its codes are never read back
-            if (lane == 0) c.prow[rt * kGM + r] = -1;
-            continue;
-        }
-        const __nv_bfloat16* hr = c.h + (size_t)(rt * kGM + r) * c.f + lane * EPL;
-        float v[EPL];
+    const int row = blockIdx.x * 8 + warp;
+    if (row >= n_rows) return;
+    const int mt = row / kGM, r = row % kGM;
+    const int slot = c.mt_slot[mt], m = c.mt_m[mt];
+    const int q = m * kGM + r;
+    if (q >= c.slot_cnt[slot]) {           // padding row: its codes are never read back
+        if (lane == 0) c.prow[row] = -1;
+        return;
+    }
+    float yscale_w = 0.f;
+    int p = 0;
+    if (lane == 0) {
+        p = c.slot_off[slot] + q;
+        const float wr = p < c.T * c.k ? c.wts[__ldg(c.perm + p)] : 1.0f;
+        yscale_w = c.tscale[c.slot_expert[slot] * 3 + 2] * wr;
+    }
+    uint8_t* tiles = c.a2 + (size_t)mt * KT * kGTile;
+    uint8_t* sf = c.a2sf + (size_t)mt * KT * kGSf;
+    const __nv_bfloat16* hr = c.h + (size_t)row * c.f + lane * EPL;
+    uint4 raw[EPL / 8];
 #pragma unroll
-        for (int i = 0; i < EPL; i += 8) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(hr + i);
-            const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                v[i + 2 * u] = __low2float(p2[u]);
-                v[i + 2 * u + 1] = __high2float(p2[u]);
-            }
-        }
-        uint32_t codes[EPL / 8];
-        uint32_t sb = 0;
-        const float s_t = quant_row<EPL>(v, codes, sb);
-        store_row_swizzled<EPL>(tiles, sf, r, lane, codes, sb);
-        if (lane == 0) {
-            // per-row epilogue data of the down GEMM
-            const int p = c.slot_off[slot] + q;
-            const float wr = p < c.T * c.k ? c.wts[__ldg(c.perm + p)] : 1.0f;
-            c.prow[rt * kGM + r] = p;
-            c.yscale[rt * kGM + r] = s_t * c.tscale[c.slot_expert[slot] * 3 + 2] * wr;
-        }
+    for (int i = 0; i < EPL / 8; ++i) raw[i] = *reinterpret_cast<const uint4*>(hr + 8 * i);
+    uint32_t codes[EPL / 8];
+    uint32_t sb = 0;
+    const float s_t = quant_row<EPL>(raw, codes, sb);
+    store_row_swizzled<EPL>(tiles, sf, r, lane, codes, sb);
+    if (lane == 0) {
+        c.prow[row] = p;
+        c.yscale[row] = s_t * yscale_w;
     }
 }
 
@@ -431,7 +443,8 @@ struct Gemm2 {
 
 // out[t] = bf16(y[shared] + y[slot 0] + ... + y[slot k-1]) summed in fp32 in
 // that order; with a residual, out = bf16(residual + that bf16 value). One
-// warp per token, 8 bytes (4 columns) per lane per step.
+// warp per token, 16 columns per lane per step; every load of a step is
+// issued before the first add.
 __global__ void __launch_bounds__(256) combine_kernel(PrefillCtx c, __nv_bfloat16* __restrict__ out,
                                                       const __nv_bfloat16* __restrict__ residual) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -441,22 +454,31 @@ __global__ void __launch_bounds__(256) combine_kernel(PrefillCtx c, __nv_bfloat1
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             rows[j + 1] = j < c.k ? c.y + (size_t)__ldg(c.inv + t * c.k + j) * c.d : rows[0];
-        for (int col = lane * 8; col < c.d; col += 256) {
-            float acc[8];
+        for (int col = lane * 16; col < c.d; col += 512) {
+            uint4 r[9][2];
 #pragma unroll
             for (int j = 0; j <= 8; ++j) {
-                if (j > c.k) break;
-                const uint4 r = __ldcs(reinterpret_cast<const uint4*>(rows[j] + col));
-                const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&r);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    acc[2 * u] = j == 0 ? __low2float(b[u]) : acc[2 * u] + __low2float(b[u]);
-                    acc[2 * u + 1] = j == 0 ? __high2float(b[u]) : acc[2 * u + 1] + __high2float(b[u]);
+                if (j <= c.k) {
+                    r[j][0] = __ldcs(reinterpret_cast<const uint4*>(rows[j] + col));
+                    r[j][1] = __ldcs(reinterpret_cast<const uint4*>(rows[j] + col + 8));
                 }
             }
-            uint32_t o[4];
+            float acc[16];
+            unpack8(r[0][0], acc);
+            unpack8(r[0][1], acc + 8);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int j = 1; j <= 8; ++j) {
+                if (j <= c.k) {
+                    float v[16];
+                    unpack8(r[j][0], v);
+                    unpack8(r[j][1], v + 8);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[i] += v[i];
+                }
+            }
+            uint32_t o[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
                 __nv_bfloat16 b0 = __float2bfloat16_rn(acc[2 * u]), b1 = __float2bfloat16_rn(acc[2 * u + 1]);
                 if (residual != nullptr) {
                     const __nv_bfloat16* rr = residual + (size_t)t * c.d + col + 2 * u;
@@ -466,6 +488,7 @@ __global__ void __launch_bounds__(256) combine_kernel(PrefillCtx c, __nv_bfloat1
                 o[u] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
             }
             *reinterpret_cast<uint4*>(out + (size_t)t * c.d + col) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(out + (size_t)t * c.d + col + 8) = make_uint4(o[4], o[5], o[6], o[7]);
         }
     }
 }
@@ -519,12 +542,12 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
     for (int t = blockIdx.x * 8 + warp; t < T; t += gridDim.x * 8) {
         for (int k0 = 0; k0 < K; k0 += 32 * EPL) {   // K = 32*EPL*chunks; each chunk is one warp row
             const __nv_bfloat16* xr = x + (size_t)t * K + k0 + lane * EPL;
-            float v[EPL];
+            uint4 raw[EPL / 8];
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) v[i] = __bfloat162float(xr[i]);
+            for (int i = 0; i < EPL / 8; ++i) raw[i] = *reinterpret_cast<const uint4*>(xr + 8 * i);
             uint32_t c[EPL / 8];
             uint32_t sb = 0;
-            const float s_t = quant_row<EPL>(v, c, sb);
+            const float s_t = quant_row<EPL>(raw, c, sb);
             uint32_t* cd = reinterpret_cast<uint32_t*>(codes + (size_t)t * (K / 2) + (k0 + lane * EPL) / 2);
 #pragma unroll
             for (int i = 0; i < EPL / 8; ++i) cd[i] = c[i];
@@ -634,7 +657,7 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     Gemm1 g1{c, 2 * s.f / kGN, s.d / kGK};
     fp4_gemm_kernel<Gemm1><<<148, kGThreads, fp4_gemm_smem<Gemm1>(), st>>>(g1, ws.status);
     mark(2);
-    quant_h_kernel<16><<<148 * 8, 256, 0, st>>>(c);
+    quant_h_kernel<16><<<(unsigned)((rt * kGM + 7) / 8), 256, 0, st>>>(c);
     mark(3);
     Gemm2 g2{c, s.d / kGN, s.f / kGK};
     fp4_gemm_kernel<Gemm2><<<148, kGThreads, fp4_gemm_smem<Gemm2>(), st>>>(g2, ws.status);
