@@ -168,14 +168,14 @@ void prof_next(flint_moe* h) {
 }
 
 cudaError_t run_layer(flint_moe* h, int layer, const __nv_bfloat16* x, int T, __nv_bfloat16* out,
-                      const __nv_bfloat16* residual, cudaStream_t st) {
+                      const __nv_bfloat16* residual, cudaStream_t st, const LayerDev* next = nullptr) {
     const LayerDev& L = h->layers[layer];
     int n = 0;
     int n_slots = 0, offs[10];
     if (h->fused && flint::fused_smem_bytes(h->s, T, h->n_sms, &n_slots, offs) != 0) {
         flint::FusedScratch fs{h->ws.logits, h->ws.hf, h->ws.gbar, h->ws.status};
         prof_record(h, 0, st);
-        cudaError_t e = flint::launch_decode_fused(h->s, L, x, T, out, residual, fs, h->n_sms, st);
+        cudaError_t e = flint::launch_decode_fused(h->s, L, x, T, out, residual, fs, h->n_sms, st, next);
         for (int k = 1; k < kProfMarks; ++k) prof_record(h, k, st);
         prof_next(h);
         h->launches += 1;
@@ -413,7 +413,8 @@ flint_status flint_moe_forward_stack(flint_moe* h, int layer0, int n_layers, voi
     if (!guard.ok) return FLINT_ECUDA;
     __nv_bfloat16* x = static_cast<__nv_bfloat16*>(hidden_dev);
     for (int l = layer0; l < layer0 + n_layers; ++l) {
-        cudaError_t e = run_layer(h, l, x, T, x, x, (cudaStream_t)stream);
+        const LayerDev* next = (l + 1 < layer0 + n_layers && h->layers[l + 1].loaded) ? &h->layers[l + 1] : nullptr;
+        cudaError_t e = run_layer(h, l, x, T, x, x, (cudaStream_t)stream, next);
         if (e != cudaSuccess) return cuda_status(e);
     }
     return FLINT_OK;

@@ -56,6 +56,11 @@ struct FusedArgs {
     // shared-memory layout (byte offsets)
     int off_slots, unit_bytes, off_down, down_bytes, off_acc, off_x16, off_h16, off_misc, off_xbf, off_ts;
     int ts_bytes;               // bytes of the tensor-scale array copied to shared memory
+    // the next layer of a stack (null: none): its routing-independent weights
+    // are prefetched into L2 while this layer finishes
+    const uint8_t* next_codes;
+    const uint8_t* next_scales;
+    const float* next_router;
 };
 
 struct Pair {
@@ -448,6 +453,26 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     if (!grid_sync(gsync, a.status)) ok = false;
 
     // ------------------------------------------------------------------ P2
+    // the next layer's P0 reads (its router rows, shared half-unit and shared
+    // down slab of this CTA) do not depend on this layer's output: request
+    // them into L2 now so that they are not DRAM round trips there
+    if (threadIdx.x == 0 && a.next_router != nullptr) {
+        for (int i = 0; i < n_re; ++i) bulk_prefetch_l2(a.next_router + (size_t)(b + i * G) * d, d * 4);
+        const int KT = d >> 7;
+        const int S = WFMT == 0 ? 64 : 128;
+        if (has_shared) {
+            for (int m = 0; m < 2; ++m) {
+                bulk_prefetch_l2(a.next_codes + ((size_t)E * 3 + m) * a.cpm + (size_t)shared_unit * KT * 512, KT * 512);
+                bulk_prefetch_l2(a.next_scales + ((size_t)E * 3 + m) * a.spm + (size_t)shared_unit * KT * S, KT * S);
+            }
+        }
+        if (down_tile >= 0) {
+            bulk_prefetch_l2(a.next_codes + ((size_t)E * 3 + 2) * a.cpm + (size_t)(2 * down_tile) * KTf * 512,
+                             2 * KTf * 512);
+            bulk_prefetch_l2(a.next_scales + ((size_t)E * 3 + 2) * a.spm + (size_t)(2 * down_tile) * KTf * S,
+                             2 * KTf * S);
+        }
+    }
     if (down_tile < 0) return;
     // stage h rows as fp16 with a power-of-two scale per (token, slot) row
     const int n_rows = T * (k + 1);
@@ -589,7 +614,7 @@ cudaError_t prepare_decode_fused() {
 
 cudaError_t launch_decode_fused(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
                                 __nv_bfloat16* out, const __nv_bfloat16* residual, const FusedScratch& fs,
-                                int n_sms, cudaStream_t st) {
+                                int n_sms, cudaStream_t st, const LayerDev* next) {
     int n_slots = 0, offs[10];
     const size_t smem = fused_smem_bytes(s, T, n_sms, &n_slots, offs);
     if (smem == 0) return cudaErrorInvalidValue;
@@ -625,6 +650,9 @@ cudaError_t launch_decode_fused(const Shape& s, const LayerDev& L, const __nv_bf
     a.off_xbf = offs[8];
     a.off_ts = offs[9];
     a.ts_bytes = (int)tscale_bytes(s);
+    a.next_codes = next != nullptr ? next->codes : nullptr;
+    a.next_scales = next != nullptr ? next->scales : nullptr;
+    a.next_router = next != nullptr ? next->router : nullptr;
     void (*kern)(FusedArgs) = s.wfmt == 0 ? decode_fused_kernel<0> : decode_fused_kernel<1>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(n_sms);

@@ -108,7 +108,7 @@ size_t fused_smem_bytes(const Shape& s, int T, int n_sms, int* n_slots_out, int 
 cudaError_t prepare_decode_fused();   // once per device: shared-memory opt-in
 cudaError_t launch_decode_fused(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
                                 __nv_bfloat16* out, const __nv_bfloat16* residual, const FusedScratch& fs,
-                                int n_sms, cudaStream_t st);
+                                int n_sms, cudaStream_t st, const LayerDev* next = nullptr);
 
 // prefill_fp4.cu: tensor-core kernels for large T
 cudaError_t prepare_prefill();   // once per device: shared-memory opt-in
