@@ -9,11 +9,11 @@ namespace flint {
 namespace {
 
 // Canonical row-major NVFP4 (codes [R][K/2], E4M3 scales [R][K/16]) ->
-// swizzled tiles: tile (rt, kt) of 128 rows x 256 elements at
-// tiles + (rt*KT + kt)*16 KiB and its scales at sf + (rt*KT + kt)*2 KiB.
+// blocks: block (rt, kt) of 128 rows x 256 elements at blocks + (rt*KT + kt) *
+// 18 KiB, its swizzled codes first and its scales after them.
 // One thread per 16 bytes of codes.
 __global__ void pack_fp4_tiles_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-                                      uint8_t* __restrict__ tiles, uint8_t* __restrict__ sf, int R, int K) {
+                                      uint8_t* __restrict__ blocks, int R, int K) {
     const int KT = K / kGK;
     const long n16 = (long)R * (K / 2) / 16;
     for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n16; i += (long)gridDim.x * blockDim.x) {
@@ -22,12 +22,12 @@ __global__ void pack_fp4_tiles_kernel(const uint8_t* __restrict__ codes, const u
         const int col = (int)(byte % (K / 2));      // byte within the row
         const int rt = row / kGM, r = row % kGM;
         const int kt = col / 128, j = col % 128;    // 128 bytes (256 elements) per k-tile
-        const size_t tile = (size_t)rt * KT + kt;
+        uint8_t* blk = blocks + ((size_t)rt * KT + kt) * kGBlk;
         const uint4 v = *reinterpret_cast<const uint4*>(codes + byte);
-        *reinterpret_cast<uint4*>(tiles + tile * kGTile + swz_offset(r, j)) = v;
+        *reinterpret_cast<uint4*>(blk + swz_offset(r, j)) = v;
         // scales: this 16-byte chunk covers 32 elements = 2 scale bytes
         const uint8_t* s = scales + (size_t)row * (K / 16) + col / 8;
-        uint8_t* d = sf + tile * kGSf + r * 16 + j / 8;
+        uint8_t* d = blk + kGTile + r * 16 + j / 8;
         d[0] = s[0];
         d[1] = s[1];
     }
@@ -35,9 +35,7 @@ __global__ void pack_fp4_tiles_kernel(const uint8_t* __restrict__ codes, const u
 
 struct DebugGemm {
     const uint8_t* a;
-    const uint8_t* asf;
     const uint8_t* b;
-    const uint8_t* bsf;
     float* d;
     int mt, nt, kt, N;
     __device__ int n_items() const { return mt * nt; }
@@ -45,16 +43,14 @@ struct DebugGemm {
     __device__ Pre pre(const Fp4Item&, int, int) const { return {}; }
     __device__ void item(int i, Fp4Item& w) const {
         const int m = i / nt, n = i % nt;
-        w.a = a + (size_t)m * kt * kGTile;
-        w.asf = asf + (size_t)m * kt * kGSf;
-        w.b = b + (size_t)n * kt * kGTile;
-        w.bsf = bsf + (size_t)n * kt * kGSf;
+        w.a = a + (size_t)m * kt * kGBlk;
+        w.b = b + (size_t)n * kt * kGBlk;
         w.kt = kt;
         w.m = m;
         w.n = n;
         w.aux = 0;
     }
-    static constexpr int kStages = 4;
+    static constexpr int kStages = 3;
     static constexpr int kEpiSmemPerWarp = 0;
     __device__ void epilogue_finish() const {}
     __device__ void epilogue(const Fp4Item& w, Pre, uint32_t taddr, int row, int half, uint8_t*) const {
@@ -74,12 +70,12 @@ struct DebugGemm {
 
 }  // namespace
 
-cudaError_t pack_fp4_tiles(const uint8_t* codes, const uint8_t* scales, uint8_t* tiles, uint8_t* sf, int R, int K,
+cudaError_t pack_fp4_tiles(const uint8_t* codes, const uint8_t* scales, uint8_t* blocks, int R, int K,
                            cudaStream_t st) {
     const long n16 = (long)R * (K / 2) / 16;
-    long blocks = (n16 + 255) / 256;
-    if (blocks > 148 * 16) blocks = 148 * 16;
-    pack_fp4_tiles_kernel<<<(int)blocks, 256, 0, st>>>(codes, scales, tiles, sf, R, K);
+    long grid = (n16 + 255) / 256;
+    if (grid > 148 * 16) grid = 148 * 16;
+    pack_fp4_tiles_kernel<<<(int)grid, 256, 0, st>>>(codes, scales, blocks, R, K);
     return cudaGetLastError();
 }
 
@@ -103,16 +99,15 @@ extern "C" flint_status flint_moe_debug_fp4_gemm(const uint8_t* a_codes, const u
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int KT = K / kGK;
     uint8_t* buf = nullptr;
-    const size_t at = (size_t)(M / kGM) * KT * kGTile, asf = (size_t)(M / kGM) * KT * kGSf;
-    const size_t bt = (size_t)(N / kGN) * KT * kGTile, bsf = (size_t)(N / kGN) * KT * kGSf;
+    const size_t ab = (size_t)(M / kGM) * KT * kGBlk, bb = (size_t)(N / kGN) * KT * kGBlk;
     uint32_t* status = nullptr;
-    if (cudaMalloc(&buf, at + asf + bt + bsf + 256) != cudaSuccess) return FLINT_ENOMEM;
-    status = reinterpret_cast<uint32_t*>(buf + at + asf + bt + bsf);
+    if (cudaMalloc(&buf, ab + bb + 256) != cudaSuccess) return FLINT_ENOMEM;
+    status = reinterpret_cast<uint32_t*>(buf + ab + bb);
     cudaError_t e = cudaMemsetAsync(status, 0, 4, st);
-    if (e == cudaSuccess) e = pack_fp4_tiles(a_codes, a_scales, buf, buf + at, M, K, st);
-    if (e == cudaSuccess) e = pack_fp4_tiles(b_codes, b_scales, buf + at + asf, buf + at + asf + bt, N, K, st);
+    if (e == cudaSuccess) e = pack_fp4_tiles(a_codes, a_scales, buf, M, K, st);
+    if (e == cudaSuccess) e = pack_fp4_tiles(b_codes, b_scales, buf + ab, N, K, st);
     if (e == cudaSuccess) {
-        DebugGemm p{buf, buf + at, buf + at + asf, buf + at + asf + bt, d, M / kGM, N / kGN, KT, N};
+        DebugGemm p{buf, buf + ab, d, M / kGM, N / kGN, KT, N};
         const int items = (M / kGM) * (N / kGN);
         fp4_gemm_kernel<DebugGemm><<<items < 148 ? items : 148, kGThreads, fp4_gemm_smem<DebugGemm>(), st>>>(p, status);
         e = cudaGetLastError();

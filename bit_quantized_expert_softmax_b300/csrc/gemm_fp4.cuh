@@ -4,24 +4,29 @@
 // per 16 elements along K.
 //
 // Operands are stored in global memory already in the shared-memory image the
-// MMA reads ("swizzled tiles"): a tile is 128 rows x 256 K-elements, 128 bytes
-// per row, rows 128 bytes apart, the 16-byte chunk c of row r stored at chunk
-// c ^ (r % 8) (the 128-byte swizzle). Its scale factors are 128 rows x 16
-// bytes, row-major. One 1-D bulk copy per tile moves it into shared memory.
+// MMA reads: a "block" (18 KiB) is one tile of 128 rows x 256 K-elements
+// (16 KiB: 128 bytes per row, rows 128 bytes apart, the 16-byte chunk c of row
+// r stored at chunk c ^ (r % 8), the 128-byte swizzle) followed by its scale
+// factors (2 KiB: 128 rows x 16 bytes, row-major). The blocks of one row tile
+// are contiguous along K, so one 1-D bulk copy moves two k-tiles of an operand,
+// codes and scales, into shared memory: a stage is two copies of 36 KiB. (The
+// bulk-copy engine moves ~0.3 us worth of copies at a time per SM whatever
+// their size, so few large copies matter more than their count of bytes.)
 //
 // Warp roles of a CTA (448 threads, one CTA per SM):
-//   warp 0      producer: bulk-copies A, B and their scales into a ring of
-//               P::kStages stages
+//   warp 0      producer: bulk-copies A and B (two k-tiles each, with their
+//               scales) into a ring of P::kStages stages
 //   warp 1      allocates tensor memory; one thread issues the MMAs
-//               (M=128, N=128, K=64 each; 4 per stage) into one of two
+//               (M=128, N=128, K=64 each; 4 per k-tile) into one of two
 //               accumulators
 //   warps 2..5  scale writers: shared memory -> tensor memory (tcgen05.st),
 //               one row (lane) per thread
 //   warps 6..13 epilogue: tensor memory -> registers -> the problem's store;
 //               two warps per lane quadrant, each taking half of the 128
 //               accumulator columns
-// Tensor memory columns: accumulators [0,128) and [128,256); per stage s the
-// A scales at 256+32s..+15 and the B scales at 256+32s+16..+31 (s < 8).
+// Tensor memory columns: accumulators [0,128) and [128,256); per stage s and
+// k-tile i of the stage the A scales at 256+64s+32i..+15 and the B scales at
+// 256+64s+32i+16..+31 (s < 4).
 //
 // Scale layout in tensor memory (per MMA of K = 64, 4 columns): lane m0 of
 // every 32-lane quadrant, column m1 (0..3) holds the four UE4M3 scales (one
@@ -36,17 +41,17 @@ namespace flint {
 constexpr int kGM = 128, kGN = 128, kGK = 256;
 constexpr int kGTile = kGM * kGK / 2;          // 16 KiB of packed E2M1
 constexpr int kGSf = kGM * kGK / 16;           // 2 KiB of UE4M3 scales
-constexpr int kGStage = 2 * kGTile + 2 * kGSf; // A, B, scales of A, scales of B
-constexpr int kGMaxStages = 8;
+constexpr int kGBlk = kGTile + kGSf;           // one k-tile of one operand with its scales
+constexpr int kGKPS = 2;                       // k-tiles per stage
+constexpr int kGStage = 2 * kGKPS * kGBlk;     // [A blocks][B blocks]
+constexpr int kGMaxStages = 4;                 // tensor-memory columns: 256 + 64 per stage
 constexpr int kGThreads = 448;
 constexpr int kGEpiWarps = 8;
 
 // One output tile of a problem.
 struct Fp4Item {
-    const uint8_t* a;    // first k-tile of A (k-tiles of one row tile are contiguous)
-    const uint8_t* asf;
-    const uint8_t* b;
-    const uint8_t* bsf;
+    const uint8_t* a;    // first block of A's row tile (blocks contiguous along K)
+    const uint8_t* b;    // first block of B's row tile
     int kt;              // number of k-tiles
     int m, n, aux;       // problem-defined (row tile, column tile, group)
 };
@@ -62,6 +67,7 @@ __host__ __device__ __forceinline__ int swz_offset(int r, int j) {
 template <class P>
 constexpr int fp4_gemm_smem() {
     static_assert(P::kStages >= 2 && P::kStages <= kGMaxStages, "stage count");
+    static_assert(256 + 64 * P::kStages <= 512, "tensor-memory columns");
     return P::kStages * kGStage + kGEpiWarps * P::kEpiSmemPerWarp + 1024;
 }
 
@@ -112,19 +118,18 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
             for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
                 const Fp4Item w = nxt;
                 if (i + (int)gridDim.x < n_items) prob.item(i + gridDim.x, nxt);
-                for (int kt = 0; kt < w.kt; ++kt, ++kcount) {
+                for (int k0 = 0; k0 < w.kt; k0 += kGKPS, ++kcount) {
                     const int s = kcount % kGStages;
                     const uint32_t use = kcount / kGStages;
                     if (use > 0 && !mbar_wait_bounded(&empty[s], (use - 1) & 1, status)) {
                         ok = false;
                         break;
                     }
+                    const int n = w.kt - k0 < kGKPS ? w.kt - k0 : kGKPS;
                     uint8_t* st = sm + s * kGStage;
-                    mbar_arrive_expect_tx(&full[s], kGStage);
-                    bulk_g2s(st, w.a + (size_t)kt * kGTile, kGTile, &full[s]);
-                    bulk_g2s(st + kGTile, w.b + (size_t)kt * kGTile, kGTile, &full[s]);
-                    bulk_g2s(st + 2 * kGTile, w.asf + (size_t)kt * kGSf, kGSf, &full[s]);
-                    bulk_g2s(st + 2 * kGTile + kGSf, w.bsf + (size_t)kt * kGSf, kGSf, &full[s]);
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * n * kGBlk));
+                    bulk_g2s(st, w.a + (size_t)k0 * kGBlk, (uint32_t)(n * kGBlk), &full[s]);
+                    bulk_g2s(st + kGKPS * kGBlk, w.b + (size_t)k0 * kGBlk, (uint32_t)(n * kGBlk), &full[s]);
                 }
             }
         }
@@ -142,7 +147,7 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
                 if (n_done >= 2 && !mbar_wait_bounded(&accempty[buf], ((n_done >> 1) - 1) & 1, status)) break;
                 tc_fence_after();
                 const uint32_t acc = tmem + buf * kGN;
-                for (int kt = 0; kt < w.kt; ++kt, ++kcount) {
+                for (int k0 = 0; k0 < w.kt; k0 += kGKPS, ++kcount) {
                     const int s = kcount % kGStages;
                     const uint32_t use = kcount / kGStages;
                     if (!mbar_wait_bounded(&sfready[s], use & 1, status)) {
@@ -150,13 +155,17 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
                         break;
                     }
                     tc_fence_after();
+                    const int n = w.kt - k0 < kGKPS ? w.kt - k0 : kGKPS;
                     const uint8_t* st = sm + s * kGStage;
-                    const uint64_t da = sdesc_kmajor_sw128(st);
-                    const uint64_t db = sdesc_kmajor_sw128(st + kGTile);
-                    const uint32_t sfa = tmem + 256 + 32 * s, sfb = sfa + 16;
+                    for (int i = 0; i < n; ++i) {
+                        const uint64_t da = sdesc_kmajor_sw128(st + i * kGBlk);
+                        const uint64_t db = sdesc_kmajor_sw128(st + (kGKPS + i) * kGBlk);
+                        const uint32_t sfa = tmem + 256 + 64 * s + 32 * i, sfb = sfa + 16;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)   // 64 E2M1 = 32 bytes = 2 descriptor units per MMA
-                        umma_nvfp4(acc, da + 2 * j, db + 2 * j, idesc, sfa + 4 * j, sfb + 4 * j, (kt | j) != 0);
+                        for (int j = 0; j < 4; ++j)   // 64 E2M1 = 32 bytes = 2 descriptor units per MMA
+                            umma_nvfp4(acc, da + 2 * j, db + 2 * j, idesc, sfa + 4 * j, sfb + 4 * j,
+                                       (k0 | i | j) != 0);
+                    }
                     umma_commit(&empty[s]);
                 }
                 umma_commit(&accfull[buf]);
@@ -175,7 +184,7 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
         for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
             const Fp4Item w = nxt;
             if (i + (int)gridDim.x < n_items) prob.item(i + gridDim.x, nxt);
-            for (int kt = 0; kt < w.kt; ++kt, ++kcount) {
+            for (int k0 = 0; k0 < w.kt; k0 += kGKPS, ++kcount) {
                 const int s = kcount % kGStages;
                 const uint32_t use = kcount / kGStages;
                 const bool got = mbar_wait_bounded(&full[s], use & 1, status);
@@ -183,14 +192,15 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
                     ok = false;
                     break;
                 }
+                const int n = w.kt - k0 < kGKPS ? w.kt - k0 : kGKPS;
                 const uint8_t* st = sm + s * kGStage;
-#pragma unroll
-                for (int op = 0; op < 2; ++op) {
-                    const uint8_t* sf = st + 2 * kGTile + op * kGSf;
+                for (int q = 0; q < 2 * n; ++q) {
+                    const int i = q >> 1, op = q & 1;
+                    const uint8_t* sf = st + (op * kGKPS + i) * kGBlk + kGTile;
                     uint4 r[4];
 #pragma unroll
                     for (int m1 = 0; m1 < 4; ++m1) r[m1] = *reinterpret_cast<const uint4*>(sf + (lane + 32 * m1) * 16);
-                    const uint32_t col = tmem + lane_base + 256 + 32 * s + 16 * op;
+                    const uint32_t col = tmem + lane_base + 256 + 64 * s + 32 * i + 16 * op;
                     // MMA j (K elements 64j..64j+63) reads word j of each row
                     tmem_st4(col + 0, r[0].x, r[1].x, r[2].x, r[3].x);
                     tmem_st4(col + 4, r[0].y, r[1].y, r[2].y, r[3].y);

@@ -133,7 +133,7 @@ cudaError_t launch_act_quant(const __nv_bfloat16* x, int T, int K, uint8_t* code
                              cudaStream_t st);
 
 // gemm_fp4.cu: swizzled-tile packing for the block-scaled FP4 GEMM
-cudaError_t pack_fp4_tiles(const uint8_t* codes, const uint8_t* scales, uint8_t* tiles, uint8_t* sf, int R, int K,
+cudaError_t pack_fp4_tiles(const uint8_t* codes, const uint8_t* scales, uint8_t* blocks, int R, int K,
                            cudaStream_t st);
 cudaError_t prepare_gemm_fp4();
 

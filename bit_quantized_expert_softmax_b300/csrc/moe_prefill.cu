@@ -108,15 +108,16 @@ __device__ __forceinline__ float quant_row(const uint4 (&raw)[EPL / 8], uint32_t
     return s_t;
 }
 
-// Write the lane's part of row r of a swizzled row tile (K elements; lane
-// owns elements [lane*EPL, (lane+1)*EPL)).
+// Write the lane's part of row r of a row tile of blocks (K elements; lane
+// owns elements [lane*EPL, (lane+1)*EPL)): codes into the swizzled tile, scales
+// after it, of the lane's k-tile block.
 template <int EPL>
-__device__ __forceinline__ void store_row_swizzled(uint8_t* tiles, uint8_t* sf, int r, int lane,
+__device__ __forceinline__ void store_row_swizzled(uint8_t* blocks, int r, int lane,
                                                    const uint32_t (&codes)[EPL / 8], uint32_t sbytes) {
     const int e0 = lane * EPL;                 // first element
     const int kt = e0 / kGK;
     const int j = (e0 % kGK) / 2;              // byte within the 128-byte row of the k-tile
-    uint8_t* t = tiles + (size_t)kt * kGTile;
+    uint8_t* t = blocks + (size_t)kt * kGBlk;
     if constexpr (EPL >= 32) {
 #pragma unroll
         for (int c = 0; c < EPL / 32; ++c)
@@ -125,7 +126,7 @@ __device__ __forceinline__ void store_row_swizzled(uint8_t* tiles, uint8_t* sf, 
     } else {
         *reinterpret_cast<uint2*>(t + swz_offset(r, j)) = make_uint2(codes[0], codes[1]);
     }
-    uint8_t* s = sf + (size_t)kt * kGSf + r * 16 + (e0 % kGK) / 16;
+    uint8_t* s = t + kGTile + r * 16 + (e0 % kGK) / 16;
     if constexpr (EPL == 64) {
         *reinterpret_cast<uint32_t*>(s) = sbytes;
     } else {
@@ -153,20 +154,16 @@ struct PrefillCtx {
     // numbered in padded-row order)
     // activations
     const __nv_bfloat16* x;
-    uint8_t* a1;
-    uint8_t* a1sf;
+    uint8_t* a1;              // gate/up A blocks [row tiles][d/256]
     float* sa;
     __nv_bfloat16* h;
-    uint8_t* a2;
-    uint8_t* a2sf;
+    uint8_t* a2;              // down A blocks [row tiles][f/256]
     int* prow;                // [padded rows] bucketed position of the row's assignment, -1: padding
     float* yscale;            // [padded rows] s_h * down tensor scale * routing weight
     __nv_bfloat16* y;         // [T*(k+1)][d] weighted contributions by bucketed position
-    // weights
+    // weights (blocks)
     const uint8_t* w1;
-    const uint8_t* w1sf;
     const uint8_t* w2;
-    const uint8_t* w2sf;
     const float* tscale;
     int T, d, f, E, k;
 };
@@ -258,8 +255,7 @@ __global__ void __launch_bounds__(256, 4) quant_x_kernel(PrefillCtx c) {
         for (int j = 0; j <= c.k; ++j) {
             const int rp = __shfl_sync(0xffffffffu, my_rp, j);
             const int rt = rp / kGM, r = rp % kGM;
-            store_row_swizzled<EPL>(c.a1 + (size_t)rt * KT * kGTile, c.a1sf + (size_t)rt * KT * kGSf, r, lane, codes,
-                                    sb);
+            store_row_swizzled<EPL>(c.a1 + (size_t)rt * KT * kGBlk, r, lane, codes, sb);
             if (lane == 0) c.sa[rp] = s_t;
         }
     }
@@ -290,8 +286,7 @@ __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
         const float wr = p < c.T * c.k ? c.wts[__ldg(c.perm + p)] : 1.0f;
         yscale_w = c.tscale[c.slot_expert[slot] * 3 + 2] * wr;
     }
-    uint8_t* tiles = c.a2 + (size_t)mt * KT * kGTile;
-    uint8_t* sf = c.a2sf + (size_t)mt * KT * kGSf;
+    uint8_t* blocks = c.a2 + (size_t)mt * KT * kGBlk;
     const __nv_bfloat16* hr = c.h + (size_t)row * c.f + lane * EPL;
     uint4 raw[EPL / 8];
 #pragma unroll
@@ -299,7 +294,7 @@ __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
     uint32_t codes[EPL / 8];
     uint32_t sb = 0;
     const float s_t = quant_row<EPL>(raw, codes, sb);
-    store_row_swizzled<EPL>(tiles, sf, r, lane, codes, sb);
+    store_row_swizzled<EPL>(blocks, r, lane, codes, sb);
     if (lane == 0) {
         c.prow[row] = p;
         c.yscale[row] = s_t * yscale_w;
@@ -310,16 +305,14 @@ __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
 struct Gemm1 {
     PrefillCtx c;
     int NT, KT;
-    static constexpr int kStages = 6;
+    static constexpr int kStages = 3;
     __device__ int n_items() const { return c.meta[2] * NT; }
     __device__ void item(int i, Fp4Item& w) const {
         const int mt = i / NT, nt = i % NT;
         const int e = c.mt_e[mt];
         const int rt = mt;
-        w.a = c.a1 + (size_t)rt * KT * kGTile;
-        w.asf = c.a1sf + (size_t)rt * KT * kGSf;
-        w.b = c.w1 + ((size_t)e * NT + nt) * KT * kGTile;
-        w.bsf = c.w1sf + ((size_t)e * NT + nt) * KT * kGSf;
+        w.a = c.a1 + (size_t)rt * KT * kGBlk;
+        w.b = c.w1 + ((size_t)e * NT + nt) * KT * kGBlk;
         w.kt = KT;
         w.m = mt;
         w.n = nt;
@@ -378,17 +371,15 @@ constexpr int kEpiPitch = 144;   // 128 bytes of a row + 16: conflict-free 16-by
 struct Gemm2 {
     PrefillCtx c;
     int NT, KT;
-    static constexpr int kStages = 5;
+    static constexpr int kStages = 2;
     static constexpr int kEpiSmemPerWarp = 32 * kEpiPitch;
     __device__ int n_items() const { return c.meta[2] * NT; }
     __device__ void item(int i, Fp4Item& w) const {
         const int mt = i / NT, nt = i % NT;
         const int e = c.mt_e[mt];
         const int rt = mt;
-        w.a = c.a2 + (size_t)rt * KT * kGTile;
-        w.asf = c.a2sf + (size_t)rt * KT * kGSf;
-        w.b = c.w2 + ((size_t)e * NT + nt) * KT * kGTile;
-        w.bsf = c.w2sf + ((size_t)e * NT + nt) * KT * kGSf;
+        w.a = c.a2 + (size_t)rt * KT * kGBlk;
+        w.b = c.w2 + ((size_t)e * NT + nt) * KT * kGBlk;
         w.kt = KT;
         w.m = mt;
         w.n = nt;
@@ -493,12 +484,13 @@ __global__ void __launch_bounds__(256) combine_kernel(PrefillCtx c, __nv_bfloat1
     }
 }
 
-// Gate/up weights -> swizzled tiles with gate and up interleaved per 64 rows:
-// N-tile nt rows 0..63 = gate rows 64nt.., rows 64..127 = up rows 64nt..
-// Down weights -> plain row tiles. One thread per 16 bytes of codes.
+// Gate/up weights -> blocks (swizzled tile + scales) with gate and up
+// interleaved per 64 rows: N-tile nt rows 0..63 = gate rows 64nt.., rows
+// 64..127 = up rows 64nt.. Down weights -> plain row tiles of blocks. One
+// thread per 16 bytes of codes.
 __global__ void pack_expert_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-                                   uint8_t* __restrict__ w1, uint8_t* __restrict__ w1sf, uint8_t* __restrict__ w2,
-                                   uint8_t* __restrict__ w2sf, int n_slots, int d, int f, size_t cpm, size_t spm) {
+                                   uint8_t* __restrict__ w1, uint8_t* __restrict__ w2, int n_slots, int d, int f,
+                                   size_t cpm, size_t spm) {
     const int NT1 = 2 * f / kGN, KT1 = d / kGK, NT2 = d / kGN, KT2 = f / kGK;
     const long per_mat16 = (long)cpm / 16;
     const long total = (long)n_slots * 3 * per_mat16;
@@ -511,25 +503,20 @@ __global__ void pack_expert_kernel(const uint8_t* __restrict__ codes, const uint
         const int kt = col / 128, j = col % 128;
         const uint8_t* src = codes + ((size_t)e * 3 + mat) * cpm + byte;
         const uint8_t* ssrc = scales + ((size_t)e * 3 + mat) * spm + (size_t)row * (K / 16) + col / 8;
-        uint8_t* tile;
-        uint8_t* sft;
+        uint8_t* blk;
         int r;
         if (mat < 2) {
             const int nt = row / 64;
             r = (row % 64) + 64 * mat;
-            const size_t t = ((size_t)e * NT1 + nt) * KT1 + kt;
-            tile = w1 + t * kGTile;
-            sft = w1sf + t * kGSf;
+            blk = w1 + (((size_t)e * NT1 + nt) * KT1 + kt) * kGBlk;
         } else {
             const int nt = row / kGN;
             r = row % kGN;
-            const size_t t = ((size_t)e * NT2 + nt) * KT2 + kt;
-            tile = w2 + t * kGTile;
-            sft = w2sf + t * kGSf;
+            blk = w2 + (((size_t)e * NT2 + nt) * KT2 + kt) * kGBlk;
         }
-        *reinterpret_cast<uint4*>(tile + swz_offset(r, j)) = *reinterpret_cast<const uint4*>(src);
-        sft[r * 16 + j / 8] = ssrc[0];
-        sft[r * 16 + j / 8 + 1] = ssrc[1];
+        *reinterpret_cast<uint4*>(blk + swz_offset(r, j)) = *reinterpret_cast<const uint4*>(src);
+        blk[kGTile + r * 16 + j / 8] = ssrc[0];
+        blk[kGTile + r * 16 + j / 8 + 1] = ssrc[1];
     }
 }
 
@@ -573,11 +560,9 @@ size_t prefill_weight_bytes(const Shape& s) {
 
 cudaError_t pack_prefill_weights(const Shape& s, const uint8_t* codes, const uint8_t* scales, uint8_t* dst,
                                  cudaStream_t st) {
-    const size_t w1 = (size_t)s.n_slots() * (2 * s.f / kGN) * (s.d / kGK) * kGTile;
-    const size_t w1sf = (size_t)s.n_slots() * (2 * s.f / kGN) * (s.d / kGK) * kGSf;
-    const size_t w2 = (size_t)s.n_slots() * (s.d / kGN) * (s.f / kGK) * kGTile;
-    pack_expert_kernel<<<148 * 16, 256, 0, st>>>(codes, scales, dst, dst + w1, dst + w1 + w1sf, dst + w1 + w1sf + w2,
-                                                s.n_slots(), s.d, s.f, s.codes_per_matrix(), s.scales_per_matrix());
+    const size_t w1 = (size_t)s.n_slots() * (2 * s.f / kGN) * (s.d / kGK) * kGBlk;
+    pack_expert_kernel<<<148 * 16, 256, 0, st>>>(codes, scales, dst, dst + w1, s.n_slots(), s.d, s.f,
+                                                s.codes_per_matrix(), s.scales_per_matrix());
     return cudaGetLastError();
 }
 
@@ -631,20 +616,14 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     c.sa = reinterpret_cast<float*>(take(rt * kGM * 4));
     c.prow = reinterpret_cast<int*>(take(rt * kGM * 4));
     c.yscale = reinterpret_cast<float*>(take(rt * kGM * 4));
-    c.a1 = take(rt * (s.d / kGK) * kGTile);
-    c.a1sf = take(rt * (s.d / kGK) * kGSf);
-    c.a2 = take(rt * (s.f / kGK) * kGTile);
-    c.a2sf = take(rt * (s.f / kGK) * kGSf);
+    c.a1 = take(rt * (s.d / kGK) * kGBlk);
+    c.a2 = take(rt * (s.f / kGK) * kGBlk);
     c.h = reinterpret_cast<__nv_bfloat16*>(take(rt * kGM * s.f * 2));
     c.y = reinterpret_cast<__nv_bfloat16*>(take((size_t)Tm * (s.k + 1) * s.d * 2));
     c.x = x;
-    const size_t w1 = (size_t)s.n_slots() * (2 * s.f / kGN) * (s.d / kGK) * kGTile;
-    const size_t w1sf = (size_t)s.n_slots() * (2 * s.f / kGN) * (s.d / kGK) * kGSf;
-    const size_t w2 = (size_t)s.n_slots() * (s.d / kGN) * (s.f / kGK) * kGTile;
+    const size_t w1 = (size_t)s.n_slots() * (2 * s.f / kGN) * (s.d / kGK) * kGBlk;
     c.w1 = L.prefill;
-    c.w1sf = L.prefill + w1;
-    c.w2 = L.prefill + w1 + w1sf;
-    c.w2sf = L.prefill + w1 + w1sf + w2;
+    c.w2 = L.prefill + w1;
     c.tscale = L.tscale;
     c.T = T;
     c.d = s.d;
