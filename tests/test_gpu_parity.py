@@ -206,6 +206,23 @@ def test_layer_tiny_q4_1(fm, T):
     assert_out_close(got, ref.out, f"tiny q4_1 T={T}")
 
 
+# Other shapes of the same layer: the smallest width, the most experts per
+# token, few experts, and widths with more k-tiles than the Flint shape; each
+# at one and two tokens (single-launch path), a ragged small batch and a batch
+# past the small-T router (multi-kernel path).
+@pytest.mark.parametrize("d,f,E,k,wfmt", [
+    (128, 128, 32, 8, synth.WFMT_NVFP4),
+    (256, 128, 64, 2, synth.WFMT_Q4_1),
+    (384, 256, 96, 1, synth.WFMT_NVFP4),
+    (1024, 384, 128, 4, synth.WFMT_Q4_1),
+])
+@pytest.mark.parametrize("T", [1, 2, 7, 70])
+def test_layer_other_shapes(fm, d, f, E, k, wfmt, T):
+    cfg = _cfg(1, d=d, f=f, n_experts=E, top_k=k, wfmt=wfmt, tokens=T, name=f"shape_{d}_{f}_{E}_{k}")
+    got, ref = _layer_parity(fm, cfg, T)
+    assert_out_close(got, ref.out, f"d={d} f={f} E={E} k={k} wfmt={wfmt} T={T}")
+
+
 @pytest.mark.parametrize("T", [1, 2])
 def test_layer_flint_decode_nvfp4(fm, T):
     cfg = _cfg(2)
