@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(256) plan_kernel(PrefillCtx c, int* meta_rw) {
 // slot). Padding rows of the tiles are never written: their products are
 // discarded by the epilogues.
 template <int EPL>
-__global__ void __launch_bounds__(256, 4) quant_x_kernel(PrefillCtx c) {
+__global__ void __launch_bounds__(256) quant_x_kernel(PrefillCtx c) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KT = c.d / kGK;
     const int shared_slot = c.meta[0] - 1;
