@@ -428,7 +428,7 @@ def main():
         ap.error("--warmup must be >= 3")
     cfg = synth.CONFIGS[args.config]
     if args.steps is None:
-        args.steps = {1: 20000, 2: 20000, 3: 10000, 4: 5000, 5: 40}[args.config]
+        args.steps = {1: 20000, 2: 20000, 3: 10000, 4: 5000, 5: 3000}[args.config]
     world, rank, local = dist_env()
     if world != args.gpus and world > 1:
         print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
