@@ -130,11 +130,14 @@ struct UnitRef {
     int np;
 };
 
-// Gate/up of up to kMaxWaveUnits half-units at once. The MMA's 16 A rows are
-// the half-unit's 8 gate rows (rows 0-7) and the same 8 up rows (rows 8-15),
-// so one m16n8k16 chain yields both projections. Warp w takes k-tile w of
-// every half-unit, then the CTA reduces the 16 warp partials in warp order
-// and writes h = silu(g) * u (fp32) for the 8 rows.
+// Gate/up of up to kMaxWaveUnits half-units. The MMA's 16 A rows are the
+// half-unit's 8 gate rows (rows 0-7) and the same 8 up rows (rows 8-15), so
+// one m16n8k16 chain yields both projections. Warp w takes k-tiles w, w+16,
+// ... of each half-unit in turn and leaves its partial in red[unit][warp];
+// then 64 threads per half-unit reduce the 16 warp partials in warp order and
+// write h = silu(g) * u (fp32) for its 8 rows. The unit loop is not unrolled:
+// this code runs once per launch, so its size (instruction fetch), not its
+// instruction-level parallelism, is what costs.
 template <int WFMT>
 __device__ void gateup_units(const FusedArgs& a, const UnitRef* units, int n_units, const __half* x16s,
                              const float* xinv, const float* tss, float* red) {
@@ -142,24 +145,19 @@ __device__ void gateup_units(const FusedArgs& a, const UnitRef* units, int n_uni
     const int g = lane >> 2, c = lane & 3;
     const int KT = a.d >> 7;
     const int S = WFMT == 0 ? 64 : 128;
-    float acc[kMaxWaveUnits][4];
-#pragma unroll
-    for (int v = 0; v < kMaxWaveUnits; ++v)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[v][j] = 0.f;
-    for (int kt = warp; kt < KT; kt += kFWarps) {
-#pragma unroll
-        for (int v = 0; v < kMaxWaveUnits; ++v) {
-            if (v >= n_units) break;
-            const UnitRef& un = units[v];
-            const uint8_t* cg = un.slab;
-            const uint8_t* cu = un.slab + KT * 512;
-            const uint8_t* sg = un.slab + 2 * KT * 512;
-            const uint8_t* su = sg + KT * S;
+#pragma unroll 1
+    for (int v = 0; v < n_units; ++v) {
+        const UnitRef un = units[v];
+        const uint8_t* cg = un.slab;
+        const uint8_t* cu = un.slab + KT * 512;
+        const uint8_t* sg = un.slab + 2 * KT * 512;
+        const uint8_t* su = sg + KT * S;
+        const int tb = (g < un.np) ? un.pairs[g].t : -1;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kt = warp; kt < KT; kt += kFWarps) {
             const uint4 wg = *reinterpret_cast<const uint4*>(cg + kt * 512 + lane * 16);
             const uint4 wu = *reinterpret_cast<const uint4*>(cu + kt * 512 + lane * 16);
             const TileScales<WFMT> sc = lds_scales<WFMT>(sg + kt * S, su + kt * S, g);
-            const int tb = (g < un.np) ? un.pairs[g].t : -1;
             uint32_t b[16];
             if (tb >= 0) {
                 lds_b16(x16s + (size_t)tb * a.d + kt * 128 + c * 32, b);
@@ -171,40 +169,36 @@ __device__ void gateup_units(const FusedArgs& a, const UnitRef* units, int n_uni
             decode_tile<WFMT>(wg, wu, sc, fa);
 #pragma unroll
             for (int st = 0; st < 8; ++st)
-                mma_16816(acc[v], fa[st][0], fa[st][1], fa[st][2], fa[st][3], b[2 * st], b[2 * st + 1]);
+                mma_16816(acc, fa[st][0], fa[st][1], fa[st][2], fa[st][3], b[2 * st], b[2 * st + 1]);
         }
+        *reinterpret_cast<float4*>(red + (size_t)(v * kFWarps + warp) * 128 + lane * 4) =
+            make_float4(acc[0], acc[1], acc[2], acc[3]);
     }
+    __syncthreads();
+    if (threadIdx.x < 64 * n_units) {
+        // thread i of unit v: fragment lane ln = i/2, column 2*(ln%4) + i%2,
+        // row ln/4; its gate sum is element ln*4 + (i%2), its up sum element + 2
+        const int v = threadIdx.x >> 6, i = threadIdx.x & 63;
+        const UnitRef& un = units[v];
+        const int ln = i >> 1, jj = i & 1;
+        const int n = 2 * (ln & 3) + jj;
+        if (n < un.np) {
+            const float* rv = red + (size_t)v * kFWarps * 128 + ln * 4 + jj;
+            float sg_ = 0.f, su_ = 0.f;
 #pragma unroll
-    for (int v = 0; v < kMaxWaveUnits; ++v) {
-        if (v >= n_units) break;
-        // cross-warp reduction of the K partials: red[warp][128]
-#pragma unroll
-        for (int j = 0; j < 4; ++j) red[warp * 128 + lane * 4 + j] = acc[v][j];
-        __syncthreads();
-        if (threadIdx.x < 64) {
-            // thread i: fragment lane ln = i/2, column 2*(ln%4) + i%2, row ln/4;
-            // its gate sum is element ln*4 + (i%2), its up sum element + 2
-            const UnitRef& un = units[v];
-            const int ln = threadIdx.x >> 1, jj = threadIdx.x & 1;
-            const int n = 2 * (ln & 3) + jj;
-            if (n < un.np) {
-                const int eg = ln * 4 + jj;
-                float sg_ = 0.f, su_ = 0.f;
-#pragma unroll
-                for (int w = 0; w < kFWarps; ++w) {
-                    sg_ += red[w * 128 + eg];
-                    su_ += red[w * 128 + eg + 2];
-                }
-                const Pair p = un.pairs[n];
-                const float gv = sg_ * tss[un.e * 3 + 0] * xinv[p.t];
-                const float uv = su_ * tss[un.e * 3 + 1] * xinv[p.t];
-                const float hv = gv / (1.0f + expf(-gv)) * uv;
-                const int row = un.g8 * 8 + (ln >> 2);
-                a.h[((size_t)p.t * (a.k + 1) + p.j) * a.f + row] = hv;
+            for (int w = 0; w < kFWarps; ++w) {
+                sg_ += rv[w * 128];
+                su_ += rv[w * 128 + 2];
             }
+            const Pair p = un.pairs[n];
+            const float gv = sg_ * tss[un.e * 3 + 0] * xinv[p.t];
+            const float uv = su_ * tss[un.e * 3 + 1] * xinv[p.t];
+            const float hv = gv / (1.0f + expf(-gv)) * uv;
+            const int row = un.g8 * 8 + (ln >> 2);
+            a.h[((size_t)p.t * (a.k + 1) + p.j) * a.f + row] = hv;
         }
-        __syncthreads();
     }
+    __syncthreads();
 }
 
 template <int WFMT>
@@ -332,14 +326,22 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     grid_arrive(gsync);
     // while the barrier completes: stage the hidden states as fp16, scaled
     // per token, fragment-permuted
+    // (thread i holds elements 4(i + 512q) .. +3, stored as half2 pairs)
     for (int t = 0; t < T; ++t) {
-        float xv[8];
+        float xv[2][4];
         float amax = 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int i = threadIdx.x + q * kFThreads;
-            xv[q] = i < d ? __bfloat162float(xbf[(size_t)t * d + i]) : 0.f;
-            amax = fmaxf(amax, fabsf(xv[q]));
+        for (int q = 0; q < 2; ++q) {
+            const int i = (threadIdx.x + q * kFThreads) * 4;
+            uint2 raw = make_uint2(0u, 0u);
+            if (i < d) raw = *reinterpret_cast<const uint2*>(xbf + (size_t)t * d + i);
+            const float2 p0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+            const float2 p1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+            xv[q][0] = p0.x;
+            xv[q][1] = p0.y;
+            xv[q][2] = p1.x;
+            xv[q][3] = p1.y;
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(p0.x), fabsf(p0.y)), fmaxf(fabsf(p1.x), fabsf(p1.y))));
         }
         amax = warp_max(amax);
         if (lane == 0) rpart[warp] = amax;
@@ -348,10 +350,15 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
 #pragma unroll
         for (int w = 0; w < kFWarps; ++w) m = fmaxf(m, rpart[w]);
         const float mult = f16_range_mult(m);
+        __half2* xrow = reinterpret_cast<__half2*>(x16s + (size_t)t * d);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int i = threadIdx.x + q * kFThreads;
-            if (i < d) x16s[(size_t)t * d + (i & ~127) + kperm_pos(i & 127)] = __float2half_rn(xv[q] * mult);
+        for (int q = 0; q < 2; ++q) {
+            const int i = (threadIdx.x + q * kFThreads) * 4;
+            if (i < d) {
+                __half2* tile = xrow + ((i & ~127) >> 1);
+                tile[kperm_pos(i & 127) >> 1] = __floats2half2_rn(xv[q][0] * mult, xv[q][1] * mult);
+                tile[kperm_pos((i & 127) + 2) >> 1] = __floats2half2_rn(xv[q][2] * mult, xv[q][3] * mult);
+            }
         }
         if (threadIdx.x == 0) xinv[t] = 1.0f / mult;
         __syncthreads();
@@ -410,35 +417,44 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     // shared expert's unit (its slab landed in P0) is computed while the
     // first wave's slabs are in flight
     const int n_rs = a.n_slots - 1;
-    bool shared_done = !has_shared;
-    for (int u0 = b; u0 < n_units || !shared_done; u0 += G * n_rs) {
-        __syncthreads();
-        if (threadIdx.x == 0 && u0 < n_units) {
-            fence_proxy_async_smem();
-            for (int s2 = 0; s2 < n_rs; ++s2) {
-                const int u = u0 + s2 * G;
-                if (u < n_units)
-                    issue_half<WFMT>(a, act[u / units_per_expert], u % units_per_expert,
-                                     slots + (size_t)s2 * a.unit_bytes, bars + s2);
+    // one gateup_units call site: each pass computes either the shared
+    // half-unit or one wave of routed half-units
+    bool shared_pending = has_shared, wave_issued = false;
+    for (int u0 = b;;) {
+        if (!wave_issued && u0 < n_units) {
+            __syncthreads();   // the previous wave's slots have been read
+            if (threadIdx.x == 0) {
+                fence_proxy_async_smem();
+                for (int s2 = 0; s2 < n_rs; ++s2) {
+                    const int u = u0 + s2 * G;
+                    if (u < n_units)
+                        issue_half<WFMT>(a, act[u / units_per_expert], u % units_per_expert,
+                                         slots + (size_t)s2 * a.unit_bytes, bars + s2);
+                }
             }
-        }
-        if (!shared_done) {
-            wait_all(bars + shared_slot, 0);
-            UnitRef su{slots + (size_t)shared_slot * a.unit_bytes, E, shared_unit, shared_pairs, T};
-            if (ok) gateup_units<WFMT>(a, &su, 1, x16s, xinv, tss, acc);
-            shared_done = true;
+            wave_issued = true;
         }
         UnitRef wave[kMaxWaveUnits];
         int nw = 0;
-        for (int s2 = 0; s2 < n_rs; ++s2) {
-            const int u = u0 + s2 * G;
-            if (u >= n_units) break;
-            const uint32_t ph = (slot_phase >> s2) & 1u;
-            wait_all(bars + s2, ph);
-            slot_phase ^= 1u << s2;
-            const int q = u / units_per_expert;
-            wave[nw++] = UnitRef{slots + (size_t)s2 * a.unit_bytes, act[q], u % units_per_expert, act_pairs + q * 2,
-                                 act_np[q]};
+        if (shared_pending) {
+            wait_all(bars + shared_slot, 0);
+            wave[nw++] = UnitRef{slots + (size_t)shared_slot * a.unit_bytes, E, shared_unit, shared_pairs, T};
+            shared_pending = false;
+        } else if (u0 < n_units) {
+            for (int s2 = 0; s2 < n_rs; ++s2) {
+                const int u = u0 + s2 * G;
+                if (u >= n_units) break;
+                const uint32_t ph = (slot_phase >> s2) & 1u;
+                wait_all(bars + s2, ph);
+                slot_phase ^= 1u << s2;
+                const int q = u / units_per_expert;
+                wave[nw++] = UnitRef{slots + (size_t)s2 * a.unit_bytes, act[q], u % units_per_expert,
+                                     act_pairs + q * 2, act_np[q]};
+            }
+            u0 += G * n_rs;
+            wave_issued = false;
+        } else {
+            break;
         }
         if (ok && nw > 0) gateup_units<WFMT>(a, wave, nw, x16s, xinv, tss, acc);
     }
@@ -476,22 +492,29 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     if (down_tile < 0) return;
     // stage h rows as fp16 with a power-of-two scale per (token, slot) row
     const int n_rows = T * (k + 1);
+    // (lane l holds elements 4(32q + l) .. +3; pairs stay adjacent under the
+    // fragment permutation, so they are stored as half2)
+    const int nq = f >> 7;
     for (int r = warp; r < n_rows; r += kFWarps) {
-        const float* hr = a.h + (size_t)r * f;
-        float hv[32];
+        const float4* hr = reinterpret_cast<const float4*>(a.h + (size_t)r * f);
+        float4 hv[8];
         float amax = 0.f;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-            const int i = lane + 32 * q;
-            hv[q] = i < f ? __ldcg(hr + i) : 0.f;
-            amax = fmaxf(amax, fabsf(hv[q]));
+        for (int q = 0; q < 8; ++q) {
+            hv[q] = q < nq ? __ldcg(hr + q * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(hv[q].x), fabsf(hv[q].y)), fmaxf(fabsf(hv[q].z), fabsf(hv[q].w))));
         }
         amax = warp_max(amax);
         const float mult = f16_range_mult(amax);
+        __half2* hrow = reinterpret_cast<__half2*>(h16s + (size_t)r * f);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-            const int i = lane + 32 * q;
-            if (i < f) h16s[(size_t)r * f + (i & ~127) + kperm_pos(i & 127)] = __float2half_rn(hv[q] * mult);
+        for (int q = 0; q < 8; ++q) {
+            if (q < nq) {
+                const int i = (q * 32 + lane) * 4;
+                __half2* tile = hrow + ((i & ~127) >> 1);
+                tile[kperm_pos(i & 127) >> 1] = __floats2half2_rn(hv[q].x * mult, hv[q].y * mult);
+                tile[kperm_pos((i & 127) + 2) >> 1] = __floats2half2_rn(hv[q].z * mult, hv[q].w * mult);
+            }
         }
         if (lane == 0) hinv[r] = 1.0f / mult;
     }
@@ -571,7 +594,7 @@ size_t fused_smem_bytes(const Shape& s, int T, int n_sms, int* n_slots_out, int 
     if ((size_t)2 * s.d * 4 > unit) return 0;
     if ((s.E + n_sms - 1) / n_sms > 2) return 0;
     if (s.d / 16 > n_sms || s.f / 8 > n_sms) return 0;
-    const size_t red = (size_t)kFWarps * 2 * 128 * 4;
+    const size_t red = (size_t)kMaxWaveUnits * kFWarps * 128 * 4;
     const size_t accb = (size_t)(max_active + 1) * 2 * 128 * 4;
     int n_rs = (units + n_sms - 1) / n_sms;                 // routed slots for one wave
     if (n_rs > 3) n_rs = 3;

@@ -44,26 +44,26 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ Lrow, int E,
     uint32_t taken = 0;
     float my_v = 0.f;   // lane j < k ends with selection j
     int my_i = 0;
+    // one selection per round; the round is not unrolled (the code runs once
+    // per token and its size, not its trip count, sets its cost)
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) {
+        uint32_t bk = 0u;
+        int bi = 0x7fffffff;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        if (j < k) {
-            uint32_t bk = 0u;
-            int bi = 0x7fffffff;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if (i < n && !((taken >> i) & 1u) && (key[i] > bk || bi == 0x7fffffff)) {
-                    bk = key[i];
-                    bi = i * 32 + lane;
-                }
+        for (int i = 0; i < 8; ++i) {
+            if (i < n && !((taken >> i) & 1u) && (key[i] > bk || bi == 0x7fffffff)) {
+                bk = key[i];
+                bi = i * 32 + lane;
             }
-            const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-            const int wi =
-                (int)__reduce_min_sync(0xffffffffu, (bk == mk && bi != 0x7fffffff) ? (uint32_t)bi : 0xffffffffu);
-            if ((wi & 31) == lane) taken |= 1u << (wi >> 5);
-            if (lane == j) {
-                my_v = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk);
-                my_i = wi;
-            }
+        }
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        const int wi =
+            (int)__reduce_min_sync(0xffffffffu, (bk == mk && bi != 0x7fffffff) ? (uint32_t)bi : 0xffffffffu);
+        if ((wi & 31) == lane) taken |= 1u << (wi >> 5);
+        if (lane == j) {
+            my_v = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk);
+            my_i = wi;
         }
     }
     // renormalised softmax over the selected logits (selection 0 is the maximum)
