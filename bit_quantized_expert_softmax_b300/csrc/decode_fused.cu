@@ -154,6 +154,7 @@ __device__ void gateup_units(const FusedArgs& a, const UnitRef* units, int n_uni
         const uint8_t* su = sg + KT * S;
         const int tb = (g < un.np) ? un.pairs[g].t : -1;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
         for (int kt = warp; kt < KT; kt += kFWarps) {
             const uint4 wg = *reinterpret_cast<const uint4*>(cg + kt * 512 + lane * 16);
             const uint4 wu = *reinterpret_cast<const uint4*>(cu + kt * 512 + lane * 16);
@@ -201,13 +202,17 @@ __device__ void gateup_units(const FusedArgs& a, const UnitRef* units, int n_uni
     __syncthreads();
 }
 
-template <int WFMT>
+template <int WFMT, int TT>
 __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a) {
+    // TT: the token count, a template parameter so that the per-token loops
+    // compile to straight code for exactly that count
+    static_assert(TT >= 1 && TT <= kFusedMaxT, "token count");
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const int G = gridDim.x, b = blockIdx.x;
-    const int T = a.T, d = a.d, f = a.f, E = a.E, k = a.k;
+    constexpr int T = TT;
+    const int d = a.d, f = a.f, E = a.E, k = a.k;
     const int KTf = f >> 7;
     const int units_per_expert = f >> 3;                 // 8-row half-units
     const int down_tiles = d >> 4;
@@ -251,6 +256,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     };
 
     if (threadIdx.x == 0) {
+#pragma unroll 1
         for (int i = 0; i < a.n_slots + 4; ++i) mbar_init(bars + i, 1);
         mbar_fence_init();
     }
@@ -270,6 +276,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
         bulk_g2s(smem + a.off_ts, a.tscale, (uint32_t)a.ts_bytes, bar_x);
         if (n_re > 0) {
             mbar_arrive_expect_tx(bar_router, (uint32_t)(n_re * d * 4));
+#pragma unroll 1
             for (int i = 0; i < n_re; ++i)
                 bulk_g2s(slots + (size_t)i * d * 4, a.router + (size_t)(b + i * G) * d, d * 4, bar_router);
         }
@@ -294,6 +301,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
         float accv[2] = {0.f, 0.f};
         if (ok && i < n_re) {
             const float* wr = reinterpret_cast<const float*>(slots) + (size_t)i * d + part * seg;
+#pragma unroll 1
             for (int q = lane * 4; q < seg; q += 128) {
                 const float4 wv = *reinterpret_cast<const float4*>(wr + q);
                 for (int t = 0; t < T; ++t) {
@@ -367,6 +375,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
 
     // ------------------------------------------------------------------ P1
     // top-k of every token, computed by every CTA from the logits in L2
+#pragma unroll 1
     for (int i = threadIdx.x; i < T * E; i += kFThreads) lg[i] = __ldcg(a.logits + i);
     __syncthreads();
     if (warp < T) topk_warp<false>(lg + warp * E, E, k, sel + warp * 8, wsel + warp * 8, b == 0 ? a.status : nullptr);
@@ -425,6 +434,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
             __syncthreads();   // the previous wave's slots have been read
             if (threadIdx.x == 0) {
                 fence_proxy_async_smem();
+#pragma unroll 1
                 for (int s2 = 0; s2 < n_rs; ++s2) {
                     const int u = u0 + s2 * G;
                     if (u < n_units)
@@ -441,6 +451,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
             wave[nw++] = UnitRef{slots + (size_t)shared_slot * a.unit_bytes, E, shared_unit, shared_pairs, T};
             shared_pending = false;
         } else if (u0 < n_units) {
+#pragma unroll 1
             for (int s2 = 0; s2 < n_rs; ++s2) {
                 const int u = u0 + s2 * G;
                 if (u >= n_units) break;
@@ -463,6 +474,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     // not compete with them; they are needed only after the next barrier
     if (threadIdx.x == 0 && down_tile >= 0 && na > 0) {
         mbar_arrive_expect_tx(bar_drouted, (uint32_t)(na * a.down_bytes));
+#pragma unroll 1
         for (int q = 0; q < na; ++q)
             issue_down<WFMT>(a, act[q], down_tile, down + (size_t)(1 + q) * a.down_bytes, bar_drouted);
     }
@@ -473,6 +485,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     // down slab of this CTA) do not depend on this layer's output: request
     // them into L2 now so that they are not DRAM round trips there
     if (threadIdx.x == 0 && a.next_router != nullptr) {
+#pragma unroll 1
         for (int i = 0; i < n_re; ++i) bulk_prefetch_l2(a.next_router + (size_t)(b + i * G) * d, d * 4);
         const int KT = d >> 7;
         const int S = WFMT == 0 ? 64 : 128;
@@ -524,6 +537,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     // two halves of the k-tiles -> acc[q][half][16 rows][8 pairs]
     const int S = WFMT == 0 ? 64 : 128;
     const int kt_half = (KTf + 1) / 2;
+#pragma unroll 1
     for (int it = warp; it < 2 * (na + 1) && ok; it += kFWarps) {
         const int q = it >> 1, hf = it & 1;
         const uint8_t* slab = down + (size_t)q * a.down_bytes;
@@ -534,6 +548,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
         const int hrow = g < np ? pp[g].t * (k + 1) + pp[g].j : -1;
         float cacc[4] = {0.f, 0.f, 0.f, 0.f};
         const int kt1 = min(KTf, (hf + 1) * kt_half);
+#pragma unroll 1
         for (int kt = hf * kt_half; kt < kt1; ++kt) {
             const uint4 wg = *reinterpret_cast<const uint4*>(cd + kt * 512 + lane * 16);
             const uint4 wh = *reinterpret_cast<const uint4*>(cd + (KTf + kt) * 512 + lane * 16);
@@ -620,7 +635,8 @@ size_t fused_smem_bytes(const Shape& s, int T, int n_sms, int* n_slots_out, int 
 }
 
 cudaError_t prepare_decode_fused() {
-    void (*kerns[2])(FusedArgs) = {decode_fused_kernel<0>, decode_fused_kernel<1>};
+    void (*kerns[4])(FusedArgs) = {decode_fused_kernel<0, 1>, decode_fused_kernel<0, 2>, decode_fused_kernel<1, 1>,
+                                   decode_fused_kernel<1, 2>};
     for (auto kern : kerns) {
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, kern);
@@ -676,7 +692,8 @@ cudaError_t launch_decode_fused(const Shape& s, const LayerDev& L, const __nv_bf
     a.next_codes = next != nullptr ? next->codes : nullptr;
     a.next_scales = next != nullptr ? next->scales : nullptr;
     a.next_router = next != nullptr ? next->router : nullptr;
-    void (*kern)(FusedArgs) = s.wfmt == 0 ? decode_fused_kernel<0> : decode_fused_kernel<1>;
+    void (*kern)(FusedArgs) = s.wfmt == 0 ? (T == 1 ? decode_fused_kernel<0, 1> : decode_fused_kernel<0, 2>)
+                                          : (T == 1 ? decode_fused_kernel<1, 1> : decode_fused_kernel<1, 2>);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(n_sms);
     cfg.blockDim = dim3(kFThreads);
