@@ -76,7 +76,7 @@ __device__ void bucket_place_block(const int* __restrict__ sel, int a0, int a1, 
         const int a = r0 + threadIdx.x;
         int e = -1;
         if (a < a1) {
-            e = sel[a];
+            e = __ldcg(sel + a);   // written earlier in this kernel or the previous one
             if (e < 0 || e >= E) {
                 if (status) atomicOr(status, kStatusBadIndex);
                 e = -1;
@@ -109,7 +109,7 @@ __device__ void bucket_place_block(const int* __restrict__ sel, int a0, int a1, 
 // Per-expert counts of a chunk into smem cnt[E] (zeroed by the caller).
 __device__ void bucket_count_block(const int* __restrict__ sel, int a0, int a1, int E, int* cnt) {
     for (int a = a0 + threadIdx.x; a < a1; a += blockDim.x) {
-        int e = sel[a];
+        const int e = __ldcg(sel + a);
         if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
     }
 }
@@ -198,6 +198,10 @@ struct RouterArgs {
 // 2*blockIdx + w/4.
 // ---------------------------------------------------------------------------
 constexpr int kTokGroup = 8;   // tokens per CTA (one warp per token)
+// arrival counters of the token groups of router_small_kernel (after the
+// ones the expert kernels use)
+constexpr int kGroupCounters = kCounters - kSmallT / kTokGroup;
+static_assert(kGroupCounters > 64, "counter ranges overlap");
 
 // grid = (E/2 expert pairs, ceil(T/8) token groups). Each CTA bulk-copies its
 // two router rows and its (up to) 8 hidden rows into shared memory; warp w
@@ -261,23 +265,31 @@ __global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouterArgs
         stage_token_block(a.x + (size_t)t * d, d, a.ws.x16 + (size_t)t * d, a.ws.xinv + t, red);
     }
 
-    // last CTA to arrive finishes the routing
+    // the last CTA of this token group takes the top-k of its tokens (a warp
+    // per token, logits read through L2) ...
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-        uint32_t prev = atomicAdd(&a.ws.counters[0], 1u);
-        s_last = (prev == gridDim.x * gridDim.y - 1);
+        const uint32_t prev = atomicAdd(&a.ws.counters[kGroupCounters + blockIdx.y], 1u);
+        s_last = (prev == gridDim.x - 1);
     }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    // top-k per token: warp per token (logits read through L2)
-    for (int t = warp; t < T; t += 8) {
-        topk_warp<true>(a.ws.logits + (size_t)t * a.E, a.E, a.k, a.ws.idx + t * a.k, a.ws.w + t * a.k,
-                        a.ws.status);
+    if (warp < nt)
+        topk_warp<true>(a.ws.logits + (size_t)(t0 + warp) * a.E, a.E, a.k, a.ws.idx + (t0 + warp) * a.k,
+                        a.ws.w + (t0 + warp) * a.k, a.ws.status);
+    if (threadIdx.x == 0) a.ws.counters[kGroupCounters + blockIdx.y] = 0u;
+    // ... and the last token group to finish buckets all of them
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t prev = atomicAdd(&a.ws.counters[0], 1u);
+        s_last = (prev == gridDim.y - 1);
     }
     __syncthreads();
-    __threadfence_block();
+    if (!s_last) return;
+    __threadfence();
     // bucketing of the T*k assignments
     for (int i = threadIdx.x; i < a.E; i += blockDim.x) s_cnt[i] = 0;
     __syncthreads();
