@@ -201,8 +201,18 @@ __device__ void combine_rows(const ExpertArgs& a, int row0, int nrows) {
     }
 }
 
+// Per pass of up to kDownPos positions the CTA stages their h (already
+// fragment-permuted by the gate/up kernel) once in shared memory as fp16,
+// k-chunk by k-chunk, instead of every warp reading it from L2 per k-tile;
+// each warp's weight loads for the chunk are issued before the staging so
+// that the DRAM and L2 round trips overlap.
+constexpr int kDownPos = 8 * kNB;   // positions per pass
+constexpr int kDownKC = 4;          // k-tiles per staged chunk
+
 template <int WFMT>
 __global__ void __launch_bounds__(kThreads) down_kernel(ExpertArgs a) {
+    __shared__ __align__(16) __half hs[kDownPos * kDownKC * 128];   // [position][chunk K], fp16
+    __shared__ float hmul[kDownPos];
     __shared__ int s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
@@ -211,6 +221,7 @@ __global__ void __launch_bounds__(kThreads) down_kernel(ExpertArgs a) {
     const int n_slots = a.ws.meta[0];
     const int n_tasks = n_slots * blocks;
     const size_t tile_bytes_s = (WFMT == 0) ? 64 : 128;
+    constexpr int kRow = kDownKC * 128;   // staged halves per position
     for (int task = blockIdx.x; task < n_tasks; task += gridDim.x) {
         const int blk = task % blocks, slot = task / blocks;
         const int e = a.ws.slot_expert[slot];
@@ -221,49 +232,66 @@ __global__ void __launch_bounds__(kThreads) down_kernel(ExpertArgs a) {
         const float tsd = a.tscale[e * 3 + 2];
         const int r16 = blk * 4 + warp;
         const size_t rtg = (size_t)(2 * r16) * KT, rth = (size_t)(2 * r16 + 1) * KT;
-        for (int n0 = 0; n0 < cnt; n0 += 8 * kNB) {
-            const int nb = min(kNB, (cnt - n0 + 7) >> 3);
+        for (int n0 = 0; n0 < cnt; n0 += kDownPos) {
+            const int np = min(kDownPos, cnt - n0);
+            const int nb = (np + 7) >> 3;
             float acc[kNB][4];
 #pragma unroll
             for (int i = 0; i < kNB; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-            int posb[kNB];
-            float multb[kNB];
+            __syncthreads();   // the previous pass is done with hs and hmul
+            if (threadIdx.x < np) hmul[threadIdx.x] = f16_range_mult(__uint_as_float(a.ws.hamax[p0 + n0 + threadIdx.x]));
+            for (int kc = 0; kc < KT; kc += kDownKC) {
+                const int nkc = min(kDownKC, KT - kc);
+                uint4 wg[kDownKC], wh[kDownKC];
+                TileScales<WFMT> sc[kDownKC];
 #pragma unroll
-            for (int nt = 0; nt < kNB; ++nt) {
-                const int n = n0 + nt * 8 + g;
-                posb[nt] = (nt < nb && n < cnt) ? p0 + n : -1;
-                multb[nt] = posb[nt] >= 0 ? f16_range_mult(__uint_as_float(a.ws.hamax[posb[nt]])) : 1.f;
-            }
-            for (int kt = 0; kt < KT; ++kt) {
-                const uint4 wg = ldg_nc_v4(cd + (rtg + kt) * 512 + lane * 16);
-                const uint4 wh = ldg_nc_v4(cd + (rth + kt) * 512 + lane * 16);
-                const TileScales<WFMT> sc = load_scales<WFMT>(sd + (rtg + kt) * tile_bytes_s,
-                                                              sd + (rth + kt) * tile_bytes_s, g);
-                uint32_t fa[8][4];
-                decode_tile<WFMT>(wg, wh, sc, fa);
-#pragma unroll
-                for (int nt = 0; nt < kNB; ++nt) {
-                    if (nt >= nb) break;
-                    uint32_t b[16];
-                    if (posb[nt] >= 0) {
-                        const float4* hp = reinterpret_cast<const float4*>(
-                            a.ws.hf + (size_t)posb[nt] * a.f + kt * 128 + c * 32);
-                        const float m = multb[nt];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            float4 v = __ldcg(hp + q);
-                            b[2 * q + 0] = pack_half2(v.x * m, v.y * m);
-                            b[2 * q + 1] = pack_half2(v.z * m, v.w * m);
-                        }
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) b[q] = 0u;
+                for (int i = 0; i < kDownKC; ++i) {
+                    if (i < nkc) {
+                        wg[i] = ldg_nc_v4(cd + (rtg + kc + i) * 512 + lane * 16);
+                        wh[i] = ldg_nc_v4(cd + (rth + kc + i) * 512 + lane * 16);
+                        sc[i] = load_scales<WFMT>(sd + (rtg + kc + i) * tile_bytes_s, sd + (rth + kc + i) * tile_bytes_s,
+                                                  g);
                     }
+                }
+                __syncthreads();   // hmul written; the previous chunk's reads of hs are done
+                const int row_f4 = nkc * 32;   // float4 of one position in this chunk
+                for (int i = threadIdx.x; i < np * row_f4; i += kThreads) {
+                    const int pl = i / row_f4, q = i - pl * row_f4;
+                    const float4 v = __ldcg(
+                        reinterpret_cast<const float4*>(a.ws.hf + (size_t)(p0 + n0 + pl) * a.f + kc * 128) + q);
+                    const float m = hmul[pl];
+                    *reinterpret_cast<uint2*>(hs + pl * kRow + q * 4) =
+                        make_uint2(pack_half2(v.x * m, v.y * m), pack_half2(v.z * m, v.w * m));
+                }
+                __syncthreads();
+                for (int i = 0; i < nkc; ++i) {
+                    uint32_t fa[8][4];
+                    decode_tile<WFMT>(wg[i], wh[i], sc[i], fa);
 #pragma unroll
-                    for (int s = 0; s < 8; ++s)
-                        mma_16816(acc[nt], fa[s][0], fa[s][1], fa[s][2], fa[s][3], b[2 * s], b[2 * s + 1]);
+                    for (int nt = 0; nt < kNB; ++nt) {
+                        if (nt >= nb) break;
+                        const int pl = nt * 8 + g;
+                        uint32_t b[16];
+                        if (pl < np) {
+                            const uint4* hp = reinterpret_cast<const uint4*>(hs + pl * kRow + i * 128 + c * 32);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const uint4 v = hp[q];
+                                b[4 * q + 0] = v.x;
+                                b[4 * q + 1] = v.y;
+                                b[4 * q + 2] = v.z;
+                                b[4 * q + 3] = v.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) b[q] = 0u;
+                        }
+#pragma unroll
+                        for (int st = 0; st < 8; ++st)
+                            mma_16816(acc[nt], fa[st][0], fa[st][1], fa[st][2], fa[st][3], b[2 * st], b[2 * st + 1]);
+                    }
                 }
             }
             // epilogue: rows g, g+8 of this warp's tile; positions 2c, 2c+1 of each n-tile
@@ -277,11 +305,11 @@ __global__ void __launch_bounds__(kThreads) down_kernel(ExpertArgs a) {
                     const int pos = p0 + n;
                     const float wr = shared ? 1.0f : a.ws.w[__ldg(a.ws.perm + pos)];
                     const float mult = f16_range_mult(__uint_as_float(a.ws.hamax[pos]));
-                    const float sc = tsd / mult * wr;
+                    const float sc_ = tsd / mult * wr;
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int row = r16 * 16 + g + hh * 8;
-                        a.ws.yw[(size_t)pos * a.d + row] = acc[nt][hh * 2 + q] * sc;
+                        a.ws.yw[(size_t)pos * a.d + row] = acc[nt][hh * 2 + q] * sc_;
                     }
                 }
             }
