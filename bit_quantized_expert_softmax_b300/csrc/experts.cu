@@ -51,17 +51,23 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertArgs a) {
     const int g = lane >> 2, c = lane & 3;
     const int KT = a.d >> 7;
     const int tiles = a.f >> 4;
-    const int n_tasks = a.ws.meta[0] * tiles;
+    // a task is (slot, 16-row tile, pass of 8*kNB positions), the pass
+    // innermost: the passes of a slot with many positions run on different
+    // CTAs at once instead of one after another (a pass beyond the slot's
+    // positions is empty)
+    const int max_pass = (a.T + 8 * kNB - 1) / (8 * kNB);
+    const int n_tasks = a.ws.meta[0] * tiles * max_pass;
     const size_t tile_bytes_s = (WFMT == 0) ? 64 : 128;
     for (int task = blockIdx.x; task < n_tasks; task += gridDim.x) {
-        const int slot = task / tiles, r16 = task - slot * tiles;
+        const int pass = task % max_pass, rest = task / max_pass;
+        const int slot = rest / tiles, r16 = rest - slot * tiles;
         const int e = a.ws.slot_expert[slot];
         const int p0 = a.ws.slot_off[slot], cnt = a.ws.slot_cnt[slot];
         const uint8_t* cbase = a.codes + (size_t)e * 3 * a.codes_per_mat;
         const uint8_t* sbase = a.scales + (size_t)e * 3 * a.scales_per_mat;
         const float tsg = a.tscale[e * 3 + 0], tsu = a.tscale[e * 3 + 1];
         const size_t rtg = (size_t)(2 * r16) * KT, rth = (size_t)(2 * r16 + 1) * KT;
-        for (int n0 = 0; n0 < cnt; n0 += 8 * kNB) {
+        for (int n0 = pass * 8 * kNB; n0 < cnt && n0 < (pass + 1) * 8 * kNB; n0 += 8 * kNB) {
             const int nb = min(kNB, (cnt - n0 + 7) >> 3);
             float accg[kNB][4], accu[kNB][4];
 #pragma unroll
@@ -208,6 +214,7 @@ __device__ void combine_rows(const ExpertArgs& a, int row0, int nrows) {
 // that the DRAM and L2 round trips overlap.
 constexpr int kDownPos = 8 * kNB;   // positions per pass
 constexpr int kDownKC = 4;          // k-tiles per staged chunk
+static_assert(kDownPos >= kFuseCombineT, "the fused combine counts one arrival per (slot, block)");
 
 template <int WFMT>
 __global__ void __launch_bounds__(kThreads) down_kernel(ExpertArgs a) {
@@ -219,11 +226,16 @@ __global__ void __launch_bounds__(kThreads) down_kernel(ExpertArgs a) {
     const int KT = a.f >> 7;
     const int blocks = a.d >> 6;
     const int n_slots = a.ws.meta[0];
-    const int n_tasks = n_slots * blocks;
+    // task = (slot, 64-row block, pass of kDownPos positions), pass innermost
+    // (with the fused combine, T <= kFuseCombineT gives one pass per slot, so
+    // each (slot, block) task still arrives exactly once)
+    const int max_pass = (a.T + kDownPos - 1) / kDownPos;
+    const int n_tasks = n_slots * blocks * max_pass;
     const size_t tile_bytes_s = (WFMT == 0) ? 64 : 128;
     constexpr int kRow = kDownKC * 128;   // staged halves per position
     for (int task = blockIdx.x; task < n_tasks; task += gridDim.x) {
-        const int blk = task % blocks, slot = task / blocks;
+        const int pass = task % max_pass, rest = task / max_pass;
+        const int blk = rest % blocks, slot = rest / blocks;
         const int e = a.ws.slot_expert[slot];
         const int p0 = a.ws.slot_off[slot], cnt = a.ws.slot_cnt[slot];
         const bool shared = (e == a.E);
@@ -232,7 +244,7 @@ __global__ void __launch_bounds__(kThreads) down_kernel(ExpertArgs a) {
         const float tsd = a.tscale[e * 3 + 2];
         const int r16 = blk * 4 + warp;
         const size_t rtg = (size_t)(2 * r16) * KT, rth = (size_t)(2 * r16 + 1) * KT;
-        for (int n0 = 0; n0 < cnt; n0 += kDownPos) {
+        for (int n0 = pass * kDownPos; n0 < cnt && n0 < (pass + 1) * kDownPos; n0 += kDownPos) {
             const int np = min(kDownPos, cnt - n0);
             const int nb = (np + 7) >> 3;
             float acc[kNB][4];
@@ -387,7 +399,8 @@ cudaError_t launch_gateup(const Shape& s, const LayerDev& L, int T, const Worksp
                           cudaStream_t st, int* n_launch) {
     ExpertArgs a = make_args(s, L, T, ws);
     const int max_slots = min(s.E, T * s.k) + s.n_shared;
-    const int grid = grid_for(max_slots * (s.f / 16));
+    const int max_pass = (T + 8 * kNB - 1) / (8 * kNB);
+    const int grid = grid_for(max_slots * (s.f / 16) * max_pass);
     if (s.wfmt == 0)
         gateup_kernel<0><<<grid, kThreads, 0, st>>>(a);
     else
@@ -403,7 +416,8 @@ cudaError_t launch_down(const Shape& s, const LayerDev& L, int T, const Workspac
     a.out = out;
     a.residual = residual;
     const int max_slots = min(s.E, T * s.k) + s.n_shared;
-    const int grid = grid_for(max_slots * (s.d / 64));
+    const int max_pass = (T + kDownPos - 1) / kDownPos;
+    const int grid = grid_for(max_slots * (s.d / 64) * max_pass);
     if (s.wfmt == 0)
         down_kernel<0><<<grid, kThreads, 0, st>>>(a);
     else
