@@ -168,10 +168,6 @@ struct PrefillCtx {
     int T, d, f, E, k;
 };
 
-__device__ __forceinline__ int ctx_token(const PrefillCtx& c, int p) {
-    return p < c.T * c.k ? __ldg(c.perm + p) / c.k : p - c.T * c.k;
-}
-
 // M-tile table: 128-row tiles of every active slot, padded offsets. One CTA
 // of 256 threads; slot i (< 256) is handled by thread i, slot 256 (the shared
 // expert when all 256 routed experts are active) by thread 0 afterwards.
@@ -231,7 +227,7 @@ __global__ void __launch_bounds__(256) plan_kernel(PrefillCtx c, int* meta_rw) {
 // slot). Padding rows of the tiles are never written: their products are
 // discarded by the epilogues.
 template <int EPL>
-__global__ void __launch_bounds__(256) quant_x_kernel(PrefillCtx c) {
+__global__ void __launch_bounds__(256, 3) quant_x_kernel(PrefillCtx c) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KT = c.d / kGK;
     const int shared_slot = c.meta[0] - 1;
@@ -262,42 +258,57 @@ __global__ void __launch_bounds__(256) quant_x_kernel(PrefillCtx c) {
 }
 
 // Quantise each h row (bf16, f elements) into the down GEMM's A tiles and
-// write the down GEMM's per-row epilogue data. One warp per padded row (the
-// grid covers the largest possible row count; warps past the actual rows
-// return); the row's lookups are issued before its h is loaded.
+// write the down GEMM's per-row epilogue data. A warp takes kQhRows
+// consecutive padded rows (one M-tile's): it loads all of their h first (the
+// buffer holds every row the grid covers, so the loads need no lookup), then
+// resolves the rows' slots and routing weights while those loads are in
+// flight. Warps past the actual rows return; padding rows get prow = -1.
+constexpr int kQhRows = 4;
+
 template <int EPL>
 __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_rows = c.meta[2] * kGM;
     const int KT = c.f / kGK;
-    const int row = blockIdx.x * 8 + warp;
-    if (row >= n_rows) return;
-    const int mt = row / kGM, r = row % kGM;
-    const int slot = c.mt_slot[mt], m = c.mt_m[mt];
-    const int q = m * kGM + r;
-    if (q >= c.slot_cnt[slot]) {           // padding row: its codes are never read back
-        if (lane == 0) c.prow[row] = -1;
-        return;
+    const int row0 = (blockIdx.x * 8 + warp) * kQhRows;
+    uint4 raw[kQhRows][EPL / 8];
+#pragma unroll
+    for (int i = 0; i < kQhRows; ++i) {
+        const __nv_bfloat16* hr = c.h + (size_t)(row0 + i) * c.f + lane * EPL;
+#pragma unroll
+        for (int j = 0; j < EPL / 8; ++j) raw[i][j] = *reinterpret_cast<const uint4*>(hr + 8 * j);
     }
+    const int n_rows = c.meta[2] * kGM;
+    if (row0 >= n_rows) return;
+    const int mt = row0 / kGM, r0 = row0 % kGM;
+    const int slot = c.mt_slot[mt], m = c.mt_m[mt];
+    // lane i < kQhRows: position and epilogue scale of row row0 + i (-1: padding)
+    int p = -1;
     float yscale_w = 0.f;
-    int p = 0;
-    if (lane == 0) {
-        p = c.slot_off[slot] + q;
-        const float wr = p < c.T * c.k ? c.wts[__ldg(c.perm + p)] : 1.0f;
-        yscale_w = c.tscale[c.slot_expert[slot] * 3 + 2] * wr;
+    if (lane < kQhRows) {
+        const int q = m * kGM + r0 + lane;
+        if (q < c.slot_cnt[slot]) {
+            p = c.slot_off[slot] + q;
+            const float wr = p < c.T * c.k ? c.wts[__ldg(c.perm + p)] : 1.0f;
+            yscale_w = c.tscale[c.slot_expert[slot] * 3 + 2] * wr;
+        }
     }
     uint8_t* blocks = c.a2 + (size_t)mt * KT * kGBlk;
-    const __nv_bfloat16* hr = c.h + (size_t)row * c.f + lane * EPL;
-    uint4 raw[EPL / 8];
 #pragma unroll
-    for (int i = 0; i < EPL / 8; ++i) raw[i] = *reinterpret_cast<const uint4*>(hr + 8 * i);
-    uint32_t codes[EPL / 8];
-    uint32_t sb = 0;
-    const float s_t = quant_row<EPL>(raw, codes, sb);
-    store_row_swizzled<EPL>(blocks, r, lane, codes, sb);
-    if (lane == 0) {
-        c.prow[row] = p;
-        c.yscale[row] = s_t * yscale_w;
+    for (int i = 0; i < kQhRows; ++i) {
+        const int pi = __shfl_sync(0xffffffffu, p, i);
+        const float ys = __shfl_sync(0xffffffffu, yscale_w, i);
+        if (pi < 0) {   // padding row: its codes are never read back
+            if (lane == 0) c.prow[row0 + i] = -1;
+            continue;
+        }
+        uint32_t codes[EPL / 8];
+        uint32_t sb = 0;
+        const float s_t = quant_row<EPL>(raw[i], codes, sb);
+        store_row_swizzled<EPL>(blocks, r0 + i, lane, codes, sb);
+        if (lane == 0) {
+            c.prow[row0 + i] = pi;
+            c.yscale[row0 + i] = s_t * ys;
+        }
     }
 }
 
@@ -636,7 +647,8 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     Gemm1 g1{c, 2 * s.f / kGN, s.d / kGK};
     fp4_gemm_kernel<Gemm1><<<148, kGThreads, fp4_gemm_smem<Gemm1>(), st>>>(g1, ws.status);
     mark(2);
-    quant_h_kernel<16><<<(unsigned)((rt * kGM + 7) / 8), 256, 0, st>>>(c);
+    static_assert(kGM % (8 * kQhRows) == 0, "a CTA's rows stay inside one M-tile");
+    quant_h_kernel<16><<<(unsigned)(rt * kGM / (8 * kQhRows)), 256, 0, st>>>(c);
     mark(3);
     Gemm2 g2{c, s.d / kGN, s.f / kGK};
     fp4_gemm_kernel<Gemm2><<<148, kGThreads, fp4_gemm_smem<Gemm2>(), st>>>(g2, ws.status);
