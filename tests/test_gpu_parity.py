@@ -207,14 +207,17 @@ def test_layer_tiny_q4_1(fm, T):
 
 
 # Other shapes of the same layer: the smallest width, the most experts per
-# token, few experts, and widths with more k-tiles than the Flint shape; each
-# at one and two tokens (single-launch path), a ragged small batch and a batch
-# past the small-T router (multi-kernel path).
+# token, few experts, widths with more k-tiles than the Flint shape, and an
+# expert width of 5 k-tiles (the down kernel stages h in chunks of 4 k-tiles:
+# one full chunk and a ragged one); each at one and two tokens (single-launch
+# path), a ragged small batch and a batch past the small-T router (multi-kernel
+# path; its shared-expert slot spans three passes of 32 positions).
 @pytest.mark.parametrize("d,f,E,k,wfmt", [
     (128, 128, 32, 8, synth.WFMT_NVFP4),
     (256, 128, 64, 2, synth.WFMT_Q4_1),
     (384, 256, 96, 1, synth.WFMT_NVFP4),
     (1024, 384, 128, 4, synth.WFMT_Q4_1),
+    (512, 640, 64, 6, synth.WFMT_NVFP4),
 ])
 @pytest.mark.parametrize("T", [1, 2, 7, 70])
 def test_layer_other_shapes(fm, d, f, E, k, wfmt, T):
