@@ -171,6 +171,64 @@ def make_layer(cfg: LayerConfig, layer: int = 0, seed: int | None = None) -> Lay
     return LayerWeights(cfg, router, bias, codes, scales, tscale)
 
 
+# ---------------------------------------------------------------------------
+# The 4-bit output head (lm_head) and the uniforms its sampler draws with
+# ---------------------------------------------------------------------------
+# The blog gives ~2.5B active parameters per token counting the output head
+# and ~2.2B for the body ("The architecture is an argument about memory
+# bandwidth", Active parameters bullet): a head of ~0.3B parameters, i.e. a
+# vocabulary of ~0.3e9 / d = ~146k rows at d = 2048; 146,432 is that figure
+# rounded to a multiple of 128.
+#
+# Head recipe: NVFP4 codes uniform over all 16 codes, E4M3 block-scale bytes
+# uniform over 0x28..0x3F, tensor scale 0.0353 * U(0.75, 1.25): weights of
+# standard deviation ~0.1, so that x ~ N(0, 1) gives logits of standard
+# deviation ~4.5 and a peaked distribution in which top-p cuts inside the
+# top-20.
+_S_HEAD_CODES, _S_HEAD_SCALES, _S_HEAD_TSCALE, _S_UNIFORM = 20, 21, 22, 23
+
+
+@dataclasses.dataclass(frozen=True)
+class HeadConfig:
+    d: int = 2048
+    vocab: int = 146_432
+    tokens: int = 1
+    seed: int = 0
+    name: str = ""
+
+
+HEAD_CONFIGS = {
+    "flint": HeadConfig(name="flint_lm_head_V146432_T1_nvfp4"),
+    "small": HeadConfig(d=512, vocab=1000, tokens=3, name="lm_head_d512_V1000_T3_nvfp4"),
+}
+
+
+@dataclasses.dataclass
+class HeadWeights:
+    """Canonical host layout of the head: codes uint8 [V, d/2] (two E2M1 codes
+    per byte, low nibble first), scales uint8 [V, d/16] (E4M3), tensor_scale
+    float32."""
+    cfg: HeadConfig
+    codes: np.ndarray
+    scales: np.ndarray
+    tensor_scale: np.float32
+
+
+def make_head(cfg: HeadConfig, seed: int | None = None) -> HeadWeights:
+    seed = cfg.seed if seed is None else seed
+    V, d = cfg.vocab, cfg.d
+    codes = _rng(seed, 0, _S_HEAD_CODES).integers(0, 256, size=(V, d // 2), dtype=np.uint8)
+    scales = _rng(seed, 0, _S_HEAD_SCALES).integers(0x28, 0x40, size=(V, d // 16), dtype=np.uint8)
+    tscale = np.float32(0.0353 * _rng(seed, 0, _S_HEAD_TSCALE).uniform(0.75, 1.25))
+    return HeadWeights(cfg, codes, scales, tscale)
+
+
+def make_uniforms(tokens: int, seed: int = 0, stream: int = 0) -> np.ndarray:
+    """float32 [tokens] in [0, 1): the sampler's random draws, one per token."""
+    u = _rng(seed, 20_000 + stream, _S_UNIFORM).random(tokens).astype(np.float32)
+    return np.minimum(u, np.nextafter(np.float32(1.0), np.float32(0.0)))
+
+
 def make_hidden(cfg: LayerConfig, tokens: int | None = None, seed: int | None = None,
                 stream: int = 0) -> np.ndarray:
     """Hidden states as bfloat16 bit patterns, uint16 [T, d]."""

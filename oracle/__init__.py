@@ -7,4 +7,4 @@ kept independent of the CUDA path: the two share no code, and neither imports
 the other. The seeded input generator
 (``bit_quantized_expert_softmax_b300.synth``) is the only thing both consume.
 """
-from . import formats, moe  # noqa: F401
+from . import formats, lm_head, moe  # noqa: F401
