@@ -369,6 +369,116 @@ def run_ours(args, cfg, world, rank, local):
     return res
 
 
+HEAD_MAX_T = 8   # tokens per output-head call (the library's limit)
+
+
+def run_head(args, world, local):
+    """The 4-bit output head and its sampler (temperature 1.0, top-k 20,
+    top-p 0.95): one step = the head GEMV of the step's tokens + one draw per
+    token, with L2 flushed between steps."""
+    import torch
+    from bit_quantized_expert_softmax_b300 import build
+    build.build()
+    from bit_quantized_expert_softmax_b300 import flint_moe as fm
+
+    hcfg = synth.HEAD_CONFIGS["flint"]
+    T, V, d = hcfg.tokens, hcfg.vocab, hcfg.d
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    m = fm.MoE(synth.LayerConfig(d=d, f=128, tokens=HEAD_MAX_T, name="head_host"), max_tokens=HEAD_MAX_T,
+               device=local)
+    hw = synth.make_head(hcfg)
+    fm.flint_moe_load_lm_head(m.h, hw.codes, hw.scales, hw.tensor_scale)
+    bits = synth.make_hidden(hcfg, tokens=T)
+    x = fm.hidden_to_device(bits, local)
+    logits = torch.empty((T, V), dtype=torch.float32, device=device)
+    u = torch.from_numpy(synth.make_uniforms(T)).to(device)
+    tokens = torch.empty((T,), dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
+
+    def step(x_in=x):
+        fm.flint_moe_lm_head(m.h, x_in, T, logits, stream)
+        fm.flint_moe_sample(m.h, logits, T, 1.0, 20, 0.95, u, tokens, None, stream)
+
+    def timed(n, fn):
+        st_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        en_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(50_000_000)
+        for i in range(n):
+            flush.zero_()
+            st_ev[i].record(stream)
+            fn()
+            en_ev[i].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in zip(st_ev, en_ev)]
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert fm.flint_moe_status(m.h) == fm.FLINT_OK
+    K = args.steps
+    barrier(world, device)
+    launches0 = fm.flint_moe_launch_count(m.h)
+    with ClockSampler(gpu_id_for(device)) as clk:
+        step_ms = timed(K, step)
+    launches = fm.flint_moe_launch_count(m.h) - launches0
+    barrier(world, device)
+    gemv_ms = timed(min(K, 2000), lambda: fm.flint_moe_lm_head(m.h, x, T, logits, stream))
+    assert fm.flint_moe_status(m.h) == fm.FLINT_OK
+    ms = max_over_ranks(statistics.mean(step_ms), world, device)
+
+    # end to end through the public API: pinned host x in, the drawn tokens out
+    x_pin = torch.from_numpy(bits.view(np.int16)).pin_memory()
+    t_pin = torch.empty((T,), dtype=torch.int32).pin_memory()
+    x_dev = torch.empty((T, d), dtype=torch.int16, device=device)
+    Ke = min(K, 2000)
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    for i in range(Ke + 3):
+        flush.zero_()
+        j = i - 3
+        if j >= 0:
+            es[j].record(stream)
+        x_dev.copy_(x_pin, non_blocking=True)
+        step(x_dev.view(torch.bfloat16))
+        t_pin.copy_(tokens, non_blocking=True)
+        if j >= 0:
+            ee[j].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(es, ee)), world, device)
+    m.close()
+    w_bytes = V * d // 2 + V * d // 16
+    return {"T": T, "V": V, "d": d, "ms": ms, "step_ms": step_ms, "gemv_us": statistics.mean(gemv_ms) * 1e3,
+            "bytes": w_bytes + T * d * 2 + T * V * 4, "weight_bytes": w_bytes, "launches": launches,
+            "clocks": clk.summary(), "e2e_ms": e2e_ms, "name": hcfg.name}
+
+
+def head_cpu_baseline(seconds: float) -> dict:
+    """The oracle's head and sampler on a bounded sample: the logits of a block
+    of the head's rows per step, scaled to the whole vocabulary."""
+    import oracle
+    hcfg = synth.HEAD_CONFIGS["flint"]
+    hw = synth.make_head(hcfg)
+    rows = 8192
+    el, n = 0.0, 0
+    while el < seconds:
+        bits = synth.make_hidden(hcfg, tokens=hcfg.tokens, stream=1 + n)
+        r0 = (n * rows) % (hcfg.vocab - rows)
+        t0 = time.perf_counter()
+        lg = oracle.lm_head.head_logits(bits, hw.codes[r0:r0 + rows], hw.scales[r0:r0 + rows], hw.tensor_scale)
+        oracle.lm_head.sample(lg.astype(np.float32), 1.0, 20, 0.95, np.full(hcfg.tokens, 0.5))
+        el += time.perf_counter() - t0
+        n += 1
+    per_step = el / n * hcfg.vocab / rows
+    return {"value": hcfg.tokens / per_step, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{n} steps of {rows} of the {hcfg.vocab} head rows (float64 oracle, {el:.1f} s), "
+                      f"scaled to the whole head"}
+
+
 def cpu_baseline(cfg, seconds: float, act_quant: bool = False) -> dict:
     """The CPU oracle (test infrastructure), timed as it stands on the host
     cores, on a bounded sample of the workload (with the NVFP4 activation
@@ -423,9 +533,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--head", action="store_true",
+                    help="the 4-bit output head (146,432 x 2048 NVFP4) and its sampler instead of an MoE config")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.head:
+        head_main(args)
+        return
     cfg = synth.CONFIGS[args.config]
     if args.steps is None:
         args.steps = {1: 20000, 2: 20000, 3: 10000, 4: 5000, 5: 3000}[args.config]
@@ -563,6 +678,49 @@ def main():
         line["step_ms_p10_p50_p90"] = [float(np.percentile(step_ms, q)) for q in (10, 50, 90)]
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds, act_quant=bool(res["plan"] & 2))
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def head_main(args):
+    import torch
+    if args.steps is None:
+        args.steps = 5000
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    r = run_head(args, world, local)
+    if rank == 0:
+        peaks = measured_peaks()
+        hbm = peaks["hbm_gbs"]
+        achieved = r["bytes"] / (r["gemv_us"] * 1e-6) / 1e9
+        srcs = ("bit_quantized_expert_softmax_b300/csrc/lm_head.cu", "bit_quantized_expert_softmax_b300/csrc/tiles.cuh",
+                "bit_quantized_expert_softmax_b300/csrc/common.cuh")
+        line = {
+            "metric": METRIC + " (output head)", "value": world * r["T"] / (r["ms"] / 1e3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 weights, f16 x",
+            "data": "synthetic",
+            "config": {"workload": f"{r['name']}: NVFP4 output head {r['V']} x {r['d']}, T={r['T']}, then one draw "
+                                   f"per token at temperature 1.0, top-k 20, top-p 0.95",
+                       "tokens_per_step": r["T"],
+                       "l2": "flushed between steps (memset of 2x L2, outside the per-step events)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": recorded_traffic("head_gemv_kernel", r["name"], source_digest(*srcs)),
+                         "kernel": "head_gemv_kernel (NVFP4 GEMV, mma.sync with tokens as rows)",
+                         "algorithmic_bytes_per_launch": r["bytes"], "avg_launch_us": r["gemv_us"],
+                         "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
+                         else "fallback 6.4 TB/s"},
+            "e2e": {"value": world * r["T"] / (r["e2e_ms"] / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": r["T"] * r["d"] * 2, "d2h_bytes_per_step": r["T"] * 4},
+            "gpu_launches": int(r["launches"]), "clocks": r["clocks"],
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = head_cpu_baseline(args.cpu_seconds)
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

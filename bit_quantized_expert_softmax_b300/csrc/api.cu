@@ -33,6 +33,13 @@ struct flint_moe {
     // events of profiled forwards: kProfMarks per forward (see prof_record)
     std::vector<cudaEvent_t> prof_events;
     int prof_max = 0, prof_n = 0;
+    // the 4-bit output head (tiled NVFP4) and its sampler's scratch
+    int head_vocab = 0;
+    float head_tscale = 0.f;
+    uint8_t* head_codes = nullptr;
+    uint8_t* head_scales = nullptr;
+    void* head_scratch = nullptr;
+    flint::HeadScratch head_hs{};
 };
 
 namespace {
@@ -427,11 +434,102 @@ void flint_moe_destroy(flint_moe* h) {
         cudaDeviceSynchronize();
         for (auto& L : h->layers) free_layer(L);
         prof_free(h);
+        cudaFree(h->head_codes);
+        cudaFree(h->head_scales);
+        cudaFree(h->head_scratch);
         cudaFree(h->ws_base);
         cudaFree(h->pws);
         if (h->load_stream) cudaStreamDestroy(h->load_stream);
     }
     delete h;
+}
+
+// ---------------------------------------------------------------------------
+// The 4-bit output head and its sampler
+// ---------------------------------------------------------------------------
+
+flint_status flint_moe_load_lm_head(flint_moe* h, int vocab, const void* codes, const void* scales,
+                                    float tensor_scale) {
+    if (h == nullptr || codes == nullptr || scales == nullptr) return FLINT_EINVAL;
+    if (vocab <= 0 || vocab % 8 != 0 || h->s.d > flint::kHeadMaxD || !isfinite(tensor_scale)) return FLINT_EINVAL;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return FLINT_ECUDA;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return FLINT_ECUDA;
+    cudaFree(h->head_codes);
+    cudaFree(h->head_scales);
+    cudaFree(h->head_scratch);
+    h->head_codes = h->head_scales = nullptr;
+    h->head_scratch = nullptr;
+    h->head_vocab = 0;
+    const size_t n_codes = (size_t)vocab * h->s.d / 2, n_scales = (size_t)vocab * h->s.d / 16;
+    const int parts = flint::head_sample_parts(vocab);
+    const size_t n_cand = (size_t)flint::kHeadMaxT * parts * 32;
+    uint8_t* stage = nullptr;
+    e = cudaMalloc(&h->head_codes, n_codes);
+    if (e == cudaSuccess) e = cudaMalloc(&h->head_scales, n_scales);
+    if (e == cudaSuccess) e = cudaMalloc(&h->head_scratch, n_cand * 8 + flint::kHeadMaxT * sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMalloc(&stage, n_codes + n_scales);
+    cudaStream_t st = h->load_stream;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(stage, codes, n_codes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(stage + n_codes, scales, n_scales, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+        e = flint::launch_repack_matrix(stage, stage + n_codes, h->head_codes, h->head_scales, vocab, h->s.d,
+                                        FLINT_W_NVFP4, st);
+    if (e == cudaSuccess) {
+        auto* base = static_cast<uint8_t*>(h->head_scratch);
+        h->head_hs.cand_key = reinterpret_cast<uint32_t*>(base);
+        h->head_hs.cand_idx = reinterpret_cast<uint32_t*>(base + n_cand * 4);
+        h->head_hs.counters = reinterpret_cast<unsigned*>(base + n_cand * 8);
+        e = cudaMemsetAsync(h->head_hs.counters, 0, flint::kHeadMaxT * sizeof(unsigned), st);
+    }
+    if (e == cudaSuccess) e = flint::prepare_head();
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    cudaFree(stage);
+    if (e != cudaSuccess) {
+        cudaFree(h->head_codes);
+        cudaFree(h->head_scales);
+        cudaFree(h->head_scratch);
+        h->head_codes = h->head_scales = nullptr;
+        h->head_scratch = nullptr;
+        return cuda_status(e);
+    }
+    h->head_vocab = vocab;
+    h->head_tscale = tensor_scale;
+    return FLINT_OK;
+}
+
+flint_status flint_moe_lm_head(flint_moe* h, const void* hidden_dev, int T, float* logits_dev, void* stream) {
+    if (h == nullptr || T < 0 || T > flint::kHeadMaxT) return FLINT_EINVAL;
+    if (h->head_vocab == 0) return FLINT_ESTATE;
+    if (T == 0) return FLINT_OK;
+    if (hidden_dev == nullptr || logits_dev == nullptr || !aligned16(hidden_dev) || !aligned16(logits_dev))
+        return FLINT_EINVAL;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return FLINT_ECUDA;
+    const cudaError_t e = flint::launch_head_gemv(h->head_codes, h->head_scales, h->head_tscale,
+                                                  static_cast<const __nv_bfloat16*>(hidden_dev), T, h->s.d,
+                                                  h->head_vocab, logits_dev, h->n_sms, (cudaStream_t)stream);
+    if (e == cudaSuccess) h->launches += 1;
+    return cuda_status(e);
+}
+
+flint_status flint_moe_sample(flint_moe* h, const float* logits_dev, int T, float temperature, int top_k,
+                              float top_p, const float* u_dev, int32_t* tokens_dev, int32_t* topk_dev,
+                              void* stream) {
+    if (h == nullptr || T < 0 || T > flint::kHeadMaxT) return FLINT_EINVAL;
+    if (h->head_vocab == 0) return FLINT_ESTATE;
+    if (!isfinite(temperature) || !(top_p > 0.f && top_p <= 1.f)) return FLINT_EINVAL;
+    if (!flint::head_sample_supported(h->head_vocab, top_k)) return FLINT_EINVAL;
+    if (T == 0) return FLINT_OK;
+    if (logits_dev == nullptr || u_dev == nullptr || tokens_dev == nullptr) return FLINT_EINVAL;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return FLINT_ECUDA;
+    const cudaError_t e = flint::launch_head_sample(logits_dev, T, h->head_vocab, temperature, top_k, top_p, u_dev,
+                                                    tokens_dev, topk_dev, h->head_hs, h->ws.status,
+                                                    (cudaStream_t)stream);
+    if (e == cudaSuccess) h->launches += 1;
+    return cuda_status(e);
 }
 
 flint_status flint_moe_status(flint_moe* h) {

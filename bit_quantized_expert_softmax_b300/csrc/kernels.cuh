@@ -137,6 +137,24 @@ cudaError_t pack_fp4_tiles(const uint8_t* codes, const uint8_t* scales, uint8_t*
                            cudaStream_t st);
 cudaError_t prepare_gemm_fp4();
 
+// lm_head.cu: the 4-bit output head and its sampling front-end
+constexpr int kHeadMaxT = 8;      // tokens per head call (the MMA's 8 token columns)
+constexpr int kHeadMaxD = 4096;   // hidden width the head's shared-memory plan covers
+struct HeadScratch {
+    uint32_t* cand_key;       // [kHeadMaxT][parts][32] candidates of the sampler's parts
+    uint32_t* cand_idx;
+    unsigned int* counters;   // [kHeadMaxT], zero between calls
+};
+size_t head_smem_bytes(int T, int d);
+cudaError_t prepare_head();
+cudaError_t launch_head_gemv(const uint8_t* codes, const uint8_t* scales, float tscale, const __nv_bfloat16* x,
+                             int T, int d, int V, float* logits, int n_sms, cudaStream_t st);
+int head_sample_parts(int V);
+bool head_sample_supported(int V, int top_k);
+cudaError_t launch_head_sample(const float* logits, int T, int V, float temperature, int top_k, float top_p,
+                               const float* u, int* tokens, int* topk_idx, const HeadScratch& hs, uint32_t* status,
+                               cudaStream_t st);
+
 // repack.cu
 cudaError_t launch_repack_matrix(const uint8_t* codes_src, const uint8_t* scales_src,
                                  uint8_t* codes_dst, uint8_t* scales_dst, int R, int K, int wfmt,

@@ -72,6 +72,9 @@ def lib() -> ctypes.CDLL:
             "flint_moe_debug_act_quant": (_I, [_P, _I, _I, _P, _P, _P, _P]),
             "flint_moe_profile_begin": (_I, [_P, _I]),
             "flint_moe_profile_end": (_I, [_P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_I)]),
+            "flint_moe_load_lm_head": (_I, [_P, _I, _P, _P, ctypes.c_float]),
+            "flint_moe_lm_head": (_I, [_P, _P, _I, _P, _P]),
+            "flint_moe_sample": (_I, [_P, _P, _I, ctypes.c_float, _I, ctypes.c_float, _P, _P, _P, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -219,6 +222,24 @@ def flint_moe_profile_end(h: int):
     n = _I()
     _check(lib().flint_moe_profile_end(h, ms, ctypes.byref(n)), "flint_moe_profile_end")
     return [float(v) for v in ms], int(n.value)
+
+
+def flint_moe_load_lm_head(h: int, codes: np.ndarray, scales: np.ndarray, tensor_scale: float) -> None:
+    """Host arrays in the canonical layout: codes uint8 [vocab, d/2], scales uint8 [vocab, d/16]."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    _check(lib().flint_moe_load_lm_head(h, codes.shape[0], codes.ctypes.data, scales.ctypes.data,
+                                        float(tensor_scale)), "flint_moe_load_lm_head")
+
+
+def flint_moe_lm_head(h: int, hidden, T: int, logits, stream=None) -> None:
+    _check(lib().flint_moe_lm_head(h, _ptr(hidden), T, _ptr(logits), _stream(stream)), "flint_moe_lm_head")
+
+
+def flint_moe_sample(h: int, logits, T: int, temperature: float, top_k: int, top_p: float, u, tokens, topk=None,
+                     stream=None) -> None:
+    _check(lib().flint_moe_sample(h, _ptr(logits), T, float(temperature), top_k, float(top_p), _ptr(u),
+                                  _ptr(tokens), _ptr(topk), _stream(stream)), "flint_moe_sample")
 
 
 def flint_moe_bucket_noalloc(idx, T: int, k: int, E: int, offsets, perm, stream=None) -> None:

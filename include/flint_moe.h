@@ -222,6 +222,50 @@ FLINT_API flint_status flint_moe_debug_fp4_gemm(const uint8_t* a_codes_dev, cons
 FLINT_API flint_status flint_moe_debug_act_quant(const void* x_dev, int T, int K, uint8_t* codes_dev,
                                                  uint8_t* scales_dev, float* rowscale_dev, void* stream);
 
+/* ---- the 4-bit output head and its sampler ---------------------------------
+ * The Flint blog ("Recursive Flint 40B-A2.5B", section "The quantisation
+ * recipe is the most transferable part") ships the output layer (lm_head)
+ * quantised to 4 bits because it is a large share of the bytes read per
+ * token; its serving defaults are temperature 1.0, top-p 0.95, top-k 20
+ * (section "The three scores, and the footnotes that come with them",
+ * Sampling bullet). */
+
+/* Copy the NVFP4 output head W [vocab x d] into the handle, repacked for the
+ * GEMV. Host pointers, canonical layout: codes uint8 [vocab][d/2] (two E2M1
+ * codes per byte, low nibble first), scales uint8 [vocab][d/16] (one E4M3
+ * byte per 16 codes of a row), tensor_scale fp32. The caller keeps ownership
+ * of the host arrays. vocab must be a positive multiple of 8. A second call
+ * replaces the head. Synchronises the device. FLINT_EINVAL on bad arguments,
+ * FLINT_ENOMEM / FLINT_ECUDA on device failures. */
+FLINT_API flint_status flint_moe_load_lm_head(flint_moe* h, int vocab, const void* codes, const void* scales,
+                                    float tensor_scale);
+
+/* logits_dev[t][v] = sum_i x[t][i] * W[v][i] for T <= 8 tokens of
+ * hidden_dev (bf16 [T][d], device, 16-byte aligned) into logits_dev (fp32
+ * [T][vocab], device, 16-byte aligned). Weights decoded to fp16 exactly,
+ * x rounded to fp16 after a power-of-two scale per token, fp32 accumulation.
+ * Asynchronous on `stream`. FLINT_ESTATE if no head is loaded, FLINT_EINVAL
+ * for T outside 0..8 or bad pointers (T = 0 does nothing). */
+FLINT_API flint_status flint_moe_lm_head(flint_moe* h, const void* hidden_dev, int T, float* logits_dev,
+                               void* stream);
+
+/* Draw one token per row of logits_dev (fp32 [T][vocab], device; the loaded
+ * head's vocab). temperature <= 0: the largest logit (equal logits: the lower
+ * index). Otherwise: the top_k largest logits (descending, ties to the lower
+ * index); softmax over them at the temperature; the smallest prefix whose
+ * probability reaches top_p (a member is kept while the sum of the ones
+ * before it is below top_p); the first kept member whose cumulative
+ * probability exceeds u[t] times the kept total. u_dev: fp32 [T] uniforms in
+ * [0, 1) (device), tokens_dev: int32 [T] (device); topk_dev, if not NULL,
+ * receives the top_k indices per token (int32 [T][top_k]; only entry 0 when
+ * temperature <= 0). 1 <= top_k <= 32, 0 < top_p <= 1, T <= 8, and
+ * ceil(vocab / 2048) * top_k <= 2048. NaN logits rank last and set
+ * FLINT_EDEVICE in the status word. Asynchronous on `stream`; calls on one
+ * handle must not overlap on the GPU (they share the handle's scratch). */
+FLINT_API flint_status flint_moe_sample(flint_moe* h, const float* logits_dev, int T, float temperature,
+                              int top_k, float top_p, const float* u_dev, int32_t* tokens_dev,
+                              int32_t* topk_dev, void* stream);
+
 /* ---- bucketing for callers that cannot allocate ---------------------------
  * The Flint blog has no counterpart to this entry point: it serves callers,
  * not the method. It computes what flint_moe_bucket computes, offsets_dev[E+1]
