@@ -173,14 +173,15 @@ def expert_forward_w4a4(wg, wu, wd, x: np.ndarray) -> np.ndarray:
 
     The pages fix NVFP4 for the weights only ("Flint", the list of the
     repository's builds); quantising the activations is the reading that the
-    FP4 x FP4 tensor-core product needs. h = silu(g) * u is rounded to
-    bfloat16 (one rounding of the float64 value) before it is quantised,
-    because that is the precision h is kept in between the two projections.
+    FP4 x FP4 tensor-core product needs. Each projection input is quantised
+    straight from its value: x as given (bf16), and h = silu(g) * u as
+    computed, with its quantisation decisions taken on float32 h like every
+    other decision here.
     """
     xq = quant_act_nvfp4(x)[3]
     g = xq @ wg.T
     u = xq @ wu.T
-    h = F.bf16_round(silu(g) * u)
+    h = silu(g) * u
     hq = quant_act_nvfp4(h.astype(np.float32))[3]
     return hq @ wd.T
 
