@@ -6,6 +6,7 @@ it travels with the source tree.
 """
 from __future__ import annotations
 
+import concurrent.futures
 import os
 import shutil
 import subprocess
@@ -53,14 +54,18 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     os.makedirs(BUILD_DIR, exist_ok=True)
     files, _ = _inputs()
-    objs = []
+    objs, cmds = [], []
     for src in files:
         obj = os.path.join(BUILD_DIR, os.path.basename(src).replace(".cu", ".o"))
         cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
-        subprocess.run(cmd, check=True)
+        cmds.append(cmd)
         objs.append(obj)
+    # one nvcc per source file, in parallel
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(len(cmds), os.cpu_count() or 1)) as pool:
+        for r in pool.map(lambda c: subprocess.run(c, check=True), cmds):
+            pass
     tmp = LIB + ".tmp"
     subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs], check=True)
     os.replace(tmp, LIB)

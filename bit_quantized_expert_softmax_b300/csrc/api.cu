@@ -328,13 +328,16 @@ flint_status flint_moe_load_weights(flint_moe* h, int layer, const flint_moe_wei
     if (!guard.ok) return FLINT_ECUDA;
     LayerDev& L = h->layers[layer];
     cudaError_t e = cudaSuccess;
+    // the bf16 hi/lo split of the router feeds only the tensor-core router,
+    // which serves T > kSmallT: handles that never see such T do not keep it
+    const bool want_split = h->prefill && s.max_tokens > flint::kSmallT && flint::router_umma_supported(s);
     if (L.codes == nullptr) {
         e = cudaMalloc(&L.router, (size_t)s.E * s.d * sizeof(float));
         if (e == cudaSuccess) e = cudaMalloc(&L.bias, (size_t)s.E * sizeof(float));
         if (e == cudaSuccess) e = cudaMalloc(&L.codes, n_codes);
         if (e == cudaSuccess) e = cudaMalloc(&L.scales, n_scales);
-        if (e == cudaSuccess) e = cudaMalloc(&L.router_hi, (size_t)s.E * s.d * 2);
-        if (e == cudaSuccess) e = cudaMalloc(&L.router_lo, (size_t)s.E * s.d * 2);
+        if (e == cudaSuccess && want_split) e = cudaMalloc(&L.router_hi, (size_t)s.E * s.d * 2);
+        if (e == cudaSuccess && want_split) e = cudaMalloc(&L.router_lo, (size_t)s.E * s.d * 2);
         if (e == cudaSuccess) e = cudaMalloc(&L.tscale, flint::tscale_bytes(s));
         if (e == cudaSuccess) e = cudaMemset(L.tscale, 0, flint::tscale_bytes(s));
         if (e == cudaSuccess && h->fp4_experts) e = cudaMalloc(&L.prefill, flint::prefill_weight_bytes(s));
@@ -342,7 +345,8 @@ flint_status flint_moe_load_weights(flint_moe* h, int layer, const flint_moe_wei
             free_layer(L);
             return cuda_status(e);
         }
-        h->weight_bytes += (size_t)s.E * s.d * 8 + (size_t)s.E * 4 + n_codes + n_scales + flint::tscale_bytes(s);
+        h->weight_bytes += (size_t)s.E * s.d * 4 + (size_t)s.E * 4 + n_codes + n_scales + flint::tscale_bytes(s);
+        if (L.router_hi != nullptr) h->weight_bytes += (size_t)s.E * s.d * 4;
         if (L.prefill != nullptr) h->weight_bytes += flint::prefill_weight_bytes(s);
     }
     L.loaded = false;
@@ -379,12 +383,12 @@ flint_status flint_moe_load_weights(flint_moe* h, int layer, const flint_moe_wei
     }
     if (e == cudaSuccess && L.prefill != nullptr)
         e = flint::pack_prefill_weights(s, stage, stage + n_codes, L.prefill, st);
-    if (e == cudaSuccess) e = flint::split_router(L.router, L.router_hi, L.router_lo, (size_t)s.E * s.d, st);
+    if (e == cudaSuccess && L.router_hi != nullptr)
+        e = flint::split_router(L.router, L.router_hi, L.router_lo, (size_t)s.E * s.d, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     cudaFree(stage);
     if (e != cudaSuccess) return cuda_status(e);
-    L.umma_router = h->prefill && flint::router_umma_supported(s) &&
-                    flint::make_tmap_bf16(&L.tmap_router_hi, L.router_hi, s.E, s.d) &&
+    L.umma_router = L.router_hi != nullptr && flint::make_tmap_bf16(&L.tmap_router_hi, L.router_hi, s.E, s.d) &&
                     flint::make_tmap_bf16(&L.tmap_router_lo, L.router_lo, s.E, s.d);
     L.loaded = true;
     return FLINT_OK;

@@ -2,20 +2,22 @@
 //
 // flint_moe_bucket runs on a handle, and creating a handle allocates the
 // per-token workspace with cudaMalloc. Some callers cannot allocate at the
-// point where they need this step: a serving loop that records its whole
-// decode step inside CUDA stream capture (cudaMalloc is not a capturable
-// operation), a process whose device memory is already reserved by another
-// allocator such as a framework's caching pool, or an embedding runtime that
-// forbids the CUDA allocator. This file gives them the same bucketing with its
-// scratch in one fixed static device array instead of a workspace.
+// point where they need this step: a process whose device memory is already
+// reserved by another allocator (a framework's caching pool holds nearly all
+// of it, so a raw cudaMalloc fails or forces that pool to release memory), a
+// plugin whose host runtime forbids allocations outside its own allocator, or
+// a latency-critical loop that cannot afford cudaMalloc's implicit device
+// synchronisation. This file gives them the same bucketing with its scratch in
+// one fixed static device array instead of a workspace.
 //
-// The scratch holds, per chunk of 2048 assignments, one int32 count and then
-// one first-output-position per expert: at most 256 chunks x 256 experts x 4 B
-// = 256 KiB. Every GPU that loads the library holds that array until the
-// process exits. Each call overwrites every scratch entry it reads before
-// reading it, so nothing carries over from the previous call; but all calls on
-// one device share the array, so two calls that overlap on the GPU (different
-// streams, or host threads racing) corrupt each other's results.
+// The scratch holds, per chunk of 2048 assignments, one first-output-position
+// per expert: at most 256 chunks x 256 experts x 4 B = 256 KiB. Every GPU that
+// loads the library holds that array until the process exits. Each call
+// overwrites every scratch entry it reads before reading it, so nothing
+// carries over from the previous call; but all calls on one device share the
+// array, so two calls that overlap on the GPU (different streams, or host
+// threads racing) corrupt each other's results.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -34,9 +36,29 @@ constexpr int kNaMaxDevices = 64;
 
 static __device__ __align__(256) int g_bucket_scratch[kNaMaxChunks * kNaMaxExperts];
 
-// Device address of g_bucket_scratch, looked up once per device.
+// Device address of g_bucket_scratch, looked up once per device and context:
+// a cudaDeviceReset gives the device a new primary context in which the
+// module, and with it the array, may sit at another address, so the address
+// is looked up again when the current context is not the one it was found in.
 void* g_scratch_addr[kNaMaxDevices];
+CUcontext g_scratch_ctx[kNaMaxDevices];
 std::mutex g_scratch_mu;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
 
 // Per-expert counts of one chunk, written for every expert.
 __global__ void __launch_bounds__(kNaThreads) na_hist(const int* __restrict__ sel, int n, int E,
@@ -61,6 +83,7 @@ __global__ void __launch_bounds__(kNaThreads) na_scan(int n_chunks, int E, int* 
     __shared__ int off[kNaMaxExperts + 1];
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int s = 0;
+#pragma unroll 8
         for (int c = 0; c < n_chunks; ++c) s += scratch[c * E + e];
         tot[e] = s;
     }
@@ -77,6 +100,7 @@ __global__ void __launch_bounds__(kNaThreads) na_scan(int n_chunks, int E, int* 
     for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = off[e];
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int run = off[e];
+#pragma unroll 8
         for (int c = 0; c < n_chunks; ++c) {
             const int h = scratch[c * E + e];
             scratch[c * E + e] = run;
@@ -136,11 +160,19 @@ extern "C" flint_status flint_moe_bucket_noalloc(const int32_t* idx_dev, int T, 
     if (dev < 0 || dev >= kNaMaxDevices) return FLINT_ENOTIMPL;
     void* scratch = nullptr;
     {
+        // the first call on a device (and the first after its context was
+        // reset) finds the array's device address; later calls reuse it
+        CtxGetCurrentFn get_ctx = ctx_get_current();
+        if (get_ctx == nullptr) return FLINT_ECUDA;
+        CUcontext ctx = nullptr;   // stays null if no context is current yet
+        if (get_ctx(&ctx) != CUDA_SUCCESS) return FLINT_ECUDA;
         std::lock_guard<std::mutex> lock(g_scratch_mu);
-        if (g_scratch_addr[dev] == nullptr) {
-            void* p = nullptr;
+        if (ctx == nullptr || g_scratch_addr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
+            void* p = nullptr;   // the lookup makes the device's primary context current
             if (cudaGetSymbolAddress(&p, g_bucket_scratch) != cudaSuccess || p == nullptr) return FLINT_ECUDA;
+            if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return FLINT_ECUDA;
             g_scratch_addr[dev] = p;
+            g_scratch_ctx[dev] = ctx;
         }
         scratch = g_scratch_addr[dev];
     }

@@ -75,12 +75,6 @@ __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
     return r;
 }
 
-__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t r;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-    return r;
-}
-
 __device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));

@@ -21,9 +21,11 @@
 //   P2  down projection of 16 output rows for every active expert, weighted
 //       combine (shared first, then slots 0..k-1) and bf16 output.
 //
-// Arithmetic matches the multi-kernel path: weights decoded to fp16 in
-// registers, activations fp16 with a power-of-two scale per token (x) or per
-// (token, slot) row (h), mma.sync m16n8k16 with fp32 accumulation.
+// Arithmetic matches the multi-kernel path: weights decoded in registers
+// (NVFP4 to exact fp16 products, q4_1 to its exact codes with d and m applied
+// per 32-element block to the fp32 accumulator), activations fp16 with a
+// power-of-two scale per token (x) or per (token, slot) row (h), mma.sync
+// m16n8k16 with fp32 accumulation.
 #include "kernels.cuh"
 #include "tiles.cuh"
 #include "topk.cuh"
@@ -168,9 +170,9 @@ __device__ void gateup_units(const FusedArgs& a, const UnitRef* units, int n_uni
             }
             uint32_t fa[8][4];
             decode_tile<WFMT>(wg, wu, sc, fa);
-#pragma unroll
-            for (int st = 0; st < 8; ++st)
-                mma_16816(acc, fa[st][0], fa[st][1], fa[st][2], fa[st][3], b[2 * st], b[2 * st + 1]);
+            float sx[4][2];
+            if constexpr (WFMT == 1) block_sums_q41(b, sx);
+            mma_k128<WFMT>(acc, fa, b, sc, sx);
         }
         *reinterpret_cast<float4*>(red + (size_t)(v * kFWarps + warp) * 128 + lane * 4) =
             make_float4(acc[0], acc[1], acc[2], acc[3]);
@@ -562,9 +564,9 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
             }
             uint32_t fa[8][4];
             decode_tile<WFMT>(wg, wh, sc, fa);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_16816(cacc, fa[s][0], fa[s][1], fa[s][2], fa[s][3], bfr[2 * s], bfr[2 * s + 1]);
+            float sx[4][2];
+            if constexpr (WFMT == 1) block_sums_q41(bfr, sx);
+            mma_k128<WFMT>(cacc, fa, bfr, sc, sx);
         }
         float* dst = acc + (size_t)it * 128;
         dst[g * 8 + 2 * c] = cacc[0];

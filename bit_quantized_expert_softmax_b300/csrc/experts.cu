@@ -7,12 +7,13 @@
 // only the selected experts' packed 4-bit tiles, once, with one 16-byte load
 // per lane per 8x128 tile, and decode them in registers.
 //
-// Arithmetic: weights are decoded to fp16 (NVFP4: E2M1 x E4M3 is exact in
-// fp16; q4_1: d*q + m rounded once to fp16 by an fma), activations are fp16
-// scaled per token (or per position) by a power of two that brings their
-// maximum into [2^14, 2^15), and mma.sync m16n8k16 accumulates in fp32. The
-// fp32 tensor scale and the inverse activation scale are applied to the
-// accumulator.
+// Arithmetic: activations are fp16 scaled per token (or per position) by a
+// power of two that brings their maximum into [2^14, 2^15), and mma.sync
+// m16n8k16 accumulates in fp32. NVFP4 weights enter the MMA as E2M1 x E4M3
+// (exact in fp16) and their fp32 tensor scale is applied to the accumulator.
+// q4_1 weights enter as their codes q (exact); per 32-element block the
+// accumulator takes d * sum(q x) + m * sum(x), so d*q + m is never rounded
+// (tiles.cuh, mma_k128). The inverse activation scale is applied last.
 #include "kernels.cuh"
 #include "tiles.cuh"
 
@@ -115,11 +116,10 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertArgs a) {
 #pragma unroll
                         for (int q = 0; q < 16; ++q) b[q] = 0u;
                     }
-#pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        mma_16816(accg[nt], fa[s][0], fa[s][1], fa[s][2], fa[s][3], b[2 * s], b[2 * s + 1]);
-                        mma_16816(accu[nt], fu[s][0], fu[s][1], fu[s][2], fu[s][3], b[2 * s], b[2 * s + 1]);
-                    }
+                    float sx[4][2];
+                    if constexpr (WFMT == 1) block_sums_q41(b, sx);
+                    mma_k128<WFMT>(accg[nt], fa, b, scg, sx);
+                    mma_k128<WFMT>(accu[nt], fu, b, scu, sx);
                 }
             }
             // reduce the four K-partials
@@ -300,9 +300,9 @@ __global__ void __launch_bounds__(kThreads) down_kernel(ExpertArgs a) {
 #pragma unroll
                             for (int q = 0; q < 16; ++q) b[q] = 0u;
                         }
-#pragma unroll
-                        for (int st = 0; st < 8; ++st)
-                            mma_16816(acc[nt], fa[st][0], fa[st][1], fa[st][2], fa[st][3], b[2 * st], b[2 * st + 1]);
+                        float sx[4][2];
+                        if constexpr (WFMT == 1) block_sums_q41(b, sx);
+                        mma_k128<WFMT>(acc[nt], fa, b, sc[i], sx);
                     }
                 }
             }

@@ -3,14 +3,15 @@
 // NVFP4 weights force the FP4 x FP4 tensor-core kind, so the activations that
 // enter each projection are quantised to NVFP4 as well (per row: an fp32 scale
 // s = amax/2688; per 16 elements: an E4M3 scale E4M3_rne((amax_b/6)/s); codes
-// E2M1_rne(v * (1/(E4M3(sb)*s)))). h enters the down projection rounded to
-// bf16 first. Pipeline for one layer (after routing and bucketing):
+// E2M1_rne(v * (1/(E4M3(sb)*s)))). h is kept in fp32 between the two
+// projections and quantised from that value. Pipeline for one layer (after
+// routing and bucketing):
 //   plan      pad every expert's rows to a multiple of 128 (M-tile table)
 //   quant_x   quantise each token's x once and write it into the swizzled A
 //             tiles of its k routed experts and of the shared expert
 //   gemm1     gate/up: [rows x d] . [2f x d]^T, each 128-column tile holds 64
 //             gate and 64 up columns of the same f range; epilogue
-//             h = silu(g)*u -> bf16
+//             h = silu(g)*u (fp32)
 //   quant_h   quantise each h row into swizzled A tiles of the down GEMM
 //   gemm2     down: [rows x f] . [d x f]^T; epilogue scales by the routing
 //             weight (1 for the shared expert) and stores the contribution in
@@ -68,6 +69,54 @@ __device__ __forceinline__ void unpack8(const uint4& r, float* v) {
     }
 }
 
+// One 16-element block given its values, the row scale s_t: the block's
+// scale byte; its codes into codes[0..1].
+__device__ __forceinline__ uint32_t quant_block16(const float (&v)[16], float s_t, uint32_t* codes) {
+    float ab = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(v[i]));
+    const float ratio = s_t > 0.f ? (ab / 6.0f) / s_t : 0.0f;
+    const uint32_t sb = f32_to_e4m3(ratio);
+    const float S = e4m3_to_f32(sb) * s_t;
+    if (S > 0.f) {
+        const float inv = 1.0f / S;
+        float q[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) q[i] = v[i] * inv;
+        codes[0] = f32x8_to_e2m1(q);
+        codes[1] = f32x8_to_e2m1(q + 8);
+    } else {
+        codes[0] = 0u;
+        codes[1] = 0u;
+    }
+    return sb;
+}
+
+// The same for a row held as fp32 (lane l: EPL consecutive elements).
+template <int EPL>
+__device__ __forceinline__ float quant_row_f32(const float4 (&raw)[EPL / 4], uint32_t (&codes)[EPL / 8],
+                                               uint32_t& sbytes) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL / 4; ++i)
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(raw[i].x), fabsf(raw[i].y)), fmaxf(fabsf(raw[i].z), fabsf(raw[i].w))));
+    const float s_t = warp_max(amax) / 2688.0f;
+    sbytes = 0u;
+#pragma unroll
+    for (int b = 0; b < EPL / 16; ++b) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[4 * i] = raw[4 * b + i].x;
+            v[4 * i + 1] = raw[4 * b + i].y;
+            v[4 * i + 2] = raw[4 * b + i].z;
+            v[4 * i + 3] = raw[4 * b + i].w;
+        }
+        sbytes |= quant_block16(v, s_t, codes + 2 * b) << (8 * b);
+    }
+    return s_t;
+}
+
 template <int EPL>
 __device__ __forceinline__ float quant_row(const uint4 (&raw)[EPL / 8], uint32_t (&codes)[EPL / 8], uint32_t& sbytes) {
     float amax = 0.f;
@@ -86,24 +135,7 @@ __device__ __forceinline__ float quant_row(const uint4 (&raw)[EPL / 8], uint32_t
         float v[16];
         unpack8(raw[2 * b], v);
         unpack8(raw[2 * b + 1], v + 8);
-        float ab = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(v[i]));
-        const float ratio = s_t > 0.f ? (ab / 6.0f) / s_t : 0.0f;
-        const uint32_t sb = f32_to_e4m3(ratio);
-        const float S = e4m3_to_f32(sb) * s_t;
-        sbytes |= sb << (8 * b);
-        if (S > 0.f) {
-            const float inv = 1.0f / S;
-            float q[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) q[i] = v[i] * inv;
-            codes[2 * b] = f32x8_to_e2m1(q);
-            codes[2 * b + 1] = f32x8_to_e2m1(q + 8);
-        } else {
-            codes[2 * b] = 0u;
-            codes[2 * b + 1] = 0u;
-        }
+        sbytes |= quant_block16(v, s_t, codes + 2 * b) << (8 * b);
     }
     return s_t;
 }
@@ -156,7 +188,7 @@ struct PrefillCtx {
     const __nv_bfloat16* x;
     uint8_t* a1;              // gate/up A blocks [row tiles][d/256]
     float* sa;
-    __nv_bfloat16* h;
+    float* h;                 // [padded rows][f] fp32
     uint8_t* a2;              // down A blocks [row tiles][f/256]
     int* prow;                // [padded rows] bucketed position of the row's assignment, -1: padding
     float* yscale;            // [padded rows] s_h * down tensor scale * routing weight
@@ -257,7 +289,7 @@ __global__ void __launch_bounds__(256, 3) quant_x_kernel(PrefillCtx c) {
     }
 }
 
-// Quantise each h row (bf16, f elements) into the down GEMM's A tiles and
+// Quantise each h row (fp32, f elements) into the down GEMM's A tiles and
 // write the down GEMM's per-row epilogue data. A warp takes kQhRows
 // consecutive padded rows (one M-tile's): it loads all of their h first (the
 // buffer holds every row the grid covers, so the loads need no lookup), then
@@ -270,12 +302,12 @@ __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KT = c.f / kGK;
     const int row0 = (blockIdx.x * 8 + warp) * kQhRows;
-    uint4 raw[kQhRows][EPL / 8];
+    float4 raw[kQhRows][EPL / 4];
 #pragma unroll
     for (int i = 0; i < kQhRows; ++i) {
-        const __nv_bfloat16* hr = c.h + (size_t)(row0 + i) * c.f + lane * EPL;
+        const float4* hr = reinterpret_cast<const float4*>(c.h + (size_t)(row0 + i) * c.f + lane * EPL);
 #pragma unroll
-        for (int j = 0; j < EPL / 8; ++j) raw[i][j] = *reinterpret_cast<const uint4*>(hr + 8 * j);
+        for (int j = 0; j < EPL / 4; ++j) raw[i][j] = __ldcs(hr + j);
     }
     const int n_rows = c.meta[2] * kGM;
     if (row0 >= n_rows) return;
@@ -303,7 +335,7 @@ __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
         }
         uint32_t codes[EPL / 8];
         uint32_t sb = 0;
-        const float s_t = quant_row<EPL>(raw[i], codes, sb);
+        const float s_t = quant_row_f32<EPL>(raw[i], codes, sb);
         store_row_swizzled<EPL>(blocks, r0 + i, lane, codes, sb);
         if (lane == 0) {
             c.prow[row0 + i] = pi;
@@ -344,7 +376,7 @@ struct Gemm1 {
     // h columns [64n + 32*half, +32): gate accumulator columns 32*half.., up 64 + 32*half..
     __device__ void epilogue(const Fp4Item& w, const Pre& pr, uint32_t taddr, int row, int half, uint8_t*) const {
         const float tg = pr.tg, tu = pr.tu;
-        __nv_bfloat16* dst = c.h + (size_t)(w.m * kGM + row) * c.f + w.n * 64 + half * 32;
+        float* dst = c.h + (size_t)(w.m * kGM + row) * c.f + w.n * 64 + half * 32;
         // all four tensor-memory loads in flight before the one wait
         uint32_t g[32], u[32];
         tmem_ld16(taddr + half * 32, g);
@@ -353,21 +385,17 @@ struct Gemm1 {
         tmem_ld16(taddr + 64 + half * 32 + 16, u + 16);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            uint32_t packed[8];
+        for (int i = 0; i < 32; i += 4) {
+            float hv[4];
 #pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-                const float g0 = __uint_as_float(g[16 * j + i]) * tg, g1 = __uint_as_float(g[16 * j + i + 1]) * tg;
-                const float u0 = __uint_as_float(u[16 * j + i]) * tu, u1 = __uint_as_float(u[16 * j + i + 1]) * tu;
+            for (int q = 0; q < 4; ++q) {
+                const float gq = __uint_as_float(g[i + q]) * tg, uq = __uint_as_float(u[i + q]) * tu;
                 // silu(g) * u with the fast exponential and division (relative
-                // error ~1e-6, far below the bf16 rounding that follows)
-                const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
-                const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
-                __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
-                packed[i / 2] = *reinterpret_cast<uint32_t*>(&hb);
+                // error ~1e-6; it can move a later FP4 code only where h sits
+                // on a rounding boundary)
+                hv[q] = __fdividef(gq, 1.0f + __expf(-gq)) * uq;
             }
-            *reinterpret_cast<uint4*>(dst + 16 * j) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            *reinterpret_cast<uint4*>(dst + 16 * j + 8) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            __stcs(reinterpret_cast<float4*>(dst + i), make_float4(hv[0], hv[1], hv[2], hv[3]));
         }
     }
 };
@@ -582,7 +610,7 @@ size_t prefill_workspace_bytes(const Shape& s, int Tm) {
     const size_t rt = (rows + kGM - 1) / kGM;
     const size_t a1 = rt * (s.d / kGK) * (kGTile + kGSf);
     const size_t a2 = rt * (s.f / kGK) * (kGTile + kGSf);
-    return 256 * 16 + rt * kGM * 4 * 3 + rt * 16 + (s.n_slots() + 2) * 4 * 2 + a1 + a2 + rt * kGM * s.f * 2 +
+    return 256 * 16 + rt * kGM * 4 * 3 + rt * 16 + (s.n_slots() + 2) * 4 * 2 + a1 + a2 + rt * kGM * s.f * 4 +
            (size_t)Tm * (s.k + 1) * s.d * 2;
 }
 
@@ -629,7 +657,7 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     c.yscale = reinterpret_cast<float*>(take(rt * kGM * 4));
     c.a1 = take(rt * (s.d / kGK) * kGBlk);
     c.a2 = take(rt * (s.f / kGK) * kGBlk);
-    c.h = reinterpret_cast<__nv_bfloat16*>(take(rt * kGM * s.f * 2));
+    c.h = reinterpret_cast<float*>(take(rt * kGM * s.f * 4));
     c.y = reinterpret_cast<__nv_bfloat16*>(take((size_t)Tm * (s.k + 1) * s.d * 2));
     c.x = x;
     const size_t w1 = (size_t)s.n_slots() * (2 * s.f / kGN) * (s.d / kGK) * kGBlk;

@@ -1,6 +1,7 @@
 // Weight repacking (canonical row-major -> tiled mma-fragment layout) and the
 // dequantisation export used to check the device layout bit for bit.
 #include "kernels.cuh"
+#include "tiles.cuh"
 
 namespace flint {
 
@@ -47,7 +48,8 @@ __global__ void repack_kernel(const uint8_t* __restrict__ codes_src, const uint8
 }
 
 // One thread per canonical element (row, k): locate its byte in the tiled
-// layout and decode it with the same conversions the expert kernels use.
+// layout and decode it with the decoders the expert kernels use (tiles.cuh):
+// NVFP4 fp32(E2M1 x E4M3 x tensor scale), q4_1 fp32(d*q + m).
 __global__ void dequant_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
                                const float* __restrict__ tscale_dev, float tscale_host, int R, int K,
                                int wfmt, float* __restrict__ out) {
@@ -66,21 +68,10 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ codes, const uint8_t*
         const uint8_t byte = codes[tile * 512 + lane * 16 + 2 * s + hi_half];
         float v;
         if (wfmt == 0) {
-            uint32_t f0, f1, f2, f3;
-            e2m1x8_to_f16x2((uint32_t)byte, f0, f1, f2, f3);
-            const uint8_t sb = scales[tile * 64 + g * 8 + s];
-            const uint32_t s2 = e4m3x2_to_f16x2((uint32_t)sb);
-            const uint32_t p = hmul2_u(f0, bcast_lo(s2));
-            const __half2 ph = *reinterpret_cast<const __half2*>(&p);
-            const float cs = nib ? __high2float(ph) : __low2float(ph);
-            v = cs * ts;
+            v = nvfp4_code_times_scale(byte, nib, scales[tile * 64 + g * 8 + s]) * ts;
         } else {
-            const int b = s >> 1;
-            const uint32_t dm = *reinterpret_cast<const uint32_t*>(scales + tile * 128 + g * 16 + b * 4);
-            const __half2 dmh = *reinterpret_cast<const __half2*>(&dm);
-            const float dd = __low2float(dmh), mm = __high2float(dmh);
-            const int q = nib ? (byte >> 4) : (byte & 0xf);
-            v = fmaf(dd, (float)q, mm);
+            const uint32_t dm = *reinterpret_cast<const uint32_t*>(scales + tile * 128 + g * 16 + (s >> 1) * 4);
+            v = q41_weight(byte, nib, dm);
         }
         out[i] = v;
     }

@@ -175,7 +175,12 @@ FLINT_API flint_status flint_moe_bucket(flint_moe* h, const int32_t* idx_dev, in
  * layout back to fp32 in canonical order: out_dev[R][K] with [R, K] =
  * [f, d] (mat 0 gate, 1 up) or [d, f] (mat 2 down); expert == n_experts is the
  * shared expert. NVFP4 values are fp32(E2M1 * E4M3 * tensor scale), q4_1
- * values fp32(d*q + m), each rounded once. Errors as flint_moe_forward. */
+ * values fp32(d*q + m), each rounded once, computed with the decoders the
+ * expert kernels use. The kernels never round a weight: they multiply by the
+ * exact E2M1 * E4M3 product (fp16) and apply the tensor scale to the fp32
+ * accumulator; for q4_1 they multiply by the exact codes q and add
+ * d * sum(q x) + m * sum(x) per 32-element block, the regrouped d*q + m.
+ * Errors as flint_moe_forward. */
 FLINT_API flint_status flint_moe_dequant(flint_moe* h, int layer, int expert, int mat, float* out_dev,
                                void* stream);
 
@@ -188,7 +193,7 @@ FLINT_API size_t flint_moe_device_bytes(const flint_moe* h);
  * Bit 1 is set for T > 64 on NVFP4 weights with d = 2048, f = 512 and one
  * shared expert when max_tokens > 64; that path quantises the activations
  * entering each expert projection to NVFP4 (flint_moe_debug_act_quant; h is
- * rounded to bf16 first), so its result is the W4A4 product, not the W4A16
+ * quantised from its fp32 value), so its result is the W4A4 product, not the W4A16
  * one the other paths compute. Setting FLINT_MOE_TCGEN05_PREFILL=0 before
  * flint_moe_create turns all these kernels off for the handle (the mma.sync
  * and CUDA-core paths remain); FLINT_MOE_FP4_EXPERTS=0 turns off only the
@@ -271,19 +276,23 @@ FLINT_API flint_status flint_moe_sample(flint_moe* h, const float* logits_dev, i
  * not the method. It computes what flint_moe_bucket computes, offsets_dev[E+1]
  * and perm_dev[T*k] from idx_dev[T][k] (experts 0..E-1), without a handle and
  * without allocating anything. flint_moe_create allocates a workspace with
- * cudaMalloc; callers that cannot allocate where they need this step (a step
- * being recorded under CUDA stream capture, a process whose device memory is
- * held by another allocator, a runtime that forbids the CUDA allocator) use
- * this instead. Its scratch is one static device array of 256 KiB inside the
- * library, which every GPU that loads the library holds until the process
- * exits. Runs on the current device.
+ * cudaMalloc; some callers cannot allocate where they need this step: a
+ * process whose device memory is already reserved by another allocator (a
+ * framework's caching pool), a plugin whose host runtime forbids allocating
+ * outside its own allocator, or a loop that cannot afford cudaMalloc's
+ * implicit device synchronisation. Its scratch is one static device array of
+ * 256 KiB inside the library, which every GPU that loads the library holds
+ * until the process exits. Runs on the current device.
  * Limits: 1 <= E <= 256, 1 <= k <= 8, T*k <= 524288; larger sizes return
  * FLINT_EINVAL and enqueue nothing. T == 0 is a no-op.
  * The first call on a device looks up the array's device address (once per
- * device, under a lock): make that first call before any stream capture.
+ * device and context, under a lock; again after cudaDeviceReset): make that
+ * first call before any stream capture.
  * All calls share the array, so calls that overlap on the GPU race and
- * corrupt each other's results. Expert indices outside 0..E-1 are dropped
- * (this entry point has no status word to report them). */
+ * corrupt each other's results. Expert indices outside 0..E-1 are dropped and
+ * nothing reports them (there is no status word): a caller that cannot rule
+ * them out checks offsets_dev[E] == T*k, which fails exactly when some were
+ * dropped; perm_dev[offsets_dev[E] .. T*k-1] is then left unwritten. */
 FLINT_API flint_status flint_moe_bucket_noalloc(const int32_t* idx_dev, int T, int k, int E,
                                                 int32_t* offsets_dev, int32_t* perm_dev, void* stream);
 

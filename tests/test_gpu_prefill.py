@@ -1,8 +1,8 @@
 """The large-T expert path on the block-scaled FP4 tensor cores (NVFP4 weights,
 d = 2048, f = 512): activation quantisation bit for bit, and whole layers
 against the oracle's quantised-activation expert (activations entering each
-projection are NVFP4 with a per-token fp32 scale; h is rounded to bfloat16
-before it is quantised)."""
+projection are NVFP4 with a per-token fp32 scale; h is quantised from its
+float32 value)."""
 import dataclasses
 
 import numpy as np
