@@ -1,12 +1,17 @@
 #!/usr/bin/env python
 """Benchmark of the Flint-shaped 4-bit sparse MoE FFN layer on B300.
 
-Default workload: one Flint-shaped MoE layer decoding one token (d=2048,
-f=512, 256 routed experts, top-6, one shared expert, NVFP4 weights, T=1),
-with the L2 cache flushed between steps. Prints one JSON line.
+Default: the headline workload is the 8192-token prefill chunk through one
+Flint-shaped MoE layer (d=2048, f=512, 256 routed experts top-6 + 1 shared,
+NVFP4 weights, Zipf-skewed router; the block-scaled FP4 tensor-core path),
+the largest single-GPU configuration. The same run also times, as
+sub-records with their own roofline, e2e and timing, the three decode
+workloads: one layer at T=1 (NVFP4), one layer at T=64 (q4_1, Zipf), and the
+47-layer stack at T=1. Prints one JSON line.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--no-subrecords]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+  python bench.py --head                 # the 4-bit output head and its sampler
 
 A step is one pass of the layer (router, top-k, bucketing, expert gate/up,
 down projection, combine) over the workload's tokens. Per-step device time is
@@ -181,6 +186,29 @@ def blas_threads() -> int:
         return os.cpu_count() or 1
 
 
+def fp4_peak(fm, device) -> dict:
+    """Dense block-scaled FP4 tensor-core throughput of this GPU, measured by
+    the library's probe (tcgen05.mma kind::mxf4nvf4, operands resident on
+    chip, one CTA per SM): a short burst per MMA width and a ~0.5 s run
+    under the clock sampler. The burst maximum is the FP4 roofline's peak."""
+    burst = {}
+    for n in (128, 256):
+        ms, flops = fm.flint_moe_probe_fp4_peak(n, 4000 if n == 256 else 8000)
+        burst[n] = flops / (ms * 1e-3) / 1e12
+    n_best = max(burst, key=burst.get)
+    iters = int(4000 * 500.0 / max(ms, 1e-3)) if n_best == 256 else int(8000 * 500.0 / max(ms, 1e-3))
+    iters = max(1000, min(iters, (1 << 24) - 1))
+    with ClockSampler(gpu_id_for(device)) as clk:
+        ms_s, flops_s = fm.flint_moe_probe_fp4_peak(n_best, iters)
+    sustained = flops_s / (ms_s * 1e-3) / 1e12
+    c = clk.summary()
+    return {"tflops": burst[n_best], "burst_tflops_by_n": {str(k): v for k, v in burst.items()},
+            "sustained_tflops": sustained, "sustained_ms": ms_s, "mma": f"M=128, N={n_best}, K=64, cta_group::1",
+            "clocks_sustained": c,
+            "tflops_per_ghz_sustained": sustained / (c["sm_mhz"] / 1e3) if c.get("sm_mhz") else None,
+            "source": "measured on this GPU by flint_moe_probe_fp4_peak (bench run)"}
+
+
 # ---------------------------------------------------------------------------
 # workload
 # ---------------------------------------------------------------------------
@@ -205,14 +233,17 @@ def algorithmic_bytes(cfg, n_active_experts: int, T: int) -> dict:
     acts = 2 * T * cfg.d * 2
     P = T * (cfg.top_k + 1)
     gateup = n_active_experts * 2 * per_mat + T * cfg.d * 2 + P * cfg.f * 4
-    fp4_gemm1 = n_active_experts * 2 * per_mat + P * (cfg.d // 2 + cfg.d // 16 + 4) + P * cfg.f * 2
+    # FP4 path: NVFP4 activation rows in (codes, E4M3 scales, fp32 row scale);
+    # gate/up writes h in fp32, down writes one bf16 contribution row per
+    # (token, expert) pair
+    fp4_gemm1 = n_active_experts * 2 * per_mat + P * (cfg.d // 2 + cfg.d // 16 + 4) + P * cfg.f * 4
     fp4_gemm2 = n_active_experts * per_mat + P * (cfg.f // 2 + cfg.f // 16 + 4) + P * cfg.d * 2
     return {"selected_expert_bytes": selected, "layer_bytes": selected + router + acts,
             "gateup_kernel_bytes": gateup, "fp4_gemm1_bytes": fp4_gemm1, "fp4_gemm2_bytes": fp4_gemm2,
             "fp4_gemm1_flops": 2 * P * cfg.d * 2 * cfg.f, "fp4_gemm2_flops": 2 * P * cfg.f * cfg.d}
 
 
-def run_ours(args, cfg, world, rank, local):
+def run_ours(cfg, world, rank, local, steps: int, warmup: int, soak_s: float = 1.0):
     import torch
     from bit_quantized_expert_softmax_b300 import build
     build.build()
@@ -299,22 +330,31 @@ def run_ours(args, cfg, world, rank, local):
         phases = fm.flint_moe_profile_end(m.h) if profile else None
         return [a.elapsed_time(b) for a, b in zip(st_ev, en_ev)], phases
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        reset()
-        step()
-    torch.cuda.synchronize()
-    status = fm.flint_moe_status(m.h)
-    assert status == fm.FLINT_OK, f"device status {status} after warm-up"
-
-    K = args.steps
-    barrier(world, device)
-    torch.cuda.synchronize()
-    launches0 = fm.flint_moe_launch_count(m.h)
-    t0 = time.perf_counter()
+    K = steps
     with ClockSampler(gpu_id_for(device)) as clk:
+        # the sampler covers warm-up, an untimed soak of >= soak_s seconds of
+        # the same steps, and the timed steps: its record describes the device
+        # under this load even when the timed region itself is short
+        for _ in range(warmup):
+            flush.zero_()
+            reset()
+            step()
+        torch.cuda.synchronize()
+        status = fm.flint_moe_status(m.h)
+        assert status == fm.FLINT_OK, f"device status {status} after warm-up"
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < soak_s:
+            for _ in range(50):
+                flush.zero_()
+                reset()
+                step()
+            torch.cuda.synchronize()
+        barrier(world, device)
+        torch.cuda.synchronize()
+        launches0 = fm.flint_moe_launch_count(m.h)
+        t0 = time.perf_counter()
         step_ms, _ = timed(K)
-    wall = time.perf_counter() - t0
+        wall = time.perf_counter() - t0
     barrier(world, device)
     launches = fm.flint_moe_launch_count(m.h) - launches0
     if graph is not None:
@@ -479,17 +519,16 @@ def head_cpu_baseline(seconds: float) -> dict:
                       f"scaled to the whole head"}
 
 
-def cpu_baseline(cfg, seconds: float, act_quant: bool = False) -> dict:
-    """The CPU oracle (test infrastructure), timed as it stands on the host
-    cores, on a bounded sample of the workload (with the NVFP4 activation
-    quantisation where the GPU path applies it)."""
+def _oracle_rate(cfg, seconds: float, act_quant: bool, max_tokens: int | None = None) -> tuple[float, str]:
+    """Tokens/s of the oracle (float64 numpy, as it stands) on a bounded
+    sample of the workload, and a description of the sample."""
     import oracle
     T = cfg.tokens
     if cfg.n_layers > 1:
-        # bounded sample of the stack: whole layers of it, one at a time
+        # the stack: whole layers of it, one at a time, scaled to all layers
         el, n = 0.0, 0
         bits = synth.make_hidden(cfg, tokens=T, stream=1)
-        while el < seconds and n < cfg.n_layers:
+        while (el < seconds or n == 0) and n < cfg.n_layers:
             L = synth.make_layer(cfg, layer=n)
             t0 = time.perf_counter()
             r = oracle.moe.moe_layer(bits, L)
@@ -497,25 +536,144 @@ def cpu_baseline(cfg, seconds: float, act_quant: bool = False) -> dict:
                 oracle.formats.bf16_array(bits) + r.out_bf16))
             el += time.perf_counter() - t0
             n += 1
-        per_token = el / n * cfg.n_layers
-        return {"value": T / per_token, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-                "sample": f"{n} of the {cfg.n_layers} layers (T={T}) through the float64 numpy oracle in "
-                          f"{el:.1f} s, scaled to the whole stack"}
+        return T / (el / n * cfg.n_layers), (f"{n} of the {cfg.n_layers} layers (T={T}) in {el:.1f} s, "
+                                             f"scaled to the whole stack")
     L = synth.make_layer(cfg)
-    done = 0
-    steps = 0
+    Ts = T if max_tokens is None else min(T, max_tokens)
+    done, steps = 0, 0
     t0 = time.perf_counter()
     while True:
         bits = synth.make_hidden(cfg, tokens=T, stream=1 + steps)
-        oracle.moe.moe_layer(bits, L, act_quant=act_quant)
-        done += T
+        r0 = (steps * Ts) % T
+        oracle.moe.moe_layer(bits[r0:r0 + Ts], L, act_quant=act_quant)
+        done += Ts
         steps += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": done / el, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"{steps} full steps of the workload ({done} tokens) through the float64 numpy "
-                      f"oracle in {el:.1f} s"}
+    what = "full steps of the workload" if Ts == T else f"samples of {Ts} of the workload's {T} tokens"
+    return done / el, f"{steps} {what} ({done} tokens) in {el:.1f} s"
+
+
+def cpu_baseline(cfg, seconds: float, act_quant: bool = False, single_tokens: int | None = None) -> dict:
+    """The CPU oracle (test infrastructure), timed as it stands on the host
+    cores on a bounded sample of the workload, with the NVFP4 activation
+    quantisation where the GPU path applies it: once with the BLAS pool at its
+    default size (all cores) and once restricted to one thread."""
+    from threadpoolctl import threadpool_limits
+    v_all, what_all = _oracle_rate(cfg, seconds, act_quant)
+    with threadpool_limits(limits=1):
+        v_one, what_one = _oracle_rate(cfg, seconds, act_quant, max_tokens=single_tokens)
+    mode = "quantised activations (NVFP4)" if act_quant else "16-bit activations"
+    return {"value": v_all, "unit": "tokens/s", "cores": blas_threads(), "nproc": os.cpu_count(), "kind": "oracle",
+            "sample": f"float64 numpy oracle, {mode}, all cores: {what_all}",
+            "single_thread": {"value": v_one, "unit": "tokens/s", "cores": 1,
+                              "sample": f"one BLAS thread: {what_one}"}}
+
+
+def kernel_roofline(cfg, res, peaks, fp4) -> dict:
+    """roofline (dominant kernel), and the per-workload extras, of one run."""
+    hbm = peaks["hbm_gbs"]
+    nb = res["bytes"]
+    out = {}
+    layer_gbs = nb["layer_bytes"] / (res["ms"] * 1e-3) / 1e9
+    hbm_src = "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured" else "fallback 6.4 TB/s"
+    if res["launches_per_forward"] == 1 and cfg.n_layers == 1:
+        k_us, k_bytes = res["ms"] * 1e3, nb["layer_bytes"]
+        kname = "decode_fused_kernel (the whole layer in one launch)"
+        srcs = ("bit_quantized_expert_softmax_b300/csrc/decode_fused.cu", "bit_quantized_expert_softmax_b300/csrc/tiles.cuh",
+                "bit_quantized_expert_softmax_b300/csrc/common.cuh")
+        kkey = "decode_fused_kernel"
+    elif res["phase_us"] is not None and res["plan"] & 2:
+        # FP4 path: the gate/up GEMM (largest phase) against the measured FP4 peak
+        ph = res["phase_us"]
+        k_us = ph["gateup"]
+        srcs = ("bit_quantized_expert_softmax_b300/csrc/moe_prefill.cu", "bit_quantized_expert_softmax_b300/csrc/gemm_fp4.cuh",
+                "bit_quantized_expert_softmax_b300/csrc/umma.cuh", "bit_quantized_expert_softmax_b300/csrc/common.cuh")
+        f1, f2 = nb["fp4_gemm1_flops"], nb["fp4_gemm2_flops"]
+        achieved = f1 / (k_us * 1e-6) / 1e12
+        g1_gbs = nb["fp4_gemm1_bytes"] / (k_us * 1e-6) / 1e9
+        layer_tflops = (f1 + f2) / (res["ms"] * 1e-3) / 1e12
+        # attainable: the slower of streaming the layer's bytes at the copy
+        # bandwidth and its FP4 FLOPs at the measured peak
+        t_bytes = nb["layer_bytes"] / (hbm * 1e9)
+        t_flops = (f1 + f2) / (fp4["tflops"] * 1e12)
+        out["roofline"] = {
+            "bound": "tensor", "achieved": achieved, "peak": fp4["tflops"], "unit": "TFLOP/s",
+            "frac": achieved / fp4["tflops"],
+            "traffic": recorded_traffic("fp4_gemm_kernel<Gemm1>", cfg.name, source_digest(*srcs)),
+            "kernel": "fp4_gemm_kernel<Gemm1> (expert gate/up, block-scaled FP4, SwiGLU epilogue)",
+            "algorithmic_flops_per_launch": f1, "algorithmic_bytes_per_launch": nb["fp4_gemm1_bytes"],
+            "avg_launch_us": k_us, "hbm_achieved_gbs": g1_gbs, "hbm_frac": g1_gbs / hbm,
+            "peak_source": "measured: dense FP4 burst of this GPU (flint_moe_probe_fp4_peak, this run)",
+        }
+        out["tensor"] = {
+            "gateup_tflops": achieved, "down_tflops": f2 / (ph["down_combine"] * 1e-6) / 1e12,
+            "layer_tflops": layer_tflops, "layer_frac_of_fp4_peak": layer_tflops / fp4["tflops"],
+            "layer_attainable_us": max(t_bytes, t_flops) * 1e6,
+            "layer_frac_of_attainable": max(t_bytes, t_flops) / (res["ms"] * 1e-3),
+            "down_hbm_frac": nb["fp4_gemm2_bytes"] / (ph["down_combine"] * 1e-6) / 1e9 / hbm,
+        }
+        out["phases_us"] = ph
+        k_us = None
+    elif res["phase_us"] is not None:
+        k_us, k_bytes = res["phase_us"]["gateup"], nb["gateup_kernel_bytes"]
+        kname = "gateup_kernel (expert gate/up, SwiGLU)"
+        srcs = ("bit_quantized_expert_softmax_b300/csrc/experts.cu", "bit_quantized_expert_softmax_b300/csrc/tiles.cuh",
+                "bit_quantized_expert_softmax_b300/csrc/common.cuh")
+        kkey = "gateup_kernel"
+        out["phases_us"] = {k: v for k, v in res["phase_us"].items()
+                            if k in ("router_topk_bucket", "gateup", "down_combine")}
+    else:
+        # the stack: one graph of n_layers single-launch layers per step
+        k_us, k_bytes = res["ms"] * 1e3 / cfg.n_layers, nb["layer_bytes"] / cfg.n_layers
+        kname = "decode_fused_kernel (per layer, inside the stack's CUDA graph)"
+        srcs = ("bit_quantized_expert_softmax_b300/csrc/decode_fused.cu", "bit_quantized_expert_softmax_b300/csrc/tiles.cuh",
+                "bit_quantized_expert_softmax_b300/csrc/common.cuh")
+        kkey = "decode_fused_kernel"
+    if k_us is not None:
+        achieved = k_bytes / (k_us * 1e-6) / 1e9
+        out["roofline"] = {
+            "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": recorded_traffic(kkey, cfg.name, source_digest(*srcs)),
+            "kernel": kname, "algorithmic_bytes_per_launch": k_bytes, "avg_launch_us": k_us,
+            "peak_source": hbm_src,
+        }
+    out["layer_hbm"] = {"bytes_per_step": nb["layer_bytes"], "selected_expert_bytes_per_step": nb["selected_expert_bytes"],
+                        "achieved_gbs": layer_gbs, "frac_of_measured": layer_gbs / hbm,
+                        "selected_frac_of_measured": nb["selected_expert_bytes"] / (res["ms"] * 1e-3) / 1e9 / hbm,
+                        "experts_read": res["n_active"]}
+    return out
+
+
+def workload_config(cfg) -> dict:
+    return {"workload": f"{cfg.name}: {cfg.n_layers} MoE layer(s), d={cfg.d}, f={cfg.f}, "
+                        f"{cfg.n_experts} routed experts top-{cfg.top_k} + 1 shared, "
+                        f"{'NVFP4' if cfg.wfmt == 0 else 'q4_1'} weights, T={cfg.tokens}"
+                        + (", Zipf(1.1) router bias" if cfg.bias == "zipf" else ""),
+            "tokens_per_step": cfg.tokens,
+            "l2": "flushed between steps (memset of 2x L2, outside the per-step events)"}
+
+
+def record(cfg, res, peaks, fp4, world) -> dict:
+    """The measured numbers of one workload: value, timing, roofline, e2e,
+    launches and clocks."""
+    r = {"value": res["value"], "unit": "tokens/s", "ms_per_step": res["ms"],
+         "dtype": "nvfp4" if res["plan"] & 2 else ("q4_1 weights, f16 activations" if cfg.wfmt == 1
+                                                   else "nvfp4 weights, f16 activations"),
+         "config": workload_config(cfg)}
+    r.update(kernel_roofline(cfg, res, peaks, fp4))
+    r["e2e"] = {"value": res["e2e_value"], "unit": "tokens/s", "h2d_bytes_per_step": cfg.tokens * cfg.d * 2,
+                "d2h_bytes_per_step": cfg.tokens * cfg.d * 2}
+    r["gpu_launches"] = int(res["launches"])
+    r["clocks"] = res["clocks"]
+    step_ms = np.array(res["step_ms"])
+    r["step_ms_p10_p50_p90"] = [float(np.percentile(step_ms, q)) for q in (10, 50, 90)]
+    return r
+
+
+# sub-records of the default run: (config, timed steps, warm-up steps)
+SUBRECORDS = [(2, 2000, 200), (3, 1000, 100), (4, 200, 10)]
 
 
 # ---------------------------------------------------------------------------
@@ -523,16 +681,62 @@ def cpu_baseline(cfg, seconds: float, act_quant: bool = False) -> dict:
 # ---------------------------------------------------------------------------
 
 
+def reference_main(args, cfg, rank):
+    """The reference arm: the CPU oracle as it stands, on the host cores, on
+    the same workload, metric and unit; each timed step is a bounded sample
+    (at most 2048 of the workload's tokens, rotating over the batch), the
+    warm-up steps 64-token samples, the whole run capped at ~2.5 minutes."""
+    if rank != 0:
+        return
+    import oracle
+    budget = 150.0
+    t_all = time.perf_counter()
+    n_keep = min(cfg.n_layers, 4)     # a stack step is timed on its first layers and scaled
+    layers = [synth.make_layer(cfg, layer=i) for i in range(n_keep)]
+    aq = fp4_expert_path(cfg)
+    Ts = min(cfg.tokens, 2048)
+    for i in range(args.warmup):
+        bits = synth.make_hidden(cfg, stream=100 + i)[:min(cfg.tokens, 64)]
+        oracle.moe.moe_layer(bits, layers[0], act_quant=aq)
+    steps = []
+    for i in range(args.steps):
+        bits = synth.make_hidden(cfg, stream=1 + i)
+        r0 = (i * Ts) % cfg.tokens
+        t0 = time.perf_counter()
+        for L in layers:
+            oracle.moe.moe_layer(bits[r0:r0 + Ts], L, act_quant=aq)
+        steps.append((time.perf_counter() - t0) * cfg.n_layers / n_keep)
+        if time.perf_counter() - t_all > budget and len(steps) >= 3:
+            break
+    ms = statistics.mean(steps) * 1e3
+    value = Ts / (ms / 1e3)
+    sample = (f"{len(steps)} steps, each the oracle on {Ts} of the workload's {cfg.tokens} tokens"
+              + (f" through {n_keep} of the {cfg.n_layers} layers, scaled" if n_keep < cfg.n_layers else "")
+              + f"; {args.warmup} warm-up steps of 64 tokens; run capped at {budget:.0f} s")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": len(steps), "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "oracle_mode": "quantised activations (NVFP4)" if aq else "16-bit activations",
+            "data": "synthetic", "config": workload_config(cfg),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle", "cores": blas_threads(),
+                             "nproc": os.cpu_count(), "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default per workload: about 1-5 s of device time)")
-    ap.add_argument("--warmup", type=int, default=100)
-    ap.add_argument("--config", type=int, default=2, choices=sorted(synth.CONFIGS))
+                    help="timed steps of the headline workload (default: about 1 s of device time)")
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=5, choices=sorted(synth.CONFIGS),
+                    help="headline workload (default 5: the 8192-token prefill)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-subrecords", action="store_true",
+                    help="time only the headline workload (default with --config other than 5)")
     ap.add_argument("--head", action="store_true",
                     help="the 4-bit output head (146,432 x 2048 NVFP4) and its sampler instead of an MoE config")
     args = ap.parse_args()
@@ -548,46 +752,8 @@ def main():
     if world != args.gpus and world > 1:
         print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
 
-    workload = {"workload": f"{cfg.name}: {cfg.n_layers} MoE layer(s), d={cfg.d}, f={cfg.f}, "
-                            f"{cfg.n_experts} routed experts top-{cfg.top_k} + 1 shared, "
-                            f"{'NVFP4' if cfg.wfmt == 0 else 'q4_1'} weights, T={cfg.tokens}"
-                            + (", Zipf(1.1) router bias" if cfg.bias == "zipf" else ""),
-                "tokens_per_step": cfg.tokens,
-                "l2": "flushed between steps (memset of 2x L2, outside the per-step events)"}
-
     if args.impl == "reference":
-        if rank != 0:
-            return
-        steps = []
-        budget = 120.0
-        t_all = time.perf_counter()
-        import oracle
-        n_keep = min(cfg.n_layers, 4)     # a stack step is timed on its first layers and scaled
-        layers = [synth.make_layer(cfg, layer=i) for i in range(n_keep)]
-        for i in range(args.warmup + args.steps):
-            bits = synth.make_hidden(cfg, stream=1 + i)
-            t0 = time.perf_counter()
-            for L in layers:
-                oracle.moe.moe_layer(bits, L, act_quant=fp4_expert_path(cfg))
-            dt = (time.perf_counter() - t0) * cfg.n_layers / n_keep
-            if i >= args.warmup:
-                steps.append(dt)
-            if time.perf_counter() - t_all > budget and len(steps) >= 3:
-                break
-        ms = statistics.mean(steps) * 1e3
-        value = cfg.tokens / (ms / 1e3)
-        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
-                "n_gpus": args.gpus, "steps": len(steps), "warmup": args.warmup, "ms_per_step": ms,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "oracle_mode": "quantised activations (NVFP4)" if fp4_expert_path(cfg) else "16-bit activations",
-                "data": "synthetic", "config": workload,
-                "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle",
-                                 "cores": blas_threads(),
-                                 "sample": f"{len(steps)} steps of the workload, one oracle call each "
-                                           f"(run capped at {budget:.0f} s)"},
-                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        reference_main(args, cfg, rank)
         return
 
     import torch
@@ -595,89 +761,37 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    res = run_ours(args, cfg, world, rank, local)
+    from bit_quantized_expert_softmax_b300 import build
+    build.build()
+    from bit_quantized_expert_softmax_b300 import flint_moe as fm
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    peaks = measured_peaks()
+    fp4 = fp4_peak(fm, device)
+    res = run_ours(cfg, world, rank, local, args.steps, args.warmup)
+    subs = {}
+    if args.config == 5 and not args.no_subrecords:
+        for c, k, w in SUBRECORDS:
+            scfg = synth.CONFIGS[c]
+            subs[scfg.name] = (scfg, k, w, run_ours(scfg, world, rank, local, k, w, soak_s=0.5))
     if rank == 0:
-        peaks = res["peaks"]
-        hbm = peaks["hbm_gbs"]
-        nb = res["bytes"]
         line = {
             "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "nvfp4" if res["plan"] & 2 else "f16", "data": "synthetic", "config": workload,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "data": "synthetic",
         }
-        layer_gbs = nb["layer_bytes"] / (res["ms"] * 1e-3) / 1e9
-        if res["launches_per_forward"] == 1 and cfg.n_layers == 1:
-            # one launch per layer: the timed step is the kernel
-            k_us = res["ms"] * 1e3
-            k_bytes = nb["layer_bytes"]
-            kname = "decode_fused_kernel (the whole layer in one launch)"
-            srcs = ("bit_quantized_expert_softmax_b300/csrc/decode_fused.cu",
-                    "bit_quantized_expert_softmax_b300/csrc/tiles.cuh",
-                    "bit_quantized_expert_softmax_b300/csrc/common.cuh")
-            kkey = "decode_fused_kernel"
-        elif res["phase_us"] is not None and res["plan"] & 2:
-            # FP4 path: the gate/up GEMM (largest phase), bound by HBM: its
-            # algorithmic bytes take longer at the measured copy bandwidth
-            # than its FLOPs at the FP4 tensor peak
-            k_us = res["phase_us"]["gateup"]
-            k_bytes = nb["fp4_gemm1_bytes"]
-            kname = "fp4_gemm_kernel<Gemm1> (expert gate/up, block-scaled FP4, SwiGLU epilogue)"
-            srcs = ("bit_quantized_expert_softmax_b300/csrc/moe_prefill.cu",
-                    "bit_quantized_expert_softmax_b300/csrc/gemm_fp4.cuh",
-                    "bit_quantized_expert_softmax_b300/csrc/umma.cuh",
-                    "bit_quantized_expert_softmax_b300/csrc/common.cuh")
-            kkey = "fp4_gemm_kernel<Gemm1>"
-            line["phases_us"] = res["phase_us"]
-            fp4_peak = peaks["bf16_tflops"] * 6.0      # nominal dense FP4 : bf16 = 13.5 : 2.25
-            line["tensor"] = {
-                "gateup_tflops": nb["fp4_gemm1_flops"] / (k_us * 1e-6) / 1e12,
-                "down_tflops": nb["fp4_gemm2_flops"] / (res["phase_us"]["down_combine"] * 1e-6) / 1e12,
-                "fp4_peak_tflops": fp4_peak,
-                "peak_source": "measured bf16 (MEASURED_PEAKS.json bf16_tflops) x 6, the nominal FP4:bf16 ratio",
-                "down_hbm_frac": nb["fp4_gemm2_bytes"] / (res["phase_us"]["down_combine"] * 1e-6) / 1e9 / hbm,
-            }
-        elif res["phase_us"] is not None:
-            k_us = res["phase_us"]["gateup"]
-            k_bytes = nb["gateup_kernel_bytes"]
-            kname = "gateup_kernel (expert gate/up, SwiGLU)"
-            srcs = ("bit_quantized_expert_softmax_b300/csrc/experts.cu",
-                    "bit_quantized_expert_softmax_b300/csrc/tiles.cuh",
-                    "bit_quantized_expert_softmax_b300/csrc/common.cuh")
-            kkey = "gateup_kernel"
-            line["phases_us"] = {k: v for k, v in res["phase_us"].items() if k in ("router_topk_bucket", "gateup",
-                                                                                    "down_combine")}
-        else:
-            # the stack: one graph of n_layers single-launch layers per step
-            k_us = res["ms"] * 1e3 / cfg.n_layers
-            k_bytes = nb["layer_bytes"] / cfg.n_layers
-            kname = "decode_fused_kernel (per layer, inside the stack's CUDA graph)"
-            srcs = ("bit_quantized_expert_softmax_b300/csrc/decode_fused.cu",
-                    "bit_quantized_expert_softmax_b300/csrc/tiles.cuh",
-                    "bit_quantized_expert_softmax_b300/csrc/common.cuh")
-            kkey = "decode_fused_kernel"
-        achieved = k_bytes / (k_us * 1e-6) / 1e9
-        line["roofline"] = {
-            "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-            "traffic": recorded_traffic(kkey, cfg.name, source_digest(*srcs)),
-            "kernel": kname, "algorithmic_bytes_per_launch": k_bytes, "avg_launch_us": k_us,
-            "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
-            else "fallback 6.4 TB/s",
-        }
-        line["layer_hbm"] = {"bytes_per_step": nb["layer_bytes"],
-                             "selected_expert_bytes_per_step": nb["selected_expert_bytes"],
-                             "achieved_gbs": layer_gbs, "frac_of_measured": layer_gbs / hbm,
-                             "selected_frac_of_measured": nb["selected_expert_bytes"] / (res["ms"] * 1e-3) / 1e9 / hbm,
-                             "experts_read": res["n_active"]}
-        line["e2e"] = {"value": res["e2e_value"], "unit": "tokens/s",
-                       "h2d_bytes_per_step": cfg.tokens * cfg.d * 2,
-                       "d2h_bytes_per_step": cfg.tokens * cfg.d * 2}
-        line["gpu_launches"] = int(res["launches"])
-        line["clocks"] = res["clocks"]
-        step_ms = np.array(res["step_ms"])
-        line["step_ms_p10_p50_p90"] = [float(np.percentile(step_ms, q)) for q in (10, 50, 90)]
+        rec = record(cfg, res, peaks, fp4, world)
+        line.update({k: v for k, v in rec.items() if k not in ("value", "unit", "ms_per_step")})
+        line["fp4_peak"] = fp4
+        if subs:
+            line["subrecords"] = {}
+            for name, (scfg, k, w, sres) in subs.items():
+                sr = record(scfg, sres, peaks, fp4, world)
+                sr.update({"steps": k, "warmup": w})
+                line["subrecords"][name] = sr
         if not args.no_cpu_baseline and world == 1:
-            line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds, act_quant=bool(res["plan"] & 2))
+            line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds, act_quant=bool(res["plan"] & 2),
+                                                single_tokens=512)
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

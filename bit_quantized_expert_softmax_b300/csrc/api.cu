@@ -129,6 +129,7 @@ Workspace carve(const Shape& s, char* base, size_t* total) {
     w.chunk_hist = cv.take<int>(n_chunks * s.E);
     w.counters = cv.take<uint32_t>(flint::kCounters);
     w.gbar = cv.take<uint32_t>(64);
+    w.dbg = cv.take<uint32_t>(64);
     w.status = cv.take<uint32_t>(1);
     *total = align_up(cv.off, 256);
     return w;
@@ -545,6 +546,15 @@ flint_status flint_moe_status(flint_moe* h) {
     uint32_t v = 0;
     e = cudaMemcpy(&v, h->ws.status, sizeof(v), cudaMemcpyDeviceToHost);
     if (e == cudaSuccess) e = cudaMemset(h->ws.status, 0, sizeof(v));
+    if (e == cudaSuccess && (v & flint::kStatusTimeout)) {
+        // a kernel left a barrier early: its arrival counters may be off, so
+        // put every counter back to its between-launches value (zero); the
+        // device is idle here
+        e = cudaMemset(h->ws.gbar, 0, 64 * sizeof(uint32_t));
+        if (e == cudaSuccess) e = cudaMemset(h->ws.counters, 0, flint::kCounters * sizeof(uint32_t));
+        if (e == cudaSuccess && h->head_hs.counters != nullptr)
+            e = cudaMemset(h->head_hs.counters, 0, flint::kHeadMaxT * sizeof(unsigned));
+    }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return FLINT_ECUDA;
     if (v & flint::kStatusTimeout) return FLINT_ETIMEOUT;
@@ -616,6 +626,52 @@ flint_status flint_moe_dequant(flint_moe* h, int layer, int expert, int mat, flo
                                                  s.wfmt == FLINT_W_NVFP4 ? L.tscale + mi : nullptr, R, K,
                                                  s.wfmt, out_dev, (cudaStream_t)stream);
     return cuda_status(e);
+}
+
+flint_status flint_moe_debug_wait_timeout(flint_moe* h, int kind, uint32_t spin_limit, void* stream) {
+    if (h == nullptr || (kind != 0 && kind != 1) || spin_limit < 1 || spin_limit > (1u << 20)) return FLINT_EINVAL;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return FLINT_ECUDA;
+    const cudaError_t e = flint::launch_wait_timeout(kind, spin_limit, reinterpret_cast<unsigned long long*>(h->ws.dbg),
+                                                     h->ws.status, (cudaStream_t)stream);
+    if (e == cudaSuccess) h->launches += 1;
+    return cuda_status(e);
+}
+
+flint_status flint_moe_probe_fp4_peak(int n, int iters, float* ms, double* flops) {
+    if ((n != 128 && n != 256) || iters < 1 || iters > (1 << 24) || ms == nullptr || flops == nullptr)
+        return FLINT_EINVAL;
+    int dev = 0, n_sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FLINT_ECUDA;
+    if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FLINT_ECUDA;
+    uint32_t* status = nullptr;
+    cudaStream_t st = nullptr;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    cudaError_t e = cudaMalloc(&status, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemset(status, 0, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreate(&e0);
+    if (e == cudaSuccess) e = cudaEventCreate(&e1);
+    // one short launch first (code, clocks), then the timed one
+    if (e == cudaSuccess) e = flint::launch_fp4_peak(n, iters / 16 + 1, n_sms, status, st);
+    if (e == cudaSuccess) e = cudaEventRecord(e0, st);
+    if (e == cudaSuccess) e = flint::launch_fp4_peak(n, iters, n_sms, status, st);
+    if (e == cudaSuccess) e = cudaEventRecord(e1, st);
+    if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+    float t = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, e0, e1);
+    uint32_t hs = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&hs, status, sizeof(hs), cudaMemcpyDeviceToHost);
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    if (st) cudaStreamDestroy(st);
+    cudaFree(status);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (hs != 0) return FLINT_ETIMEOUT;
+    *ms = t;
+    // per MMA: M = 128, N = n, K = 64; four MMAs per iteration on every SM
+    *flops = 2.0 * 128.0 * n * 64.0 * 4.0 * (double)iters * n_sms;
+    return FLINT_OK;
 }
 
 size_t flint_moe_device_bytes(const flint_moe* h) {

@@ -200,14 +200,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
     return ok != 0;
 }
 
-// Bounded wait for an mbarrier phase. Returns false (and records a timeout in
-// the status word) if the phase does not complete within the limit.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, uint32_t* status) {
-    for (uint32_t it = 0; it < (1u << 22); ++it) {
+// Bounded wait for an mbarrier phase: at most `limit` polls. Returns false
+// (and records a timeout in the status word) if the phase does not complete
+// within the limit.
+constexpr uint32_t kMbarSpinLimit = 1u << 22;
+
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t phase, uint32_t* status, uint32_t limit) {
+    for (uint32_t it = 0; it < limit; ++it) {
         if (mbar_try_wait(bar, phase)) return true;
     }
     if (status) atomicOr(status, kStatusTimeout);
     return false;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, uint32_t* status) {
+    return mbar_wait_limit(bar, phase, status, kMbarSpinLimit);
+}
+
+// A ring of n_stages shared-memory stages, each filled by bulk copies that
+// complete on full[stage]; fill number i (i = 0, 1, ...) uses stage i % n at
+// phase i / n. After `fills` fills were issued, wait (bounded) until the last
+// fill of every stage has landed. A producer that leaves its loop early (a
+// wait of its own or of another role gave up) calls this before the CTA
+// exits, so that no copy it issued still writes the CTA's shared memory
+// afterwards. Earlier fills of a stage have always landed (the next fill of a
+// stage is issued only after its consumers released the previous one), so the
+// parity wait cannot be satisfied by an older phase. Stages whose last fill
+// was already consumed return at once.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int n_stages, uint32_t fills, uint32_t* status) {
+    for (int s = 0; s < n_stages; ++s) {
+        if (fills > (uint32_t)s) {
+            const uint32_t last_use = (fills - 1 - (uint32_t)s) / (uint32_t)n_stages;
+            mbar_wait_bounded(&full[s], last_use & 1u, status);
+        }
+    }
 }
 
 // Grid-wide barrier for a kernel whose CTAs are all resident (cooperative
@@ -280,14 +306,16 @@ __device__ __forceinline__ void grid_arrive(GridSync& gs) {
     if (threadIdx.x == 0) red_release_gpu_add_u64(gs.count, 1ull);
 }
 
-__device__ __forceinline__ bool grid_wait(GridSync& gs, uint32_t* status) {
+constexpr uint32_t kGridSpinLimit = 1u << 26;
+
+__device__ __forceinline__ bool grid_wait(GridSync& gs, uint32_t* status, uint32_t limit = kGridSpinLimit) {
     __shared__ uint32_t s_okw;
     if (threadIdx.x == 0) {
         uint32_t ok = 1;
         const unsigned long long target = gs.base + (unsigned long long)gs.n * gs.passed;
         uint32_t it = 0;
         while (ld_acquire_gpu_u64(gs.count) < target) {
-            if (++it > (1u << 26)) {
+            if (++it > limit) {
                 atomicOr(status, kStatusTimeout);
                 ok = 0;
                 break;
@@ -310,7 +338,7 @@ __device__ __forceinline__ bool grid_sync(GridSync& gs, uint32_t* status) {
         red_release_gpu_add_u64(gs.count, 1ull);
         uint32_t it = 0;
         while (ld_acquire_gpu_u64(gs.count) < target) {
-            if (++it > (1u << 26)) {
+            if (++it > kGridSpinLimit) {
                 atomicOr(status, kStatusTimeout);
                 ok = 0;
                 break;

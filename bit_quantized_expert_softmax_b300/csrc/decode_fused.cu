@@ -250,6 +250,23 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
 
     bool ok = true;
     uint32_t slot_phase = 0;   // bit s: parity of slot s's next completion
+    // thread 0 (the only thread that issues bulk copies): bit i of pend = a
+    // copy was issued on barrier bars[i], whose phase of parity bit i of
+    // pend_par it completes. No copy is issued once a wait has given up, so
+    // at exit drain() waits (bounded) for exactly the copies that may still
+    // be in flight and none of them writes shared memory after the CTA is gone.
+    uint32_t pend = 0, pend_par = 0;
+    auto mark_issued = [&](int i, uint32_t parity) {
+        pend |= 1u << i;
+        pend_par = (pend_par & ~(1u << i)) | (parity << i);
+    };
+    auto drain = [&]() {
+        if (threadIdx.x == 0) {
+#pragma unroll 1
+            for (int i = 0; i < a.n_slots + 4; ++i)
+                if ((pend >> i) & 1u) mbar_wait_bounded(bars + i, (pend_par >> i) & 1u, a.status);
+        }
+    };
     // CTA-uniform bounded wait: every thread waits, and the CTA proceeds only
     // if all of them saw the phase complete.
     auto wait_all = [&](uint64_t* bar, uint32_t ph) {
@@ -276,16 +293,22 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
         mbar_arrive_expect_tx(bar_x, (uint32_t)(T * d * 2 + a.ts_bytes));
         bulk_g2s(smem + a.off_xbf, a.x, (uint32_t)(T * d * 2), bar_x);
         bulk_g2s(smem + a.off_ts, a.tscale, (uint32_t)a.ts_bytes, bar_x);
+        mark_issued(a.n_slots + 3, 0u);
         if (n_re > 0) {
             mbar_arrive_expect_tx(bar_router, (uint32_t)(n_re * d * 4));
 #pragma unroll 1
             for (int i = 0; i < n_re; ++i)
                 bulk_g2s(slots + (size_t)i * d * 4, a.router + (size_t)(b + i * G) * d, d * 4, bar_router);
+            mark_issued(a.n_slots, 0u);
         }
-        if (has_shared) issue_half<WFMT>(a, E, shared_unit, slots + (size_t)shared_slot * a.unit_bytes, bars + shared_slot);
+        if (has_shared) {
+            issue_half<WFMT>(a, E, shared_unit, slots + (size_t)shared_slot * a.unit_bytes, bars + shared_slot);
+            mark_issued(shared_slot, 0u);
+        }
         if (down_tile >= 0) {
             mbar_arrive_expect_tx(bar_dshared, (uint32_t)a.down_bytes);
             issue_down<WFMT>(a, E, down_tile, down, bar_dshared);
+            mark_issued(a.n_slots + 1, 0u);
         }
     }
     if (threadIdx.x >= 32 && threadIdx.x < 32 + n_re) bias_s[threadIdx.x - 32] = __ldg(a.bias + b + (threadIdx.x - 32) * G);
@@ -432,16 +455,18 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     // half-unit or one wave of routed half-units
     bool shared_pending = has_shared, wave_issued = false;
     for (int u0 = b;;) {
-        if (!wave_issued && u0 < n_units) {
+        if (!wave_issued && u0 < n_units && ok) {
             __syncthreads();   // the previous wave's slots have been read
             if (threadIdx.x == 0) {
                 fence_proxy_async_smem();
 #pragma unroll 1
                 for (int s2 = 0; s2 < n_rs; ++s2) {
                     const int u = u0 + s2 * G;
-                    if (u < n_units)
+                    if (u < n_units) {
                         issue_half<WFMT>(a, act[u / units_per_expert], u % units_per_expert,
                                          slots + (size_t)s2 * a.unit_bytes, bars + s2);
+                        mark_issued(s2, (slot_phase >> s2) & 1u);
+                    }
                 }
             }
             wave_issued = true;
@@ -474,11 +499,12 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     // routed down slabs for this CTA's output tile (slab 0 is the shared
     // expert), requested once the gate/up slabs have landed so that they do
     // not compete with them; they are needed only after the next barrier
-    if (threadIdx.x == 0 && down_tile >= 0 && na > 0) {
+    if (threadIdx.x == 0 && down_tile >= 0 && na > 0 && ok) {
         mbar_arrive_expect_tx(bar_drouted, (uint32_t)(na * a.down_bytes));
 #pragma unroll 1
         for (int q = 0; q < na; ++q)
             issue_down<WFMT>(a, act[q], down_tile, down + (size_t)(1 + q) * a.down_bytes, bar_drouted);
+        mark_issued(a.n_slots + 2, 0u);
     }
     if (!grid_sync(gsync, a.status)) ok = false;
 
@@ -504,7 +530,10 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
                              2 * KTf * S);
         }
     }
-    if (down_tile < 0) return;
+    if (down_tile < 0) {
+        drain();
+        return;
+    }
     // stage h rows as fp16 with a power-of-two scale per (token, slot) row
     const int n_rows = T * (k + 1);
     // (lane l holds elements 4(32q + l) .. +3; pairs stay adjacent under the
@@ -535,6 +564,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     }
     wait_all(bar_dshared, 0);
     if (na > 0) wait_all(bar_drouted, 0);
+    drain();   // returns at once unless a wait above gave up
     // down products: warps 2q and 2q+1 (slab q = shared, then routed) run the
     // two halves of the k-tiles -> acc[q][half][16 rows][8 pairs]
     const int S = WFMT == 0 ? 64 : 128;

@@ -83,7 +83,8 @@ template <class P>
 __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, uint32_t* status) {
     extern __shared__ uint8_t graw[];
     constexpr int kGStages = P::kStages;
-    __shared__ __align__(8) uint64_t full[kGStages], sfready[kGStages], empty[kGStages], accfull[2], accempty[2];
+    __shared__ __align__(8) uint64_t full[kGStages], sfready[kGStages], empty[kGStages], accfull[2], accempty[2],
+        mma_done;
     __shared__ uint32_t tmem_base;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(graw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -97,6 +98,7 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
             mbar_init(&accfull[b], 1);
             mbar_init(&accempty[b], kGEpiWarps);
         }
+        mbar_init(&mma_done, 1);
         mbar_fence_init();
     }
     if (warp == 1) {
@@ -132,6 +134,9 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
                     bulk_g2s(st + kGKPS * kGBlk, w.b + (size_t)k0 * kGBlk, (uint32_t)(n * kGBlk), &full[s]);
                 }
             }
+            // every copy issued has landed before the CTA can exit, also when
+            // a role gave up early
+            drain_ring(full, kGStages, kcount, status);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -171,6 +176,10 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
                 umma_commit(&accfull[buf]);
                 ++n_done;
             }
+            // every MMA issued has completed before the tensor memory is
+            // released, also when a wait gave up early
+            umma_commit(&mma_done);
+            mbar_wait_bounded(&mma_done, 0, status);
         }
     } else if (warp < 6) {
         // scale writers: every quadrant writes the same 32 x 16-byte image:

@@ -70,6 +70,7 @@ struct Workspace {
     int* chunk_hist;      // [n_chunks][E]
     uint32_t* counters;   // [kCounters] arrival counters (self-resetting)
     uint32_t* gbar;       // [64]  grid-barrier count ([0]) and generation ([32])
+    uint32_t* dbg;        // [64]  the timeout check's own barrier counter
     uint32_t* status;     // device status word
 };
 
@@ -154,6 +155,13 @@ bool head_sample_supported(int V, int top_k);
 cudaError_t launch_head_sample(const float* logits, int T, int V, float temperature, int top_k, float top_p,
                                const float* u, int* tokens, int* topk_idx, const HeadScratch& hs, uint32_t* status,
                                cudaStream_t st);
+
+// debug_wait.cu: bounded waits that run out (kind 0 mbarrier, 1 grid barrier)
+cudaError_t launch_wait_timeout(int kind, uint32_t limit, unsigned long long* count, uint32_t* status,
+                                cudaStream_t st);
+
+// fp4_peak.cu: dense block-scaled FP4 tensor-core throughput probe
+cudaError_t launch_fp4_peak(int n, int iters, int n_sms, uint32_t* status, cudaStream_t st);
 
 // repack.cu
 cudaError_t launch_repack_matrix(const uint8_t* codes_src, const uint8_t* scales_src,

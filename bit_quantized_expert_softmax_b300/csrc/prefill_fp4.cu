@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
     if (warp == 0 && lane == 0) {
         // producer
+        uint32_t fills = 0;
         for (int kb = 0; kb < a.nkb; ++kb) {
             const int s = kb % kRStages;
             if (kb >= kRStages && !mbar_wait_bounded(&empty[s], (uint32_t)((kb / kRStages - 1) & 1), a.status))
@@ -73,7 +74,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
             tma_load_2d(st, &mx, kb * kRK, m0, &full[s]);
             tma_load_2d(st + kRTileBytes, &mwh, kb * kRK, n0, &full[s]);
             tma_load_2d(st + 2 * kRTileBytes, &mwl, kb * kRK, n0, &full[s]);
+            ++fills;
         }
+        drain_ring(full, kRStages, fills, a.status);   // no copy still in flight at exit
     } else if (warp == 1 && lane == 0) {
         // MMA issue
         const uint32_t idesc = idesc_bf16_f32(kRM, kRN);
@@ -95,6 +98,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
             umma_commit(&empty[s]);
         }
         umma_commit(&done);
+        mbar_wait_bounded(&done, 0, a.status);   // no MMA still running when the TMEM is released
     } else if (warp >= 2) {
         // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (rows of the tile)
         const int quad = warp & 3;

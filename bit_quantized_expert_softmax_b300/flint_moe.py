@@ -75,6 +75,9 @@ def lib() -> ctypes.CDLL:
             "flint_moe_load_lm_head": (_I, [_P, _I, _P, _P, ctypes.c_float]),
             "flint_moe_lm_head": (_I, [_P, _P, _I, _P, _P]),
             "flint_moe_sample": (_I, [_P, _P, _I, ctypes.c_float, _I, ctypes.c_float, _P, _P, _P, _P]),
+            "flint_moe_probe_fp4_peak": (_I, [_I, _I, ctypes.POINTER(ctypes.c_float),
+                                              ctypes.POINTER(ctypes.c_double)]),
+            "flint_moe_debug_wait_timeout": (_I, [_P, _I, ctypes.c_uint32, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -240,6 +243,18 @@ def flint_moe_sample(h: int, logits, T: int, temperature: float, top_k: int, top
                      stream=None) -> None:
     _check(lib().flint_moe_sample(h, _ptr(logits), T, float(temperature), top_k, float(top_p), _ptr(u),
                                   _ptr(tokens), _ptr(topk), _stream(stream)), "flint_moe_sample")
+
+
+def flint_moe_probe_fp4_peak(n: int, iters: int) -> tuple[float, float]:
+    """(milliseconds, FLOPs) of the dense FP4 tensor-core probe on the current device."""
+    ms = ctypes.c_float(0.0)
+    flops = ctypes.c_double(0.0)
+    _check(lib().flint_moe_probe_fp4_peak(n, iters, ctypes.byref(ms), ctypes.byref(flops)), "flint_moe_probe_fp4_peak")
+    return float(ms.value), float(flops.value)
+
+
+def flint_moe_debug_wait_timeout(h: int, kind: int, spin_limit: int, stream=None) -> None:
+    _check(lib().flint_moe_debug_wait_timeout(h, kind, spin_limit, _stream(stream)), "flint_moe_debug_wait_timeout")
 
 
 def flint_moe_bucket_noalloc(idx, T: int, k: int, E: int, offsets, perm, stream=None) -> None:

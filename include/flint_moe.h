@@ -298,6 +298,29 @@ FLINT_API flint_status flint_moe_bucket_noalloc(const int32_t* idx_dev, int T, i
 
 /* ---- measurement hooks ---------------------------------------------------- */
 
+/* Dense block-scaled FP4 tensor-core throughput of the current device, the
+ * denominator of the FP4 roofline fractions. Every SM runs iters x 4
+ * back-to-back tcgen05.mma kind::mxf4nvf4 (scale_vec::4X) of M = 128, N = n
+ * (128 or 256), K = 64 on operands resident in shared and tensor memory, one
+ * CTA per SM; the timed launch follows one short untimed launch. Writes the
+ * launch's CUDA-event time to *ms and the FLOPs it performed (2*M*N*K per MMA)
+ * to *flops. Synchronous; allocates a 4-byte status word. Errors:
+ * FLINT_EINVAL (n, iters outside 1..2^24, NULL), FLINT_ECUDA, FLINT_ETIMEOUT
+ * (the bounded wait for the MMAs gave up). The Flint blog has no counterpart:
+ * it is measurement infrastructure. */
+FLINT_API flint_status flint_moe_probe_fp4_peak(int n, int iters, float* ms, double* flops);
+
+/* Run one kernel whose bounded wait is made to run out, with the given limit
+ * of polls (1 .. 2^20): kind 0 waits on an mbarrier that never completes,
+ * kind 1 on a grid barrier (cooperative launch of 2 CTAs) that one CTA never
+ * reaches. The kernel records FLINT_ETIMEOUT in the handle's status word and
+ * returns; nothing hangs and no copy is in flight. flint_moe_status then
+ * reports FLINT_ETIMEOUT and puts the handle's barrier counters back to their
+ * idle state, after which the handle is usable. A check of the failure path
+ * of every bounded wait in the kernels; the blog has no counterpart.
+ * Asynchronous on `stream`. FLINT_EINVAL on bad arguments. */
+FLINT_API flint_status flint_moe_debug_wait_timeout(flint_moe* h, int kind, uint32_t spin_limit, void* stream);
+
 /* Number of kernels this handle has launched so far (all entry points). */
 FLINT_API uint64_t flint_moe_launch_count(const flint_moe* h);
 
