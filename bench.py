@@ -555,15 +555,30 @@ def _oracle_rate(cfg, seconds: float, act_quant: bool, max_tokens: int | None = 
     return done / el, f"{steps} {what} ({done} tokens) in {el:.1f} s"
 
 
+ONE_THREAD_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+                  "BLIS_NUM_THREADS": "1", "VECLIB_MAXIMUM_THREADS": "1", "NUMEXPR_NUM_THREADS": "1"}
+
+
+def _oracle_rate_one_thread(cfg_id: int, seconds: float, act_quant: bool, max_tokens: int | None):
+    """_oracle_rate in a child process whose BLAS pool has one thread (the
+    pool size is fixed when numpy loads, so it is set in the child's
+    environment)."""
+    env = dict(os.environ, **ONE_THREAD_ENV)
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-rate", str(cfg_id), str(seconds),
+           "1" if act_quant else "0", str(max_tokens or 0)]
+    out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600, check=True).stdout
+    d = json.loads(out.strip().splitlines()[-1])
+    return d["value"], d["sample"]
+
+
 def cpu_baseline(cfg, seconds: float, act_quant: bool = False, single_tokens: int | None = None) -> dict:
     """The CPU oracle (test infrastructure), timed as it stands on the host
     cores on a bounded sample of the workload, with the NVFP4 activation
     quantisation where the GPU path applies it: once with the BLAS pool at its
-    default size (all cores) and once restricted to one thread."""
-    from threadpoolctl import threadpool_limits
+    default size (all cores) and once in a child process with one thread."""
     v_all, what_all = _oracle_rate(cfg, seconds, act_quant)
-    with threadpool_limits(limits=1):
-        v_one, what_one = _oracle_rate(cfg, seconds, act_quant, max_tokens=single_tokens)
+    cfg_id = next(i for i, c in synth.CONFIGS.items() if c.name == cfg.name)
+    v_one, what_one = _oracle_rate_one_thread(cfg_id, seconds, act_quant, single_tokens)
     mode = "quantised activations (NVFP4)" if act_quant else "16-bit activations"
     return {"value": v_all, "unit": "tokens/s", "cores": blas_threads(), "nproc": os.cpu_count(), "kind": "oracle",
             "sample": f"float64 numpy oracle, {mode}, all cores: {what_all}",
@@ -725,6 +740,13 @@ def reference_main(args, cfg, rank):
 
 
 def main():
+    if len(sys.argv) == 6 and sys.argv[1] == "--oracle-rate":
+        # child of cpu_baseline: one oracle timing, printed as JSON
+        cfg = synth.CONFIGS[int(sys.argv[2])]
+        mt = int(sys.argv[5])
+        v, what = _oracle_rate(cfg, float(sys.argv[3]), sys.argv[4] == "1", max_tokens=mt or None)
+        print(json.dumps({"value": v, "sample": what}))
+        return
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
@@ -734,6 +756,8 @@ def main():
                     help="headline workload (default 5: the 8192-token prefill)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--soak", type=float, default=1.0,
+                    help="seconds of untimed steps under the clock sampler just before the timed steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-subrecords", action="store_true",
                     help="time only the headline workload (default with --config other than 5)")
@@ -768,12 +792,12 @@ def main():
     torch.cuda.set_device(device)
     peaks = measured_peaks()
     fp4 = fp4_peak(fm, device)
-    res = run_ours(cfg, world, rank, local, args.steps, args.warmup)
+    res = run_ours(cfg, world, rank, local, args.steps, args.warmup, soak_s=args.soak)
     subs = {}
     if args.config == 5 and not args.no_subrecords:
         for c, k, w in SUBRECORDS:
             scfg = synth.CONFIGS[c]
-            subs[scfg.name] = (scfg, k, w, run_ours(scfg, world, rank, local, k, w, soak_s=0.5))
+            subs[scfg.name] = (scfg, k, w, run_ours(scfg, world, rank, local, k, w, soak_s=min(0.5, args.soak)))
     if rank == 0:
         line = {
             "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world,

@@ -45,15 +45,19 @@ struct DebugGemm {
         const int m = i / nt, n = i % nt;
         w.a = a + (size_t)m * kt * kGBlk;
         w.b = b + (size_t)n * kt * kGBlk;
+        w.b2 = nullptr;
         w.kt = kt;
         w.m = m;
         w.n = n;
         w.aux = 0;
     }
     static constexpr int kStages = 3;
+    static constexpr int kNB = 1;
     static constexpr int kEpiSmemPerWarp = 0;
     __device__ void epilogue_finish() const {}
-    __device__ void epilogue(const Fp4Item& w, Pre, uint32_t taddr, int row, int half, uint8_t*) const {
+    template <class Release>
+    __device__ void epilogue(const Fp4Item& w, Pre, uint32_t taddr, int row, int half, uint8_t*,
+                             Release release) const {
         float* dst = d + (size_t)(w.m * kGM + row) * N + w.n * kGN;
 #pragma unroll 1
         for (int c = 4 * half; c < 4 * half + 4; ++c) {
@@ -65,6 +69,7 @@ struct DebugGemm {
                 *reinterpret_cast<float4*>(dst + c * 16 + i) = make_float4(
                     __uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
         }
+        release();
     }
 };
 

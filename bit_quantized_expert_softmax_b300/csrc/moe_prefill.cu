@@ -10,10 +10,11 @@
 //   quant_x   quantise each token's x once and write it into the swizzled A
 //             tiles of its k routed experts and of the shared expert
 //   gemm1     gate/up: [rows x d] . [2f x d]^T, each 128-column tile holds 64
-//             gate and 64 up columns of the same f range; epilogue
-//             h = silu(g)*u (fp32)
+//             gate and 64 up columns of the same f range, two such tiles per
+//             item sharing the A k-tiles; epilogue h = silu(g)*u (fp32)
 //   quant_h   quantise each h row into swizzled A tiles of the down GEMM
-//   gemm2     down: [rows x f] . [d x f]^T; epilogue scales by the routing
+//   gemm2     down: [rows x f] . [d x f]^T, each M-tile's A tile held in
+//             shared memory across its 16 N-tiles; epilogue scales by the routing
 //             weight (1 for the shared expert) and stores the contribution in
 //             bf16, one row per (token, expert) assignment
 //   combine   out[t] = bf16(shared + slot 0 + ... + slot k-1), summed in fp32
@@ -344,21 +345,26 @@ __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
     }
 }
 
-// gate/up GEMM: item = (M-tile, N-tile of 64 gate + 64 up columns)
+// gate/up GEMM: item = (M-tile, pair of N-tiles); N-tile nt holds 64 gate
+// and 64 up columns of the same f range, so the pair yields h columns
+// [128 pair, 128 pair + 128). Both N-tiles share each A k-tile in shared
+// memory (the engine's kNB = 2).
 struct Gemm1 {
     PrefillCtx c;
-    int NT, KT;
-    static constexpr int kStages = 3;
-    __device__ int n_items() const { return c.meta[2] * NT; }
+    int NT, KT;   // N-tiles (2f/128) and k-tiles (d/256)
+    static constexpr int kStages = 2;
+    static constexpr int kNB = 2;
+    __device__ int n_items() const { return c.meta[2] * (NT / 2); }
     __device__ void item(int i, Fp4Item& w) const {
-        const int mt = i / NT, nt = i % NT;
+        const int np = NT / 2;
+        const int mt = i / np, pair = i % np;
         const int e = c.mt_e[mt];
-        const int rt = mt;
-        w.a = c.a1 + (size_t)rt * KT * kGBlk;
-        w.b = c.w1 + ((size_t)e * NT + nt) * KT * kGBlk;
+        w.a = c.a1 + (size_t)mt * KT * kGBlk;
+        w.b = c.w1 + ((size_t)e * NT + 2 * pair) * KT * kGBlk;
+        w.b2 = w.b + (size_t)KT * kGBlk;
         w.kt = KT;
         w.m = mt;
-        w.n = nt;
+        w.n = pair;
         w.aux = e;
     }
     // Padding rows are computed too (from whatever their tiles hold) and their
@@ -373,35 +379,51 @@ struct Gemm1 {
     }
     static constexpr int kEpiSmemPerWarp = 0;
     __device__ void epilogue_finish() const {}
-    // h columns [64n + 32*half, +32): gate accumulator columns 32*half.., up 64 + 32*half..
-    __device__ void epilogue(const Fp4Item& w, const Pre& pr, uint32_t taddr, int row, int half, uint8_t*) const {
+    // For each N-tile b of the pair: h columns [64 (2 pair + b) + 32 half, +32)
+    // from gate accumulator columns 32 half.. and up columns 64 + 32 half..,
+    // in two rounds of 16 columns; each round's four tensor-memory loads are
+    // issued before its one wait, and the accumulators are released as soon
+    // as the second round has been read.
+    template <class Release>
+    __device__ void epilogue(const Fp4Item& w, const Pre& pr, uint32_t taddr, int row, int half, uint8_t*,
+                             Release release) const {
         const float tg = pr.tg, tu = pr.tu;
-        float* dst = c.h + (size_t)(w.m * kGM + row) * c.f + w.n * 64 + half * 32;
-        // all four tensor-memory loads in flight before the one wait
-        uint32_t g[32], u[32];
-        tmem_ld16(taddr + half * 32, g);
-        tmem_ld16(taddr + half * 32 + 16, g + 16);
-        tmem_ld16(taddr + 64 + half * 32, u);
-        tmem_ld16(taddr + 64 + half * 32 + 16, u + 16);
-        tmem_ld_wait();
+        float* dst0 = c.h + (size_t)(w.m * kGM + row) * c.f + 2 * w.n * 64 + half * 32;
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-            float hv[4];
+        for (int r = 0; r < 2; ++r) {
+            uint32_t g[2][16], u[2][16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float gq = __uint_as_float(g[i + q]) * tg, uq = __uint_as_float(u[i + q]) * tu;
-                // silu(g) * u with the fast exponential and division (relative
-                // error ~1e-6; it can move a later FP4 code only where h sits
-                // on a rounding boundary)
-                hv[q] = __fdividef(gq, 1.0f + __expf(-gq)) * uq;
+            for (int b = 0; b < 2; ++b) {
+                const uint32_t t = taddr + b * kGN + half * 32 + 16 * r;
+                tmem_ld16(t, g[b]);
+                tmem_ld16(t + 64, u[b]);
             }
-            __stcs(reinterpret_cast<float4*>(dst + i), make_float4(hv[0], hv[1], hv[2], hv[3]));
+            tmem_ld_wait();
+            if (r == 1) release();
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                float* dst = dst0 + b * 64 + 16 * r;
+#pragma unroll
+                for (int i = 0; i < 16; i += 4) {
+                    float hv[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float gq = __uint_as_float(g[b][i + q]) * tg, uq = __uint_as_float(u[b][i + q]) * tu;
+                        // silu(g) * u with the fast exponential and division
+                        // (relative error ~1e-6; it can move a later FP4 code
+                        // only where h sits on a rounding boundary)
+                        hv[q] = __fdividef(gq, 1.0f + __expf(-gq)) * uq;
+                    }
+                    __stcs(reinterpret_cast<float4*>(dst + i), make_float4(hv[0], hv[1], hv[2], hv[3]));
+                }
+            }
         }
     }
 };
 
-// down GEMM: item = (M-tile, N-tile of 128 output columns) of every slot,
-// shared expert included. Each epilogue thread scales its row by
+// down GEMM epilogue of one (M-tile, N-tile of 128 output columns)
+// accumulator, every slot's M-tiles including the shared expert's; run by
+// fp4_gemm_resa_kernel through Gemm2R. Each epilogue thread scales its row by
 // s_h * tensor scale * routing weight and rounds it to bf16; the warp stages
 // its 32 rows x 64 columns in shared memory and writes them, transposed, to
 // the rows of their assignments (routed: bucketed position p < T*k; shared:
@@ -410,29 +432,11 @@ constexpr int kEpiPitch = 144;   // 128 bytes of a row + 16: conflict-free 16-by
 struct Gemm2 {
     PrefillCtx c;
     int NT, KT;
-    static constexpr int kStages = 2;
     static constexpr int kEpiSmemPerWarp = 32 * kEpiPitch;
-    __device__ int n_items() const { return c.meta[2] * NT; }
-    __device__ void item(int i, Fp4Item& w) const {
-        const int mt = i / NT, nt = i % NT;
-        const int e = c.mt_e[mt];
-        const int rt = mt;
-        w.a = c.a2 + (size_t)rt * KT * kGBlk;
-        w.b = c.w2 + ((size_t)e * NT + nt) * KT * kGBlk;
-        w.kt = KT;
-        w.m = mt;
-        w.n = nt;
-        w.aux = e;
-    }
     struct Pre {
         int p;           // bucketed position (shared expert: T*k + token); -1: padding row
         float scale;
     };
-    __device__ Pre pre(const Fp4Item& w, int row, int) const {
-        const int rp = w.m * kGM + row;
-        return {c.prow[rp], c.yscale[rp]};
-    }
-    __device__ void epilogue_finish() const {}
     __device__ void epilogue(const Fp4Item& w, const Pre& pr, uint32_t taddr, int row, int half,
                              uint8_t* epi) const {
         const int p = pr.p;
@@ -468,6 +472,34 @@ struct Gemm2 {
                 *reinterpret_cast<uint4*>(c.y + (size_t)pr * c.d + w.n * kGN + half * 64 + chunk * 8) = v;
         }
         __syncwarp();
+    }
+};
+
+// The down GEMM with each M-tile's A tile resident (fp4_gemm_resa_kernel):
+// one item per M-tile, its 16 N-tiles in turn; the epilogue is Gemm2's.
+struct Gemm2R {
+    Gemm2 g;
+    static constexpr int kStages = 3;
+    static constexpr int kNT = 16;   // d / 128 output column tiles (d = 2048)
+    static constexpr int kEpiSmemPerWarp = Gemm2::kEpiSmemPerWarp;
+    using Pre = Gemm2::Pre;
+    __device__ int n_mtiles() const { return g.c.meta[2]; }
+    __device__ const uint8_t* a_blocks(int mt) const { return g.c.a2 + (size_t)mt * kRKT * kGBlk; }
+    __device__ const uint8_t* b_blocks(int mt, int n) const {
+        return g.c.w2 + ((size_t)__ldg(g.c.mt_e + mt) * kNT + n) * kRKT * kGBlk;
+    }
+    __device__ Pre pre(int mt, int row, int) const {
+        const int rp = mt * kGM + row;
+        return {g.c.prow[rp], g.c.yscale[rp]};
+    }
+    __device__ void epilogue(int mt, int n, const Pre& pr, uint32_t taddr, int row, int half, uint8_t* epi) const {
+        Fp4Item w;
+        w.a = w.b = nullptr;
+        w.kt = kRKT;
+        w.m = mt;
+        w.n = n;
+        w.aux = 0;
+        g.epilogue(w, pr, taddr, row, half, epi);
     }
 };
 
@@ -618,8 +650,8 @@ cudaError_t prepare_prefill_fp4() {
     cudaError_t e = cudaFuncSetAttribute(fp4_gemm_kernel<Gemm1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          fp4_gemm_smem<Gemm1>());
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fp4_gemm_kernel<Gemm2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 fp4_gemm_smem<Gemm2>());
+        e = cudaFuncSetAttribute(fp4_gemm_resa_kernel<Gemm2R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 fp4_gemm_resa_smem<Gemm2R>());
     if (e != cudaSuccess) cudaGetLastError();
     return e;
 }
@@ -678,8 +710,9 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     static_assert(kGM % (8 * kQhRows) == 0, "a CTA's rows stay inside one M-tile");
     quant_h_kernel<16><<<(unsigned)(rt * kGM / (8 * kQhRows)), 256, 0, st>>>(c);
     mark(3);
-    Gemm2 g2{c, s.d / kGN, s.f / kGK};
-    fp4_gemm_kernel<Gemm2><<<148, kGThreads, fp4_gemm_smem<Gemm2>(), st>>>(g2, ws.status);
+    static_assert(Gemm2R::kNT * kGN == 2048 && kRKT * kGK == 512, "the Flint shape (d = 2048, f = 512)");
+    Gemm2R g2{Gemm2{c, s.d / kGN, s.f / kGK}};
+    fp4_gemm_resa_kernel<Gemm2R><<<148, kGThreads, fp4_gemm_resa_smem<Gemm2R>(), st>>>(g2, ws.status);
     mark(4);
     combine_kernel<<<(T + 7) / 8 < 148 * 8 ? (T + 7) / 8 : 148 * 8, 256, 0, st>>>(c, out, residual);
     mark(5);
