@@ -26,6 +26,8 @@ struct flint_moe {
     uint64_t launches = 0;
     int n_sms = 0;
     bool fused = true;           // single-launch decode for T <= kFusedMaxT
+    bool stack = true;           // the whole decode stack in one launch (T <= kFusedMaxT)
+    flint::StackLayer* stack_table = nullptr;   // [n_layers] device table of the layers' pointers
     bool prefill = true;         // tensor-core (tcgen05) kernels for large T
     bool fp4_experts = false;    // block-scaled FP4 expert GEMMs for T > kSmallT
     void* pws = nullptr;         // their workspace (swizzled activation tiles, h, fp32 sums)
@@ -75,6 +77,7 @@ void free_layer(LayerDev& L) {
     cudaFree(L.scales);
     cudaFree(L.tscale);
     cudaFree(L.prefill);
+    cudaFree(L.router_t);
     L = LayerDev{};
 }
 
@@ -130,6 +133,8 @@ Workspace carve(const Shape& s, char* base, size_t* total) {
     w.counters = cv.take<uint32_t>(flint::kCounters);
     w.gbar = cv.take<uint32_t>(64);
     w.dbg = cv.take<uint32_t>(64);
+    w.racc = cv.take<unsigned long long>((size_t)2 * flint::kFusedMaxT * s.E);
+    w.rnf = cv.take<uint32_t>((size_t)2 * flint::kFusedMaxT * s.E);
     w.status = cv.take<uint32_t>(1);
     *total = align_up(cv.off, 256);
     return w;
@@ -257,6 +262,10 @@ flint_status flint_moe_create(const flint_moe_config* cfg, flint_moe** out) {
     }
     if (h->fused && flint::prepare_decode_fused() != cudaSuccess) h->fused = false;
     {
+        const char* env = getenv("FLINT_MOE_STACK_KERNEL");
+        h->stack = h->fused && !(env != nullptr && env[0] == '0');
+    }
+    {
         const char* env = getenv("FLINT_MOE_TCGEN05_PREFILL");
         if (env != nullptr && env[0] == '0') h->prefill = false;
     }
@@ -292,9 +301,15 @@ flint_status flint_moe_create(const flint_moe_config* cfg, flint_moe** out) {
         }
     }
     e = cudaMemset(h->ws_base, 0, total);
+    if (e == cudaSuccess && h->stack) {
+        e = cudaMalloc(&h->stack_table, (size_t)cfg->n_layers * sizeof(flint::StackLayer));
+        if (e == cudaSuccess) e = cudaMemset(h->stack_table, 0, (size_t)cfg->n_layers * sizeof(flint::StackLayer));
+    }
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->load_stream, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
+        cudaFree(h->stack_table);
+        cudaFree(h->pws);
         cudaFree(h->ws_base);
         delete h;
         return cuda_status(e);
@@ -342,12 +357,14 @@ flint_status flint_moe_load_weights(flint_moe* h, int layer, const flint_moe_wei
         if (e == cudaSuccess) e = cudaMalloc(&L.tscale, flint::tscale_bytes(s));
         if (e == cudaSuccess) e = cudaMemset(L.tscale, 0, flint::tscale_bytes(s));
         if (e == cudaSuccess && h->fp4_experts) e = cudaMalloc(&L.prefill, flint::prefill_weight_bytes(s));
+        if (e == cudaSuccess && h->stack) e = cudaMalloc(&L.router_t, (size_t)s.E * s.d * sizeof(float));
         if (e != cudaSuccess) {
             free_layer(L);
             return cuda_status(e);
         }
         h->weight_bytes += (size_t)s.E * s.d * 4 + (size_t)s.E * 4 + n_codes + n_scales + flint::tscale_bytes(s);
         if (L.router_hi != nullptr) h->weight_bytes += (size_t)s.E * s.d * 4;
+        if (L.router_t != nullptr) h->weight_bytes += (size_t)s.E * s.d * 4;
         if (L.prefill != nullptr) h->weight_bytes += flint::prefill_weight_bytes(s);
     }
     L.loaded = false;
@@ -386,6 +403,11 @@ flint_status flint_moe_load_weights(flint_moe* h, int layer, const flint_moe_wei
         e = flint::pack_prefill_weights(s, stage, stage + n_codes, L.prefill, st);
     if (e == cudaSuccess && L.router_hi != nullptr)
         e = flint::split_router(L.router, L.router_hi, L.router_lo, (size_t)s.E * s.d, st);
+    if (e == cudaSuccess && L.router_t != nullptr) e = flint::transpose_router(L.router, L.router_t, s.E, s.d, st);
+    if (e == cudaSuccess && h->stack_table != nullptr) {
+        const flint::StackLayer sl{L.codes, L.scales, L.tscale, L.router_t, L.bias};
+        e = cudaMemcpyAsync(h->stack_table + layer, &sl, sizeof(sl), cudaMemcpyHostToDevice, st);
+    }
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     cudaFree(stage);
     if (e != cudaSuccess) return cuda_status(e);
@@ -424,6 +446,14 @@ flint_status flint_moe_forward_stack(flint_moe* h, int layer0, int n_layers, voi
     DeviceGuard guard(h->device);
     if (!guard.ok) return FLINT_ECUDA;
     __nv_bfloat16* x = static_cast<__nv_bfloat16*>(hidden_dev);
+    if (h->stack && T <= flint::kFusedMaxT && flint::stack_smem_bytes(h->s, T, h->n_sms) != 0) {
+        // every layer in one persistent launch
+        flint::FusedScratch fs{h->ws.logits, h->ws.hf, h->ws.gbar, h->ws.status};
+        const cudaError_t e = flint::launch_decode_stack(h->s, h->stack_table + layer0, n_layers, x, T, fs,
+                                                         h->ws.racc, h->ws.rnf, h->n_sms, (cudaStream_t)stream);
+        if (e == cudaSuccess) h->launches += 1;
+        return cuda_status(e);
+    }
     for (int l = layer0; l < layer0 + n_layers; ++l) {
         const LayerDev* next = (l + 1 < layer0 + n_layers && h->layers[l + 1].loaded) ? &h->layers[l + 1] : nullptr;
         cudaError_t e = run_layer(h, l, x, T, x, x, (cudaStream_t)stream, next);
@@ -444,6 +474,7 @@ void flint_moe_destroy(flint_moe* h) {
         cudaFree(h->head_scratch);
         cudaFree(h->ws_base);
         cudaFree(h->pws);
+        cudaFree(h->stack_table);
         if (h->load_stream) cudaStreamDestroy(h->load_stream);
     }
     delete h;
@@ -554,6 +585,9 @@ flint_status flint_moe_status(flint_moe* h) {
         if (e == cudaSuccess) e = cudaMemset(h->ws.counters, 0, flint::kCounters * sizeof(uint32_t));
         if (e == cudaSuccess && h->head_hs.counters != nullptr)
             e = cudaMemset(h->head_hs.counters, 0, flint::kHeadMaxT * sizeof(unsigned));
+        // the decode stack's router accumulators are zero between launches
+        if (e == cudaSuccess) e = cudaMemset(h->ws.racc, 0, (size_t)2 * flint::kFusedMaxT * h->s.E * 8);
+        if (e == cudaSuccess) e = cudaMemset(h->ws.rnf, 0, (size_t)2 * flint::kFusedMaxT * h->s.E * 4);
     }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return FLINT_ECUDA;

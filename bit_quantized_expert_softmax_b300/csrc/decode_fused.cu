@@ -626,6 +626,457 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// The decode stack in one launch: all layers of flint_moe_forward_stack for
+// T <= 2 tokens, x <- bf16(x + MoE_l(x)) for l = 0 .. n-1, in one persistent
+// cooperative kernel (the one-dispatch decode of the whole forward that the
+// Flint blog's Metal megakernel does, section "The quantization recipe is the
+// most transferable part"). Per layer two grid barriers instead of a launch:
+//
+//   P1  every CTA: logits of this layer from the fixed-point accumulators,
+//       top-k, routed gate/up half-units (slabs bulk-copied as soon as the
+//       experts are known), h to global; requests this CTA's routed down
+//       slabs and, for the next layer, its shared half-unit and router slab.
+//   --- grid barrier ---
+//   P2  the d/16 row-owner CTAs: down products and combine of their 16 rows,
+//       x_{l+1} = bf16(x_l + out) in place, then the next layer's router
+//       logits restricted to those 16 rows (W_r^T rows, prefetched during P1),
+//       added into fixed-point accumulators.
+//   --- grid barrier ---
+//
+// The router logits of layer l+1 are thus sums over the 128 row-owner CTAs of
+// partial dot products; they are accumulated as 64-bit integers in units of
+// 2^-32 (each partial rounded once to that grid), so the sum is the same
+// whatever order the CTAs arrive in and every run gives the same bits. The
+// accumulators and their non-finite flags are zero between launches.
+// ---------------------------------------------------------------------------
+constexpr double kRaccScale = 4294967296.0;   // 2^32 units per logit
+
+struct StackArgs {
+    FusedArgs f;                     // shape, shared-memory plan, h scratch, barrier counter, status
+    const StackLayer* layers;        // [n] device table, in stack order
+    int n;
+    __nv_bfloat16* x;                // [T][d] hidden, updated in place
+    unsigned long long* racc;        // [2][T][E] fixed-point router logits
+    uint32_t* rnf;                   // [2][T][E] non-finite partial seen
+    int off_rslab;                   // shared-memory offset of the router slab [16][E] fp32
+};
+
+// Row owners: partial logits of 16 rows of x (xr[t][r], fp32 of bf16) with the
+// router slab (rslab[r][e] = W_r[e][16 dt + r]) into racc/rnf.
+template <int TT>
+__device__ void router_partials(const StackArgs& sa, const float* rslab, const float* xr, int buf) {
+    const int E = sa.f.E;
+    for (int i = threadIdx.x; i < TT * E; i += kFThreads) {
+        const int t = i / E, e = i - (i / E) * E;
+        float p = 0.f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) p = fmaf(rslab[r * E + e], xr[t * 16 + r], p);
+        const size_t o = ((size_t)buf * TT + t) * E + e;
+        if (!(fabsf(p) <= 1.0e9f)) {   // non-finite, or beyond the fixed-point range
+            atomicOr(sa.rnf + o, 1u);
+        } else {
+            const long long q = __double2ll_rn((double)p * kRaccScale);
+            atomicAdd(sa.racc + o, (unsigned long long)q);
+        }
+    }
+}
+
+template <int WFMT, int TT>
+__global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa) {
+    static_assert(TT >= 1 && TT <= kFusedMaxT, "token count");
+    extern __shared__ __align__(128) uint8_t smem[];
+    const FusedArgs a0 = sa.f;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int G = gridDim.x, b = blockIdx.x;
+    constexpr int T = TT;
+    const int d = a0.d, f = a0.f, E = a0.E, k = a0.k;
+    const int KTf = f >> 7;
+    const int units_per_expert = f >> 3;
+    const int down_tiles = d >> 4;
+    const int down_tile = b - (G - down_tiles);          // the last d/16 CTAs own 16 rows each
+    const int shared_unit = G - 1 - b;                   // the last f/8 CTAs do the shared gate/up
+
+    uint8_t* slots = smem + a0.off_slots;
+    uint8_t* down = smem + a0.off_down;
+    float* acc = reinterpret_cast<float*>(smem + a0.off_acc);
+    __half* x16s = reinterpret_cast<__half*>(smem + a0.off_x16);
+    __half* h16s = reinterpret_cast<__half*>(smem + a0.off_h16);
+    uint8_t* misc = smem + a0.off_misc;
+    float* tss = reinterpret_cast<float*>(smem + a0.off_ts);
+    float* rslab = reinterpret_cast<float*>(smem + sa.off_rslab);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc);              // [n_slots + 4]
+    const int i_rslab = a0.n_slots, i_dshared = a0.n_slots + 1, i_drouted = a0.n_slots + 2;
+    float* xinv = reinterpret_cast<float*>(misc + 128);              // [2]
+    float* hinv = xinv + 4;                                          // [2*(k+1)] <= 18
+    float* rpart = hinv + 20;                                        // [16][2]
+    float* lg = rpart + 32;                                          // [2][256]
+    int* sel = reinterpret_cast<int*>(lg + 2 * 256);                 // [2][8]
+    float* wsel = reinterpret_cast<float*>(sel + 16);                // [2][8]
+    int* act = reinterpret_cast<int*>(wsel + 16);                    // [17]
+    int* act_np = act + 17;                                          // [17]
+    Pair* act_pairs = reinterpret_cast<Pair*>(act_np + 17);          // [17][2]
+    int* nact = reinterpret_cast<int*>(act_pairs + 34);              // [1]
+    Pair* shared_pairs = reinterpret_cast<Pair*>(nact + 2);          // [2]
+    int* cmap = reinterpret_cast<int*>(shared_pairs + 2 + 2);        // [2][8]
+    float* xr = reinterpret_cast<float*>(misc + 3072);               // [2][16] x_{l+1} rows of this CTA
+
+    bool ok = true;
+    uint32_t ph = 0;   // bit i: parity of the next completion of bars[i] (uniform over the CTA)
+    auto wait_bar = [&](int i) {
+        const bool w = ok ? mbar_wait_bounded(bars + i, (ph >> i) & 1u, a0.status) : false;
+        ph ^= 1u << i;
+        ok = __syncthreads_and(w ? 1 : 0) != 0;
+    };
+    // thread 0 issues every bulk copy; pend/pend_par track the ones that may
+    // still be in flight (see decode_fused_kernel)
+    uint32_t pend = 0, pend_par = 0;
+    auto mark_issued = [&](int i) {
+        pend |= 1u << i;
+        pend_par = (pend_par & ~(1u << i)) | (((ph >> i) & 1u) << i);
+    };
+    auto drain = [&]() {
+        if (threadIdx.x == 0) {
+#pragma unroll 1
+            for (int i = 0; i < a0.n_slots + 4; ++i)
+                if ((pend >> i) & 1u) mbar_wait_bounded(bars + i, (pend_par >> i) & 1u, a0.status);
+        }
+    };
+    auto layer_args = [&](int li) {
+        FusedArgs al = a0;
+        const StackLayer L = sa.layers[li];
+        al.codes = L.codes;
+        al.scales = L.scales;
+        al.tscale = L.tscale;
+        al.bias = L.bias;
+        return al;
+    };
+
+    if (threadIdx.x == 0) {
+#pragma unroll 1
+        for (int i = 0; i < a0.n_slots + 4; ++i) mbar_init(bars + i, 1);
+        mbar_fence_init();
+    }
+    if (threadIdx.x < T) {
+        shared_pairs[threadIdx.x].t = threadIdx.x;
+        shared_pairs[threadIdx.x].j = k;
+    }
+    __syncthreads();
+    const int shared_slot = a0.n_slots - 1;
+    const bool has_shared = shared_unit >= 0 && shared_unit < units_per_expert;
+    const uint32_t rslab_bytes = (uint32_t)(16 * E * 4);
+
+    // ---- prologue: layer 0's routing-independent slabs, and its router
+    // logits from the input rows (row owners)
+    {
+        const FusedArgs al = layer_args(0);
+        if (threadIdx.x == 0) {
+            if (has_shared) {
+                issue_half<WFMT>(al, E, shared_unit, slots + (size_t)shared_slot * al.unit_bytes, bars + shared_slot);
+                mark_issued(shared_slot);
+            }
+            if (down_tile >= 0) {
+                mbar_arrive_expect_tx(bars + i_dshared, (uint32_t)al.down_bytes);
+                issue_down<WFMT>(al, E, down_tile, down, bars + i_dshared);
+                mark_issued(i_dshared);
+                mbar_arrive_expect_tx(bars + i_rslab, rslab_bytes);
+                bulk_g2s(rslab, sa.layers[0].router_t + (size_t)16 * down_tile * E, rslab_bytes, bars + i_rslab);
+                mark_issued(i_rslab);
+            }
+        }
+    }
+    GridSync gsync = grid_sync_init(a0.bar_count, (uint32_t)G);   // includes a __syncthreads
+    if (down_tile >= 0) {
+        if (threadIdx.x < T * 16) {
+            const int t = threadIdx.x / 16, r = threadIdx.x % 16;
+            xr[t * 16 + r] = __bfloat162float(sa.x[(size_t)t * d + 16 * down_tile + r]);
+        }
+        wait_bar(i_rslab);
+        if (ok) router_partials<T>(sa, rslab, xr, 0);
+    }
+    if (!grid_sync(gsync, a0.status)) ok = false;
+
+#pragma unroll 1
+    for (int li = 0; li < sa.n && ok; ++li) {
+        const FusedArgs al = layer_args(li);
+        const int buf = li & 1;
+        const bool last = li + 1 == sa.n;
+        // ------------------------------------------------------------ P1
+        for (int i = threadIdx.x; i < 3 * (E + 1); i += kFThreads) tss[i] = __ldg(al.tscale + i);
+        // logits of this layer
+        for (int i = threadIdx.x; i < T * E; i += kFThreads) {
+            const size_t o = (size_t)buf * T * E + i;
+            const long long q = (long long)__ldcg(sa.racc + o);
+            const float v = (float)((double)q * (1.0 / kRaccScale)) + __ldg(al.bias + (i % E));
+            lg[(i / E) * 256 + (i % E)] = __ldcg(sa.rnf + o) ? __int_as_float(0x7fc00000) : v;
+        }
+        // the other accumulator is filled by this layer's P2; its last readers
+        // finished before the previous layer's barriers
+        if (b == 0) {
+            for (int i = threadIdx.x; i < T * E; i += kFThreads) {
+                sa.racc[(size_t)(buf ^ 1) * T * E + i] = 0ull;
+                sa.rnf[(size_t)(buf ^ 1) * T * E + i] = 0u;
+            }
+        }
+        // stage x_l as fp16, scaled per token, fragment-permuted
+        for (int t = 0; t < T; ++t) {
+            float xv[2][4];
+            float amax = 0.f;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int i = (threadIdx.x + q * kFThreads) * 4;
+                uint2 raw = make_uint2(0u, 0u);
+                if (i < d) raw = __ldcg(reinterpret_cast<const uint2*>(sa.x + (size_t)t * d + i));
+                const float2 p0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+                const float2 p1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+                xv[q][0] = p0.x;
+                xv[q][1] = p0.y;
+                xv[q][2] = p1.x;
+                xv[q][3] = p1.y;
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(p0.x), fabsf(p0.y)), fmaxf(fabsf(p1.x), fabsf(p1.y))));
+            }
+            amax = warp_max(amax);
+            if (lane == 0) rpart[warp] = amax;
+            __syncthreads();
+            float m = 0.f;
+#pragma unroll
+            for (int w = 0; w < kFWarps; ++w) m = fmaxf(m, rpart[w]);
+            const float mult = f16_range_mult(m);
+            __half2* xrow = reinterpret_cast<__half2*>(x16s + (size_t)t * d);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int i = (threadIdx.x + q * kFThreads) * 4;
+                if (i < d) {
+                    __half2* tile = xrow + ((i & ~127) >> 1);
+                    tile[kperm_pos(i & 127) >> 1] = __floats2half2_rn(xv[q][0] * mult, xv[q][1] * mult);
+                    tile[kperm_pos((i & 127) + 2) >> 1] = __floats2half2_rn(xv[q][2] * mult, xv[q][3] * mult);
+                }
+            }
+            if (threadIdx.x == 0) xinv[t] = 1.0f / mult;
+            __syncthreads();
+        }
+        if (warp < T) topk_warp<false>(lg + warp * 256, E, k, sel + warp * 8, wsel + warp * 8, b == 0 ? a0.status : nullptr);
+        __syncthreads();
+        if (T == 1) {
+            if (threadIdx.x < k) {
+                const int j = threadIdx.x;
+                act[j] = sel[j];
+                act_np[j] = 1;
+                act_pairs[j * 2] = Pair{0, j};
+                cmap[j] = (j + 1) * 4;
+                if (j == 0) *nact = k;
+            }
+        } else if (warp == 0) {
+            const int n = T * k;
+            const int t = lane / k, j = lane - (lane / k) * k;
+            const int e = lane < n ? sel[t * 8 + j] : -1 - lane;
+            int first = lane, p = 0;
+            for (int i = 0; i < n; ++i) {
+                const int ei = __shfl_sync(0xffffffffu, e, i);
+                if (i < lane && ei == e) {
+                    if (first == lane) first = i;
+                    ++p;
+                }
+            }
+            const uint32_t firsts = __ballot_sync(0xffffffffu, lane < n && first == lane);
+            const int q = __popc(firsts & ((1u << first) - 1u));
+            const uint32_t same = __match_any_sync(0xffffffffu, e);
+            if (lane < n) {
+                if (first == lane) {
+                    act[q] = e;
+                    act_np[q] = __popc(same);
+                }
+                act_pairs[q * 2 + p] = Pair{t, j};
+                cmap[t * 8 + j] = (q + 1) * 4 + p;
+            }
+            if (lane == 0) *nact = __popc(firsts);
+        }
+        __syncthreads();
+        const int na = *nact;
+        const int n_units = na * units_per_expert;
+        const int n_rs = a0.n_slots - 1;
+        bool shared_pending = has_shared, wave_issued = false;
+        for (int u0 = b;;) {
+            if (!wave_issued && u0 < n_units && ok) {
+                __syncthreads();   // the previous wave's slots have been read
+                if (threadIdx.x == 0) {
+                    fence_proxy_async_smem();
+#pragma unroll 1
+                    for (int s2 = 0; s2 < n_rs; ++s2) {
+                        const int u = u0 + s2 * G;
+                        if (u < n_units) {
+                            issue_half<WFMT>(al, act[u / units_per_expert], u % units_per_expert,
+                                             slots + (size_t)s2 * al.unit_bytes, bars + s2);
+                            mark_issued(s2);
+                        }
+                    }
+                }
+                wave_issued = true;
+            }
+            UnitRef wave[kMaxWaveUnits];
+            int nw = 0;
+            if (shared_pending) {
+                wait_bar(shared_slot);
+                wave[nw++] = UnitRef{slots + (size_t)shared_slot * al.unit_bytes, E, shared_unit, shared_pairs, T};
+                shared_pending = false;
+            } else if (u0 < n_units) {
+#pragma unroll 1
+                for (int s2 = 0; s2 < n_rs; ++s2) {
+                    const int u = u0 + s2 * G;
+                    if (u >= n_units) break;
+                    wait_bar(s2);
+                    const int q = u / units_per_expert;
+                    wave[nw++] = UnitRef{slots + (size_t)s2 * al.unit_bytes, act[q], u % units_per_expert,
+                                         act_pairs + q * 2, act_np[q]};
+                }
+                u0 += G * n_rs;
+                wave_issued = false;
+            } else {
+                break;
+            }
+            if (ok && nw > 0) gateup_units<WFMT>(al, wave, nw, x16s, xinv, tss, acc);
+        }
+        // requests that need no more than this point: this CTA's routed down
+        // slabs (P2), the next layer's shared half-unit (its slot is free
+        // now) and the next layer's router slab (read in P2)
+        __syncthreads();
+        if (threadIdx.x == 0 && ok) {
+            fence_proxy_async_smem();
+            if (down_tile >= 0 && na > 0) {
+                mbar_arrive_expect_tx(bars + i_drouted, (uint32_t)(na * al.down_bytes));
+#pragma unroll 1
+                for (int q = 0; q < na; ++q)
+                    issue_down<WFMT>(al, act[q], down_tile, down + (size_t)(1 + q) * al.down_bytes, bars + i_drouted);
+                mark_issued(i_drouted);
+            }
+            if (!last) {
+                const FusedArgs an = layer_args(li + 1);
+                if (has_shared) {
+                    issue_half<WFMT>(an, E, shared_unit, slots + (size_t)shared_slot * an.unit_bytes,
+                                     bars + shared_slot);
+                    mark_issued(shared_slot);
+                }
+                if (down_tile >= 0) {
+                    mbar_arrive_expect_tx(bars + i_rslab, rslab_bytes);
+                    bulk_g2s(rslab, sa.layers[li + 1].router_t + (size_t)16 * down_tile * E, rslab_bytes,
+                             bars + i_rslab);
+                    mark_issued(i_rslab);
+                }
+            }
+        }
+        if (ok && !grid_sync(gsync, a0.status)) ok = false;
+        if (!ok) break;
+        // ------------------------------------------------------------ P2
+        if (last && b == 0) {   // every reader of this layer's accumulators has passed the barrier
+            for (int i = threadIdx.x; i < T * E; i += kFThreads) {
+                sa.racc[(size_t)buf * T * E + i] = 0ull;
+                sa.rnf[(size_t)buf * T * E + i] = 0u;
+            }
+        }
+        if (down_tile >= 0) {
+            const int n_rows = T * (k + 1);
+            const int nq = f >> 7;
+            for (int r = warp; r < n_rows; r += kFWarps) {
+                const float4* hr = reinterpret_cast<const float4*>(al.h + (size_t)r * f);
+                float4 hv[8];
+                float amax = 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    hv[q] = q < nq ? __ldcg(hr + q * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(hv[q].x), fabsf(hv[q].y)), fmaxf(fabsf(hv[q].z), fabsf(hv[q].w))));
+                }
+                amax = warp_max(amax);
+                const float mult = f16_range_mult(amax);
+                __half2* hrow = reinterpret_cast<__half2*>(h16s + (size_t)r * f);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (q < nq) {
+                        const int i = (q * 32 + lane) * 4;
+                        __half2* tile = hrow + ((i & ~127) >> 1);
+                        tile[kperm_pos(i & 127) >> 1] = __floats2half2_rn(hv[q].x * mult, hv[q].y * mult);
+                        tile[kperm_pos((i & 127) + 2) >> 1] = __floats2half2_rn(hv[q].z * mult, hv[q].w * mult);
+                    }
+                }
+                if (lane == 0) hinv[r] = 1.0f / mult;
+            }
+            wait_bar(i_dshared);
+            if (na > 0) wait_bar(i_drouted);
+            const int S = WFMT == 0 ? 64 : 128;
+            const int kt_half = (KTf + 1) / 2;
+#pragma unroll 1
+            for (int it = warp; it < 2 * (na + 1) && ok; it += kFWarps) {
+                const int q = it >> 1, hf = it & 1;
+                const uint8_t* slab = down + (size_t)q * al.down_bytes;
+                const uint8_t* cd = slab;
+                const uint8_t* sd = slab + 2 * KTf * 512;
+                const int np = q == 0 ? T : act_np[q - 1];
+                const Pair* pp = q == 0 ? shared_pairs : act_pairs + (q - 1) * 2;
+                const int hrow = g < np ? pp[g].t * (k + 1) + pp[g].j : -1;
+                float cacc[4] = {0.f, 0.f, 0.f, 0.f};
+                const int kt1 = min(KTf, (hf + 1) * kt_half);
+#pragma unroll 1
+                for (int kt = hf * kt_half; kt < kt1; ++kt) {
+                    const uint4 wg = *reinterpret_cast<const uint4*>(cd + kt * 512 + lane * 16);
+                    const uint4 wh = *reinterpret_cast<const uint4*>(cd + (KTf + kt) * 512 + lane * 16);
+                    const TileScales<WFMT> sc = lds_scales<WFMT>(sd + kt * S, sd + (KTf + kt) * S, g);
+                    uint32_t bfr[16];
+                    if (hrow >= 0) {
+                        lds_b16(h16s + (size_t)hrow * f + kt * 128 + c * 32, bfr);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) bfr[i] = 0u;
+                    }
+                    uint32_t fa[8][4];
+                    decode_tile<WFMT>(wg, wh, sc, fa);
+                    float sx[4][2];
+                    if constexpr (WFMT == 1) block_sums_q41(bfr, sx);
+                    mma_k128<WFMT>(cacc, fa, bfr, sc, sx);
+                }
+                float* dst = acc + (size_t)it * 128;
+                dst[g * 8 + 2 * c] = cacc[0];
+                dst[g * 8 + 2 * c + 1] = cacc[1];
+                dst[(g + 8) * 8 + 2 * c] = cacc[2];
+                dst[(g + 8) * 8 + 2 * c + 1] = cacc[3];
+            }
+            __syncthreads();
+            // combine, residual in place: x[t][row] <- bf16(x + bf16(y_shared + sum_j w_j y_j))
+            if (threadIdx.x < T * 16 && ok) {
+                const int t = threadIdx.x / 16, rr = threadIdx.x % 16;
+                const int orow = down_tile * 16 + rr;
+                float v = (acc[rr * 8 + t] + acc[128 + rr * 8 + t]) * tss[E * 3 + 2] * hinv[t * (k + 1) + k];
+                for (int j = 0; j < k; ++j) {
+                    const int e = sel[t * 8 + j];
+                    const int qp = cmap[t * 8 + j];
+                    const float* aq = acc + (size_t)(qp >> 2) * 256 + rr * 8 + (qp & 3);
+                    const float y = aq[0] + aq[128];
+                    v += wsel[t * 8 + j] * (y * tss[e * 3 + 2] * hinv[t * (k + 1) + j]);
+                }
+                const __nv_bfloat16 o = __float2bfloat16_rn(v);
+                const float r = __bfloat162float(__ldcg(sa.x + (size_t)t * d + orow));
+                const __nv_bfloat16 xn = __float2bfloat16_rn(r + __bfloat162float(o));
+                sa.x[(size_t)t * d + orow] = xn;
+                xr[t * 16 + rr] = __bfloat162float(xn);
+            }
+            __syncthreads();   // down slabs read; xr written
+            if (!last) {
+                if (threadIdx.x == 0 && ok) {   // the next layer's shared down slab (slot 0 is free)
+                    fence_proxy_async_smem();
+                    const FusedArgs an = layer_args(li + 1);
+                    mbar_arrive_expect_tx(bars + i_dshared, (uint32_t)an.down_bytes);
+                    issue_down<WFMT>(an, E, down_tile, down, bars + i_dshared);
+                    mark_issued(i_dshared);
+                }
+                wait_bar(i_rslab);
+                if (ok) router_partials<T>(sa, rslab, xr, buf ^ 1);
+            }
+        }
+        if (!last && ok && !grid_sync(gsync, a0.status)) ok = false;
+    }
+    drain();
+}
+
 }  // namespace
 
 // Shared-memory plan of the fused kernel; 0 if it does not fit.
@@ -669,18 +1120,110 @@ size_t fused_smem_bytes(const Shape& s, int T, int n_sms, int* n_slots_out, int 
 cudaError_t prepare_decode_fused() {
     void (*kerns[4])(FusedArgs) = {decode_fused_kernel<0, 1>, decode_fused_kernel<0, 2>, decode_fused_kernel<1, 1>,
                                    decode_fused_kernel<1, 2>};
-    for (auto kern : kerns) {
+    void (*skerns[4])(StackArgs) = {decode_stack_kernel<0, 1>, decode_stack_kernel<0, 2>, decode_stack_kernel<1, 1>,
+                                    decode_stack_kernel<1, 2>};
+    auto opt_in = [](const void* kern) {
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, kern);
         if (e == cudaSuccess && fa.sharedSizeBytes + kFusedDynSmemMax > kMaxSmemOptin) e = cudaErrorInvalidValue;
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedDynSmemMax);
-        if (e != cudaSuccess) {
-            cudaGetLastError();   // leave no error behind for later launch checks
-            return e;
-        }
+        if (e != cudaSuccess) cudaGetLastError();   // leave no error behind for later launch checks
+        return e;
+    };
+    for (auto kern : kerns) {
+        const cudaError_t e = opt_in(reinterpret_cast<const void*>(kern));
+        if (e != cudaSuccess) return e;
+    }
+    for (auto kern : skerns) {
+        const cudaError_t e = opt_in(reinterpret_cast<const void*>(kern));
+        if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+// The stack kernel's plan: the single-layer plan plus the router slab.
+static size_t stack_plan(const Shape& s, int T, int n_sms, int* n_slots, int offs[10], int* off_rslab) {
+    const size_t base = fused_smem_bytes(s, T, n_sms, n_slots, offs);
+    if (base == 0 || s.d / 16 > n_sms) return 0;
+    const size_t off = (base + 127) / 128 * 128;
+    const size_t total = off + (size_t)16 * s.E * 4;
+    if (total > kFusedDynSmemMax) return 0;
+    *off_rslab = (int)off;
+    return total;
+}
+
+size_t stack_smem_bytes(const Shape& s, int T, int n_sms) {
+    int n_slots = 0, offs[10], off_rslab = 0;
+    return stack_plan(s, T, n_sms, &n_slots, offs, &off_rslab);
+}
+
+namespace {
+__global__ void transpose_router_kernel(const float* __restrict__ w, float* __restrict__ wt, int E, int d) {
+    const long n = (long)E * d;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        const int e = (int)(i / d), j = (int)(i % d);
+        wt[(size_t)j * E + e] = w[i];
+    }
+}
+}  // namespace
+
+cudaError_t transpose_router(const float* w, float* wt, int E, int d, cudaStream_t st) {
+    transpose_router_kernel<<<148 * 4, 256, 0, st>>>(w, wt, E, d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_stack(const Shape& s, const StackLayer* layers_dev, int n_layers, __nv_bfloat16* x, int T,
+                                const FusedScratch& fs, unsigned long long* racc, uint32_t* rnf, int n_sms,
+                                cudaStream_t st) {
+    int n_slots = 0, offs[10], off_rslab = 0;
+    const size_t smem = stack_plan(s, T, n_sms, &n_slots, offs, &off_rslab);
+    if (smem == 0 || n_layers < 1 || T < 1 || T > kFusedMaxT) return cudaErrorInvalidValue;
+    StackArgs sa;
+    FusedArgs& a = sa.f;
+    a = FusedArgs{};
+    a.cpm = s.codes_per_matrix();
+    a.spm = s.scales_per_matrix();
+    a.T = T;
+    a.d = s.d;
+    a.f = s.f;
+    a.E = s.E;
+    a.k = s.k;
+    a.logits = fs.logits;
+    a.h = fs.h;
+    a.bar_count = reinterpret_cast<unsigned long long*>(fs.bar);
+    a.status = fs.status;
+    a.n_slots = n_slots;
+    a.off_slots = offs[0];
+    a.unit_bytes = offs[1];
+    a.off_down = offs[2];
+    a.down_bytes = offs[3];
+    a.off_acc = offs[4];
+    a.off_x16 = offs[5];
+    a.off_h16 = offs[6];
+    a.off_misc = offs[7];
+    a.off_xbf = offs[8];
+    a.off_ts = offs[9];
+    a.ts_bytes = (int)tscale_bytes(s);
+    sa.layers = layers_dev;
+    sa.n = n_layers;
+    sa.x = x;
+    sa.racc = racc;
+    sa.rnf = rnf;
+    sa.off_rslab = off_rslab;
+    void (*kern)(StackArgs) = s.wfmt == 0 ? (T == 1 ? decode_stack_kernel<0, 1> : decode_stack_kernel<0, 2>)
+                                          : (T == 1 ? decode_stack_kernel<1, 1> : decode_stack_kernel<1, 2>);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_sms);
+    cfg.blockDim = dim3(kFThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, sa);
 }
 
 cudaError_t launch_decode_fused(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,

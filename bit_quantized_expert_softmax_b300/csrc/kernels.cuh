@@ -33,7 +33,18 @@ struct LayerDev {
     CUtensorMap tmap_router_hi, tmap_router_lo;   // 128x64 swizzled boxes of the two
     bool umma_router = false;
     uint8_t* prefill = nullptr;     // swizzled FP4 tiles of all experts (large-T path), or null
+    float* router_t = nullptr;      // [d][E] W_r transposed (the one-launch decode stack), or null
     bool loaded = false;
+};
+
+// One layer of the one-launch decode stack (a device table of these, in
+// stack order).
+struct StackLayer {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    const float* tscale;
+    const float* router_t;   // [d][E]
+    const float* bias;       // [E]
 };
 
 struct Shape {
@@ -71,6 +82,8 @@ struct Workspace {
     uint32_t* counters;   // [kCounters] arrival counters (self-resetting)
     uint32_t* gbar;       // [64]  grid-barrier count ([0]) and generation ([32])
     uint32_t* dbg;        // [64]  the timeout check's own barrier counter
+    unsigned long long* racc;   // [2][kFusedMaxT][E] fixed-point router logits of the decode stack
+    uint32_t* rnf;              // [2][kFusedMaxT][E] their non-finite flags
     uint32_t* status;     // device status word
 };
 
@@ -107,6 +120,13 @@ cudaError_t launch_down(const Shape& s, const LayerDev& L, int T, const Workspac
 constexpr int kFusedMaxT = 2;
 size_t fused_smem_bytes(const Shape& s, int T, int n_sms, int* n_slots_out, int offs[10]);
 cudaError_t prepare_decode_fused();   // once per device: shared-memory opt-in
+// the whole decode stack in one cooperative launch (T <= kFusedMaxT); 0 if
+// its shared-memory plan does not fit
+size_t stack_smem_bytes(const Shape& s, int T, int n_sms);
+cudaError_t launch_decode_stack(const Shape& s, const StackLayer* layers_dev, int n_layers, __nv_bfloat16* x, int T,
+                                const FusedScratch& fs, unsigned long long* racc, uint32_t* rnf, int n_sms,
+                                cudaStream_t st);
+cudaError_t transpose_router(const float* w, float* wt, int E, int d, cudaStream_t st);
 cudaError_t launch_decode_fused(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
                                 __nv_bfloat16* out, const __nv_bfloat16* residual, const FusedScratch& fs,
                                 int n_sms, cudaStream_t st, const LayerDev* next = nullptr);
