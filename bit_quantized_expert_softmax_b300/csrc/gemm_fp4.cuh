@@ -42,7 +42,6 @@ constexpr int kGM = 128, kGN = 128, kGK = 256;
 constexpr int kGTile = kGM * kGK / 2;          // 16 KiB of packed E2M1
 constexpr int kGSf = kGM * kGK / 16;           // 2 KiB of UE4M3 scales
 constexpr int kGBlk = kGTile + kGSf;           // one k-tile of one operand with its scales
-constexpr int kGKPS = 2;                       // k-tiles per stage
 constexpr int kGMaxStages = 4;                 // tensor-memory columns: 256 + 64 per stage
 constexpr int kGThreads = 448;
 constexpr int kGEpiWarps = 8;
@@ -65,8 +64,9 @@ struct Fp4Item {
 //           (256 columns: B0's tile, then B1's), single-buffered; per stage 96
 //           scale-factor columns at 256 + 96s. Each A k-tile then feeds two
 //           N-tiles: 3 blocks taken in per 2 block products instead of 4.
-__host__ __device__ constexpr int fp4_stage_bytes(int nb) { return (1 + nb) * kGKPS * kGBlk; }
-__host__ __device__ constexpr int fp4_sf_cols(int nb) { return 32 * (1 + nb); }   // per stage
+// (kps: k-tiles per stage, P::kKPS)
+__host__ __device__ constexpr int fp4_stage_bytes(int nb, int kps) { return (1 + nb) * kps * kGBlk; }
+__host__ __device__ constexpr int fp4_sf_cols(int nb, int kps) { return 16 * (1 + nb) * kps; }   // per stage
 
 // Byte offset of element pair byte `j` (0..127) of row `r` (0..127) inside a
 // swizzled tile.
@@ -80,8 +80,9 @@ template <class P>
 constexpr int fp4_gemm_smem() {
     static_assert(P::kStages >= 2 && P::kStages <= kGMaxStages, "stage count");
     static_assert(P::kNB == 1 || P::kNB == 2, "B tiles per item");
-    static_assert(256 + fp4_sf_cols(P::kNB) * P::kStages <= 512, "tensor-memory columns");
-    return P::kStages * fp4_stage_bytes(P::kNB) + kGEpiWarps * P::kEpiSmemPerWarp + 1024;
+    static_assert(P::kKPS == 1 || P::kKPS == 2, "k-tiles per stage");
+    static_assert(256 + fp4_sf_cols(P::kNB, P::kKPS) * P::kStages <= 512, "tensor-memory columns");
+    return P::kStages * fp4_stage_bytes(P::kNB, P::kKPS) + kGEpiWarps * P::kEpiSmemPerWarp + 1024;
 }
 
 // A problem P provides kStages, kEpiSmemPerWarp, n_items(), item(i, w), a
@@ -97,8 +98,9 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
     extern __shared__ uint8_t graw[];
     constexpr int kGStages = P::kStages;
     constexpr int kNB = P::kNB;
-    constexpr int kStageB = fp4_stage_bytes(kNB);
-    constexpr int kSfCols = fp4_sf_cols(kNB);
+    constexpr int kKPS = P::kKPS;
+    constexpr int kStageB = fp4_stage_bytes(kNB, kKPS);
+    constexpr int kSfCols = fp4_sf_cols(kNB, kKPS);
     constexpr int kNBuf = kNB == 1 ? 2 : 1;   // accumulator buffers
     __shared__ __align__(8) uint64_t full[kGStages], sfready[kGStages], empty[kGStages], accfull[2], accempty[2],
         mma_done;
@@ -137,20 +139,20 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
             for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
                 const Fp4Item w = nxt;
                 if (i + (int)gridDim.x < n_items) prob.item(i + gridDim.x, nxt);
-                for (int k0 = 0; k0 < w.kt; k0 += kGKPS, ++kcount) {
+                for (int k0 = 0; k0 < w.kt; k0 += kKPS, ++kcount) {
                     const int s = kcount % kGStages;
                     const uint32_t use = kcount / kGStages;
                     if (use > 0 && !mbar_wait_bounded(&empty[s], (use - 1) & 1, status)) {
                         ok = false;
                         break;
                     }
-                    const int n = w.kt - k0 < kGKPS ? w.kt - k0 : kGKPS;
+                    const int n = w.kt - k0 < kKPS ? w.kt - k0 : kKPS;
                     uint8_t* st = sm + s * kStageB;
                     mbar_arrive_expect_tx(&full[s], (uint32_t)((1 + kNB) * n * kGBlk));
                     bulk_g2s(st, w.a + (size_t)k0 * kGBlk, (uint32_t)(n * kGBlk), &full[s]);
-                    bulk_g2s(st + kGKPS * kGBlk, w.b + (size_t)k0 * kGBlk, (uint32_t)(n * kGBlk), &full[s]);
+                    bulk_g2s(st + kKPS * kGBlk, w.b + (size_t)k0 * kGBlk, (uint32_t)(n * kGBlk), &full[s]);
                     if constexpr (kNB == 2)
-                        bulk_g2s(st + 2 * kGKPS * kGBlk, w.b2 + (size_t)k0 * kGBlk, (uint32_t)(n * kGBlk), &full[s]);
+                        bulk_g2s(st + 2 * kKPS * kGBlk, w.b2 + (size_t)k0 * kGBlk, (uint32_t)(n * kGBlk), &full[s]);
                 }
             }
             // every copy issued has landed before the CTA can exit, also when
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
                     break;
                 tc_fence_after();
                 const uint32_t acc = tmem + buf * kGN;
-                for (int k0 = 0; k0 < w.kt; k0 += kGKPS, ++kcount) {
+                for (int k0 = 0; k0 < w.kt; k0 += kKPS, ++kcount) {
                     const int s = kcount % kGStages;
                     const uint32_t use = kcount / kGStages;
                     if (!mbar_wait_bounded(&sfready[s], use & 1, status)) {
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
                         break;
                     }
                     tc_fence_after();
-                    const int n = w.kt - k0 < kGKPS ? w.kt - k0 : kGKPS;
+                    const int n = w.kt - k0 < kKPS ? w.kt - k0 : kKPS;
                     const uint8_t* st = sm + s * kStageB;
                     for (int i = 0; i < n; ++i) {
                         const uint64_t da = sdesc_kmajor_sw128(st + i * kGBlk);
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
                         const uint32_t sfa = tmem + 256 + kSfCols * s + 16 * (1 + kNB) * i;
 #pragma unroll
                         for (int b = 0; b < kNB; ++b) {
-                            const uint64_t db = sdesc_kmajor_sw128(st + ((1 + b) * kGKPS + i) * kGBlk);
+                            const uint64_t db = sdesc_kmajor_sw128(st + ((1 + b) * kKPS + i) * kGBlk);
                             const uint32_t sfb = sfa + 16 * (1 + b);
 #pragma unroll
                             for (int j = 0; j < 4; ++j)   // 64 E2M1 = 32 bytes = 2 descriptor units per MMA
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
         for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
             const Fp4Item w = nxt;
             if (i + (int)gridDim.x < n_items) prob.item(i + gridDim.x, nxt);
-            for (int k0 = 0; k0 < w.kt; k0 += kGKPS, ++kcount) {
+            for (int k0 = 0; k0 < w.kt; k0 += kKPS, ++kcount) {
                 const int s = kcount % kGStages;
                 const uint32_t use = kcount / kGStages;
                 const bool got = mbar_wait_bounded(&full[s], use & 1, status);
@@ -227,11 +229,11 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
                     ok = false;
                     break;
                 }
-                const int n = w.kt - k0 < kGKPS ? w.kt - k0 : kGKPS;
+                const int n = w.kt - k0 < kKPS ? w.kt - k0 : kKPS;
                 const uint8_t* st = sm + s * kStageB;
                 for (int q = 0; q < (1 + kNB) * n; ++q) {
                     const int i = q / (1 + kNB), op = q % (1 + kNB);   // op 0: A, 1 + b: B tile b
-                    const uint8_t* sf = st + (op * kGKPS + i) * kGBlk + kGTile;
+                    const uint8_t* sf = st + (op * kKPS + i) * kGBlk + kGTile;
                     uint4 r[4];
 #pragma unroll
                     for (int m1 = 0; m1 < 4; ++m1) r[m1] = *reinterpret_cast<const uint4*>(sf + (lane + 32 * m1) * 16);
@@ -299,23 +301,28 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
 namespace flint {
 
 // ---------------------------------------------------------------------------
-// Variant with a resident A operand, for products whose K is short (two
-// k-tiles): a work item is one 128-row A tile (an "M-tile") and all P::kNT
-// B tiles of its expert. The A tile (codes and scales of its kKT k-tiles) is
-// bulk-copied once into one of two A slots and its scale factors written to
-// tensor memory once; the B tiles stream through a ring of P::kStages stages
-// of one N-tile each (kKT k-tiles), and each N-tile's accumulator goes to the
-// epilogue as in fp4_gemm_kernel. Per M-tile the SMs take in one A tile plus
-// the expert's B tiles instead of one A tile per N-tile.
+// Variant with a resident A operand prepared in the kernel, for products
+// whose K is short (two k-tiles): a work item is one 128-row A tile (an
+// "M-tile") and all P::kNT B tiles of its expert. Four A-prep warps build
+// the A tile (codes and scales of its kKT k-tiles) straight into one of two
+// shared-memory A slots from the problem's source rows (prob.prep_a), one
+// M-tile ahead, together with two per-row values the epilogue reads
+// (prob.pre_from); the scale writers copy its scale factors to tensor memory
+// once. The B tiles stream through a ring of P::kStages stages of one N-tile
+// each, and each N-tile's accumulator goes to the epilogue as in
+// fp4_gemm_kernel. Per M-tile the SMs take in the A tile's source rows once
+// and the expert's B tiles.
 //
-// Roles: warp 0 producer (A tiles one M-tile ahead, B tiles); warp 1 tensor
-// memory and MMA issue; warps 2..5 scale writers (A scales once per M-tile,
-// B scales per stage); warps 6..13 epilogue. Tensor memory: accumulators
+// Roles: warp 0 producer (B tiles); warp 1 tensor memory and MMA issue;
+// warps 2..5 scale writers (A scales once per M-tile, B scales per stage);
+// warps 6..13 epilogue; warps 14..17 A prep. Tensor memory: accumulators
 // [0,256), A scales of slot a at 256 + 32a (k-tile i: + 16i), B scales of
 // stage s at 320 + 32s (k-tile i: + 16i).
 // ---------------------------------------------------------------------------
 constexpr int kRKT = 2;                        // k-tiles per item (K = 512)
 constexpr int kRStageBytes = kRKT * kGBlk;     // one N-tile of B, or one A tile
+constexpr int kRPrepWarps = 4;
+constexpr int kRThreads = kGThreads + 32 * kRPrepWarps;
 
 template <class P>
 constexpr int fp4_gemm_resa_smem() {
@@ -324,13 +331,15 @@ constexpr int fp4_gemm_resa_smem() {
 }
 
 template <class P>
-__global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_resa_kernel(const P prob, uint32_t* status) {
+__global__ void __launch_bounds__(kRThreads, 1) fp4_gemm_resa_kernel(const P prob, uint32_t* status) {
     extern __shared__ uint8_t graw[];
     constexpr int kS = P::kStages;
     constexpr int kNT = P::kNT;
     __shared__ __align__(8) uint64_t full[kS], sfready[kS], empty[kS], afull[2], asfready[2], aempty[2],
         accfull[2], accempty[2], mma_done;
     __shared__ uint32_t tmem_base;
+    __shared__ int rowi[2][kGM];      // per A slot and tile row: the problem's row value (int)
+    __shared__ float rowf[2][kGM];    // and (float)
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(graw) + 1023) & ~uintptr_t(1023));
     uint8_t* aslot = sm;                                  // [2][kRStageBytes]
     uint8_t* bring = sm + 2 * kRStageBytes;               // [kS][kRStageBytes]
@@ -342,7 +351,7 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_resa_kernel(const P pro
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&afull[b], 1);
+            mbar_init(&afull[b], kRPrepWarps);
             mbar_init(&asfready[b], 4);
             mbar_init(&aempty[b], 1);
             mbar_init(&accfull[b], 1);
@@ -363,13 +372,9 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_resa_kernel(const P pro
 
     if (warp == 0) {
         if (lane == 0) {
-            uint32_t bfills = 0, afills = 0;
+            uint32_t bfills = 0;
             bool ok = true;
-            for (int mt = blockIdx.x; mt < n_mt && ok; mt += gridDim.x, ++afills) {
-                const int a = afills & 1;
-                if (afills >= 2 && !mbar_wait_bounded(&aempty[a], ((afills >> 1) - 1) & 1, status)) break;
-                mbar_arrive_expect_tx(&afull[a], kRStageBytes);
-                bulk_g2s(aslot + a * kRStageBytes, prob.a_blocks(mt), kRStageBytes, &afull[a]);
+            for (int mt = blockIdx.x; mt < n_mt && ok; mt += gridDim.x) {
                 for (int n = 0; n < kNT; ++n, ++bfills) {
                     const int s = bfills % kS;
                     const uint32_t use = bfills / kS;
@@ -381,9 +386,7 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_resa_kernel(const P pro
                     bulk_g2s(bring + s * kRStageBytes, prob.b_blocks(mt, n), kRStageBytes, &full[s]);
                 }
             }
-            // every copy issued has landed before the CTA can exit
-            drain_ring(full, kS, bfills, status);
-            drain_ring(afull, 2, afills, status);
+            drain_ring(full, kS, bfills, status);   // every copy issued has landed before the CTA can exit
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -464,18 +467,23 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_resa_kernel(const P pro
                 if (lane == 0) mbar_arrive(&sfready[s]);
             }
         }
-    } else {
+    } else if (warp < 6 + kGEpiWarps) {
         // epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31 and the
-        // columns [64*half, 64*half + 64) of the accumulator
+        // columns [64*half, 64*half + 64) of the accumulator. An M-tile's
+        // row values are read before its first accumulator is waited for;
+        // the A prep rewrites them only after that M-tile's last MMAs, which
+        // cannot complete before the epilogue is within two accumulators of
+        // them.
         const int quad = warp & 3;
         const int half = (warp - 6) >> 2;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         uint8_t* epi = sm + 2 * kRStageBytes + kS * kRStageBytes + (warp - 6) * P::kEpiSmemPerWarp;
-        uint32_t n_done = 0;
+        uint32_t n_done = 0, acount = 0;
         bool ok = true;
-        for (int mt = blockIdx.x; mt < n_mt && ok; mt += gridDim.x) {
-            const typename P::Pre pw = prob.pre(mt, row, half);
+        for (int mt = blockIdx.x; mt < n_mt && ok; mt += gridDim.x, ++acount) {
+            const int a = acount & 1;
+            typename P::Pre pw{};
             for (int n = 0; n < kNT; ++n) {
                 const uint32_t buf = n_done & 1;
                 const bool got = mbar_wait_bounded(&accfull[buf], (n_done >> 1) & 1, status);
@@ -484,12 +492,34 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_resa_kernel(const P pro
                     break;
                 }
                 tc_fence_after();
+                if (n == 0) {
+                    // the row values were written before afull[a] completed
+                    // (long since: this M-tile's MMAs have run), so this wait
+                    // returns at once and orders the reads after those writes
+                    mbar_wait_bounded(&afull[a], (acount >> 1) & 1, status);
+                    pw = prob.pre_from(rowi[a][row], rowf[a][row]);
+                }
                 prob.epilogue(mt, n, pw, tmem + lane_base + buf * kGN, row, half, epi);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&accempty[buf]);
                 ++n_done;
             }
+        }
+    } else {
+        // A prep: warp q of 4 builds rows 32q .. 32q+31 of the A tile
+        const int wq = warp - 6 - kGEpiWarps;
+        uint32_t acount = 0;
+        for (int mt = blockIdx.x; mt < n_mt; mt += gridDim.x, ++acount) {
+            const int a = acount & 1;
+            if (acount >= 2) {
+                const bool got = mbar_wait_bounded(&aempty[a], ((acount >> 1) - 1) & 1, status);
+                if (!__all_sync(0xffffffffu, got)) break;
+            }
+            prob.prep_a(mt, aslot + a * kRStageBytes, rowi[a], rowf[a], wq, lane);
+            fence_proxy_async_smem();   // the tile is read by the tensor core (async proxy)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull[a]);
         }
     }
     tc_fence_before();

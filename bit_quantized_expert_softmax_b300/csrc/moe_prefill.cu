@@ -12,9 +12,9 @@
 //   gemm1     gate/up: [rows x d] . [2f x d]^T, each 128-column tile holds 64
 //             gate and 64 up columns of the same f range, two such tiles per
 //             item sharing the A k-tiles; epilogue h = silu(g)*u (fp32)
-//   quant_h   quantise each h row into swizzled A tiles of the down GEMM
-//   gemm2     down: [rows x f] . [d x f]^T, each M-tile's A tile held in
-//             shared memory across its 16 N-tiles; epilogue scales by the routing
+//   gemm2     down: [rows x f] . [d x f]^T; per M-tile the kernel quantises
+//             the tile's fp32 h rows into its A tile in shared memory and
+//             keeps it there across its 16 N-tiles; epilogue scales by the routing
 //             weight (1 for the shared expert) and stores the contribution in
 //             bf16, one row per (token, expert) assignment
 //   combine   out[t] = bf16(shared + slot 0 + ... + slot k-1), summed in fp32
@@ -190,9 +190,6 @@ struct PrefillCtx {
     uint8_t* a1;              // gate/up A blocks [row tiles][d/256]
     float* sa;
     float* h;                 // [padded rows][f] fp32
-    uint8_t* a2;              // down A blocks [row tiles][f/256]
-    int* prow;                // [padded rows] bucketed position of the row's assignment, -1: padding
-    float* yscale;            // [padded rows] s_h * down tensor scale * routing weight
     __nv_bfloat16* y;         // [T*(k+1)][d] weighted contributions by bucketed position
     // weights (blocks)
     const uint8_t* w1;
@@ -290,60 +287,9 @@ __global__ void __launch_bounds__(256, 3) quant_x_kernel(PrefillCtx c) {
     }
 }
 
-// Quantise each h row (fp32, f elements) into the down GEMM's A tiles and
-// write the down GEMM's per-row epilogue data. A warp takes kQhRows
-// consecutive padded rows (one M-tile's): it loads all of their h first (the
-// buffer holds every row the grid covers, so the loads need no lookup), then
-// resolves the rows' slots and routing weights while those loads are in
-// flight. Warps past the actual rows return; padding rows get prow = -1.
+// Rows of h quantised per M-tile inside the down GEMM (Gemm2R::prep_a), four
+// rows per warp at a time.
 constexpr int kQhRows = 4;
-
-template <int EPL>
-__global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int KT = c.f / kGK;
-    const int row0 = (blockIdx.x * 8 + warp) * kQhRows;
-    float4 raw[kQhRows][EPL / 4];
-#pragma unroll
-    for (int i = 0; i < kQhRows; ++i) {
-        const float4* hr = reinterpret_cast<const float4*>(c.h + (size_t)(row0 + i) * c.f + lane * EPL);
-#pragma unroll
-        for (int j = 0; j < EPL / 4; ++j) raw[i][j] = __ldcs(hr + j);
-    }
-    const int n_rows = c.meta[2] * kGM;
-    if (row0 >= n_rows) return;
-    const int mt = row0 / kGM, r0 = row0 % kGM;
-    const int slot = c.mt_slot[mt], m = c.mt_m[mt];
-    // lane i < kQhRows: position and epilogue scale of row row0 + i (-1: padding)
-    int p = -1;
-    float yscale_w = 0.f;
-    if (lane < kQhRows) {
-        const int q = m * kGM + r0 + lane;
-        if (q < c.slot_cnt[slot]) {
-            p = c.slot_off[slot] + q;
-            const float wr = p < c.T * c.k ? c.wts[__ldg(c.perm + p)] : 1.0f;
-            yscale_w = c.tscale[c.slot_expert[slot] * 3 + 2] * wr;
-        }
-    }
-    uint8_t* blocks = c.a2 + (size_t)mt * KT * kGBlk;
-#pragma unroll
-    for (int i = 0; i < kQhRows; ++i) {
-        const int pi = __shfl_sync(0xffffffffu, p, i);
-        const float ys = __shfl_sync(0xffffffffu, yscale_w, i);
-        if (pi < 0) {   // padding row: its codes are never read back
-            if (lane == 0) c.prow[row0 + i] = -1;
-            continue;
-        }
-        uint32_t codes[EPL / 8];
-        uint32_t sb = 0;
-        const float s_t = quant_row_f32<EPL>(raw[i], codes, sb);
-        store_row_swizzled<EPL>(blocks, r0 + i, lane, codes, sb);
-        if (lane == 0) {
-            c.prow[row0 + i] = pi;
-            c.yscale[row0 + i] = s_t * ys;
-        }
-    }
-}
 
 // gate/up GEMM: item = (M-tile, pair of N-tiles); N-tile nt holds 64 gate
 // and 64 up columns of the same f range, so the pair yields h columns
@@ -352,8 +298,9 @@ __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
 struct Gemm1 {
     PrefillCtx c;
     int NT, KT;   // N-tiles (2f/128) and k-tiles (d/256)
-    static constexpr int kStages = 2;
+    static constexpr int kStages = 4;
     static constexpr int kNB = 2;
+    static constexpr int kKPS = 1;   // one A k-tile and the two B k-tiles per stage
     __device__ int n_items() const { return c.meta[2] * (NT / 2); }
     __device__ void item(int i, Fp4Item& w) const {
         const int np = NT / 2;
@@ -476,7 +423,11 @@ struct Gemm2 {
 };
 
 // The down GEMM with each M-tile's A tile resident (fp4_gemm_resa_kernel):
-// one item per M-tile, its 16 N-tiles in turn; the epilogue is Gemm2's.
+// one item per M-tile, its 16 N-tiles in turn; the epilogue is Gemm2's. The
+// A tile is h of the M-tile's 128 rows quantised to NVFP4 in the kernel
+// (prep_a), from the fp32 h the gate/up GEMM wrote: per row its position
+// (-1: padding) and the epilogue scale s_h * down tensor scale * routing
+// weight go to the epilogue through shared memory.
 struct Gemm2R {
     Gemm2 g;
     static constexpr int kStages = 3;
@@ -484,17 +435,58 @@ struct Gemm2R {
     static constexpr int kEpiSmemPerWarp = Gemm2::kEpiSmemPerWarp;
     using Pre = Gemm2::Pre;
     __device__ int n_mtiles() const { return g.c.meta[2]; }
-    __device__ const uint8_t* a_blocks(int mt) const { return g.c.a2 + (size_t)mt * kRKT * kGBlk; }
     __device__ const uint8_t* b_blocks(int mt, int n) const {
         return g.c.w2 + ((size_t)__ldg(g.c.mt_e + mt) * kNT + n) * kRKT * kGBlk;
     }
-    __device__ Pre pre(int mt, int row, int) const {
-        const int rp = mt * kGM + row;
-        return {g.c.prow[rp], g.c.yscale[rp]};
+    __device__ Pre pre_from(int p, float scale) const { return {p, scale}; }
+    // Rows 32 wq .. 32 wq + 31 of M-tile mt, four at a time, their h loads
+    // issued before the rows' lookups (one warp; lane l holds elements
+    // 16 l .. 16 l + 15 of a row).
+    __device__ void prep_a(int mt, uint8_t* blocks, int* rowp, float* rowscale, int wq, int lane) const {
+        const PrefillCtx& c = g.c;
+        const int slot = __ldg(c.mt_slot + mt), m = __ldg(c.mt_m + mt);
+        const int cnt = __ldg(c.slot_cnt + slot), off = __ldg(c.slot_off + slot);
+        const float tsd = __ldg(c.tscale + __ldg(c.slot_expert + slot) * 3 + 2);
+#pragma unroll 1
+        for (int r0 = 32 * wq; r0 < 32 * wq + 32; r0 += kQhRows) {
+            float4 raw[kQhRows][4];
+#pragma unroll
+            for (int i = 0; i < kQhRows; ++i) {
+                const float4* hr = reinterpret_cast<const float4*>(c.h + ((size_t)mt * kGM + r0 + i) * c.f + lane * 16);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) raw[i][j] = __ldcs(hr + j);
+            }
+            int p = -1;
+            float ys = 0.f;
+            if (lane < kQhRows) {
+                const int q = m * kGM + r0 + lane;
+                if (q < cnt) {
+                    p = off + q;
+                    ys = tsd * (p < c.T * c.k ? __ldg(c.wts + __ldg(c.perm + p)) : 1.0f);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kQhRows; ++i) {
+                const int pi = __shfl_sync(0xffffffffu, p, i);
+                const float ysi = __shfl_sync(0xffffffffu, ys, i);
+                if (pi < 0) {   // padding row: its products are discarded by the epilogue
+                    if (lane == 0) rowp[r0 + i] = -1;
+                    continue;
+                }
+                uint32_t codes[2];
+                uint32_t sb = 0;
+                const float s_t = quant_row_f32<16>(raw[i], codes, sb);
+                store_row_swizzled<16>(blocks, r0 + i, lane, codes, sb);
+                if (lane == 0) {
+                    rowp[r0 + i] = pi;
+                    rowscale[r0 + i] = s_t * ysi;
+                }
+            }
+        }
     }
     __device__ void epilogue(int mt, int n, const Pre& pr, uint32_t taddr, int row, int half, uint8_t* epi) const {
         Fp4Item w;
-        w.a = w.b = nullptr;
+        w.a = w.b = w.b2 = nullptr;
         w.kt = kRKT;
         w.m = mt;
         w.n = n;
@@ -641,8 +633,7 @@ size_t prefill_workspace_bytes(const Shape& s, int Tm) {
     const size_t rows = (size_t)Tm * (s.k + 1) + (size_t)kGM * (s.n_slots() + 1);
     const size_t rt = (rows + kGM - 1) / kGM;
     const size_t a1 = rt * (s.d / kGK) * (kGTile + kGSf);
-    const size_t a2 = rt * (s.f / kGK) * (kGTile + kGSf);
-    return 256 * 16 + rt * kGM * 4 * 3 + rt * 16 + (s.n_slots() + 2) * 4 * 2 + a1 + a2 + rt * kGM * s.f * 4 +
+    return 256 * 16 + rt * kGM * 4 + rt * 16 + (s.n_slots() + 2) * 4 * 2 + a1 + rt * kGM * s.f * 4 +
            (size_t)Tm * (s.k + 1) * s.d * 2;
 }
 
@@ -685,10 +676,7 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     c.mt_m = reinterpret_cast<int*>(take(rt * 4));
     c.mt_e = reinterpret_cast<int*>(take(rt * 4));
     c.sa = reinterpret_cast<float*>(take(rt * kGM * 4));
-    c.prow = reinterpret_cast<int*>(take(rt * kGM * 4));
-    c.yscale = reinterpret_cast<float*>(take(rt * kGM * 4));
     c.a1 = take(rt * (s.d / kGK) * kGBlk);
-    c.a2 = take(rt * (s.f / kGK) * kGBlk);
     c.h = reinterpret_cast<float*>(take(rt * kGM * s.f * 4));
     c.y = reinterpret_cast<__nv_bfloat16*>(take((size_t)Tm * (s.k + 1) * s.d * 2));
     c.x = x;
@@ -707,16 +695,15 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     Gemm1 g1{c, 2 * s.f / kGN, s.d / kGK};
     fp4_gemm_kernel<Gemm1><<<148, kGThreads, fp4_gemm_smem<Gemm1>(), st>>>(g1, ws.status);
     mark(2);
-    static_assert(kGM % (8 * kQhRows) == 0, "a CTA's rows stay inside one M-tile");
-    quant_h_kernel<16><<<(unsigned)(rt * kGM / (8 * kQhRows)), 256, 0, st>>>(c);
+    static_assert(kGM % (kRPrepWarps * kQhRows) == 0, "the prep warps' rows tile an M-tile");
     mark(3);
     static_assert(Gemm2R::kNT * kGN == 2048 && kRKT * kGK == 512, "the Flint shape (d = 2048, f = 512)");
     Gemm2R g2{Gemm2{c, s.d / kGN, s.f / kGK}};
-    fp4_gemm_resa_kernel<Gemm2R><<<148, kGThreads, fp4_gemm_resa_smem<Gemm2R>(), st>>>(g2, ws.status);
+    fp4_gemm_resa_kernel<Gemm2R><<<148, kRThreads, fp4_gemm_resa_smem<Gemm2R>(), st>>>(g2, ws.status);
     mark(4);
     combine_kernel<<<(T + 7) / 8 < 148 * 8 ? (T + 7) / 8 : 148 * 8, 256, 0, st>>>(c, out, residual);
     mark(5);
-    *n_launch += 6;
+    *n_launch += 5;
     return cudaGetLastError();
 }
 
