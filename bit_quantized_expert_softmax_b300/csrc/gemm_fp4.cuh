@@ -301,28 +301,23 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
 namespace flint {
 
 // ---------------------------------------------------------------------------
-// Variant with a resident A operand prepared in the kernel, for products
-// whose K is short (two k-tiles): a work item is one 128-row A tile (an
-// "M-tile") and all P::kNT B tiles of its expert. Four A-prep warps build
-// the A tile (codes and scales of its kKT k-tiles) straight into one of two
-// shared-memory A slots from the problem's source rows (prob.prep_a), one
-// M-tile ahead, together with two per-row values the epilogue reads
-// (prob.pre_from); the scale writers copy its scale factors to tensor memory
-// once. The B tiles stream through a ring of P::kStages stages of one N-tile
-// each, and each N-tile's accumulator goes to the epilogue as in
-// fp4_gemm_kernel. Per M-tile the SMs take in the A tile's source rows once
-// and the expert's B tiles.
+// Variant with a resident A operand, for products whose K is short (two
+// k-tiles): a work item is one 128-row A tile (an "M-tile") and all P::kNT
+// B tiles of its expert. The A tile (codes and scales of its kKT k-tiles) is
+// bulk-copied once into one of two A slots and its scale factors written to
+// tensor memory once; the B tiles stream through a ring of P::kStages stages
+// of one N-tile each (kKT k-tiles), and each N-tile's accumulator goes to the
+// epilogue as in fp4_gemm_kernel. Per M-tile the SMs take in one A tile plus
+// the expert's B tiles instead of one A tile per N-tile.
 //
-// Roles: warp 0 producer (B tiles); warp 1 tensor memory and MMA issue;
-// warps 2..5 scale writers (A scales once per M-tile, B scales per stage);
-// warps 6..13 epilogue; warps 14..17 A prep. Tensor memory: accumulators
+// Roles: warp 0 producer (A tiles one M-tile ahead, B tiles); warp 1 tensor
+// memory and MMA issue; warps 2..5 scale writers (A scales once per M-tile,
+// B scales per stage); warps 6..13 epilogue. Tensor memory: accumulators
 // [0,256), A scales of slot a at 256 + 32a (k-tile i: + 16i), B scales of
 // stage s at 320 + 32s (k-tile i: + 16i).
 // ---------------------------------------------------------------------------
 constexpr int kRKT = 2;                        // k-tiles per item (K = 512)
 constexpr int kRStageBytes = kRKT * kGBlk;     // one N-tile of B, or one A tile
-constexpr int kRPrepWarps = 4;
-constexpr int kRThreads = kGThreads + 32 * kRPrepWarps;
 
 template <class P>
 constexpr int fp4_gemm_resa_smem() {
@@ -331,15 +326,13 @@ constexpr int fp4_gemm_resa_smem() {
 }
 
 template <class P>
-__global__ void __launch_bounds__(kRThreads, 1) fp4_gemm_resa_kernel(const P prob, uint32_t* status) {
+__global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_resa_kernel(const P prob, uint32_t* status) {
     extern __shared__ uint8_t graw[];
     constexpr int kS = P::kStages;
     constexpr int kNT = P::kNT;
     __shared__ __align__(8) uint64_t full[kS], sfready[kS], empty[kS], afull[2], asfready[2], aempty[2],
         accfull[2], accempty[2], mma_done;
     __shared__ uint32_t tmem_base;
-    __shared__ int rowi[2][kGM];      // per A slot and tile row: the problem's row value (int)
-    __shared__ float rowf[2][kGM];    // and (float)
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(graw) + 1023) & ~uintptr_t(1023));
     uint8_t* aslot = sm;                                  // [2][kRStageBytes]
     uint8_t* bring = sm + 2 * kRStageBytes;               // [kS][kRStageBytes]
@@ -351,7 +344,7 @@ __global__ void __launch_bounds__(kRThreads, 1) fp4_gemm_resa_kernel(const P pro
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&afull[b], kRPrepWarps);
+            mbar_init(&afull[b], 1);
             mbar_init(&asfready[b], 4);
             mbar_init(&aempty[b], 1);
             mbar_init(&accfull[b], 1);
@@ -372,9 +365,13 @@ __global__ void __launch_bounds__(kRThreads, 1) fp4_gemm_resa_kernel(const P pro
 
     if (warp == 0) {
         if (lane == 0) {
-            uint32_t bfills = 0;
+            uint32_t bfills = 0, afills = 0;
             bool ok = true;
-            for (int mt = blockIdx.x; mt < n_mt && ok; mt += gridDim.x) {
+            for (int mt = blockIdx.x; mt < n_mt && ok; mt += gridDim.x, ++afills) {
+                const int a = afills & 1;
+                if (afills >= 2 && !mbar_wait_bounded(&aempty[a], ((afills >> 1) - 1) & 1, status)) break;
+                mbar_arrive_expect_tx(&afull[a], kRStageBytes);
+                bulk_g2s(aslot + a * kRStageBytes, prob.a_blocks(mt), kRStageBytes, &afull[a]);
                 for (int n = 0; n < kNT; ++n, ++bfills) {
                     const int s = bfills % kS;
                     const uint32_t use = bfills / kS;
@@ -386,7 +383,9 @@ __global__ void __launch_bounds__(kRThreads, 1) fp4_gemm_resa_kernel(const P pro
                     bulk_g2s(bring + s * kRStageBytes, prob.b_blocks(mt, n), kRStageBytes, &full[s]);
                 }
             }
-            drain_ring(full, kS, bfills, status);   // every copy issued has landed before the CTA can exit
+            // every copy issued has landed before the CTA can exit
+            drain_ring(full, kS, bfills, status);
+            drain_ring(afull, 2, afills, status);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -467,23 +466,18 @@ __global__ void __launch_bounds__(kRThreads, 1) fp4_gemm_resa_kernel(const P pro
                 if (lane == 0) mbar_arrive(&sfready[s]);
             }
         }
-    } else if (warp < 6 + kGEpiWarps) {
+    } else {
         // epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31 and the
-        // columns [64*half, 64*half + 64) of the accumulator. An M-tile's
-        // row values are read before its first accumulator is waited for;
-        // the A prep rewrites them only after that M-tile's last MMAs, which
-        // cannot complete before the epilogue is within two accumulators of
-        // them.
+        // columns [64*half, 64*half + 64) of the accumulator
         const int quad = warp & 3;
         const int half = (warp - 6) >> 2;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         uint8_t* epi = sm + 2 * kRStageBytes + kS * kRStageBytes + (warp - 6) * P::kEpiSmemPerWarp;
-        uint32_t n_done = 0, acount = 0;
+        uint32_t n_done = 0;
         bool ok = true;
-        for (int mt = blockIdx.x; mt < n_mt && ok; mt += gridDim.x, ++acount) {
-            const int a = acount & 1;
-            typename P::Pre pw{};
+        for (int mt = blockIdx.x; mt < n_mt && ok; mt += gridDim.x) {
+            const typename P::Pre pw = prob.pre(mt, row, half);
             for (int n = 0; n < kNT; ++n) {
                 const uint32_t buf = n_done & 1;
                 const bool got = mbar_wait_bounded(&accfull[buf], (n_done >> 1) & 1, status);
@@ -492,34 +486,12 @@ __global__ void __launch_bounds__(kRThreads, 1) fp4_gemm_resa_kernel(const P pro
                     break;
                 }
                 tc_fence_after();
-                if (n == 0) {
-                    // the row values were written before afull[a] completed
-                    // (long since: this M-tile's MMAs have run), so this wait
-                    // returns at once and orders the reads after those writes
-                    mbar_wait_bounded(&afull[a], (acount >> 1) & 1, status);
-                    pw = prob.pre_from(rowi[a][row], rowf[a][row]);
-                }
                 prob.epilogue(mt, n, pw, tmem + lane_base + buf * kGN, row, half, epi);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&accempty[buf]);
                 ++n_done;
             }
-        }
-    } else {
-        // A prep: warp q of 4 builds rows 32q .. 32q+31 of the A tile
-        const int wq = warp - 6 - kGEpiWarps;
-        uint32_t acount = 0;
-        for (int mt = blockIdx.x; mt < n_mt; mt += gridDim.x, ++acount) {
-            const int a = acount & 1;
-            if (acount >= 2) {
-                const bool got = mbar_wait_bounded(&aempty[a], ((acount >> 1) - 1) & 1, status);
-                if (!__all_sync(0xffffffffu, got)) break;
-            }
-            prob.prep_a(mt, aslot + a * kRStageBytes, rowi[a], rowf[a], wq, lane);
-            fence_proxy_async_smem();   // the tile is read by the tensor core (async proxy)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&afull[a]);
         }
     }
     tc_fence_before();

@@ -12,13 +12,15 @@
 //   gemm1     gate/up: [rows x d] . [2f x d]^T, each 128-column tile holds 64
 //             gate and 64 up columns of the same f range, two such tiles per
 //             item sharing the A k-tiles; epilogue h = silu(g)*u (fp32)
-//   gemm2     down: [rows x f] . [d x f]^T; per M-tile the kernel quantises
-//             the tile's fp32 h rows into its A tile in shared memory and
-//             keeps it there across its 16 N-tiles; epilogue scales by the routing
+//   quant_h   quantise each fp32 h row into swizzled A tiles of the down GEMM
+//   gemm2     down: [rows x f] . [d x f]^T, each M-tile's A tile held in
+//             shared memory across its 16 N-tiles; epilogue scales by the routing
 //             weight (1 for the shared expert) and stores the contribution in
 //             bf16, one row per (token, expert) assignment
 //   combine   out[t] = bf16(shared + slot 0 + ... + slot k-1), summed in fp32
 //             in that order (deterministic), plus the optional residual
+#include <algorithm>
+
 #include "../../include/flint_moe.h"
 #include "gemm_fp4.cuh"
 #include "kernels.cuh"
@@ -190,6 +192,9 @@ struct PrefillCtx {
     uint8_t* a1;              // gate/up A blocks [row tiles][d/256]
     float* sa;
     float* h;                 // [padded rows][f] fp32
+    uint8_t* a2;              // down A blocks [row tiles][f/256]
+    int* prow;                // [padded rows] bucketed position of the row's assignment, -1: padding
+    float* yscale;            // [padded rows] s_h * down tensor scale * routing weight
     __nv_bfloat16* y;         // [T*(k+1)][d] weighted contributions by bucketed position
     // weights (blocks)
     const uint8_t* w1;
@@ -287,9 +292,61 @@ __global__ void __launch_bounds__(256, 3) quant_x_kernel(PrefillCtx c) {
     }
 }
 
-// Rows of h quantised per M-tile inside the down GEMM (Gemm2R::prep_a), four
-// rows per warp at a time.
+// Quantise each h row (fp32, f elements) into the down GEMM's A tiles and
+// write the down GEMM's per-row epilogue data. A warp takes kQhRows
+// consecutive padded rows (one M-tile's): it loads all of their h first (the
+// buffer holds every row the grid covers, so the loads need no lookup), then
+// resolves the rows' slots and routing weights while those loads are in
+// flight. Warps past the actual rows return; padding rows get prow = -1.
 constexpr int kQhRows = 4;
+
+template <int EPL>
+__global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KT = c.f / kGK;
+    // last CTA first: the gate/up GEMM wrote the high rows last
+    const int row0 = ((gridDim.x - 1 - blockIdx.x) * 8 + warp) * kQhRows;
+    float4 raw[kQhRows][EPL / 4];
+#pragma unroll
+    for (int i = 0; i < kQhRows; ++i) {
+        const float4* hr = reinterpret_cast<const float4*>(c.h + (size_t)(row0 + i) * c.f + lane * EPL);
+#pragma unroll
+        for (int j = 0; j < EPL / 4; ++j) raw[i][j] = __ldcs(hr + j);
+    }
+    const int n_rows = c.meta[2] * kGM;
+    if (row0 >= n_rows) return;
+    const int mt = row0 / kGM, r0 = row0 % kGM;
+    const int slot = c.mt_slot[mt], m = c.mt_m[mt];
+    // lane i < kQhRows: position and epilogue scale of row row0 + i (-1: padding)
+    int p = -1;
+    float yscale_w = 0.f;
+    if (lane < kQhRows) {
+        const int q = m * kGM + r0 + lane;
+        if (q < c.slot_cnt[slot]) {
+            p = c.slot_off[slot] + q;
+            const float wr = p < c.T * c.k ? c.wts[__ldg(c.perm + p)] : 1.0f;
+            yscale_w = c.tscale[c.slot_expert[slot] * 3 + 2] * wr;
+        }
+    }
+    uint8_t* blocks = c.a2 + (size_t)mt * KT * kGBlk;
+#pragma unroll
+    for (int i = 0; i < kQhRows; ++i) {
+        const int pi = __shfl_sync(0xffffffffu, p, i);
+        const float ys = __shfl_sync(0xffffffffu, yscale_w, i);
+        if (pi < 0) {   // padding row: its codes are never read back
+            if (lane == 0) c.prow[row0 + i] = -1;
+            continue;
+        }
+        uint32_t codes[EPL / 8];
+        uint32_t sb = 0;
+        const float s_t = quant_row_f32<EPL>(raw[i], codes, sb);
+        store_row_swizzled<EPL>(blocks, r0 + i, lane, codes, sb);
+        if (lane == 0) {
+            c.prow[row0 + i] = pi;
+            c.yscale[row0 + i] = s_t * ys;
+        }
+    }
+}
 
 // gate/up GEMM: item = (M-tile, pair of N-tiles); N-tile nt holds 64 gate
 // and 64 up columns of the same f range, so the pair yields h columns
@@ -361,7 +418,9 @@ struct Gemm1 {
                         // only where h sits on a rounding boundary)
                         hv[q] = __fdividef(gq, 1.0f + __expf(-gq)) * uq;
                     }
-                    __stcs(reinterpret_cast<float4*>(dst + i), make_float4(hv[0], hv[1], hv[2], hv[3]));
+                    // plain stores: the last-written rows are still in L2 when the h
+            // quantiser, which walks the rows from the end, reads them
+            *reinterpret_cast<float4*>(dst + i) = make_float4(hv[0], hv[1], hv[2], hv[3]);
                 }
             }
         }
@@ -423,11 +482,7 @@ struct Gemm2 {
 };
 
 // The down GEMM with each M-tile's A tile resident (fp4_gemm_resa_kernel):
-// one item per M-tile, its 16 N-tiles in turn; the epilogue is Gemm2's. The
-// A tile is h of the M-tile's 128 rows quantised to NVFP4 in the kernel
-// (prep_a), from the fp32 h the gate/up GEMM wrote: per row its position
-// (-1: padding) and the epilogue scale s_h * down tensor scale * routing
-// weight go to the epilogue through shared memory.
+// one item per M-tile, its 16 N-tiles in turn; the epilogue is Gemm2's.
 struct Gemm2R {
     Gemm2 g;
     static constexpr int kStages = 3;
@@ -435,54 +490,13 @@ struct Gemm2R {
     static constexpr int kEpiSmemPerWarp = Gemm2::kEpiSmemPerWarp;
     using Pre = Gemm2::Pre;
     __device__ int n_mtiles() const { return g.c.meta[2]; }
+    __device__ const uint8_t* a_blocks(int mt) const { return g.c.a2 + (size_t)mt * kRKT * kGBlk; }
     __device__ const uint8_t* b_blocks(int mt, int n) const {
         return g.c.w2 + ((size_t)__ldg(g.c.mt_e + mt) * kNT + n) * kRKT * kGBlk;
     }
-    __device__ Pre pre_from(int p, float scale) const { return {p, scale}; }
-    // Rows 32 wq .. 32 wq + 31 of M-tile mt, four at a time, their h loads
-    // issued before the rows' lookups (one warp; lane l holds elements
-    // 16 l .. 16 l + 15 of a row).
-    __device__ void prep_a(int mt, uint8_t* blocks, int* rowp, float* rowscale, int wq, int lane) const {
-        const PrefillCtx& c = g.c;
-        const int slot = __ldg(c.mt_slot + mt), m = __ldg(c.mt_m + mt);
-        const int cnt = __ldg(c.slot_cnt + slot), off = __ldg(c.slot_off + slot);
-        const float tsd = __ldg(c.tscale + __ldg(c.slot_expert + slot) * 3 + 2);
-#pragma unroll 1
-        for (int r0 = 32 * wq; r0 < 32 * wq + 32; r0 += kQhRows) {
-            float4 raw[kQhRows][4];
-#pragma unroll
-            for (int i = 0; i < kQhRows; ++i) {
-                const float4* hr = reinterpret_cast<const float4*>(c.h + ((size_t)mt * kGM + r0 + i) * c.f + lane * 16);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) raw[i][j] = __ldcs(hr + j);
-            }
-            int p = -1;
-            float ys = 0.f;
-            if (lane < kQhRows) {
-                const int q = m * kGM + r0 + lane;
-                if (q < cnt) {
-                    p = off + q;
-                    ys = tsd * (p < c.T * c.k ? __ldg(c.wts + __ldg(c.perm + p)) : 1.0f);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < kQhRows; ++i) {
-                const int pi = __shfl_sync(0xffffffffu, p, i);
-                const float ysi = __shfl_sync(0xffffffffu, ys, i);
-                if (pi < 0) {   // padding row: its products are discarded by the epilogue
-                    if (lane == 0) rowp[r0 + i] = -1;
-                    continue;
-                }
-                uint32_t codes[2];
-                uint32_t sb = 0;
-                const float s_t = quant_row_f32<16>(raw[i], codes, sb);
-                store_row_swizzled<16>(blocks, r0 + i, lane, codes, sb);
-                if (lane == 0) {
-                    rowp[r0 + i] = pi;
-                    rowscale[r0 + i] = s_t * ysi;
-                }
-            }
-        }
+    __device__ Pre pre(int mt, int row, int) const {
+        const int rp = mt * kGM + row;
+        return {g.c.prow[rp], g.c.yscale[rp]};
     }
     __device__ void epilogue(int mt, int n, const Pre& pr, uint32_t taddr, int row, int half, uint8_t* epi) const {
         Fp4Item w;
@@ -608,6 +622,43 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __r
     }
 }
 
+// NVFP4 quantisation of a bf16 weight matrix with one fp32 tensor scale: the
+// amax of the matrix (fp32 bits, atomically maxed: non-negative floats order
+// as their bit patterns), then one thread per 16-element block, then the
+// tensor scale written over the amax.
+__global__ void __launch_bounds__(256) weight_amax_kernel(const __nv_bfloat16* __restrict__ w, long n8,
+                                                          uint32_t* __restrict__ amax_bits) {
+    float m = 0.f;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n8; i += (long)gridDim.x * blockDim.x) {
+        float v[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(w) + i), v);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) m = fmaxf(m, fabsf(v[u]));
+    }
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0 && m > 0.f) atomicMax(amax_bits, __float_as_uint(m));
+}
+
+__global__ void __launch_bounds__(256) weight_quant_kernel(const __nv_bfloat16* __restrict__ w, long n_blocks,
+                                                           const uint32_t* __restrict__ amax_bits,
+                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    const float s = __uint_as_float(*amax_bits) / 2688.0f;
+    for (long b = blockIdx.x * (long)blockDim.x + threadIdx.x; b < n_blocks; b += (long)gridDim.x * blockDim.x) {
+        const uint4* src = reinterpret_cast<const uint4*>(w + b * 16);
+        float v[16];
+        unpack8(__ldg(src), v);
+        unpack8(__ldg(src + 1), v + 8);
+        uint32_t c[2];
+        const uint32_t sb = quant_block16(v, s, c);
+        *reinterpret_cast<uint2*>(codes + b * 8) = make_uint2(c[0], c[1]);
+        scales[b] = (uint8_t)sb;
+    }
+}
+
+__global__ void weight_scale_kernel(float* tensor_scale) {
+    *tensor_scale = __uint_as_float(*reinterpret_cast<const uint32_t*>(tensor_scale)) / 2688.0f;
+}
+
 }  // namespace
 
 // The row quantisers use 64 (x) and 16 (h) elements per lane: d = 2048, f = 512.
@@ -633,7 +684,8 @@ size_t prefill_workspace_bytes(const Shape& s, int Tm) {
     const size_t rows = (size_t)Tm * (s.k + 1) + (size_t)kGM * (s.n_slots() + 1);
     const size_t rt = (rows + kGM - 1) / kGM;
     const size_t a1 = rt * (s.d / kGK) * (kGTile + kGSf);
-    return 256 * 16 + rt * kGM * 4 + rt * 16 + (s.n_slots() + 2) * 4 * 2 + a1 + rt * kGM * s.f * 4 +
+    const size_t a2 = rt * (s.f / kGK) * (kGTile + kGSf);
+    return 256 * 16 + rt * kGM * 4 * 3 + rt * 16 + (s.n_slots() + 2) * 4 * 2 + a1 + a2 + rt * kGM * s.f * 4 +
            (size_t)Tm * (s.k + 1) * s.d * 2;
 }
 
@@ -676,7 +728,10 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     c.mt_m = reinterpret_cast<int*>(take(rt * 4));
     c.mt_e = reinterpret_cast<int*>(take(rt * 4));
     c.sa = reinterpret_cast<float*>(take(rt * kGM * 4));
+    c.prow = reinterpret_cast<int*>(take(rt * kGM * 4));
+    c.yscale = reinterpret_cast<float*>(take(rt * kGM * 4));
     c.a1 = take(rt * (s.d / kGK) * kGBlk);
+    c.a2 = take(rt * (s.f / kGK) * kGBlk);
     c.h = reinterpret_cast<float*>(take(rt * kGM * s.f * 4));
     c.y = reinterpret_cast<__nv_bfloat16*>(take((size_t)Tm * (s.k + 1) * s.d * 2));
     c.x = x;
@@ -695,15 +750,16 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     Gemm1 g1{c, 2 * s.f / kGN, s.d / kGK};
     fp4_gemm_kernel<Gemm1><<<148, kGThreads, fp4_gemm_smem<Gemm1>(), st>>>(g1, ws.status);
     mark(2);
-    static_assert(kGM % (kRPrepWarps * kQhRows) == 0, "the prep warps' rows tile an M-tile");
+    static_assert(kGM % (8 * kQhRows) == 0, "a CTA's rows stay inside one M-tile");
+    quant_h_kernel<16><<<(unsigned)(rt * kGM / (8 * kQhRows)), 256, 0, st>>>(c);
     mark(3);
     static_assert(Gemm2R::kNT * kGN == 2048 && kRKT * kGK == 512, "the Flint shape (d = 2048, f = 512)");
     Gemm2R g2{Gemm2{c, s.d / kGN, s.f / kGK}};
-    fp4_gemm_resa_kernel<Gemm2R><<<148, kRThreads, fp4_gemm_resa_smem<Gemm2R>(), st>>>(g2, ws.status);
+    fp4_gemm_resa_kernel<Gemm2R><<<148, kGThreads, fp4_gemm_resa_smem<Gemm2R>(), st>>>(g2, ws.status);
     mark(4);
     combine_kernel<<<(T + 7) / 8 < 148 * 8 ? (T + 7) / 8 : 148 * 8, 256, 0, st>>>(c, out, residual);
     mark(5);
-    *n_launch += 5;
+    *n_launch += 6;
     return cudaGetLastError();
 }
 
@@ -733,4 +789,27 @@ extern "C" flint_status flint_moe_debug_act_quant(const void* x_dev, int T, int 
     const cudaError_t e = flint::launch_act_quant(static_cast<const __nv_bfloat16*>(x_dev), T, K, codes_dev,
                                                   scales_dev, rowscale_dev, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FLINT_OK : FLINT_ECUDA;
+}
+
+extern "C" flint_status flint_moe_quantize_nvfp4(const void* w_dev, int R, int K, uint8_t* codes_dev,
+                                                 uint8_t* scales_dev, float* tensor_scale_dev, void* stream) {
+    using namespace flint;
+    if (R < 1 || K < 16 || K % 16 != 0) return FLINT_EINVAL;
+    if (w_dev == nullptr || codes_dev == nullptr || scales_dev == nullptr || tensor_scale_dev == nullptr)
+        return FLINT_EINVAL;
+    if (((uintptr_t)w_dev & 15u) || ((uintptr_t)codes_dev & 7u) || ((uintptr_t)tensor_scale_dev & 3u))
+        return FLINT_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long n = (long)R * K;
+    const auto* w = static_cast<const __nv_bfloat16*>(w_dev);
+    uint32_t* amax = reinterpret_cast<uint32_t*>(tensor_scale_dev);
+    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return FLINT_ECUDA;
+    const long n8 = n / 8, nb = n / 16;
+    const int g1 = (int)std::min<long>((n8 + 255) / 256, 148L * 8);
+    const int g2 = (int)std::min<long>((nb + 255) / 256, 148L * 16);
+    weight_amax_kernel<<<g1, 256, 0, st>>>(w, n8, amax);
+    weight_quant_kernel<<<g2, 256, 0, st>>>(w, nb, amax, codes_dev, scales_dev);
+    weight_scale_kernel<<<1, 1, 0, st>>>(tensor_scale_dev);
+    return cudaGetLastError() == cudaSuccess ? FLINT_OK : FLINT_ECUDA;
 }

@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
             "flint_moe_probe_fp4_peak": (_I, [_I, _I, ctypes.POINTER(ctypes.c_float),
                                               ctypes.POINTER(ctypes.c_double)]),
             "flint_moe_debug_wait_timeout": (_I, [_P, _I, ctypes.c_uint32, _P]),
+            "flint_moe_quantize_nvfp4": (_I, [_P, _I, _I, _P, _P, _P, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -251,6 +252,11 @@ def flint_moe_probe_fp4_peak(n: int, iters: int) -> tuple[float, float]:
     flops = ctypes.c_double(0.0)
     _check(lib().flint_moe_probe_fp4_peak(n, iters, ctypes.byref(ms), ctypes.byref(flops)), "flint_moe_probe_fp4_peak")
     return float(ms.value), float(flops.value)
+
+
+def flint_moe_quantize_nvfp4(w, R: int, K: int, codes, scales, tensor_scale, stream=None) -> None:
+    _check(lib().flint_moe_quantize_nvfp4(_ptr(w), R, K, _ptr(codes), _ptr(scales), _ptr(tensor_scale),
+                                          _stream(stream)), "flint_moe_quantize_nvfp4")
 
 
 def flint_moe_debug_wait_timeout(h: int, kind: int, spin_limit: int, stream=None) -> None:

@@ -233,6 +233,23 @@ FLINT_API flint_status flint_moe_debug_fp4_gemm(const uint8_t* a_codes_dev, cons
 FLINT_API flint_status flint_moe_debug_act_quant(const void* x_dev, int T, int K, uint8_t* codes_dev,
                                                  uint8_t* scales_dev, float* rowscale_dev, void* stream);
 
+/* NVFP4 quantisation of one bf16 weight matrix on the GPU, into the canonical
+ * NVFP4 layout flint_moe_load_weights and flint_moe_load_lm_head accept. The
+ * Flint blog ships NVFP4 weights ("Recursive Flint 40B-A2.5B", section "What
+ * actually shipped", NVFP4 GGUF bullet) and gives no quantisation procedure;
+ * this is the activation rule of flint_moe_debug_act_quant with one fp32
+ * tensor scale for the whole matrix: s = amax(|w|)/2688; per 16 consecutive
+ * elements of a row sb = E4M3_rne((amax_16/6)/s); codes
+ * E2M1_rne(w * (1/(E4M3(sb)*s))), all in fp32, ties to even, saturating.
+ * w_dev: bf16 [R][K] (device, 16-byte aligned); codes_dev: [R][K/2], element
+ * 2i in the low nibble (8-byte aligned); scales_dev: [R][K/16] E4M3 bytes;
+ * tensor_scale_dev: one fp32 (4-byte aligned; used as scratch until the last
+ * of the three kernels writes s). An all-zero matrix gives s = 0, zero
+ * scales and codes. Asynchronous on `stream`. Errors: FLINT_EINVAL (R < 1, K
+ * not a positive multiple of 16, NULL, misaligned), FLINT_ECUDA. */
+FLINT_API flint_status flint_moe_quantize_nvfp4(const void* w_dev, int R, int K, uint8_t* codes_dev,
+                                                uint8_t* scales_dev, float* tensor_scale_dev, void* stream);
+
 /* ---- the 4-bit output head and its sampler ---------------------------------
  * The Flint blog ("Recursive Flint 40B-A2.5B", section "The quantisation
  * recipe is the most transferable part") ships the output layer (lm_head)

@@ -168,6 +168,42 @@ def quant_act_nvfp4(v: np.ndarray):
     return codes.reshape(T, K), sb, s_t, deq.reshape(T, K)
 
 
+def quant_weight_nvfp4(w: np.ndarray):
+    """Quantise one weight matrix [R, K] (float32 values, e.g. of bf16
+    weights) to NVFP4 with one float32 tensor scale for the whole matrix.
+
+    The pages ship NVFP4 weights ("Flint", the NVFP4 GGUF build) and give no
+    quantisation procedure; the reading is the activation rule with the
+    per-row scale replaced by the per-tensor one that NVFP4 weights carry, all
+    decisions in float32:
+      s    = amax(|w|) / 2688                   (2688 = 6 * 448), float32
+      sb_b = E4M3_rne( (amax_b / 6) / s )       per 16 consecutive elements of a row
+      S_b  = E4M3(sb_b) * s,  r_b = 1 / S_b     float32
+      code = E2M1_rne( w * r_b )                ties to even, saturating at 6
+    An all-zero matrix, or a block with S_b == 0, gets codes 0 and scale 0.
+    Returns (codes uint8 [R, K] one code per element, scale bytes uint8
+    [R, K/16], tensor scale float32, dequantised values float64 [R, K])."""
+    v = np.asarray(w, dtype=np.float32)
+    R, K = v.shape
+    s = np.float32(np.abs(v).max() / np.float32(2688.0)) if v.size else np.float32(0.0)
+    blocks = v.reshape(R, K // 16, 16)
+    amax_b = np.abs(blocks).max(axis=2)
+    if s > 0:
+        ratio = ((amax_b / np.float32(6.0)).astype(np.float32) / s).astype(np.float32)
+    else:
+        ratio = np.zeros_like(amax_b, dtype=np.float32)
+    sb = F.e4m3_encode_rne_nonneg(ratio)
+    S = (F.E4M3_TABLE[sb].astype(np.float32) * s).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        inv = (np.float32(1.0) / S).astype(np.float32)
+        r = (blocks * inv[:, :, None]).astype(np.float32)
+    r = np.where(S[:, :, None] > 0, r, np.float32(0.0))
+    codes = F.e2m1_encode_rne(r)
+    codes = np.where(S[:, :, None] > 0, codes, 0).astype(np.uint8)
+    deq = F.E2M1_TABLE[codes] * F.E4M3_TABLE[sb][:, :, None] * float(s)
+    return codes.reshape(R, K), sb, s, deq.reshape(R, K)
+
+
 def expert_forward_w4a4(wg, wu, wd, x: np.ndarray) -> np.ndarray:
     """Expert with NVFP4-quantised activations entering each projection.
 

@@ -393,3 +393,74 @@ def test_bits_per_parameter_against_file_sizes():
     cfg = synth.CONFIGS[2]
     assert cfg.expert_bytes == 3 * (cfg.f * cfg.d // 2 + cfg.f * cfg.d // 16 + 4)
     assert synth.CONFIGS[3].expert_bytes == 3 * cfg.f * cfg.d * 5 // 8
+
+
+# ---------------------------------------------------------------------------
+# weight quantisation (NVFP4, one tensor scale per matrix)
+# ---------------------------------------------------------------------------
+
+
+def test_weight_quant_single_row_is_the_pinned_row_rule():
+    """With one row the per-tensor scale is the per-row one, so the weight
+    quantiser must reproduce the activation quantiser (itself pinned by the
+    hand-worked golden examples) bit for bit."""
+    rng = np.random.default_rng(21)
+    for scale in (1e-3, 1.0, 37.0):
+        v = (rng.standard_normal((1, 256)) * scale).astype(np.float32)
+        c1, sb1, s1, d1 = M.quant_weight_nvfp4(v)
+        c2, sb2, s2, d2 = M.quant_act_nvfp4(v)
+        assert np.array_equal(c1, c2) and np.array_equal(sb1, sb2)
+        assert np.float32(s1) == s2[0]
+        assert np.array_equal(d1, d2)
+
+
+def test_weight_quant_brute_force_nearest_grid_value():
+    """Every element's code is the nearest point of its block's grid
+    {E2M1 values} x S_b (ties to the even code), found by brute force over
+    the 16 codes; the tensor scale and block bytes follow their definitions."""
+    rng = np.random.default_rng(22)
+    v = (rng.standard_normal((5, 64)) * np.exp(rng.uniform(-3, 3, size=(5, 1)))).astype(np.float32)
+    v[2, 16:32] = 0.0                                     # an all-zero block
+    codes, sb, s, deq = M.quant_weight_nvfp4(v)
+    assert s == np.float32(np.float32(np.abs(v).max()) / np.float32(2688.0))
+    for r in range(5):
+        for b in range(4):
+            blk = v[r, 16 * b:16 * b + 16]
+            amax_b = np.float32(np.abs(blk).max())
+            want_sb = F.e4m3_encode_rne_nonneg(np.array([np.float32(amax_b / np.float32(6.0)) / s],
+                                                        dtype=np.float32))[0]
+            assert sb[r, b] == want_sb
+            S = np.float32(F.E4M3_TABLE[want_sb] * s)
+            for i in range(16):
+                if S == 0:
+                    assert codes[r, 16 * b + i] == 0
+                    continue
+                x = np.float32(blk[i] * np.float32(np.float32(1.0) / S))
+                dist = [abs(float(x) - F.e2m1_value(c)) for c in range(16)]
+                best = min(dist)
+                cands = [c for c in range(16) if dist[c] == best]
+                if x > 6.0:
+                    cands = [7]
+                if x < -6.0:
+                    cands = [15]
+                got = int(codes[r, 16 * b + i])
+                if len(cands) > 1:    # a tie: the even mantissa (code bit 0 clear); +-0 both fine
+                    cands = [c for c in cands if c & 1 == 0] or cands
+                assert got in cands or (F.e2m1_value(got) == 0.0 and best == abs(float(x))), (r, b, i, got, cands)
+
+
+def test_weight_quant_round_trip_and_zero():
+    rng = np.random.default_rng(23)
+    # values already on one NVFP4 grid (every 16-block reaches the 6.0 code,
+    # so every block scale byte is 448's) get their codes back exactly
+    codes = rng.integers(0, 16, size=(4, 32))
+    codes[:, 0] = 7
+    codes[:, 16] = 15                                     # -6.0
+    vals = F.E2M1_TABLE[codes] * 0.25
+    c, sb, s, deq = M.quant_weight_nvfp4(vals.astype(np.float32))
+    assert np.all(sb == 0x7E)
+    assert np.array_equal(F.E2M1_TABLE[c], F.E2M1_TABLE[codes])   # +-0 may swap sign codes
+    assert np.allclose(deq, vals, rtol=2.0 ** -22, atol=0)
+    z = np.zeros((3, 48), dtype=np.float32)
+    c, sb, s, deq = M.quant_weight_nvfp4(z)
+    assert s == 0 and not c.any() and not sb.any() and not deq.any()
