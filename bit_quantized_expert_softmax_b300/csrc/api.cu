@@ -133,8 +133,9 @@ Workspace carve(const Shape& s, char* base, size_t* total) {
     w.counters = cv.take<uint32_t>(flint::kCounters);
     w.gbar = cv.take<uint32_t>(64);
     w.dbg = cv.take<uint32_t>(64);
-    w.racc = cv.take<unsigned long long>((size_t)2 * flint::kFusedMaxT * s.E);
-    w.rnf = cv.take<uint32_t>((size_t)2 * flint::kFusedMaxT * s.E);
+    w.gbar8 = cv.take<unsigned long long>((size_t)flint::kGridGroups * flint::kGridGroupStride);
+    w.racc = cv.take<unsigned long long>((size_t)2 * flint::kRaccCopies * flint::kFusedMaxT * s.E);
+    w.rnf = cv.take<uint32_t>((size_t)2 * flint::kRaccCopies * flint::kFusedMaxT * s.E);
     w.status = cv.take<uint32_t>(1);
     *total = align_up(cv.off, 256);
     return w;
@@ -450,7 +451,8 @@ flint_status flint_moe_forward_stack(flint_moe* h, int layer0, int n_layers, voi
         // every layer in one persistent launch
         flint::FusedScratch fs{h->ws.logits, h->ws.hf, h->ws.gbar, h->ws.status};
         const cudaError_t e = flint::launch_decode_stack(h->s, h->stack_table + layer0, n_layers, x, T, fs,
-                                                         h->ws.racc, h->ws.rnf, h->n_sms, (cudaStream_t)stream);
+                                                         h->ws.gbar8, h->ws.racc, h->ws.rnf, h->n_sms,
+                                                         (cudaStream_t)stream);
         if (e == cudaSuccess) h->launches += 1;
         return cuda_status(e);
     }
@@ -586,8 +588,11 @@ flint_status flint_moe_status(flint_moe* h) {
         if (e == cudaSuccess && h->head_hs.counters != nullptr)
             e = cudaMemset(h->head_hs.counters, 0, flint::kHeadMaxT * sizeof(unsigned));
         // the decode stack's router accumulators are zero between launches
-        if (e == cudaSuccess) e = cudaMemset(h->ws.racc, 0, (size_t)2 * flint::kFusedMaxT * h->s.E * 8);
-        if (e == cudaSuccess) e = cudaMemset(h->ws.rnf, 0, (size_t)2 * flint::kFusedMaxT * h->s.E * 4);
+        const size_t nacc = (size_t)2 * flint::kRaccCopies * flint::kFusedMaxT * h->s.E;
+        if (e == cudaSuccess) e = cudaMemset(h->ws.racc, 0, nacc * 8);
+        if (e == cudaSuccess) e = cudaMemset(h->ws.rnf, 0, nacc * 4);
+        if (e == cudaSuccess)
+            e = cudaMemset(h->ws.gbar8, 0, (size_t)flint::kGridGroups * flint::kGridGroupStride * 8);
     }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return FLINT_ECUDA;

@@ -268,6 +268,12 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned 
     return v;
 }
 
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void red_release_gpu_add_u64(unsigned long long* p, unsigned long long v) {
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
@@ -349,6 +355,78 @@ __device__ __forceinline__ bool grid_sync(GridSync& gs, uint32_t* status) {
     }
     __syncthreads();
     return s_ok != 0;
+}
+
+// Grid barrier with the arrivals spread over kGridGroups counters, 128 bytes
+// apart: CTA b counts into counter b % kGridGroups, so at most
+// ceil(n_ctas / kGridGroups) same-address atomics queue at one L2 slice per
+// barrier instead of n_ctas. A waiter polls all counters. Each counter is a
+// multiple of its group's size between kernels. Same bounded waits as GridSync.
+constexpr int kGridGroups = 8;
+constexpr int kGridGroupStride = 16;   // unsigned long long: 128 bytes
+
+struct GridSync8 {
+    unsigned long long* count;   // [kGridGroups * kGridGroupStride]
+    unsigned long long base[kGridGroups];
+    uint32_t n_ctas;
+    uint32_t passed;
+};
+
+__device__ __forceinline__ uint32_t grid_group_size(uint32_t n_ctas, int i) {
+    return (n_ctas + kGridGroups - 1 - (uint32_t)i) / kGridGroups;
+}
+
+// Call by every thread at kernel start, before this CTA's first arrival.
+__device__ __forceinline__ GridSync8 grid_sync8_init(unsigned long long* count, uint32_t n_ctas) {
+    __shared__ unsigned long long s_base8[kGridGroups];
+    if (threadIdx.x < kGridGroups) {
+        const uint32_t n = grid_group_size(n_ctas, threadIdx.x);
+        const unsigned long long c = ld_acquire_gpu_u64(count + threadIdx.x * kGridGroupStride);
+        s_base8[threadIdx.x] = n ? c - c % n : c;   // fewer than n arrivals of this group can precede ours
+    }
+    __syncthreads();
+    GridSync8 g;
+    g.count = count;
+#pragma unroll
+    for (int i = 0; i < kGridGroups; ++i) g.base[i] = s_base8[i];
+    g.n_ctas = n_ctas;
+    g.passed = 0;
+    return g;
+}
+
+__device__ __forceinline__ bool grid_sync8(GridSync8& gs, uint32_t* status) {
+    __shared__ uint32_t s_ok8;
+    __syncthreads();
+    gs.passed += 1;
+    if (threadIdx.x == 0) {
+        red_release_gpu_add_u64(gs.count + (blockIdx.x % kGridGroups) * kGridGroupStride, 1ull);
+        uint32_t ok = 1, it = 0;
+        for (;;) {
+            bool done = true;
+            // relaxed polls (all eight in flight at once), then one fence:
+            // the fence after observing every release makes this an acquire
+#pragma unroll
+            for (int i = 0; i < kGridGroups; ++i) {
+                const unsigned long long target =
+                    gs.base[i] + (unsigned long long)grid_group_size(gs.n_ctas, i) * gs.passed;
+                const bool r = ld_relaxed_gpu_u64(gs.count + i * kGridGroupStride) >= target;
+                done = done & r;
+            }
+            if (done) {
+                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                break;
+            }
+            if (++it > kGridSpinLimit) {
+                atomicOr(status, kStatusTimeout);
+                ok = 0;
+                break;
+            }
+            if (it > 256) __nanosleep(32);
+        }
+        s_ok8 = ok;
+    }
+    __syncthreads();
+    return s_ok8 != 0;
 }
 
 }  // namespace flint

@@ -654,26 +654,29 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
 constexpr double kRaccScale = 4294967296.0;   // 2^32 units per logit
 
 struct StackArgs {
-    FusedArgs f;                     // shape, shared-memory plan, h scratch, barrier counter, status
+    FusedArgs f;                     // shape, shared-memory plan, h scratch, status
+    unsigned long long* gbar8;       // grid-barrier counters (GridSync8)
     const StackLayer* layers;        // [n] device table, in stack order
     int n;
     __nv_bfloat16* x;                // [T][d] hidden, updated in place
-    unsigned long long* racc;        // [2][T][E] fixed-point router logits
-    uint32_t* rnf;                   // [2][T][E] non-finite partial seen
+    unsigned long long* racc;        // [2][kRaccCopies][T][E] fixed-point router logits
+    uint32_t* rnf;                   // [2][kRaccCopies][T][E] non-finite partial seen
     int off_rslab;                   // shared-memory offset of the router slab [16][E] fp32
 };
 
 // Row owners: partial logits of 16 rows of x (xr[t][r], fp32 of bf16) with the
-// router slab (rslab[r][e] = W_r[e][16 dt + r]) into racc/rnf.
+// router slab (rslab[r][e] = W_r[e][16 dt + r]) into copy `copy` of
+// racc/rnf (the owners spread over kRaccCopies copies, so that fewer atomics
+// queue on one address; the readers add the copies, exactly).
 template <int TT>
-__device__ void router_partials(const StackArgs& sa, const float* rslab, const float* xr, int buf) {
+__device__ void router_partials(const StackArgs& sa, const float* rslab, const float* xr, int buf, int copy) {
     const int E = sa.f.E;
     for (int i = threadIdx.x; i < TT * E; i += kFThreads) {
         const int t = i / E, e = i - (i / E) * E;
         float p = 0.f;
 #pragma unroll
         for (int r = 0; r < 16; ++r) p = fmaf(rslab[r * E + e], xr[t * 16 + r], p);
-        const size_t o = ((size_t)buf * TT + t) * E + e;
+        const size_t o = (((size_t)buf * kRaccCopies + copy) * TT + t) * E + e;
         if (!(fabsf(p) <= 1.0e9f)) {   // non-finite, or beyond the fixed-point range
             atomicOr(sa.rnf + o, 1u);
         } else {
@@ -787,16 +790,16 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
             }
         }
     }
-    GridSync gsync = grid_sync_init(a0.bar_count, (uint32_t)G);   // includes a __syncthreads
+    GridSync8 gsync = grid_sync8_init(sa.gbar8, (uint32_t)G);   // includes a __syncthreads
     if (down_tile >= 0) {
         if (threadIdx.x < T * 16) {
             const int t = threadIdx.x / 16, r = threadIdx.x % 16;
             xr[t * 16 + r] = __bfloat162float(sa.x[(size_t)t * d + 16 * down_tile + r]);
         }
         wait_bar(i_rslab);
-        if (ok) router_partials<T>(sa, rslab, xr, 0);
+        if (ok) router_partials<T>(sa, rslab, xr, 0, down_tile % kRaccCopies);
     }
-    if (!grid_sync(gsync, a0.status)) ok = false;
+    if (!grid_sync8(gsync, a0.status)) ok = false;
 
 #pragma unroll 1
     for (int li = 0; li < sa.n && ok; ++li) {
@@ -804,20 +807,51 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
         const int buf = li & 1;
         const bool last = li + 1 == sa.n;
         // ------------------------------------------------------------ P1
-        for (int i = threadIdx.x; i < 3 * (E + 1); i += kFThreads) tss[i] = __ldg(al.tscale + i);
-        // logits of this layer
-        for (int i = threadIdx.x; i < T * E; i += kFThreads) {
-            const size_t o = (size_t)buf * T * E + i;
-            const long long q = (long long)__ldcg(sa.racc + o);
-            const float v = (float)((double)q * (1.0 / kRaccScale)) + __ldg(al.bias + (i % E));
-            lg[(i / E) * 256 + (i % E)] = __ldcg(sa.rnf + o) ? __int_as_float(0x7fc00000) : v;
+        // every independent load of the layer start is issued first: tensor
+        // scales, this thread's logit accumulators (all copies) and bias, and
+        // its elements of x_l (T <= 2, so at most T*E = 512 logits: one per thread)
+        const int n_ts = 3 * (E + 1);
+        const float ts0 = threadIdx.x < n_ts ? __ldg(al.tscale + threadIdx.x) : 0.f;
+        const float ts1 = threadIdx.x + kFThreads < n_ts ? __ldg(al.tscale + threadIdx.x + kFThreads) : 0.f;
+        long long qsum = 0;
+        uint32_t nf = 0;
+        float bias_v = 0.f;
+        if (threadIdx.x < T * E) {
+            unsigned long long qv[kRaccCopies];
+            uint32_t fv[kRaccCopies];
+#pragma unroll
+            for (int cpy = 0; cpy < kRaccCopies; ++cpy) {
+                const size_t o = (((size_t)buf * kRaccCopies + cpy) * T) * E + threadIdx.x;
+                qv[cpy] = __ldcg(sa.racc + o);
+                fv[cpy] = __ldcg(sa.rnf + o);
+            }
+            bias_v = __ldg(al.bias + (threadIdx.x % E));
+#pragma unroll
+            for (int cpy = 0; cpy < kRaccCopies; ++cpy) {
+                qsum += (long long)qv[cpy];
+                nf |= fv[cpy];
+            }
+        }
+        uint2 xraw[T][2];
+#pragma unroll
+        for (int t = 0; t < T; ++t)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int i = (threadIdx.x + q * kFThreads) * 4;
+                xraw[t][q] = i < d ? __ldcg(reinterpret_cast<const uint2*>(sa.x + (size_t)t * d + i)) : make_uint2(0u, 0u);
+            }
+        if (threadIdx.x < n_ts) tss[threadIdx.x] = ts0;
+        if (threadIdx.x + kFThreads < n_ts) tss[threadIdx.x + kFThreads] = ts1;
+        if (threadIdx.x < T * E) {
+            const float v = (float)((double)qsum * (1.0 / kRaccScale)) + bias_v;
+            lg[(threadIdx.x / E) * 256 + (threadIdx.x % E)] = nf ? __int_as_float(0x7fc00000) : v;
         }
         // the other accumulator is filled by this layer's P2; its last readers
         // finished before the previous layer's barriers
         if (b == 0) {
-            for (int i = threadIdx.x; i < T * E; i += kFThreads) {
-                sa.racc[(size_t)(buf ^ 1) * T * E + i] = 0ull;
-                sa.rnf[(size_t)(buf ^ 1) * T * E + i] = 0u;
+            for (int i = threadIdx.x; i < kRaccCopies * T * E; i += kFThreads) {
+                sa.racc[(size_t)(buf ^ 1) * kRaccCopies * T * E + i] = 0ull;
+                sa.rnf[(size_t)(buf ^ 1) * kRaccCopies * T * E + i] = 0u;
             }
         }
         // stage x_l as fp16, scaled per token, fragment-permuted
@@ -826,9 +860,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
             float amax = 0.f;
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                const int i = (threadIdx.x + q * kFThreads) * 4;
-                uint2 raw = make_uint2(0u, 0u);
-                if (i < d) raw = __ldcg(reinterpret_cast<const uint2*>(sa.x + (size_t)t * d + i));
+                const uint2 raw = xraw[t][q];
                 const float2 p0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
                 const float2 p1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
                 xv[q][0] = p0.x;
@@ -966,13 +998,13 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
                 }
             }
         }
-        if (ok && !grid_sync(gsync, a0.status)) ok = false;
+        if (ok && !grid_sync8(gsync, a0.status)) ok = false;
         if (!ok) break;
         // ------------------------------------------------------------ P2
         if (last && b == 0) {   // every reader of this layer's accumulators has passed the barrier
-            for (int i = threadIdx.x; i < T * E; i += kFThreads) {
-                sa.racc[(size_t)buf * T * E + i] = 0ull;
-                sa.rnf[(size_t)buf * T * E + i] = 0u;
+            for (int i = threadIdx.x; i < kRaccCopies * T * E; i += kFThreads) {
+                sa.racc[(size_t)buf * kRaccCopies * T * E + i] = 0ull;
+                sa.rnf[(size_t)buf * kRaccCopies * T * E + i] = 0u;
             }
         }
         if (down_tile >= 0) {
@@ -1069,10 +1101,10 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
                     mark_issued(i_dshared);
                 }
                 wait_bar(i_rslab);
-                if (ok) router_partials<T>(sa, rslab, xr, buf ^ 1);
+                if (ok) router_partials<T>(sa, rslab, xr, buf ^ 1, down_tile % kRaccCopies);
             }
         }
-        if (!last && ok && !grid_sync(gsync, a0.status)) ok = false;
+        if (!last && ok && !grid_sync8(gsync, a0.status)) ok = false;
     }
     drain();
 }
@@ -1174,8 +1206,8 @@ cudaError_t transpose_router(const float* w, float* wt, int E, int d, cudaStream
 }
 
 cudaError_t launch_decode_stack(const Shape& s, const StackLayer* layers_dev, int n_layers, __nv_bfloat16* x, int T,
-                                const FusedScratch& fs, unsigned long long* racc, uint32_t* rnf, int n_sms,
-                                cudaStream_t st) {
+                                const FusedScratch& fs, unsigned long long* gbar8, unsigned long long* racc,
+                                uint32_t* rnf, int n_sms, cudaStream_t st) {
     int n_slots = 0, offs[10], off_rslab = 0;
     const size_t smem = stack_plan(s, T, n_sms, &n_slots, offs, &off_rslab);
     if (smem == 0 || n_layers < 1 || T < 1 || T > kFusedMaxT) return cudaErrorInvalidValue;
@@ -1208,6 +1240,7 @@ cudaError_t launch_decode_stack(const Shape& s, const StackLayer* layers_dev, in
     sa.layers = layers_dev;
     sa.n = n_layers;
     sa.x = x;
+    sa.gbar8 = gbar8;
     sa.racc = racc;
     sa.rnf = rnf;
     sa.off_rslab = off_rslab;

@@ -82,8 +82,9 @@ struct Workspace {
     uint32_t* counters;   // [kCounters] arrival counters (self-resetting)
     uint32_t* gbar;       // [64]  grid-barrier count ([0]) and generation ([32])
     uint32_t* dbg;        // [64]  the timeout check's own barrier counter
-    unsigned long long* racc;   // [2][kFusedMaxT][E] fixed-point router logits of the decode stack
-    uint32_t* rnf;              // [2][kFusedMaxT][E] their non-finite flags
+    unsigned long long* gbar8;  // [kGridGroups * kGridGroupStride] the decode stack's grid-barrier counters
+    unsigned long long* racc;   // [2][kRaccCopies][kFusedMaxT][E] fixed-point router logits of the decode stack
+    uint32_t* rnf;              // [2][kRaccCopies][kFusedMaxT][E] their non-finite flags
     uint32_t* status;     // device status word
 };
 
@@ -97,6 +98,7 @@ struct FusedScratch {
 
 constexpr int kCounters = 1024;
 constexpr int kBucketChunk = 2048;      // assignments per bucketing CTA
+constexpr int kRaccCopies = 8;          // copies of the decode stack's router accumulators (atomics spread)
 constexpr int kSmallT = 64;             // fused router (logits + top-k + bucketing) up to this many tokens
 constexpr int kFuseCombineT = 8;        // combine in the down kernel's last CTA up to this many tokens
 
@@ -107,7 +109,7 @@ cudaError_t launch_router(const Shape& s, const LayerDev& L, const __nv_bfloat16
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int* idx, float* w,
                         cudaStream_t st);
 cudaError_t launch_bucket(const Shape& s, const int* idx, int T, const Workspace& ws,
-                          cudaStream_t st, int* n_launch);
+                          cudaStream_t st, int* n_launch, bool reset_hamax = true);
 
 // experts.cu: gate/up (one launch), then down + combine (one or two launches)
 cudaError_t launch_gateup(const Shape& s, const LayerDev& L, int T, const Workspace& ws,
@@ -124,8 +126,8 @@ cudaError_t prepare_decode_fused();   // once per device: shared-memory opt-in
 // its shared-memory plan does not fit
 size_t stack_smem_bytes(const Shape& s, int T, int n_sms);
 cudaError_t launch_decode_stack(const Shape& s, const StackLayer* layers_dev, int n_layers, __nv_bfloat16* x, int T,
-                                const FusedScratch& fs, unsigned long long* racc, uint32_t* rnf, int n_sms,
-                                cudaStream_t st);
+                                const FusedScratch& fs, unsigned long long* gbar8, unsigned long long* racc,
+                                uint32_t* rnf, int n_sms, cudaStream_t st);
 cudaError_t transpose_router(const float* w, float* wt, int E, int d, cudaStream_t st);
 cudaError_t launch_decode_fused(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
                                 __nv_bfloat16* out, const __nv_bfloat16* residual, const FusedScratch& fs,

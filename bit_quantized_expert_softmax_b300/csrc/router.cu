@@ -366,6 +366,7 @@ __global__ void __launch_bounds__(256) token_prep_kernel(RouterArgs a) {
 struct BucketArgs {
     const int* sel;
     int n, T, E, k, n_shared;
+    int reset_hamax;   // clear the per-position h maxima the 16-bit-activation expert kernels accumulate
     Workspace ws;
 };
 
@@ -401,8 +402,10 @@ __global__ void __launch_bounds__(256) bucket_scan_kernel(BucketArgs a, int n_ch
             run += h;
         }
     }
-    const int P = a.T * (a.k + a.n_shared);
-    for (int i = threadIdx.x; i < P; i += blockDim.x) a.ws.hamax[i] = 0u;
+    if (a.reset_hamax) {
+        const int P = a.T * (a.k + a.n_shared);
+        for (int i = threadIdx.x; i < P; i += blockDim.x) a.ws.hamax[i] = 0u;
+    }
 }
 
 __global__ void __launch_bounds__(256) bucket_place_kernel(BucketArgs a) {
@@ -441,8 +444,9 @@ RouterArgs make_args(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, 
 }  // namespace
 
 cudaError_t launch_bucket(const Shape& s, const int* idx, int T, const Workspace& ws,
-                          cudaStream_t st, int* n_launch) {
+                          cudaStream_t st, int* n_launch, bool reset_hamax) {
     BucketArgs b;
+    b.reset_hamax = reset_hamax ? 1 : 0;
     b.sel = idx;
     b.n = T * s.k;
     b.T = T;
@@ -487,7 +491,8 @@ cudaError_t launch_router(const Shape& s, const LayerDev& L, const __nv_bfloat16
     }
     token_prep_kernel<<<(T + 7) / 8, 256, 0, st>>>(a);
     *n_launch += 2;
-    return launch_bucket(s, ws.idx, T, ws, st, n_launch);
+    // the FP4 expert path (no fp16 staging) does not use the h maxima
+    return launch_bucket(s, ws.idx, T, ws, st, n_launch, stage_x16);
 }
 
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int* idx, float* w,
