@@ -120,6 +120,7 @@ Workspace carve(const Shape& s, char* base, size_t* total) {
     w.perm = cv.take<int>(Tm * s.k);
     w.inv = cv.take<int>(Tm * s.k);
     w.offsets = cv.take<int>(s.E + 1);
+    w.ecount = cv.take<int>(s.E);
     w.slot_expert = cv.take<int>(s.E + 1);
     w.slot_off = cv.take<int>(s.E + 1);
     w.slot_cnt = cv.take<int>(s.E + 1);
@@ -197,7 +198,7 @@ cudaError_t run_layer(flint_moe* h, int layer, const __nv_bfloat16* x, int T, __
     }
     if (T > flint::kSmallT && h->fp4_experts && L.prefill != nullptr) {
         prof_record(h, 0, st);
-        cudaError_t e = flint::launch_router(h->s, L, x, T, h->ws, st, &n, false);
+        cudaError_t e = flint::launch_router_fp4(h->s, L, x, T, h->ws, st, &n);
         prof_record(h, 1, st);
         if (e == cudaSuccess)
             e = flint::launch_prefill_experts(h->s, L, x, T, h->ws, static_cast<uint8_t*>(h->pws), h->s.max_tokens,
@@ -593,6 +594,7 @@ flint_status flint_moe_status(flint_moe* h) {
         if (e == cudaSuccess) e = cudaMemset(h->ws.rnf, 0, nacc * 4);
         if (e == cudaSuccess)
             e = cudaMemset(h->ws.gbar8, 0, (size_t)flint::kGridGroups * flint::kGridGroupStride * 8);
+        if (e == cudaSuccess) e = cudaMemset(h->ws.ecount, 0, (size_t)h->s.E * sizeof(int));
     }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return FLINT_ECUDA;
@@ -735,7 +737,7 @@ int flint_moe_forward_launches(const flint_moe* h, int T) {
     int n_slots = 0, offs[10];
     if (h->fused && flint::fused_smem_bytes(h->s, T, h->n_sms, &n_slots, offs) != 0) return 1;
     const int router = (T <= flint::kSmallT && h->s.d <= 2560) ? 1 : 2 + 3;
-    if (T > flint::kSmallT && h->fp4_experts) return router + 6;
+    if (T > flint::kSmallT && h->fp4_experts) return 2 + 6;   // logits, top-k and ranks; 6 expert-path kernels
     const int down = T <= flint::kFuseCombineT ? 1 : 2;
     return router + 1 + down;
 }

@@ -69,6 +69,7 @@ struct Workspace {
     int* perm;            // [Tm*k]  sorted position -> assignment t*k+j
     int* inv;             // [Tm*k]  assignment -> sorted position
     int* offsets;         // [E+1]
+    int* ecount;          // [E]    per-expert assignment counters of the FP4 path (zero between forwards)
     int* slot_expert;     // [E+1]  active slot -> expert (E = shared)
     int* slot_off;        // [E+1]  first position of the slot
     int* slot_cnt;        // [E+1]  positions of the slot
@@ -108,6 +109,9 @@ cudaError_t launch_router(const Shape& s, const LayerDev& L, const __nv_bfloat16
                           const Workspace& ws, cudaStream_t st, int* n_launch, bool stage_x16 = true);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int* idx, float* w,
                         cudaStream_t st);
+// the FP4 path's routing: logits, top-k and per-expert ranks (ws.inv, ws.ecount)
+cudaError_t launch_router_fp4(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T, const Workspace& ws,
+                              cudaStream_t st, int* n_launch);
 cudaError_t launch_bucket(const Shape& s, const int* idx, int T, const Workspace& ws,
                           cudaStream_t st, int* n_launch, bool reset_hamax = true);
 

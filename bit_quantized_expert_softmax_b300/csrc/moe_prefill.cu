@@ -6,7 +6,9 @@
 // E2M1_rne(v * (1/(E4M3(sb)*s)))). h is kept in fp32 between the two
 // projections and quantised from that value. Pipeline for one layer (after
 // routing and bucketing):
-//   plan      pad every expert's rows to a multiple of 128 (M-tile table)
+//   (routing: logits, top-k and each assignment's rank within its expert)
+//   plan      offsets, active slots, every slot's rows padded to a multiple
+//             of 128 (M-tile table)
 //   quant_x   quantise each token's x once and write it into the swizzled A
 //             tiles of its k routed experts and of the shared expert
 //   gemm1     gate/up: [rows x d] . [2f x d]^T, each 128-column tile holds 64
@@ -171,14 +173,14 @@ __device__ __forceinline__ void store_row_swizzled(uint8_t* blocks, int r, int l
 
 struct PrefillCtx {
     // routing / bucketing results
-    const int* perm;
+    int* perm;                // sorted position -> assignment (written by quant_x)
     const float* wts;
     const int* slot_expert;
     const int* slot_off;
     const int* slot_cnt;
     const int* meta;          // [0] active slots, [2] M-tiles (written by the plan kernel)
     const int* idx;           // [T][k] selected experts
-    const int* inv;           // [T*k] position of assignment t*k+j in bucketed order
+    int* inv;                 // [T*k] rank of assignment t*k+j within its expert, then (quant_x) its bucketed position
     // plan
     int* poff;                // [slots] first padded row of each slot
     int* slot_of;             // [E+1] slot of each active expert
@@ -203,18 +205,25 @@ struct PrefillCtx {
     int T, d, f, E, k;
 };
 
-// M-tile table: 128-row tiles of every active slot, padded offsets. One CTA
-// of 256 threads; slot i (< 256) is handled by thread i, slot 256 (the shared
-// expert when all 256 routed experts are active) by thread 0 afterwards.
-__global__ void __launch_bounds__(256) plan_kernel(PrefillCtx c, int* meta_rw) {
+// Counts -> offsets -> slots -> M-tile table, in one CTA of 256 threads
+// (expert e = thread e): the exclusive scan of the per-expert counts gives
+// the offsets and the active slots (experts with assignments, in expert
+// order, then the shared expert); each slot's rows are padded to whole
+// 128-row M-tiles. The counters are zeroed for the next forward.
+__global__ void __launch_bounds__(256) scan_plan_kernel(PrefillCtx c, int* __restrict__ ecount,
+                                                        int* __restrict__ offsets, int* __restrict__ slot_expert,
+                                                        int* __restrict__ slot_off, int* __restrict__ slot_cnt,
+                                                        int* __restrict__ meta) {
     __shared__ int wsum[8];
-    __shared__ int s_base[257];
-    __shared__ int s_total;
-    const int n_slots = c.meta[0];
+    __shared__ int s_cnt[258], s_exp[258], s_base[258];
+    __shared__ int s_ns, s_total;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int i = threadIdx.x;
-    const int mt = i < n_slots ? (c.slot_cnt[i] + kGM - 1) / kGM : 0;
-    int x = mt;
+    const int e = threadIdx.x;
+    const int cnt = e < c.E ? ecount[e] : 0;
+    if (e < c.E) ecount[e] = 0;
+    // exclusive scan of (count | active << 20)
+    int x = cnt | ((cnt > 0 ? 1 : 0) << 20);
+    const int v = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -232,29 +241,78 @@ __global__ void __launch_bounds__(256) plan_kernel(PrefillCtx c, int* meta_rw) {
         s_total = run;
     }
     __syncthreads();
+    const int excl = wsum[warp] + x - v;
+    const int off = excl & 0xfffff, slot = excl >> 20;
+    if (e < c.E) {
+        offsets[e] = off;
+        if (cnt > 0) {
+            slot_expert[slot] = e;
+            slot_off[slot] = off;
+            slot_cnt[slot] = cnt;
+            s_cnt[slot] = cnt;
+            s_exp[slot] = e;
+        }
+    }
+    if (threadIdx.x == 0) {
+        const int n_assign = s_total & 0xfffff;
+        const int ns = s_total >> 20;
+        offsets[c.E] = n_assign;
+        slot_expert[ns] = c.E;            // the shared expert: every token, after the routed positions
+        slot_off[ns] = c.T * c.k;
+        slot_cnt[ns] = c.T;
+        s_cnt[ns] = c.T;
+        s_exp[ns] = c.E;
+        s_ns = ns + 1;
+        meta[0] = ns + 1;
+        meta[1] = c.T;
+    }
+    __syncthreads();
+    // M-tiles per slot and their exclusive scan (slots 0..255 by thread; a
+    // 257th slot, possible only with all 256 experts active, by thread 0)
+    const int n_slots = s_ns;
+    const int i = threadIdx.x;
+    const int mt = i < n_slots ? (s_cnt[i] + kGM - 1) / kGM : 0;
+    x = mt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    __syncthreads();
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int w = 0; w < 8; ++w) {
+            const int t = wsum[w];
+            wsum[w] = run;
+            run += t;
+        }
+        s_total = run;
+    }
+    __syncthreads();
     s_base[i] = wsum[warp] + x - mt;
     if (threadIdx.x == 0) {
         int run = s_total;
         for (int sl = 256; sl < n_slots; ++sl) {
             s_base[sl] = run;
-            run += (c.slot_cnt[sl] + kGM - 1) / kGM;
+            run += (s_cnt[sl] + kGM - 1) / kGM;
         }
         s_total = run;
     }
     __syncthreads();
     for (int sl = threadIdx.x; sl < n_slots; sl += blockDim.x) {
         const int base = s_base[sl];
-        const int m_tiles = (c.slot_cnt[sl] + kGM - 1) / kGM;
+        const int m_tiles = (s_cnt[sl] + kGM - 1) / kGM;
         c.poff[sl] = base * kGM;
-        c.slot_of[c.slot_expert[sl]] = sl;
-        const int e = c.slot_expert[sl];
+        c.slot_of[s_exp[sl]] = sl;
         for (int m = 0; m < m_tiles; ++m) {
             c.mt_slot[base + m] = sl;
             c.mt_m[base + m] = m;
-            c.mt_e[base + m] = e;
+            c.mt_e[base + m] = s_exp[sl];
         }
     }
-    if (threadIdx.x == 0) meta_rw[2] = s_total;
+    if (threadIdx.x == 0) meta[2] = s_total;
 }
 
 // Quantise x[t] once per token (one warp per token) and write the row into
@@ -271,8 +329,15 @@ __global__ void __launch_bounds__(256, 3) quant_x_kernel(PrefillCtx c) {
         // that their dependent lookups overlap the load and the quantisation
         int my_rp = 0;
         if (lane < c.k) {
-            const int slot = c.slot_of[__ldg(c.idx + t * c.k + lane)];
-            my_rp = c.poff[slot] + (__ldg(c.inv + t * c.k + lane) - c.slot_off[slot]);
+            // the assignment's rank within its expert (token_rank_kernel) gives
+            // its padded row and its bucketed position
+            const int a = t * c.k + lane;
+            const int slot = c.slot_of[c.idx[a]];
+            const int rank = c.inv[a];
+            my_rp = c.poff[slot] + rank;
+            const int pos = c.slot_off[slot] + rank;
+            c.inv[a] = pos;
+            c.perm[pos] = a;
         } else if (lane == c.k) {
             my_rp = c.poff[shared_slot] + t;
         }
@@ -784,7 +849,7 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     c.f = s.f;
     c.E = s.E;
     c.k = s.k;
-    plan_kernel<<<1, 256, 0, st>>>(c, ws.meta);
+    scan_plan_kernel<<<1, 256, 0, st>>>(c, ws.ecount, ws.offsets, ws.slot_expert, ws.slot_off, ws.slot_cnt, ws.meta);
     quant_x_kernel<64><<<(T + 7) / 8 < 148 * 8 ? (T + 7) / 8 : 148 * 8, 256, 0, st>>>(c);
     mark(1);
     Gemm1 g1{c, 2 * s.f / kGN, s.d / kGK};

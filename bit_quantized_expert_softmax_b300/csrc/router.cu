@@ -418,6 +418,25 @@ __global__ void __launch_bounds__(256) bucket_place_kernel(BucketArgs a) {
     bucket_place_block(a.sel, a0, a1, a.E, base, wcnt, a.ws.perm, a.ws.inv, a.ws.status);
 }
 
+// Routing of the FP4 prefill path: top-k and renormalised weights per token
+// (a warp per token) and, for each of the token's k assignments, its rank
+// within its expert, taken with one atomic per assignment into ws.ecount and
+// left in ws.inv (the quantiser of x turns it into the bucketed position).
+// The order of the rows inside an expert is free on that path -- every row is
+// computed on its own and the combine reads rows by assignment -- so the
+// atomics' arrival order changes no result.
+__global__ void __launch_bounds__(256) token_rank_kernel(RouterArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= a.T) return;
+    topk_warp<false>(a.ws.logits + (size_t)t * a.E, a.E, a.k, a.ws.idx + t * a.k, a.ws.w + t * a.k, a.ws.status);
+    __syncwarp();
+    if (lane < a.k) {
+        const int e = a.ws.idx[t * a.k + lane];
+        a.ws.inv[t * a.k + lane] = atomicAdd(a.ws.ecount + e, 1);
+    }
+}
+
 __global__ void __launch_bounds__(256) topk_only_kernel(const float* logits, int T, int E, int k,
                                                         int* idx, float* w) {
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -493,6 +512,22 @@ cudaError_t launch_router(const Shape& s, const LayerDev& L, const __nv_bfloat16
     *n_launch += 2;
     // the FP4 expert path (no fp16 staging) does not use the h maxima
     return launch_bucket(s, ws.idx, T, ws, st, n_launch, stage_x16);
+}
+
+cudaError_t launch_router_fp4(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T, const Workspace& ws,
+                              cudaStream_t st, int* n_launch) {
+    RouterArgs a = make_args(s, L, x, T, ws);
+    a.stage_x16 = 0;
+    if (L.umma_router) {
+        const cudaError_t e = launch_router_umma(s, L, x, T, ws.logits, ws.status, st);
+        if (e != cudaSuccess) return e;
+    } else {
+        dim3 g1((T + kLTok - 1) / kLTok, (s.E + kLExp - 1) / kLExp);
+        router_logits_tiled<<<g1, 256, 0, st>>>(a);
+    }
+    token_rank_kernel<<<(T + 7) / 8, 256, 0, st>>>(a);
+    *n_launch += 2;
+    return cudaGetLastError();
 }
 
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int* idx, float* w,
