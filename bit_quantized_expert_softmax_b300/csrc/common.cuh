@@ -394,12 +394,18 @@ __device__ __forceinline__ GridSync8 grid_sync8_init(unsigned long long* count, 
     return g;
 }
 
-__device__ __forceinline__ bool grid_sync8(GridSync8& gs, uint32_t* status) {
-    __shared__ uint32_t s_ok8;
+// Split form: grid_arrive8 publishes this CTA's writes (ordered by its
+// __syncthreads) and counts it in; grid_wait8, after independent work, waits
+// for every CTA of the same pass. grid_sync8 = both.
+__device__ __forceinline__ void grid_arrive8(GridSync8& gs) {
     __syncthreads();
     gs.passed += 1;
+    if (threadIdx.x == 0) red_release_gpu_add_u64(gs.count + (blockIdx.x % kGridGroups) * kGridGroupStride, 1ull);
+}
+
+__device__ __forceinline__ bool grid_wait8(GridSync8& gs, uint32_t* status) {
+    __shared__ uint32_t s_ok8;
     if (threadIdx.x == 0) {
-        red_release_gpu_add_u64(gs.count + (blockIdx.x % kGridGroups) * kGridGroupStride, 1ull);
         uint32_t ok = 1, it = 0;
         for (;;) {
             bool done = true;
@@ -427,6 +433,11 @@ __device__ __forceinline__ bool grid_sync8(GridSync8& gs, uint32_t* status) {
     }
     __syncthreads();
     return s_ok8 != 0;
+}
+
+__device__ __forceinline__ bool grid_sync8(GridSync8& gs, uint32_t* status) {
+    grid_arrive8(gs);
+    return grid_wait8(gs, status);
 }
 
 }  // namespace flint

@@ -747,15 +747,18 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
                 if ((pend >> i) & 1u) mbar_wait_bounded(bars + i, (pend_par >> i) & 1u, a0.status);
         }
     };
-    auto layer_args = [&](int li) {
+    auto args_of = [&](const StackLayer& L) {
         FusedArgs al = a0;
-        const StackLayer L = sa.layers[li];
         al.codes = L.codes;
         al.scales = L.scales;
         al.tscale = L.tscale;
         al.bias = L.bias;
         return al;
     };
+    // the pointer table entries of the current and the next layer, each
+    // loaded one layer ahead so that no request waits on a table read
+    StackLayer Lc = sa.layers[0];
+    StackLayer Ln = sa.n > 1 ? sa.layers[1] : Lc;
 
     if (threadIdx.x == 0) {
 #pragma unroll 1
@@ -774,7 +777,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
     // ---- prologue: layer 0's routing-independent slabs, and its router
     // logits from the input rows (row owners)
     {
-        const FusedArgs al = layer_args(0);
+        const FusedArgs al = args_of(Lc);
         if (threadIdx.x == 0) {
             if (has_shared) {
                 issue_half<WFMT>(al, E, shared_unit, slots + (size_t)shared_slot * al.unit_bytes, bars + shared_slot);
@@ -785,7 +788,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
                 issue_down<WFMT>(al, E, down_tile, down, bars + i_dshared);
                 mark_issued(i_dshared);
                 mbar_arrive_expect_tx(bars + i_rslab, rslab_bytes);
-                bulk_g2s(rslab, sa.layers[0].router_t + (size_t)16 * down_tile * E, rslab_bytes, bars + i_rslab);
+                bulk_g2s(rslab, Lc.router_t + (size_t)16 * down_tile * E, rslab_bytes, bars + i_rslab);
                 mark_issued(i_rslab);
             }
         }
@@ -803,9 +806,10 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
 
 #pragma unroll 1
     for (int li = 0; li < sa.n && ok; ++li) {
-        const FusedArgs al = layer_args(li);
+        const FusedArgs al = args_of(Lc);
         const int buf = li & 1;
         const bool last = li + 1 == sa.n;
+        const StackLayer Lnn = li + 2 < sa.n ? sa.layers[li + 2] : Ln;   // used from the next layer on
         // ------------------------------------------------------------ P1
         // every independent load of the layer start is issued first: tensor
         // scales, this thread's logit accumulators (all copies) and bias, and
@@ -970,10 +974,11 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
             }
             if (ok && nw > 0) gateup_units<WFMT>(al, wave, nw, x16s, xinv, tss, acc);
         }
-        // requests that need no more than this point: this CTA's routed down
-        // slabs (P2), the next layer's shared half-unit (its slot is free
-        // now) and the next layer's router slab (read in P2)
-        __syncthreads();
+        // h is written: count this CTA in at the barrier, then, while the
+        // barrier completes, request this CTA's routed down slabs (P2), the
+        // next layer's shared half-unit (its slot is free now) and the next
+        // layer's router slab (read in P2)
+        if (ok) grid_arrive8(gsync);
         if (threadIdx.x == 0 && ok) {
             fence_proxy_async_smem();
             if (down_tile >= 0 && na > 0) {
@@ -984,7 +989,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
                 mark_issued(i_drouted);
             }
             if (!last) {
-                const FusedArgs an = layer_args(li + 1);
+                const FusedArgs an = args_of(Ln);
                 if (has_shared) {
                     issue_half<WFMT>(an, E, shared_unit, slots + (size_t)shared_slot * an.unit_bytes,
                                      bars + shared_slot);
@@ -992,13 +997,12 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
                 }
                 if (down_tile >= 0) {
                     mbar_arrive_expect_tx(bars + i_rslab, rslab_bytes);
-                    bulk_g2s(rslab, sa.layers[li + 1].router_t + (size_t)16 * down_tile * E, rslab_bytes,
-                             bars + i_rslab);
+                    bulk_g2s(rslab, Ln.router_t + (size_t)16 * down_tile * E, rslab_bytes, bars + i_rslab);
                     mark_issued(i_rslab);
                 }
             }
         }
-        if (ok && !grid_sync8(gsync, a0.status)) ok = false;
+        if (ok && !grid_wait8(gsync, a0.status)) ok = false;
         if (!ok) break;
         // ------------------------------------------------------------ P2
         if (last && b == 0) {   // every reader of this layer's accumulators has passed the barrier
@@ -1095,7 +1099,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
             if (!last) {
                 if (threadIdx.x == 0 && ok) {   // the next layer's shared down slab (slot 0 is free)
                     fence_proxy_async_smem();
-                    const FusedArgs an = layer_args(li + 1);
+                    const FusedArgs an = args_of(Ln);
                     mbar_arrive_expect_tx(bars + i_dshared, (uint32_t)an.down_bytes);
                     issue_down<WFMT>(an, E, down_tile, down, bars + i_dshared);
                     mark_issued(i_dshared);
@@ -1105,6 +1109,8 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
             }
         }
         if (!last && ok && !grid_sync8(gsync, a0.status)) ok = false;
+        Lc = Ln;
+        Ln = Lnn;
     }
     drain();
 }

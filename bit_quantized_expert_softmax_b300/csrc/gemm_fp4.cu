@@ -54,6 +54,7 @@ struct DebugGemm {
     static constexpr int kStages = 3;
     static constexpr int kNB = 1;
     static constexpr int kKPS = 2;
+    static constexpr bool kBPair = false;
     static constexpr int kEpiSmemPerWarp = 0;
     __device__ void epilogue_finish() const {}
     template <class Release>

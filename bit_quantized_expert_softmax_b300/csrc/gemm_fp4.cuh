@@ -64,7 +64,11 @@ struct Fp4Item {
 //           (256 columns: B0's tile, then B1's), single-buffered; per stage 96
 //           scale-factor columns at 256 + 96s. Each A k-tile then feeds two
 //           N-tiles: 3 blocks taken in per 2 block products instead of 4.
-// (kps: k-tiles per stage, P::kKPS)
+// (kps: k-tiles per stage, P::kKPS). With P::kBPair (kNB = 2 only) the two
+// B row tiles of an item are stored interleaved by k-tile in global memory
+// (B0 k-tile 0, B1 k-tile 0, B0 k-tile 1, ...), so one bulk copy brings both:
+// two copies per stage instead of three (the bulk-copy engine's throughput
+// per SM follows the number of copies in flight more than their size).
 __host__ __device__ constexpr int fp4_stage_bytes(int nb, int kps) { return (1 + nb) * kps * kGBlk; }
 __host__ __device__ constexpr int fp4_sf_cols(int nb, int kps) { return 16 * (1 + nb) * kps; }   // per stage
 
@@ -101,6 +105,10 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
     constexpr int kKPS = P::kKPS;
     constexpr int kStageB = fp4_stage_bytes(kNB, kKPS);
     constexpr int kSfCols = fp4_sf_cols(kNB, kKPS);
+    constexpr bool kBPair = P::kBPair;
+    static_assert(!kBPair || kNB == 2, "interleaved B needs two B tiles");
+    // block index inside a stage of B tile b, k-tile i (A k-tile i is block i)
+    auto bblk = [](int b, int i) { return kBPair ? kKPS + 2 * i + b : (1 + b) * kKPS + i; };
     constexpr int kNBuf = kNB == 1 ? 2 : 1;   // accumulator buffers
     __shared__ __align__(8) uint64_t full[kGStages], sfready[kGStages], empty[kGStages], accfull[2], accempty[2],
         mma_done;
@@ -150,9 +158,14 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
                     uint8_t* st = sm + s * kStageB;
                     mbar_arrive_expect_tx(&full[s], (uint32_t)((1 + kNB) * n * kGBlk));
                     bulk_g2s(st, w.a + (size_t)k0 * kGBlk, (uint32_t)(n * kGBlk), &full[s]);
-                    bulk_g2s(st + kKPS * kGBlk, w.b + (size_t)k0 * kGBlk, (uint32_t)(n * kGBlk), &full[s]);
-                    if constexpr (kNB == 2)
-                        bulk_g2s(st + 2 * kKPS * kGBlk, w.b2 + (size_t)k0 * kGBlk, (uint32_t)(n * kGBlk), &full[s]);
+                    if constexpr (kBPair) {
+                        bulk_g2s(st + kKPS * kGBlk, w.b + (size_t)2 * k0 * kGBlk, (uint32_t)(2 * n * kGBlk), &full[s]);
+                    } else {
+                        bulk_g2s(st + kKPS * kGBlk, w.b + (size_t)k0 * kGBlk, (uint32_t)(n * kGBlk), &full[s]);
+                        if constexpr (kNB == 2)
+                            bulk_g2s(st + 2 * kKPS * kGBlk, w.b2 + (size_t)k0 * kGBlk, (uint32_t)(n * kGBlk),
+                                     &full[s]);
+                    }
                 }
             }
             // every copy issued has landed before the CTA can exit, also when
@@ -191,7 +204,7 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
                         const uint32_t sfa = tmem + 256 + kSfCols * s + 16 * (1 + kNB) * i;
 #pragma unroll
                         for (int b = 0; b < kNB; ++b) {
-                            const uint64_t db = sdesc_kmajor_sw128(st + ((1 + b) * kKPS + i) * kGBlk);
+                            const uint64_t db = sdesc_kmajor_sw128(st + bblk(b, i) * kGBlk);
                             const uint32_t sfb = sfa + 16 * (1 + b);
 #pragma unroll
                             for (int j = 0; j < 4; ++j)   // 64 E2M1 = 32 bytes = 2 descriptor units per MMA
@@ -233,7 +246,7 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
                 const uint8_t* st = sm + s * kStageB;
                 for (int q = 0; q < (1 + kNB) * n; ++q) {
                     const int i = q / (1 + kNB), op = q % (1 + kNB);   // op 0: A, 1 + b: B tile b
-                    const uint8_t* sf = st + (op * kKPS + i) * kGBlk + kGTile;
+                    const uint8_t* sf = st + (op == 0 ? i : bblk(op - 1, i)) * kGBlk + kGTile;
                     uint4 r[4];
 #pragma unroll
                     for (int m1 = 0; m1 < 4; ++m1) r[m1] = *reinterpret_cast<const uint4*>(sf + (lane + 32 * m1) * 16);

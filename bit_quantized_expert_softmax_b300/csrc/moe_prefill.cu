@@ -357,99 +357,60 @@ __global__ void __launch_bounds__(256, 3) quant_x_kernel(PrefillCtx c) {
     }
 }
 
-// Quantise each h row (fp32, f = 512 elements) into the down GEMM's A tiles
-// and write the down GEMM's per-row epilogue data. Persistent: one CTA per
-// SM streams groups of 32 consecutive padded rows (64 KiB, contiguous in h)
-// into a ring of shared-memory stages with one bulk copy each, so the reads
-// run at copy-engine speed; each of the 8 warps quantises 4 rows of a group
-// from shared memory (lane l holds elements 16 l .. 16 l + 15). Padding rows
-// get prow = -1 and are not quantised (their products are discarded).
-constexpr int kQhRows = 4;                    // rows per warp per group
-constexpr int kQhGroup = 8 * kQhRows;         // rows per group (one bulk copy)
-constexpr int kQhStages = 3;
-constexpr int kQhGroupBytes = kQhGroup * 512 * 4;
-constexpr int kQhSmem = kQhStages * kQhGroupBytes + 128;
+// Quantise each h row (fp32, f elements) into the down GEMM's A tiles and
+// write the down GEMM's per-row epilogue data. A warp takes kQhRows
+// consecutive padded rows (one M-tile's): it loads all of their h first (the
+// buffer holds every row the grid covers, so the loads need no lookup), then
+// resolves the rows' slots and routing weights while those loads are in
+// flight. Warps past the actual rows return; padding rows get prow = -1.
+constexpr int kQhRows = 4;
 
-__global__ void __launch_bounds__(256, 1) quant_h_kernel(PrefillCtx c, uint32_t* status) {
-    extern __shared__ __align__(128) uint8_t qsm[];
-    __shared__ __align__(8) uint64_t full[kQhStages], empty[kQhStages];
+template <int EPL>
+__global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int KT = 512 / kGK;
-    const int n_groups = c.meta[2] * (kGM / kQhGroup);
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kQhStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 8);
-        }
-        mbar_fence_init();
-    }
-    __syncthreads();
-    uint32_t fills = 0;   // thread 0: groups requested
-    auto issue = [&](int g) {
-        const int s = fills % kQhStages;
-        const uint32_t use = fills / kQhStages;
-        if (use > 0 && !mbar_wait_bounded(&empty[s], (use - 1) & 1, status)) return false;
-        mbar_arrive_expect_tx(&full[s], kQhGroupBytes);
-        bulk_g2s(qsm + (size_t)s * kQhGroupBytes, c.h + (size_t)g * kQhGroup * 512, kQhGroupBytes, &full[s]);
-        ++fills;
-        return true;
-    };
-    bool ok = true;
-    if (threadIdx.x == 0) {
-        for (int j = 0; j < kQhStages && ok; ++j) {
-            const int g = blockIdx.x + j * gridDim.x;
-            if (g < n_groups) ok = issue(g);
-        }
-    }
-    uint32_t used = 0;
-    for (int g = blockIdx.x; g < n_groups; g += gridDim.x, ++used) {
-        const int s = used % kQhStages;
-        const bool got = mbar_wait_bounded(&full[s], (used / kQhStages) & 1, status);
-        if (!__all_sync(0xffffffffu, got)) break;
-        const int row0 = g * kQhGroup + warp * kQhRows;
-        const int mt = row0 / kGM, r0 = row0 % kGM;
-        const int slot = __ldg(c.mt_slot + mt), m = __ldg(c.mt_m + mt);
-        // lane i < kQhRows: position and epilogue scale of row row0 + i (-1: padding)
-        int p = -1;
-        float yscale_w = 0.f;
-        if (lane < kQhRows) {
-            const int q = m * kGM + r0 + lane;
-            if (q < __ldg(c.slot_cnt + slot)) {
-                p = __ldg(c.slot_off + slot) + q;
-                const float wr = p < c.T * c.k ? __ldg(c.wts + __ldg(c.perm + p)) : 1.0f;
-                yscale_w = __ldg(c.tscale + __ldg(c.slot_expert + slot) * 3 + 2) * wr;
-            }
-        }
-        const float4* rows = reinterpret_cast<const float4*>(qsm + (size_t)s * kQhGroupBytes) + (size_t)warp * kQhRows * 128;
-        uint8_t* blocks = c.a2 + (size_t)mt * KT * kGBlk;
+    const int KT = c.f / kGK;
+    // last CTA first: the gate/up GEMM wrote the high rows last
+    const int row0 = ((gridDim.x - 1 - blockIdx.x) * 8 + warp) * kQhRows;
+    float4 raw[kQhRows][EPL / 4];
 #pragma unroll
-        for (int i = 0; i < kQhRows; ++i) {
-            const int pi = __shfl_sync(0xffffffffu, p, i);
-            const float ys = __shfl_sync(0xffffffffu, yscale_w, i);
-            if (pi < 0) {
-                if (lane == 0) c.prow[row0 + i] = -1;
-                continue;
-            }
-            float4 raw[4];
+    for (int i = 0; i < kQhRows; ++i) {
+        const float4* hr = reinterpret_cast<const float4*>(c.h + (size_t)(row0 + i) * c.f + lane * EPL);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) raw[j] = rows[i * 128 + lane * 4 + j];
-            uint32_t codes[2];
-            uint32_t sb = 0;
-            const float s_t = quant_row_f32<16>(raw, codes, sb);
-            store_row_swizzled<16>(blocks, r0 + i, lane, codes, sb);
-            if (lane == 0) {
-                c.prow[row0 + i] = pi;
-                c.yscale[row0 + i] = s_t * ys;
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);   // this warp is done with the stage
-        if (threadIdx.x == 0 && ok) {
-            const int gn = g + kQhStages * gridDim.x;
-            if (gn < n_groups) ok = issue(gn);
+        for (int j = 0; j < EPL / 4; ++j) raw[i][j] = __ldcs(hr + j);
+    }
+    const int n_rows = c.meta[2] * kGM;
+    if (row0 >= n_rows) return;
+    const int mt = row0 / kGM, r0 = row0 % kGM;
+    const int slot = c.mt_slot[mt], m = c.mt_m[mt];
+    // lane i < kQhRows: position and epilogue scale of row row0 + i (-1: padding)
+    int p = -1;
+    float yscale_w = 0.f;
+    if (lane < kQhRows) {
+        const int q = m * kGM + r0 + lane;
+        if (q < c.slot_cnt[slot]) {
+            p = c.slot_off[slot] + q;
+            const float wr = p < c.T * c.k ? c.wts[__ldg(c.perm + p)] : 1.0f;
+            yscale_w = c.tscale[c.slot_expert[slot] * 3 + 2] * wr;
         }
     }
-    if (threadIdx.x == 0) drain_ring(full, kQhStages, fills, status);   // no copy still in flight at exit
+    uint8_t* blocks = c.a2 + (size_t)mt * KT * kGBlk;
+#pragma unroll
+    for (int i = 0; i < kQhRows; ++i) {
+        const int pi = __shfl_sync(0xffffffffu, p, i);
+        const float ys = __shfl_sync(0xffffffffu, yscale_w, i);
+        if (pi < 0) {   // padding row: its codes are never read back
+            if (lane == 0) c.prow[row0 + i] = -1;
+            continue;
+        }
+        uint32_t codes[EPL / 8];
+        uint32_t sb = 0;
+        const float s_t = quant_row_f32<EPL>(raw[i], codes, sb);
+        store_row_swizzled<EPL>(blocks, r0 + i, lane, codes, sb);
+        if (lane == 0) {
+            c.prow[row0 + i] = pi;
+            c.yscale[row0 + i] = s_t * ys;
+        }
+    }
 }
 
 // gate/up GEMM: item = (M-tile, pair of N-tiles); N-tile nt holds 64 gate
@@ -459,17 +420,18 @@ __global__ void __launch_bounds__(256, 1) quant_h_kernel(PrefillCtx c, uint32_t*
 struct Gemm1 {
     PrefillCtx c;
     int NT, KT;   // N-tiles (2f/128) and k-tiles (d/256)
-    static constexpr int kStages = 4;
+    static constexpr int kStages = 2;
     static constexpr int kNB = 2;
-    static constexpr int kKPS = 1;   // one A k-tile and the two B k-tiles per stage
+    static constexpr int kKPS = 2;          // two A k-tiles and the pair's four B k-tiles per stage
+    static constexpr bool kBPair = true;    // the pair's B tiles interleaved by k-tile: one copy
     __device__ int n_items() const { return c.meta[2] * (NT / 2); }
     __device__ void item(int i, Fp4Item& w) const {
         const int np = NT / 2;
         const int mt = i / np, pair = i % np;
         const int e = c.mt_e[mt];
         w.a = c.a1 + (size_t)mt * KT * kGBlk;
-        w.b = c.w1 + ((size_t)e * NT + 2 * pair) * KT * kGBlk;
-        w.b2 = w.b + (size_t)KT * kGBlk;
+        w.b = c.w1 + ((size_t)e * NT + 2 * pair) * KT * kGBlk;   // the pair's 2*KT interleaved blocks
+        w.b2 = nullptr;
         w.kt = KT;
         w.m = mt;
         w.n = pair;
@@ -667,8 +629,10 @@ __global__ void __launch_bounds__(256) combine_kernel(PrefillCtx c, __nv_bfloat1
 
 // Gate/up weights -> blocks (swizzled tile + scales) with gate and up
 // interleaved per 64 rows: N-tile nt rows 0..63 = gate rows 64nt.., rows
-// 64..127 = up rows 64nt.. Down weights -> plain row tiles of blocks. One
-// thread per 16 bytes of codes.
+// 64..127 = up rows 64nt..; N-tiles 2p and 2p+1 form pair p, whose blocks are
+// stored interleaved by k-tile (nt 2p k-tile kt, nt 2p+1 k-tile kt, ...).
+// Down weights -> plain row tiles of blocks. One thread per 16 bytes of
+// codes.
 __global__ void pack_expert_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
                                    uint8_t* __restrict__ w1, uint8_t* __restrict__ w2, int n_slots, int d, int f,
                                    size_t cpm, size_t spm) {
@@ -689,7 +653,7 @@ __global__ void pack_expert_kernel(const uint8_t* __restrict__ codes, const uint
         if (mat < 2) {
             const int nt = row / 64;
             r = (row % 64) + 64 * mat;
-            blk = w1 + (((size_t)e * NT1 + nt) * KT1 + kt) * kGBlk;
+            blk = w1 + ((((size_t)e * (NT1 / 2) + nt / 2) * KT1 + kt) * 2 + (nt & 1)) * kGBlk;
         } else {
             const int nt = row / kGN;
             r = row % kGN;
@@ -799,7 +763,6 @@ cudaError_t prepare_prefill_fp4() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fp4_gemm_resa_kernel<Gemm2R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  fp4_gemm_resa_smem<Gemm2R>());
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(quant_h_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQhSmem);
     if (e != cudaSuccess) cudaGetLastError();
     return e;
 }
@@ -855,8 +818,8 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     Gemm1 g1{c, 2 * s.f / kGN, s.d / kGK};
     fp4_gemm_kernel<Gemm1><<<148, kGThreads, fp4_gemm_smem<Gemm1>(), st>>>(g1, ws.status);
     mark(2);
-    static_assert(kGM % kQhGroup == 0, "a group of rows stays inside one M-tile");
-    quant_h_kernel<<<148, 256, kQhSmem, st>>>(c, ws.status);
+    static_assert(kGM % (8 * kQhRows) == 0, "a CTA's rows stay inside one M-tile");
+    quant_h_kernel<16><<<(unsigned)(rt * kGM / (8 * kQhRows)), 256, 0, st>>>(c);
     mark(3);
     static_assert(Gemm2R::kNT * kGN == 2048 && kRKT * kGK == 512, "the Flint shape (d = 2048, f = 512)");
     Gemm2R g2{Gemm2{c, s.d / kGN, s.f / kGK}};
