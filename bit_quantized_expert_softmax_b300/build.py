@@ -20,7 +20,7 @@ LIB = os.path.join(HERE, "libflint_moe.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
 SOURCES = ["api.cu", "router.cu", "experts.cu", "repack.cu", "prefill_fp4.cu", "gemm_fp4.cu", "decode_fused.cu", "bucket_noalloc.cu",
-           "moe_prefill.cu", "lm_head.cu", "debug_wait.cu", "fp4_peak.cu"]
+           "moe_prefill.cu", "lm_head.cu", "debug_wait.cu", "fp4_peak.cu", "attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -28,6 +28,12 @@ class flint_moe_config(ctypes.Structure):
                 ("max_tokens", ctypes.c_int), ("n_layers", ctypes.c_int), ("device", ctypes.c_int)]
 
 
+class flint_moe_attn_config(ctypes.Structure):
+    _fields_ = [("n_heads", ctypes.c_int), ("n_kv", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("window", ctypes.c_int), ("cap", ctypes.c_int), ("rope", ctypes.c_int),
+                ("rope_theta", ctypes.c_float), ("eps", ctypes.c_float)]
+
+
 class flint_moe_weights(ctypes.Structure):
     _fields_ = [("router", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
                 ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
@@ -79,6 +85,8 @@ def lib() -> ctypes.CDLL:
                                               ctypes.POINTER(ctypes.c_double)]),
             "flint_moe_debug_wait_timeout": (_I, [_P, _I, ctypes.c_uint32, _P]),
             "flint_moe_quantize_nvfp4": (_I, [_P, _I, _I, _P, _P, _P, _P]),
+            "flint_moe_attn_decode": (_I, [ctypes.POINTER(flint_moe_attn_config), _I, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                       _P, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -252,6 +260,15 @@ def flint_moe_probe_fp4_peak(n: int, iters: int) -> tuple[float, float]:
     flops = ctypes.c_double(0.0)
     _check(lib().flint_moe_probe_fp4_peak(n, iters, ctypes.byref(ms), ctypes.byref(flops)), "flint_moe_probe_fp4_peak")
     return float(ms.value), float(flops.value)
+
+
+def flint_moe_attn_decode(n_heads: int, n_kv: int, window: int, cap: int, rope: bool, B: int, q, k, v, k_cache, v_cache,
+                      pos, q_norm_w, k_norm_w, sinks, out, rope_theta: float = 10000.0, eps: float = 1e-6,
+                      stream=None) -> None:
+    cfg = flint_moe_attn_config(n_heads, n_kv, 128, window, cap, 1 if rope else 0, rope_theta, eps)
+    _check(lib().flint_moe_attn_decode(ctypes.byref(cfg), B, _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(pos), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(sinks), _ptr(out),
+                                   _stream(stream)), "flint_moe_attn_decode")
 
 
 def flint_moe_quantize_nvfp4(w, R: int, K: int, codes, scales, tensor_scale, stream=None) -> None:

@@ -250,6 +250,48 @@ FLINT_API flint_status flint_moe_debug_act_quant(const void* x_dev, int T, int K
 FLINT_API flint_status flint_moe_quantize_nvfp4(const void* w_dev, int R, int K, uint8_t* codes_dev,
                                                 uint8_t* scales_dev, float* tensor_scale_dev, void* stream);
 
+/* ---- decode attention ------------------------------------------------------
+ * One decode step of a Flint-shaped attention layer ("Recursive Flint
+ * 40B-A2.5B", section "The architecture is an argument about memory
+ * bandwidth", Attention and Position-encoding bullets): 32 query heads and 4
+ * key-value heads of dimension 128; 35 sliding-window layers with a 513-token
+ * window (the current token and the 512 before it) and 14 full-attention
+ * layers; rotary positions on the sliding-window layers only; per-head QK
+ * RMSNorm and learned per-head attention sinks. The blog gives no formulas;
+ * the readings: q_h <- rmsnorm(q_h) * q_norm_w and k <- rmsnorm(k) * k_norm_w
+ * over the head dimension (eps); rotation of the pairs (i, i+64) by
+ * pos * theta^(-i/64) when rope = 1; scores q.k / sqrt(128) over the window's
+ * keys (query head h reads key head h / 8); the sink logit joins the softmax
+ * denominator only. */
+typedef struct {
+    int n_heads;       /* query heads: 8 per key-value head (32 in Flint) */
+    int n_kv;          /* key-value heads (4 in Flint), 1..64 */
+    int head_dim;      /* 128 */
+    int window;        /* positions attended, the current one included: 513 for sliding-window layers, 0 = all */
+    int cap;           /* cache slots per sequence and key-value head; position p lives in slot p % cap;
+                          cap >= window for sliding-window layers, cap > every position for full attention */
+    int rope;          /* 1: rotary positions (sliding-window layers); 0: none */
+    float rope_theta;  /* rotary base (10000 here; the blog does not give it) */
+    float eps;         /* RMSNorm epsilon (1e-6) */
+} flint_moe_attn_config;
+
+/* For each of B sequences, attend its new token at position pos_dev[b] (int32,
+ * >= 0): q_dev bf16 [B][n_heads][128], k_dev and v_dev bf16 [B][n_kv][128]
+ * (the projections, before norm and rotation); k_cache_dev and v_cache_dev
+ * bf16 [B][n_kv][cap][128] (16-byte aligned) hold the keys (normed, rotated)
+ * and values of earlier positions; q_norm_w_dev and k_norm_w_dev fp32 [128];
+ * sinks_dev fp32 [n_heads]; out_dev bf16 [B][n_heads][128]. Reads the cache
+ * slots of positions pos-1 down to the window's start, then writes the new
+ * key (normed, rotated) and value, bf16, to slot pos % cap. The current token
+ * attends to its own key and value unrounded. All pointers are device
+ * pointers; asynchronous on `stream`. Errors: FLINT_EINVAL (configuration,
+ * B < 0, NULL, misaligned cache), FLINT_ECUDA. */
+FLINT_API flint_status flint_moe_attn_decode(const flint_moe_attn_config* cfg, int B, const void* q_dev, const void* k_dev,
+                                         const void* v_dev, void* k_cache_dev, void* v_cache_dev,
+                                         const int32_t* pos_dev, const float* q_norm_w_dev,
+                                         const float* k_norm_w_dev, const float* sinks_dev, void* out_dev,
+                                         void* stream);
+
 /* ---- the 4-bit output head and its sampler ---------------------------------
  * The Flint blog ("Recursive Flint 40B-A2.5B", section "The quantisation
  * recipe is the most transferable part") ships the output layer (lm_head)
