@@ -761,6 +761,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-subrecords", action="store_true",
                     help="time only the headline workload (default with --config other than 5)")
+    ap.add_argument("--attn", action="store_true",
+                    help="one decode step of a sliding-window attention layer (64 sequences) instead of an MoE config")
     ap.add_argument("--head", action="store_true",
                     help="the 4-bit output head (146,432 x 2048 NVFP4) and its sampler instead of an MoE config")
     args = ap.parse_args()
@@ -768,6 +770,9 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.head:
         head_main(args)
+        return
+    if args.attn:
+        attn_main(args)
         return
     cfg = synth.CONFIGS[args.config]
     if args.steps is None:
@@ -816,6 +821,153 @@ def main():
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds, act_quant=bool(res["plan"] & 2),
                                                 single_tokens=512)
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+ATTN_B, ATTN_POS, ATTN_CAP = 64, 4096, 520   # sequences, position of the decoded token, cache slots
+
+
+def run_attn(args, world, local):
+    """One decode step of a sliding-window attention layer for ATTN_B
+    sequences whose window is full (position 4096: 512 cached positions plus
+    the new token), with L2 flushed between steps."""
+    import torch
+    from bit_quantized_expert_softmax_b300 import build
+    build.build()
+    from bit_quantized_expert_softmax_b300 import flint_moe as fm
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    rng = np.random.default_rng(0)
+    B, H, KV, cap = ATTN_B, 32, 4, ATTN_CAP
+
+    def bf16(shape, scale=1.0):
+        return (torch.from_numpy(rng.standard_normal(shape).astype(np.float32) * scale)
+                .to(torch.bfloat16).to(device))
+    q, k, v = bf16((B, H, 128)), bf16((B, KV, 128)), bf16((B, KV, 128))
+    kc, vc = bf16((B, KV, cap, 128)), bf16((B, KV, cap, 128))
+    wq = torch.from_numpy((1 + 0.1 * rng.standard_normal(128)).astype(np.float32)).to(device)
+    wk = torch.from_numpy((1 + 0.1 * rng.standard_normal(128)).astype(np.float32)).to(device)
+    sinks = torch.from_numpy(rng.standard_normal(H).astype(np.float32)).to(device)
+    pos = torch.full((B,), ATTN_POS, dtype=torch.int32, device=device)
+    out = torch.empty((B, H, 128), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.current_stream(device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
+
+    def step(qq=q, oo=out):
+        fm.flint_moe_attn_decode(H, KV, 513, cap, True, B, qq, k, v, kc, vc, pos, wq, wk, sinks, oo, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    st_ev = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    en_ev = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    with ClockSampler(gpu_id_for(device)) as clk:
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < args.soak:
+            for _ in range(50):
+                flush.zero_()
+                step()
+            torch.cuda.synchronize()
+        torch.cuda._sleep(50_000_000)
+        for i in range(K):
+            flush.zero_()
+            st_ev[i].record(stream)
+            step()
+            en_ev[i].record(stream)
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in zip(st_ev, en_ev)]
+    ms = max_over_ranks(statistics.mean(step_ms), world, device)
+    # end to end: q, k, v from pinned host memory, the output back
+    q_pin = q.cpu().pin_memory()
+    o_pin = torch.empty_like(out, device="cpu").pin_memory()
+    q_dev = torch.empty_like(q)
+    Ke = min(K, 2000)
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    for i in range(Ke + 3):
+        flush.zero_()
+        j = i - 3
+        if j >= 0:
+            es[j].record(stream)
+        q_dev.copy_(q_pin, non_blocking=True)
+        step(q_dev, out)
+        o_pin.copy_(out, non_blocking=True)
+        if j >= 0:
+            ee[j].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(es, ee)), world, device)
+    kv_bytes = B * KV * 512 * 128 * 2 * 2              # cached keys and values read
+    io_bytes = B * (H + 2 * KV) * 128 * 2 + B * H * 128 * 2 + B * KV * 128 * 2 * 2
+    return {"ms": ms, "step_ms": step_ms, "bytes": kv_bytes + io_bytes, "clocks": clk.summary(), "e2e_ms": e2e_ms,
+            "B": B, "h2d": B * H * 128 * 2, "d2h": B * H * 128 * 2}
+
+
+def attn_cpu_baseline(seconds: float) -> dict:
+    import oracle.attention as OA
+    rng = np.random.default_rng(1)
+    cap = ATTN_CAP
+    q = rng.standard_normal((32, 128))
+    k = rng.standard_normal((4, 128))
+    v = rng.standard_normal((4, 128))
+    kc = oracle_bits(rng.standard_normal((4, cap, 128)))
+    vc = oracle_bits(rng.standard_normal((4, cap, 128)))
+    w = np.ones(128)
+    sinks = rng.standard_normal(32)
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds or n == 0:
+        OA.decode_step(q, k, v, kc, vc, ATTN_POS, w, w, sinks)
+        n += 1
+    el = time.perf_counter() - t0
+    return {"value": n / el, "unit": "tokens/s", "cores": blas_threads(), "nproc": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} single-sequence decode steps through the float64 oracle in {el:.1f} s"}
+
+
+def oracle_bits(v):
+    import oracle
+    return oracle.formats.bf16_bits(oracle.formats.bf16_round(v))
+
+
+def attn_main(args):
+    import torch
+    if args.steps is None:
+        args.steps = 2000
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    r = run_attn(args, world, local)
+    if rank == 0:
+        peaks = measured_peaks()
+        hbm = peaks["hbm_gbs"]
+        achieved = r["bytes"] / (r["ms"] * 1e-3) / 1e9
+        line = {
+            "metric": "attention decode tokens/s", "value": world * r["B"] / (r["ms"] / 1e3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 cache, f32 math",
+            "data": "synthetic",
+            "config": {"workload": f"sliding-window attention layer decode: {r['B']} sequences at position {ATTN_POS} "
+                                   f"(513-token window full), 32 query / 4 key-value heads of 128, QK RMSNorm, "
+                                   f"rotary positions, sinks, bf16 cache",
+                       "tokens_per_step": r["B"],
+                       "l2": "flushed between steps (memset of 2x L2, outside the per-step events)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": None, "kernel": "attn_decode_kernel (one step, the whole layer)",
+                         "algorithmic_bytes_per_launch": r["bytes"], "avg_launch_us": r["ms"] * 1e3,
+                         "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
+                         else "fallback 6.4 TB/s"},
+            "e2e": {"value": world * r["B"] / (r["e2e_ms"] / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
+                    "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": args.steps, "clocks": r["clocks"],
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = attn_cpu_baseline(min(args.cpu_seconds, 10.0))
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
