@@ -858,41 +858,45 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
                 sa.rnf[(size_t)(buf ^ 1) * kRaccCopies * T * E + i] = 0u;
             }
         }
-        // stage x_l as fp16, scaled per token, fragment-permuted
-        for (int t = 0; t < T; ++t) {
-            float xv[2][4];
-            float amax = 0.f;
+        // x_l as fp16, scaled per token, fragment-permuted: staged after the
+        // routed slabs have been requested, so that it overlaps their latency
+        auto stage_x = [&]() {
+            for (int t = 0; t < T; ++t) {
+                float xv[2][4];
+                float amax = 0.f;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const uint2 raw = xraw[t][q];
-                const float2 p0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-                const float2 p1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-                xv[q][0] = p0.x;
-                xv[q][1] = p0.y;
-                xv[q][2] = p1.x;
-                xv[q][3] = p1.y;
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(p0.x), fabsf(p0.y)), fmaxf(fabsf(p1.x), fabsf(p1.y))));
-            }
-            amax = warp_max(amax);
-            if (lane == 0) rpart[warp] = amax;
-            __syncthreads();
-            float m = 0.f;
-#pragma unroll
-            for (int w = 0; w < kFWarps; ++w) m = fmaxf(m, rpart[w]);
-            const float mult = f16_range_mult(m);
-            __half2* xrow = reinterpret_cast<__half2*>(x16s + (size_t)t * d);
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int i = (threadIdx.x + q * kFThreads) * 4;
-                if (i < d) {
-                    __half2* tile = xrow + ((i & ~127) >> 1);
-                    tile[kperm_pos(i & 127) >> 1] = __floats2half2_rn(xv[q][0] * mult, xv[q][1] * mult);
-                    tile[kperm_pos((i & 127) + 2) >> 1] = __floats2half2_rn(xv[q][2] * mult, xv[q][3] * mult);
+                for (int q = 0; q < 2; ++q) {
+                    const uint2 raw = xraw[t][q];
+                    const float2 p0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+                    const float2 p1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+                    xv[q][0] = p0.x;
+                    xv[q][1] = p0.y;
+                    xv[q][2] = p1.x;
+                    xv[q][3] = p1.y;
+                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(p0.x), fabsf(p0.y)), fmaxf(fabsf(p1.x), fabsf(p1.y))));
                 }
+                amax = warp_max(amax);
+                if (lane == 0) rpart[warp] = amax;
+                __syncthreads();
+                float m = 0.f;
+#pragma unroll
+                for (int w = 0; w < kFWarps; ++w) m = fmaxf(m, rpart[w]);
+                const float mult = f16_range_mult(m);
+                __half2* xrow = reinterpret_cast<__half2*>(x16s + (size_t)t * d);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int i = (threadIdx.x + q * kFThreads) * 4;
+                    if (i < d) {
+                        __half2* tile = xrow + ((i & ~127) >> 1);
+                        tile[kperm_pos(i & 127) >> 1] = __floats2half2_rn(xv[q][0] * mult, xv[q][1] * mult);
+                        tile[kperm_pos((i & 127) + 2) >> 1] = __floats2half2_rn(xv[q][2] * mult, xv[q][3] * mult);
+                    }
+                }
+                if (threadIdx.x == 0) xinv[t] = 1.0f / mult;
+                __syncthreads();
             }
-            if (threadIdx.x == 0) xinv[t] = 1.0f / mult;
-            __syncthreads();
-        }
+        };
+        __syncthreads();   // the logits are in shared memory
         if (warp < T) topk_warp<false>(lg + warp * 256, E, k, sel + warp * 8, wsel + warp * 8, b == 0 ? a0.status : nullptr);
         __syncthreads();
         if (T == 1) {
@@ -933,7 +937,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
         const int na = *nact;
         const int n_units = na * units_per_expert;
         const int n_rs = a0.n_slots - 1;
-        bool shared_pending = has_shared, wave_issued = false;
+        bool shared_pending = has_shared, wave_issued = false, x_staged = false;
         for (int u0 = b;;) {
             if (!wave_issued && u0 < n_units && ok) {
                 __syncthreads();   // the previous wave's slots have been read
@@ -950,6 +954,10 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
                     }
                 }
                 wave_issued = true;
+            }
+            if (!x_staged) {
+                stage_x();
+                x_staged = true;
             }
             UnitRef wave[kMaxWaveUnits];
             int nw = 0;

@@ -420,18 +420,18 @@ __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
 struct Gemm1 {
     PrefillCtx c;
     int NT, KT;   // N-tiles (2f/128) and k-tiles (d/256)
-    static constexpr int kStages = 2;
+    static constexpr int kStages = 4;
     static constexpr int kNB = 2;
-    static constexpr int kKPS = 2;          // two A k-tiles and the pair's four B k-tiles per stage
-    static constexpr bool kBPair = true;    // the pair's B tiles interleaved by k-tile: one copy
+    static constexpr int kKPS = 1;          // one A k-tile and the pair's two B k-tiles per stage
+    static constexpr bool kBPair = false;
     __device__ int n_items() const { return c.meta[2] * (NT / 2); }
     __device__ void item(int i, Fp4Item& w) const {
         const int np = NT / 2;
         const int mt = i / np, pair = i % np;
         const int e = c.mt_e[mt];
         w.a = c.a1 + (size_t)mt * KT * kGBlk;
-        w.b = c.w1 + ((size_t)e * NT + 2 * pair) * KT * kGBlk;   // the pair's 2*KT interleaved blocks
-        w.b2 = nullptr;
+        w.b = c.w1 + ((size_t)e * NT + 2 * pair) * KT * kGBlk;
+        w.b2 = w.b + (size_t)KT * kGBlk;
         w.kt = KT;
         w.m = mt;
         w.n = pair;
@@ -629,10 +629,8 @@ __global__ void __launch_bounds__(256) combine_kernel(PrefillCtx c, __nv_bfloat1
 
 // Gate/up weights -> blocks (swizzled tile + scales) with gate and up
 // interleaved per 64 rows: N-tile nt rows 0..63 = gate rows 64nt.., rows
-// 64..127 = up rows 64nt..; N-tiles 2p and 2p+1 form pair p, whose blocks are
-// stored interleaved by k-tile (nt 2p k-tile kt, nt 2p+1 k-tile kt, ...).
-// Down weights -> plain row tiles of blocks. One thread per 16 bytes of
-// codes.
+// 64..127 = up rows 64nt.. Down weights -> plain row tiles of blocks. One
+// thread per 16 bytes of codes.
 __global__ void pack_expert_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
                                    uint8_t* __restrict__ w1, uint8_t* __restrict__ w2, int n_slots, int d, int f,
                                    size_t cpm, size_t spm) {
@@ -653,7 +651,7 @@ __global__ void pack_expert_kernel(const uint8_t* __restrict__ codes, const uint
         if (mat < 2) {
             const int nt = row / 64;
             r = (row % 64) + 64 * mat;
-            blk = w1 + ((((size_t)e * (NT1 / 2) + nt / 2) * KT1 + kt) * 2 + (nt & 1)) * kGBlk;
+            blk = w1 + (((size_t)e * NT1 + nt) * KT1 + kt) * kGBlk;
         } else {
             const int nt = row / kGN;
             r = row % kGN;
