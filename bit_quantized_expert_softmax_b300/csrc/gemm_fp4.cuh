@@ -287,7 +287,19 @@ __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, ui
             }
             const uint32_t buf = n_done % kNBuf;
             const bool got = mbar_wait_bounded(&accfull[buf], (n_done / kNBuf) & 1, status);
-            if (!__all_sync(0xffffffffu, got)) break;
+            // all epilogue warps agree on the outcome (named barrier 2), so a
+            // problem's epilogue may synchronise them (named barrier 1)
+            // without waiting for a warp that has left
+            uint32_t all_got;
+            asm volatile(
+                "{\n\t.reg .pred p, q;\n\t"
+                "setp.ne.u32 p, %1, 0;\n\t"
+                "barrier.cta.red.and.pred q, 2, %2, p;\n\t"
+                "selp.u32 %0, 1, 0, q;\n\t}"
+                : "=r"(all_got)
+                : "r"((uint32_t)got), "n"(kGEpiWarps * 32)
+                : "memory");
+            if (!all_got) break;
             tc_fence_after();
             // the problem's epilogue reads the accumulator(s) and calls
             // release() as soon as it no longer needs tensor memory

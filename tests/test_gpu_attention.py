@@ -116,7 +116,7 @@ def test_two_steps_through_the_cache(fm):
 def test_attn_rejects_bad_arguments(fm):
     for kw in [dict(window=513, cap=512), dict(window=-1, cap=10), dict(window=0, cap=0)]:
         with pytest.raises(fm.FlintError) as ei:
-            fm.flint_moe_attn_decode(32, 4, kw["window"], kw["cap"], True, 1, *([None] * 11))
+            fm.flint_moe_attn_decode(32, 4, kw["window"], kw["cap"], True, 1, *([None] * 10))
         assert ei.value.code == fm.FLINT_EINVAL
     with pytest.raises(fm.FlintError):
-        fm.flint_moe_attn_decode(30, 4, 513, 513, True, 1, *([None] * 11))   # not 8 query heads per key head
+        fm.flint_moe_attn_decode(30, 4, 513, 513, True, 1, *([None] * 10))   # not 8 query heads per key head
