@@ -14,8 +14,7 @@
 //   gemm1     gate/up: [rows x d] . [2f x d]^T, each 128-column tile holds 64
 //             gate and 64 up columns of the same f range, two such tiles per
 //             item sharing the A k-tiles; epilogue h = silu(g)*u (fp32)
-//             the M-tile's last pair to finish quantises its 128 h rows
-//             (read back from L2) into the down GEMM's swizzled A tile
+//   quant_h   quantise each fp32 h row into swizzled A tiles of the down GEMM
 //   gemm2     down: [rows x f] . [d x f]^T, each M-tile's A tile held in
 //             shared memory across its 16 N-tiles; epilogue scales by the routing
 //             weight (1 for the shared expert) and stores the contribution in
@@ -197,7 +196,6 @@ struct PrefillCtx {
     float* h;                 // [padded rows][f] fp32
     uint8_t* a2;              // down A blocks [row tiles][f/256]
     int* prow;                // [padded rows] bucketed position of the row's assignment, -1: padding
-    int* mt_done;             // [M-tiles] gate/up pairs finished (zero between forwards)
     float* yscale;            // [padded rows] s_h * down tensor scale * routing weight
     __nv_bfloat16* y;         // [T*(k+1)][d] weighted contributions by bucketed position
     // weights (blocks)
@@ -359,7 +357,61 @@ __global__ void __launch_bounds__(256, 3) quant_x_kernel(PrefillCtx c) {
     }
 }
 
-constexpr int kQhRows = 4;   // h rows quantised together by one warp
+// Quantise each h row (fp32, f elements) into the down GEMM's A tiles and
+// write the down GEMM's per-row epilogue data. A warp takes kQhRows
+// consecutive padded rows (one M-tile's): it loads all of their h first (the
+// buffer holds every row the grid covers, so the loads need no lookup), then
+// resolves the rows' slots and routing weights while those loads are in
+// flight. Warps past the actual rows return; padding rows get prow = -1.
+constexpr int kQhRows = 4;
+
+template <int EPL>
+__global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KT = c.f / kGK;
+    // last CTA first: the gate/up GEMM wrote the high rows last
+    const int row0 = ((gridDim.x - 1 - blockIdx.x) * 8 + warp) * kQhRows;
+    float4 raw[kQhRows][EPL / 4];
+#pragma unroll
+    for (int i = 0; i < kQhRows; ++i) {
+        const float4* hr = reinterpret_cast<const float4*>(c.h + (size_t)(row0 + i) * c.f + lane * EPL);
+#pragma unroll
+        for (int j = 0; j < EPL / 4; ++j) raw[i][j] = __ldcs(hr + j);
+    }
+    const int n_rows = c.meta[2] * kGM;
+    if (row0 >= n_rows) return;
+    const int mt = row0 / kGM, r0 = row0 % kGM;
+    const int slot = c.mt_slot[mt], m = c.mt_m[mt];
+    // lane i < kQhRows: position and epilogue scale of row row0 + i (-1: padding)
+    int p = -1;
+    float yscale_w = 0.f;
+    if (lane < kQhRows) {
+        const int q = m * kGM + r0 + lane;
+        if (q < c.slot_cnt[slot]) {
+            p = c.slot_off[slot] + q;
+            const float wr = p < c.T * c.k ? c.wts[__ldg(c.perm + p)] : 1.0f;
+            yscale_w = c.tscale[c.slot_expert[slot] * 3 + 2] * wr;
+        }
+    }
+    uint8_t* blocks = c.a2 + (size_t)mt * KT * kGBlk;
+#pragma unroll
+    for (int i = 0; i < kQhRows; ++i) {
+        const int pi = __shfl_sync(0xffffffffu, p, i);
+        const float ys = __shfl_sync(0xffffffffu, yscale_w, i);
+        if (pi < 0) {   // padding row: its codes are never read back
+            if (lane == 0) c.prow[row0 + i] = -1;
+            continue;
+        }
+        uint32_t codes[EPL / 8];
+        uint32_t sb = 0;
+        const float s_t = quant_row_f32<EPL>(raw[i], codes, sb);
+        store_row_swizzled<EPL>(blocks, r0 + i, lane, codes, sb);
+        if (lane == 0) {
+            c.prow[row0 + i] = pi;
+            c.yscale[row0 + i] = s_t * ys;
+        }
+    }
+}
 
 // gate/up GEMM: item = (M-tile, pair of N-tiles); N-tile nt holds 64 gate
 // and 64 up columns of the same f range, so the pair yields h columns
@@ -432,71 +484,9 @@ struct Gemm1 {
                         // only where h sits on a rounding boundary)
                         hv[q] = __fdividef(gq, 1.0f + __expf(-gq)) * uq;
                     }
-                    // plain stores: the rows are read back through L2 when the
-                    // M-tile's last pair quantises them
-                    *reinterpret_cast<float4*>(dst + i) = make_float4(hv[0], hv[1], hv[2], hv[3]);
-                }
-            }
-        }
-        // the M-tile's last pair to finish quantises the M-tile's 128 h rows
-        // (every pair's columns, read back through L2) into the down GEMM's
-        // A tile: h goes from the fp32 accumulators to NVFP4 without a pass
-        // of its own. The epilogue's 8 warps take 16 rows each.
-        __shared__ int s_last;
-        const int ew = half * 4 + (row >> 5), lane = row & 31;
-        __threadfence();   // this thread's h stores are visible before the count
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (ew == 0 && lane == 0) s_last = atomicAdd(c.mt_done + w.m, 1) == NT / 2 - 1;
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (s_last) {
-            __threadfence();
-            quantise_h_rows(w.m, 16 * ew, lane);
-            if (ew == 0 && lane == 0) c.mt_done[w.m] = 0;
-        }
-    }
-
-    // Rows r0 .. r0 + 15 of M-tile mt, four at a time (one warp; lane l holds
-    // elements 16 l .. 16 l + 15 of a row): NVFP4 codes and scales into the
-    // swizzled A tile, and each row's bucketed position (-1: padding) and
-    // epilogue scale s_h * down tensor scale * routing weight.
-    __device__ void quantise_h_rows(int mt, int r0, int lane) const {
-        const int slot = __ldcg(c.mt_slot + mt), m = __ldcg(c.mt_m + mt);
-        const int cnt = __ldcg(c.slot_cnt + slot), off = __ldcg(c.slot_off + slot);
-        const float tsd = __ldg(c.tscale + __ldcg(c.slot_expert + slot) * 3 + 2);
-        uint8_t* blocks = c.a2 + (size_t)mt * (512 / kGK) * kGBlk;
-#pragma unroll 1
-        for (int rr = r0; rr < r0 + 16; rr += kQhRows) {
-            float4 raw[kQhRows][4];
-#pragma unroll
-            for (int i = 0; i < kQhRows; ++i) {
-                const float4* hr = reinterpret_cast<const float4*>(c.h + ((size_t)mt * kGM + rr + i) * c.f + lane * 16);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) raw[i][j] = __ldcg(hr + j);
-            }
-            int p = -1;
-            float ys = 0.f;
-            if (lane < kQhRows) {
-                const int q = m * kGM + rr + lane;
-                if (q < cnt) {
-                    p = off + q;
-                    ys = tsd * (p < c.T * c.k ? __ldcg(c.wts + __ldcg(c.perm + p)) : 1.0f);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < kQhRows; ++i) {
-                const int pi = __shfl_sync(0xffffffffu, p, i);
-                const float ysi = __shfl_sync(0xffffffffu, ys, i);
-                if (pi < 0) {
-                    if (lane == 0) c.prow[mt * kGM + rr + i] = -1;
-                    continue;
-                }
-                uint32_t codes[2];
-                uint32_t sb = 0;
-                const float s_t = quant_row_f32<16>(raw[i], codes, sb);
-                store_row_swizzled<16>(blocks, rr + i, lane, codes, sb);
-                if (lane == 0) {
-                    c.prow[mt * kGM + rr + i] = pi;
-                    c.yscale[mt * kGM + rr + i] = s_t * ysi;
+                    // plain stores: the last-written rows are still in L2 when the h
+            // quantiser, which walks the rows from the end, reads them
+            *reinterpret_cast<float4*>(dst + i) = make_float4(hv[0], hv[1], hv[2], hv[3]);
                 }
             }
         }
@@ -761,8 +751,7 @@ size_t prefill_workspace_bytes(const Shape& s, int Tm) {
     const size_t rt = (rows + kGM - 1) / kGM;
     const size_t a1 = rt * (s.d / kGK) * (kGTile + kGSf);
     const size_t a2 = rt * (s.f / kGK) * (kGTile + kGSf);
-    return 256 * 16 + rt * kGM * 4 * 3 + rt * 16 + rt * 4 + 256 + (s.n_slots() + 2) * 4 * 2 + a1 + a2 +
-           rt * kGM * s.f * 4 +
+    return 256 * 16 + rt * kGM * 4 * 3 + rt * 16 + (s.n_slots() + 2) * 4 * 2 + a1 + a2 + rt * kGM * s.f * 4 +
            (size_t)Tm * (s.k + 1) * s.d * 2;
 }
 
@@ -806,7 +795,6 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     c.mt_e = reinterpret_cast<int*>(take(rt * 4));
     c.sa = reinterpret_cast<float*>(take(rt * kGM * 4));
     c.prow = reinterpret_cast<int*>(take(rt * kGM * 4));
-    c.mt_done = reinterpret_cast<int*>(take(rt * 4));
     c.yscale = reinterpret_cast<float*>(take(rt * kGM * 4));
     c.a1 = take(rt * (s.d / kGK) * kGBlk);
     c.a2 = take(rt * (s.f / kGK) * kGBlk);
@@ -828,14 +816,16 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     Gemm1 g1{c, 2 * s.f / kGN, s.d / kGK};
     fp4_gemm_kernel<Gemm1><<<148, kGThreads, fp4_gemm_smem<Gemm1>(), st>>>(g1, ws.status);
     mark(2);
-    mark(3);   // (h was quantised by the gate/up GEMM)
+    static_assert(kGM % (8 * kQhRows) == 0, "a CTA's rows stay inside one M-tile");
+    quant_h_kernel<16><<<(unsigned)(rt * kGM / (8 * kQhRows)), 256, 0, st>>>(c);
+    mark(3);
     static_assert(Gemm2R::kNT * kGN == 2048 && kRKT * kGK == 512, "the Flint shape (d = 2048, f = 512)");
     Gemm2R g2{Gemm2{c, s.d / kGN, s.f / kGK}};
     fp4_gemm_resa_kernel<Gemm2R><<<148, kGThreads, fp4_gemm_resa_smem<Gemm2R>(), st>>>(g2, ws.status);
     mark(4);
     combine_kernel<<<(T + 7) / 8 < 148 * 8 ? (T + 7) / 8 : 148 * 8, 256, 0, st>>>(c, out, residual);
     mark(5);
-    *n_launch += 5;
+    *n_launch += 6;
     return cudaGetLastError();
 }
 
