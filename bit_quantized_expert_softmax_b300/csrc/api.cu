@@ -277,7 +277,7 @@ flint_status flint_moe_create(const flint_moe_config* cfg, flint_moe** out) {
         h->fp4_experts = h->prefill && !(env != nullptr && env[0] == '0') && cfg->max_tokens > flint::kSmallT &&
                          flint::prefill_fp4_supported(h->s) && flint::prepare_prefill_fp4() == cudaSuccess;
     }
-    if (flint::prepare_router() != cudaSuccess) {
+    if (flint::prepare_router() != cudaSuccess || flint::prepare_experts() != cudaSuccess) {
         delete h;
         return FLINT_ECUDA;
     }
@@ -738,8 +738,7 @@ int flint_moe_forward_launches(const flint_moe* h, int T) {
     if (h->fused && flint::fused_smem_bytes(h->s, T, h->n_sms, &n_slots, offs) != 0) return 1;
     const int router = (T <= flint::kSmallT && h->s.d <= 2560) ? 1 : 2 + 3;
     if (T > flint::kSmallT && h->fp4_experts) return 2 + 6;   // logits, top-k and ranks; 6 expert-path kernels
-    const int down = T <= flint::kFuseCombineT ? 1 : 2;
-    return router + 1 + down;
+    return router + flint::expert_launches(h->s, T);
 }
 
 flint_status flint_moe_profile_begin(flint_moe* h, int max_forwards) {

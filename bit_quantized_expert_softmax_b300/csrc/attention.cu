@@ -6,13 +6,15 @@
 // architecture is an argument about memory bandwidth", Attention and
 // Position-encoding bullets).
 //
-// One CTA per (sequence, key-value head), one warp per query head of the
-// group. The window's keys and values (bf16 cache rows) stream through
-// shared memory in tiles of 64 positions with 16-byte asynchronous copies,
-// two tiles in flight; each warp keeps an online softmax (running max, sum
-// and the 128-wide output accumulator, four dimensions per lane) in fp32.
-// The current token's key and value enter unrounded and are then stored,
-// bf16, in its cache slot.
+// One CTA per (sequence, key-value head), two per SM. The window's keys and
+// values (bf16 cache rows) stream through shared memory in tiles of 64
+// positions with 16-byte asynchronous copies, three tiles in flight. Both
+// contractions of a tile run on the tensor cores (mma.sync, bf16 operands,
+// fp32 accumulation), the group's 8 query heads as the MMA's N; the query and
+// the probabilities enter as bf16 hi + lo pairs, so the scores and the
+// weighted sum keep about 16 significant bits per operand. The softmax is
+// online (running max and sum per head, in fp32). The current token's key and
+// value enter unrounded and are then stored, bf16, in its cache slot.
 #include "../../include/flint_moe.h"
 #include "kernels.cuh"
 
@@ -76,15 +78,67 @@ __device__ __forceinline__ void norm_rope(float (&v)[4], const float* w, int lan
     }
 }
 
-constexpr int kASmem = 4 * kATileBytes;   // two buffers of key rows, two of value rows
+// bf16 x bf16 -> fp32 m16n8k16 (A row-major 16 x 16, B "col" 16 x 8)
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
-__global__ void __launch_bounds__(256) attn_decode_kernel(AttnArgs a) {
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+
+// v = hi + lo with hi = bf16(v), lo = bf16(v - hi): together ~16 significant bits
+__device__ __forceinline__ void split_bf16x2(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+constexpr int kAStages = 3;                                // tiles of key and value rows in flight
+constexpr int kASmem = kAStages * 2 * kATileBytes;
+
+// Shared scratch besides the tiles.
+struct AttnShared {
+    union {
+        float qs[kAGroup][kAD];       // normed (rotated) query heads, fp32 (before the tile loop)
+        float sc[2][kAGroup][kATile]; // scores of the tile: the q_hi and q_lo parts, [head][key]
+    };
+    float kcur[kAD], vcur[kAD];       // the current token's key (normed, rotated) and value
+    uint32_t ph[kAGroup][kATile / 2]; // probabilities of the tile, bf16 hi parts, [head][key pair]
+    uint32_t pl[kAGroup][kATile / 2]; // and lo parts
+    float corr[kAGroup];              // per head: rescale of the accumulators for this tile
+    float fin_a[kAGroup], fin_b[kAGroup], fin_inv[kAGroup];   // the final current-token / sink fold
+};
+
+// One CTA per (key-value head g, sequence b); warp w is query head 8 g + w
+// for the softmax and owns output dimensions 16 w .. 16 w + 15 for P.V.
+// Per tile of 64 cached positions:
+//   scores  S[key][head] = K[key][:] . Q[head][:] on the tensor cores, keys as
+//           M (four 16-key m-tiles), the group's 8 heads as N, Q split into
+//           bf16 hi + lo (warps 0-3: hi, 4-7: lo; one m-tile each)
+//   softmax warp h: running max, rescale factor, p = exp(s - max), row sum
+//   P.V     O^T[dim][head] += V^T[dim][key] . P^T[key][head], V^T by
+//           transposing loads of the value rows, P split into hi + lo
+// so both contractions keep about fp32 accuracy.
+__global__ void __launch_bounds__(256, 2) attn_decode_kernel(AttnArgs a) {
     extern __shared__ __align__(16) uint8_t asmem[];
-    uint8_t* ks[2] = {asmem, asmem + kATileBytes};
-    uint8_t* vs[2] = {asmem + 2 * kATileBytes, asmem + 3 * kATileBytes};
-    __shared__ __align__(16) float qs[kAGroup][kAD];
-    __shared__ __align__(16) float kcur[kAD], vcur[kAD];
+    __shared__ __align__(16) AttnShared sh;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, cq = lane & 3;
     const int g = blockIdx.x, b = blockIdx.y;
     const int h = g * kAGroup + warp;
     const int pos = a.pos[b];
@@ -94,22 +148,31 @@ __global__ void __launch_bounds__(256) attn_decode_kernel(AttnArgs a) {
     const __nv_bfloat16* kcg = a.kc + cache_base * kAD;
     const __nv_bfloat16* vcg = a.vc + cache_base * kAD;
     const int n_tiles = (n_prev + kATile - 1) / kATile;
+    auto kbuf = [&](int st) { return asmem + (size_t)st * 2 * kATileBytes; };
+    auto vbuf = [&](int st) { return asmem + (size_t)st * 2 * kATileBytes + kATileBytes; };
 
-    // request the first two tiles of cached rows before anything else
-    auto load_tile = [&](int tile, int buf) {
+    // rows past the window's end are zero-filled: their probabilities are 0
+    // and 0 * (stale bits) must not make a NaN
+    auto load_tile = [&](int tile, int st) {
         const int p0 = first + tile * kATile;
+        uint8_t* kd = kbuf(st);
+        uint8_t* vd = vbuf(st);
         for (int i = threadIdx.x; i < kATile * 16; i += blockDim.x) {
             const int r = i >> 4, c = i & 15;
             if (p0 + r < pos) {
                 const size_t slot = (size_t)((p0 + r) % a.cap);
-                cp_async16(ks[buf] + r * kARow + c * 16, kcg + slot * kAD + c * 8);
-                cp_async16(vs[buf] + r * kARow + c * 16, vcg + slot * kAD + c * 8);
+                cp_async16(kd + r * kARow + c * 16, kcg + slot * kAD + c * 8);
+                cp_async16(vd + r * kARow + c * 16, vcg + slot * kAD + c * 8);
+            } else {
+                *reinterpret_cast<uint4*>(kd + r * kARow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(vd + r * kARow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
         cp_async_commit();
     };
-    if (n_tiles > 0) load_tile(0, 0);
-    if (n_tiles > 1) load_tile(1, 1);
+#pragma unroll
+    for (int t = 0; t < kAStages - 1; ++t)
+        if (t < n_tiles) load_tile(t, t); else cp_async_commit();
 
     // this warp's query head, and (warp 0) the current key and value
     float q[4];
@@ -119,7 +182,7 @@ __global__ void __launch_bounds__(256) attn_decode_kernel(AttnArgs a) {
         for (int i = 0; i < 4; ++i) q[i] = __bfloat162float(qr[lane + 32 * i]);
         norm_rope(q, a.wq, lane, pos, a);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) qs[warp][lane + 32 * i] = q[i];
+        for (int i = 0; i < 4; ++i) sh.qs[warp][lane + 32 * i] = q[i];
     }
     if (warp == 0) {
         float kv[4];
@@ -130,110 +193,136 @@ __global__ void __launch_bounds__(256) attn_decode_kernel(AttnArgs a) {
         norm_rope(kv, a.wk, lane, pos, a);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            kcur[lane + 32 * i] = kv[i];
-            vcur[lane + 32 * i] = __bfloat162float(vr[lane + 32 * i]);
+            sh.kcur[lane + 32 * i] = kv[i];
+            sh.vcur[lane + 32 * i] = __bfloat162float(vr[lane + 32 * i]);
         }
     }
     __syncthreads();
+    // B fragments of Q^T (k = dimension, n = head) for the 8 k-steps: the hi
+    // part for warps 0-3, the lo part for warps 4-7
+    const int part = warp >> 2, mt = warp & 3;
+    uint32_t qb[8][2];
+#pragma unroll
+    for (int st = 0; st < 8; ++st) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int dim = 16 * st + 2 * cq + 8 * r;
+            uint32_t hi, lo;
+            split_bf16x2(sh.qs[gq][dim], sh.qs[gq][dim + 1], hi, lo);
+            qb[st][r] = part ? lo : hi;
+        }
+    }
+    __syncthreads();   // qs is read; the tile loop reuses its memory for the scores
 
     const float scale = rsqrtf((float)kAD);   // 1/sqrt(128), exact: 2^-3.5 rounded once
-    float m = -INFINITY, l = 0.f;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const float4* q4 = reinterpret_cast<const float4*>(qs[warp]);
+    float m = -INFINITY, l = 0.f;             // warp h's running max and sum (every lane)
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};      // O^T: dims 16 w + gq (+8), heads 2 cq (+1)
+    const int d0 = 16 * warp;
     for (int tile = 0; tile < n_tiles; ++tile) {
-        const int buf = tile & 1;
-        if (tile + 1 < n_tiles) cp_async_wait<1>(); else cp_async_wait<0>();
-        __syncthreads();
+        const int stg = tile % kAStages;
+        cp_async_wait<kAStages - 2>();
+        __syncthreads();   // the tile has landed; every warp is done with the previous tile
+        if (tile + kAStages - 1 < n_tiles) load_tile(tile + kAStages - 1, (tile + kAStages - 1) % kAStages);
+        else cp_async_commit();
         const int p0 = first + tile * kATile;
         const int nk = min(kATile, pos - p0);
-        // scores of keys lane and lane + 32
-        float s[2];
+        const uint8_t* kt = kbuf(stg);
+        const uint8_t* vt = vbuf(stg);
+        // scores of keys 16 mt .. 16 mt + 15 against the 8 heads (one Q part)
+        {
+            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+            const int j = lane >> 3, r = lane & 7;
+            const uint8_t* rowp = kt + (size_t)(16 * mt + r + 8 * (j & 1)) * kARow + 16 * (j >> 1);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int r = lane + 32 * j;
-            float dot = 0.f;
-            if (r < nk) {
-                const uint4* kr = reinterpret_cast<const uint4*>(ks[buf] + r * kARow);
-#pragma unroll 4
-                for (int c = 0; c < 16; ++c) {
-                    const uint4 kw = kr[c];
-                    const float4 qa = q4[2 * c], qb = q4[2 * c + 1];
-                    const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kw);
-                    const float2 k01 = __bfloat1622float2(k2[0]), k23 = __bfloat1622float2(k2[1]);
-                    const float2 k45 = __bfloat1622float2(k2[2]), k67 = __bfloat1622float2(k2[3]);
-                    dot = fmaf(qa.x, k01.x, dot);
-                    dot = fmaf(qa.y, k01.y, dot);
-                    dot = fmaf(qa.z, k23.x, dot);
-                    dot = fmaf(qa.w, k23.y, dot);
-                    dot = fmaf(qb.x, k45.x, dot);
-                    dot = fmaf(qb.y, k45.y, dot);
-                    dot = fmaf(qb.z, k67.x, dot);
-                    dot = fmaf(qb.w, k67.y, dot);
-                }
-                s[j] = dot * scale;
-            } else {
-                s[j] = -INFINITY;
+            for (int st = 0; st < 8; ++st) {
+                uint32_t af[4];
+                ldsm_x4(af, rowp + 32 * st);
+                mma_bf16_16816(sacc, af[0], af[1], af[2], af[3], qb[st][0], qb[st][1]);
+            }
+            const int k0 = 16 * mt + gq;
+            sh.sc[part][2 * cq][k0] = sacc[0];
+            sh.sc[part][2 * cq + 1][k0] = sacc[1];
+            sh.sc[part][2 * cq][k0 + 8] = sacc[2];
+            sh.sc[part][2 * cq + 1][k0 + 8] = sacc[3];
+        }
+        __syncthreads();
+        // softmax update of head `warp`: lane L takes keys 2L, 2L + 1
+        {
+            float sv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int key = 2 * lane + u;
+                sv[u] = key < nk ? (sh.sc[0][warp][key] + sh.sc[1][warp][key]) * scale : -INFINITY;
+            }
+            const float m_new = fmaxf(m, warp_max(fmaxf(sv[0], sv[1])));
+            const float corr = expf(m - m_new);   // 0 on the first tile (m = -inf)
+            const float p0v = expf(sv[0] - m_new), p1v = expf(sv[1] - m_new);
+            l = l * corr + warp_sum(p0v + p1v);
+            m = m_new;
+            uint32_t hi, lo;
+            split_bf16x2(p0v, p1v, hi, lo);
+            sh.ph[warp][lane] = hi;
+            sh.pl[warp][lane] = lo;
+            if (lane == 0) sh.corr[warp] = corr;
+        }
+        __syncthreads();
+        // O^T[dims d0..d0+15][heads] = corr * O^T + V^T . P^T
+        {
+            const float c0 = sh.corr[2 * cq], c1 = sh.corr[2 * cq + 1];
+            acc[0] *= c0;
+            acc[1] *= c1;
+            acc[2] *= c0;
+            acc[3] *= c1;
+            const int j = lane >> 3, r = lane & 7;
+#pragma unroll
+            for (int st = 0; st < 4; ++st) {
+                uint32_t af[4];
+                ldsm_x4_t(af, vt + (size_t)(16 * st + r + 8 * (j >> 1)) * kARow + 2 * (d0 + 8 * (j & 1)));
+                const int pr = 8 * st + cq;
+                mma_bf16_16816(acc, af[0], af[1], af[2], af[3], sh.ph[gq][pr], sh.ph[gq][pr + 4]);
+                mma_bf16_16816(acc, af[0], af[1], af[2], af[3], sh.pl[gq][pr], sh.pl[gq][pr + 4]);
             }
         }
-        const float tmax = warp_max(fmaxf(s[0], s[1]));
-        const float m_new = fmaxf(m, tmax);
-        const float corr = expf(m - m_new);   // 0 on the first tile (m = -inf)
-        float p[2];
-        p[0] = expf(s[0] - m_new);
-        p[1] = expf(s[1] - m_new);
-        l = l * corr + warp_sum(p[0] + p[1]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] *= corr;
-        m = m_new;
-        // acc[d] += sum_r p_r V[r][d]
-        for (int r = 0; r < nk; ++r) {
-            const float pr = __shfl_sync(0xffffffffu, p[r >> 5], r & 31);
-            const __nv_bfloat16* vrow = reinterpret_cast<const __nv_bfloat16*>(vs[buf] + r * kARow);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = fmaf(pr, __bfloat162float(vrow[lane + 32 * i]), acc[i]);
-        }
-        __syncthreads();   // every warp is done with this buffer
-        if (tile + 2 < n_tiles) load_tile(tile + 2, buf);
     }
-    // the current token, unrounded
+    cp_async_wait<0>();
+    // the current token (unrounded), then the sink (denominator only), per head
     {
         float dot = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) dot = fmaf(q[i], kcur[lane + 32 * i], dot);
+        for (int i = 0; i < 4; ++i) dot = fmaf(q[i], sh.kcur[lane + 32 * i], dot);
         const float sc = warp_sum(dot) * scale;
-        const float m_new = fmaxf(m, sc);
-        const float corr = expf(m - m_new);
-        const float pc = expf(sc - m_new);
-        l = l * corr + pc;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] = acc[i] * corr + pc * vcur[lane + 32 * i];
-        m = m_new;
-    }
-    // the sink joins the denominator only
-    {
+        const float m1 = fmaxf(m, sc);
+        const float corr1 = expf(m - m1);
+        const float pc = expf(sc - m1);
+        const float l1 = l * corr1 + pc;
         const float sk = __ldg(a.sinks + h);
-        const float m_new = fmaxf(m, sk);
-        const float corr = expf(m - m_new);
-        l = l * corr + expf(sk - m_new);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] *= corr;
+        const float m2 = fmaxf(m1, sk);
+        const float corr2 = expf(m1 - m2);
+        const float l2 = l1 * corr2 + expf(sk - m2);
+        if (lane == 0) {
+            sh.fin_a[warp] = corr1 * corr2;
+            sh.fin_b[warp] = pc * corr2;
+            sh.fin_inv[warp] = 1.0f / l2;
+        }
     }
-    const float inv = 1.0f / l;
-    __nv_bfloat16* o = a.out + ((size_t)b * a.H + h) * kAD;
+    __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 4; ++i) o[lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
+    for (int i = 0; i < 4; ++i) {
+        const int head = 2 * cq + (i & 1), dim = d0 + gq + 8 * (i >> 1);
+        const float o = (acc[i] * sh.fin_a[head] + sh.fin_b[head] * sh.vcur[dim]) * sh.fin_inv[head];
+        a.out[((size_t)b * a.H + g * kAGroup + head) * kAD + dim] = __float2bfloat16_rn(o);
+    }
     // store the current key and value, bf16, in the position's slot (outside
     // the window that was read: cap >= window)
     if (warp == 0) {
         const size_t slot = (size_t)(pos % a.cap);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            a.kc[(cache_base + slot) * kAD + lane + 32 * i] = __float2bfloat16_rn(kcur[lane + 32 * i]);
-            a.vc[(cache_base + slot) * kAD + lane + 32 * i] = __float2bfloat16_rn(vcur[lane + 32 * i]);
+            a.kc[(cache_base + slot) * kAD + lane + 32 * i] = __float2bfloat16_rn(sh.kcur[lane + 32 * i]);
+            a.vc[(cache_base + slot) * kAD + lane + 32 * i] = __float2bfloat16_rn(sh.vcur[lane + 32 * i]);
         }
     }
 }
-
 }  // namespace
 
 }  // namespace flint
@@ -276,7 +365,9 @@ extern "C" flint_status flint_moe_attn_decode(const flint_moe_attn_config* cfg, 
     static bool opted_in = false;   // the attribute is per device function, set once
     if (!opted_in) {
         if (cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kASmem) !=
-            cudaSuccess) {
+                cudaSuccess ||
+            cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
+                cudaSuccess) {
             cudaGetLastError();
             return FLINT_ECUDA;
         }

@@ -69,19 +69,6 @@ struct Pair {
     int t, j;   // token, slot (j == k: shared expert)
 };
 
-template <int WFMT>
-__device__ __forceinline__ TileScales<WFMT> lds_scales(const uint8_t* base_g, const uint8_t* base_h, int g) {
-    TileScales<WFMT> s;
-    if constexpr (WFMT == 0) {
-        s.g = *reinterpret_cast<const uint2*>(base_g + g * 8);
-        s.h = *reinterpret_cast<const uint2*>(base_h + g * 8);
-    } else {
-        s.g = *reinterpret_cast<const uint4*>(base_g + g * 16);
-        s.h = *reinterpret_cast<const uint4*>(base_h + g * 16);
-    }
-    return s;
-}
-
 __device__ __forceinline__ void lds_b16(const __half* p, uint32_t (&b)[16]) {
     const uint4* q = reinterpret_cast<const uint4*>(p);
 #pragma unroll

@@ -42,6 +42,20 @@ __device__ __forceinline__ TileScales<1> load_scales<1>(const uint8_t* base_g, c
     return s;
 }
 
+// The same scales read from shared memory (a staged copy of the tile layout).
+template <int WFMT>
+__device__ __forceinline__ TileScales<WFMT> lds_scales(const uint8_t* base_g, const uint8_t* base_h, int g) {
+    TileScales<WFMT> s;
+    if constexpr (WFMT == 0) {
+        s.g = *reinterpret_cast<const uint2*>(base_g + g * 8);
+        s.h = *reinterpret_cast<const uint2*>(base_h + g * 8);
+    } else {
+        s.g = *reinterpret_cast<const uint4*>(base_g + g * 16);
+        s.h = *reinterpret_cast<const uint4*>(base_h + g * 16);
+    }
+    return s;
+}
+
 __device__ __forceinline__ uint32_t u4_get(const uint4& v, int i) {
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }

@@ -226,6 +226,36 @@ def test_layer_other_shapes(fm, d, f, E, k, wfmt, T):
     assert_out_close(got, ref.out, f"d={d} f={f} E={E} k={k} wfmt={wfmt} T={T}")
 
 
+@pytest.mark.parametrize("ring", ["1", "0"])
+@pytest.mark.parametrize("wfmt,T", [(synth.WFMT_NVFP4, 9), (synth.WFMT_Q4_1, 33), (synth.WFMT_Q4_1, 64)])
+def test_expert_kernel_variants(fm, monkeypatch, ring, wfmt, T):
+    """Batched decode (8 < T <= 64) runs the ring-fed expert kernels by
+    default and the register-streaming ones with FLINT_MOE_RING_EXPERTS=0
+    (read at every launch). Both against the oracle on the Flint shape with
+    the skewed router, twice in a row (the ring kernels' task counters reset
+    themselves), and the kernels the library launches for a forward are the
+    ones it reports."""
+    monkeypatch.setenv("FLINT_MOE_RING_EXPERTS", ring)
+    cfg = _cfg(3, wfmt=wfmt)
+    L = synth.make_layer(cfg)
+    bits = synth.make_hidden(cfg, tokens=T)
+    m = _moe(fm, cfg, [L], T)
+    ref = M.moe_layer(bits, L)
+    idx = torch.empty((T, cfg.top_k), dtype=torch.int32, device="cuda")
+    fm.flint_moe_router(m.h, 0, fm.hidden_to_device(bits), T, None, idx, None)
+    torch.cuda.synchronize()
+    same = compare_routing(idx.cpu().numpy(), ref.sel, ref.logits, cfg.top_k)
+    assert same.mean() >= 0.95
+    outs = []
+    for _ in range(2):
+        n0 = fm.flint_moe_launch_count(m.h)
+        outs.append(_forward(fm, m, bits))
+        assert fm.flint_moe_launch_count(m.h) - n0 == fm.flint_moe_forward_launches(m.h, T)
+    m.close()
+    assert np.array_equal(outs[0], outs[1])
+    assert_out_close(outs[0][same], ref.out[same], f"ring={ring} wfmt={wfmt} T={T}")
+
+
 @pytest.mark.parametrize("T", [1, 2])
 def test_layer_flint_decode_nvfp4(fm, T):
     cfg = _cfg(2)
