@@ -12,6 +12,7 @@ workloads: one layer at T=1 (NVFP4), one layer at T=64 (q4_1, Zipf), and the
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--no-subrecords]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
   python bench.py --head                 # the 4-bit output head and its sampler
+  python bench.py --attn                 # one decode step of a sliding-window attention layer
 
 A step is one pass of the layer (router, top-k, bucketing, expert gate/up,
 down projection, combine) over the workload's tokens. Per-step device time is
@@ -633,19 +634,23 @@ def kernel_roofline(cfg, res, peaks, fp4) -> dict:
         k_us = None
     elif res["phase_us"] is not None:
         k_us, k_bytes = res["phase_us"]["gateup"], nb["gateup_kernel_bytes"]
-        kname = "gateup_kernel (expert gate/up, SwiGLU)"
+        ring = 8 < cfg.tokens <= 64 and os.environ.get("FLINT_MOE_RING_EXPERTS", "1") != "0"
+        kkey = "gateup_ring_kernel" if ring else "gateup_kernel"
+        kname = f"{kkey} (expert gate/up, SwiGLU)"
         srcs = ("bit_quantized_expert_softmax_b300/csrc/experts.cu", "bit_quantized_expert_softmax_b300/csrc/tiles.cuh",
                 "bit_quantized_expert_softmax_b300/csrc/common.cuh")
-        kkey = "gateup_kernel"
         out["phases_us"] = {k: v for k, v in res["phase_us"].items()
                             if k in ("router_topk_bucket", "gateup", "down_combine")}
     else:
-        # the stack: one graph of n_layers single-launch layers per step
+        # the stack: all layers in one persistent launch per step (per-layer
+        # figures: the step's time and bytes over the layers)
+        one_launch = os.environ.get("FLINT_MOE_STACK_KERNEL", "1") != "0"
         k_us, k_bytes = res["ms"] * 1e3 / cfg.n_layers, nb["layer_bytes"] / cfg.n_layers
-        kname = "decode_fused_kernel (per layer, inside the stack's CUDA graph)"
+        kkey = "decode_stack_kernel" if one_launch else "decode_fused_kernel"
+        kname = (f"{kkey} (per layer, one launch for the whole stack)" if one_launch
+                 else f"{kkey} (per layer, inside the stack's CUDA graph)")
         srcs = ("bit_quantized_expert_softmax_b300/csrc/decode_fused.cu", "bit_quantized_expert_softmax_b300/csrc/tiles.cuh",
                 "bit_quantized_expert_softmax_b300/csrc/common.cuh")
-        kkey = "decode_fused_kernel"
     if k_us is not None:
         achieved = k_bytes / (k_us * 1e-6) / 1e9
         out["roofline"] = {
@@ -958,7 +963,9 @@ def attn_main(args):
                        "tokens_per_step": r["B"],
                        "l2": "flushed between steps (memset of 2x L2, outside the per-step events)"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": None, "kernel": "attn_decode_kernel (one step, the whole layer)",
+                         "traffic": recorded_traffic("attn_decode_kernel", f"attn_decode_B{r['B']}_pos{ATTN_POS}",
+                                                     source_digest("bit_quantized_expert_softmax_b300/csrc/attention.cu")),
+                         "kernel": "attn_decode_kernel (one step, the whole layer)",
                          "algorithmic_bytes_per_launch": r["bytes"], "avg_launch_us": r["ms"] * 1e3,
                          "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
                          else "fallback 6.4 TB/s"},

@@ -111,15 +111,19 @@ __device__ __forceinline__ void split_bf16x2(float v0, float v1, uint32_t& hi, u
 constexpr int kAStages = 3;                                // tiles of key and value rows in flight
 constexpr int kASmem = kAStages * 2 * kATileBytes;
 
-// Shared scratch besides the tiles.
+// Shared scratch besides the tiles. The score and probability rows are
+// padded so that the MMA fragments' stores and loads (lane (g, c) at row
+// 2c / g, column g / c) fall in distinct banks.
+constexpr int kAScRow = kATile + 4;
+constexpr int kAPRow = kATile / 2 + 4;
 struct AttnShared {
     union {
         float qs[kAGroup][kAD];       // normed (rotated) query heads, fp32 (before the tile loop)
-        float sc[2][kAGroup][kATile]; // scores of the tile: the q_hi and q_lo parts, [head][key]
+        float sc[2][kAGroup][kAScRow]; // scores of the tile: the q_hi and q_lo parts, [head][key]
     };
     float kcur[kAD], vcur[kAD];       // the current token's key (normed, rotated) and value
-    uint32_t ph[kAGroup][kATile / 2]; // probabilities of the tile, bf16 hi parts, [head][key pair]
-    uint32_t pl[kAGroup][kATile / 2]; // and lo parts
+    uint32_t ph[kAGroup][kAPRow];     // probabilities of the tile, bf16 hi parts, [head][key pair]
+    uint32_t pl[kAGroup][kAPRow];     // and lo parts
     float corr[kAGroup];              // per head: rescale of the accumulators for this tile
     float fin_a[kAGroup], fin_b[kAGroup], fin_inv[kAGroup];   // the final current-token / sink fold
 };
@@ -249,11 +253,10 @@ __global__ void __launch_bounds__(256, 2) attn_decode_kernel(AttnArgs a) {
         // softmax update of head `warp`: lane L takes keys 2L, 2L + 1
         {
             float sv[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int key = 2 * lane + u;
-                sv[u] = key < nk ? (sh.sc[0][warp][key] + sh.sc[1][warp][key]) * scale : -INFINITY;
-            }
+            const float2 s_hi = *reinterpret_cast<const float2*>(&sh.sc[0][warp][2 * lane]);
+            const float2 s_lo = *reinterpret_cast<const float2*>(&sh.sc[1][warp][2 * lane]);
+            sv[0] = 2 * lane < nk ? (s_hi.x + s_lo.x) * scale : -INFINITY;
+            sv[1] = 2 * lane + 1 < nk ? (s_hi.y + s_lo.y) * scale : -INFINITY;
             const float m_new = fmaxf(m, warp_max(fmaxf(sv[0], sv[1])));
             const float corr = expf(m - m_new);   // 0 on the first tile (m = -inf)
             const float p0v = expf(sv[0] - m_new), p1v = expf(sv[1] - m_new);

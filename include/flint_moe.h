@@ -283,8 +283,12 @@ typedef struct {
  * sinks_dev fp32 [n_heads]; out_dev bf16 [B][n_heads][128]. Reads the cache
  * slots of positions pos-1 down to the window's start, then writes the new
  * key (normed, rotated) and value, bf16, to slot pos % cap. The current token
- * attends to its own key and value unrounded. All pointers are device
- * pointers; asynchronous on `stream`. Errors: FLINT_EINVAL (configuration,
+ * attends to its own key and value unrounded. Arithmetic: the scores and the
+ * weighted sum of values run on the tensor cores with fp32 accumulation; the
+ * cached keys and values enter as stored (bf16), the normed query and the
+ * softmax probabilities as bf16 hi + lo pairs (about 16 significant bits);
+ * the softmax itself is fp32. All pointers are device pointers; asynchronous
+ * on `stream`. Errors: FLINT_EINVAL (configuration,
  * B < 0, NULL, misaligned cache), FLINT_ECUDA. */
 FLINT_API flint_status flint_moe_attn_decode(const flint_moe_attn_config* cfg, int B, const void* q_dev, const void* k_dev,
                                          const void* v_dev, void* k_cache_dev, void* v_cache_dev,
