@@ -281,9 +281,11 @@ def run_ours(cfg, world, rank, local, steps: int, warmup: int, soak_s: float = 1
     if n_layers > 1:
         xs = x.clone()
         # one CUDA graph per token for the whole stack
+        n0 = fm.flint_moe_launch_count(m.h)
+        fm.flint_moe_forward_stack(m.h, 0, n_layers, xs, T, stream)   # warm, outside capture
+        torch.cuda.synchronize()
+        stack_launches = fm.flint_moe_launch_count(m.h) - n0   # 1 for the one-launch kernel
         try:
-            fm.flint_moe_forward_stack(m.h, 0, n_layers, xs, T, stream)   # warm, outside capture
-            torch.cuda.synchronize()
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph):
                 fm.flint_moe_forward_stack(m.h, 0, n_layers, xs, T, torch.cuda.current_stream())
@@ -302,7 +304,7 @@ def run_ours(cfg, world, rank, local, steps: int, warmup: int, soak_s: float = 1
 
         def reset():      # every step decodes the same token from the same input
             xs.copy_(x)
-        launches_per_step = launches_per_forward * n_layers
+        launches_per_step = stack_launches
     else:
         def step():
             fm.flint_moe_forward(m.h, 0, x, T, out, stream)
@@ -642,9 +644,10 @@ def kernel_roofline(cfg, res, peaks, fp4) -> dict:
         out["phases_us"] = {k: v for k, v in res["phase_us"].items()
                             if k in ("router_topk_bucket", "gateup", "down_combine")}
     else:
-        # the stack: all layers in one persistent launch per step (per-layer
-        # figures: the step's time and bytes over the layers)
-        one_launch = os.environ.get("FLINT_MOE_STACK_KERNEL", "1") != "0"
+        # the stack (per-layer figures: the step's time and bytes over the
+        # layers): one single-layer launch per layer, replayed from a CUDA
+        # graph; FLINT_MOE_STACK_KERNEL=1: all layers in one persistent launch
+        one_launch = os.environ.get("FLINT_MOE_STACK_KERNEL", "0") == "1"
         k_us, k_bytes = res["ms"] * 1e3 / cfg.n_layers, nb["layer_bytes"] / cfg.n_layers
         kkey = "decode_stack_kernel" if one_launch else "decode_fused_kernel"
         kname = (f"{kkey} (per layer, one launch for the whole stack)" if one_launch

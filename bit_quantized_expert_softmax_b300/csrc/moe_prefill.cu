@@ -193,7 +193,7 @@ struct PrefillCtx {
     const __nv_bfloat16* x;
     uint8_t* a1;              // gate/up A blocks [row tiles][d/256]
     float* sa;
-    float* h;                 // [padded rows][f] fp32
+    float* h;                 // fp32, blocked: see h_at
     uint8_t* a2;              // down A blocks [row tiles][f/256]
     int* prow;                // [padded rows] bucketed position of the row's assignment, -1: padding
     float* yscale;            // [padded rows] s_h * down tensor scale * routing weight
@@ -363,23 +363,46 @@ __global__ void __launch_bounds__(256, 3) quant_x_kernel(PrefillCtx c) {
 // buffer holds every row the grid covers, so the loads need no lookup), then
 // resolves the rows' slots and routing weights while those loads are in
 // flight. Warps past the actual rows return; padding rows get prow = -1.
-constexpr int kQhRows = 4;
+// h between the two GEMMs, fp32, blocked so that a warp of the gate/up
+// epilogue (one accumulator row per lane) stores 512 contiguous bytes: per
+// M-tile, per 16-column chunk, per float4 of the chunk, the M-tile's 128 rows
+// one after another.
+__device__ __forceinline__ float4* h_at(float* h, int f, int mt, int chunk, int q4, int row) {
+    return reinterpret_cast<float4*>(h) + ((((size_t)mt * (f / 16) + chunk) * 4 + q4) * kGM + row);
+}
 
+constexpr int kQhRows = 4;                       // rows per warp
+constexpr int kQhCtaRows = 8 * kQhRows;          // rows per CTA (8 warps): 32 consecutive rows of one M-tile
+constexpr int kQhPitch = 512 + 4;                // floats per staged row (f = 512; padded: conflict-free stores)
+constexpr int kQhSmem = kQhCtaRows * kQhPitch * 4;
+
+// Quantise each h row (fp32) into the down GEMM's A tiles and write the down
+// GEMM's per-row epilogue data. A CTA takes 32 consecutive rows: it reads them
+// from the blocked h with every warp load covering 512 contiguous bytes (32
+// rows of one 16-byte piece), stages them row-major in shared memory, then
+// each warp quantises 4 rows (lane l: elements 16 l .. 16 l + 15), resolving
+// the rows' slots and routing weights while the loads are in flight. Padding
+// rows get prow = -1.
 template <int EPL>
 __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
+    static_assert(EPL == 16, "a lane's elements are one 16-column chunk of the row");
+    extern __shared__ __align__(16) float qhs[];   // [kQhCtaRows][kQhPitch]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KT = c.f / kGK;
     // last CTA first: the gate/up GEMM wrote the high rows last
-    const int row0 = ((gridDim.x - 1 - blockIdx.x) * 8 + warp) * kQhRows;
-    float4 raw[kQhRows][EPL / 4];
+    const int rb = (gridDim.x - 1 - blockIdx.x) * kQhCtaRows;
+    if (rb >= c.meta[2] * kGM) return;
+    const int mt_b = rb / kGM, rin = rb % kGM;
+    // all of this thread's loads first (thread t: row t % 32, pieces t / 32 + 8 k)
+    constexpr int kPer = kQhCtaRows * (512 / 4) / 256;
+    const int r_t = threadIdx.x % kQhCtaRows, cq0 = threadIdx.x / kQhCtaRows;
+    float4 v[kPer];
 #pragma unroll
-    for (int i = 0; i < kQhRows; ++i) {
-        const float4* hr = reinterpret_cast<const float4*>(c.h + (size_t)(row0 + i) * c.f + lane * EPL);
-#pragma unroll
-        for (int j = 0; j < EPL / 4; ++j) raw[i][j] = __ldcs(hr + j);
+    for (int k = 0; k < kPer; ++k) {
+        const int cq = cq0 + 8 * k;   // chunk * 4 + float4 of the chunk
+        v[k] = *h_at(c.h, c.f, mt_b, cq >> 2, cq & 3, rin + r_t);
     }
-    const int n_rows = c.meta[2] * kGM;
-    if (row0 >= n_rows) return;
+    const int row0 = rb + warp * kQhRows;
     const int mt = row0 / kGM, r0 = row0 % kGM;
     const int slot = c.mt_slot[mt], m = c.mt_m[mt];
     // lane i < kQhRows: position and epilogue scale of row row0 + i (-1: padding)
@@ -394,6 +417,15 @@ __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
         }
     }
     uint8_t* blocks = c.a2 + (size_t)mt * KT * kGBlk;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) *reinterpret_cast<float4*>(qhs + r_t * kQhPitch + (cq0 + 8 * k) * 4) = v[k];
+    __syncthreads();   // the CTA's rows are staged
+    float4 raw[kQhRows][EPL / 4];
+#pragma unroll
+    for (int i = 0; i < kQhRows; ++i)
+#pragma unroll
+        for (int j = 0; j < EPL / 4; ++j)
+            raw[i][j] = *reinterpret_cast<const float4*>(qhs + (warp * kQhRows + i) * kQhPitch + lane * EPL + 4 * j);
 #pragma unroll
     for (int i = 0; i < kQhRows; ++i) {
         const int pi = __shfl_sync(0xffffffffu, p, i);
@@ -458,7 +490,7 @@ struct Gemm1 {
     __device__ void epilogue(const Fp4Item& w, const Pre& pr, uint32_t taddr, int row, int half, uint8_t*,
                              Release release) const {
         const float tg = pr.tg, tu = pr.tu;
-        float* dst0 = c.h + (size_t)(w.m * kGM + row) * c.f + 2 * w.n * 64 + half * 32;
+        // 16-column chunk of (b, r): 8 pair + 4 b + 2 half + r
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             uint32_t g[2][16], u[2][16];
@@ -472,7 +504,7 @@ struct Gemm1 {
             if (r == 1) release();
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
-                float* dst = dst0 + b * 64 + 16 * r;
+                const int chunk = 8 * w.n + 4 * b + 2 * half + r;
 #pragma unroll
                 for (int i = 0; i < 16; i += 4) {
                     float hv[4];
@@ -484,9 +516,10 @@ struct Gemm1 {
                         // only where h sits on a rounding boundary)
                         hv[q] = __fdividef(gq, 1.0f + __expf(-gq)) * uq;
                     }
-                    // plain stores: the last-written rows are still in L2 when the h
-            // quantiser, which walks the rows from the end, reads them
-            *reinterpret_cast<float4*>(dst + i) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+                    // the warp's 32 rows write 512 contiguous bytes; the rows
+                    // written last are still in L2 when the h quantiser, which
+                    // walks the rows from the end, reads them
+                    *h_at(c.h, c.f, w.m, chunk, i >> 2, row) = make_float4(hv[0], hv[1], hv[2], hv[3]);
                 }
             }
         }
@@ -761,6 +794,8 @@ cudaError_t prepare_prefill_fp4() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fp4_gemm_resa_kernel<Gemm2R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  fp4_gemm_resa_smem<Gemm2R>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(quant_h_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQhSmem);
     if (e != cudaSuccess) cudaGetLastError();
     return e;
 }
@@ -817,7 +852,8 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     fp4_gemm_kernel<Gemm1><<<148, kGThreads, fp4_gemm_smem<Gemm1>(), st>>>(g1, ws.status);
     mark(2);
     static_assert(kGM % (8 * kQhRows) == 0, "a CTA's rows stay inside one M-tile");
-    quant_h_kernel<16><<<(unsigned)(rt * kGM / (8 * kQhRows)), 256, 0, st>>>(c);
+    static_assert(kQhCtaRows * kQhPitch >= kQhCtaRows * (512 + 4), "staging pitch");
+    quant_h_kernel<16><<<(unsigned)(rt * kGM / kQhCtaRows), 256, kQhSmem, st>>>(c);
     mark(3);
     static_assert(Gemm2R::kNT * kGN == 2048 && kRKT * kGK == 512, "the Flint shape (d = 2048, f = 512)");
     Gemm2R g2{Gemm2{c, s.d / kGN, s.f / kGK}};

@@ -320,7 +320,7 @@ def test_stack_47_layers_T1(fm, monkeypatch):
     Every layer is checked against the oracle on the oracle's own input x_l
     (full size, per-layer weights): the single-layer forward, and the
     one-launch stack kernel run on that one layer. The per-layer path of the
-    stack (FLINT_MOE_STACK_KERNEL=0) must equal the GPU chain of single-layer
+    stack (the default) must equal the GPU chain of single-layer
     forwards bit for bit; the one-launch stack computes the router logits in
     another summation order (fixed-point partials per 16 rows), so it is held
     to bit-for-bit determinism run to run and to the end-to-end drift bound.
@@ -330,10 +330,10 @@ def test_stack_47_layers_T1(fm, monkeypatch):
     than the per-layer one."""
     cfg = _cfg(4)
     bits = synth.make_hidden(cfg)
+    monkeypatch.setenv("FLINT_MOE_STACK_KERNEL", "1")
     m = fm.MoE(cfg, max_tokens=1, n_layers=cfg.n_layers)
-    monkeypatch.setenv("FLINT_MOE_STACK_KERNEL", "0")
-    m_chain = fm.MoE(cfg, max_tokens=1, n_layers=cfg.n_layers)
     monkeypatch.delenv("FLINT_MOE_STACK_KERNEL")
+    m_chain = fm.MoE(cfg, max_tokens=1, n_layers=cfg.n_layers)
     ref_bits = bits.copy()
     idx = torch.empty((1, cfg.top_k), dtype=torch.int32, device="cuda")
     for i in range(cfg.n_layers):          # one layer in host memory at a time
@@ -385,14 +385,16 @@ def test_stack_47_layers_T1(fm, monkeypatch):
 
 
 @pytest.mark.parametrize("wfmt,T", [(0, 2), (1, 1), (1, 2)])
-def test_one_launch_stack_other_variants(fm, wfmt, T):
+def test_one_launch_stack_other_variants(fm, monkeypatch, wfmt, T):
     """The one-launch stack kernel for two tokens and for q4_1 weights, on a
     4-layer stack of the tiny shape: each layer against the oracle on the
     oracle's own input, and the whole stack against the oracle chain."""
     cfg = dataclasses.replace(_cfg(1), wfmt=wfmt, n_layers=4, down_scale=0.25)
     layers = [synth.make_layer(cfg, layer=i) for i in range(cfg.n_layers)]
     bits = synth.make_hidden(cfg, tokens=T)
+    monkeypatch.setenv("FLINT_MOE_STACK_KERNEL", "1")
     m = _moe(fm, cfg, layers, T)
+    monkeypatch.delenv("FLINT_MOE_STACK_KERNEL")
     assert fm.flint_moe_forward_launches(m.h, T) == 1
     ref_bits = bits.copy()
     for i, L in enumerate(layers):
