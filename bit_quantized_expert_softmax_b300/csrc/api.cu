@@ -736,7 +736,7 @@ int flint_moe_forward_launches(const flint_moe* h, int T) {
     if (T == 0) return 0;
     int n_slots = 0, offs[10];
     if (h->fused && flint::fused_smem_bytes(h->s, T, h->n_sms, &n_slots, offs) != 0) return 1;
-    const int router = (T <= flint::kSmallT && h->s.d <= 2560) ? 1 : 2 + 3;
+    const int router = flint::router_fused(h->s, T) ? 1 : 2 + 3;
     if (T > flint::kSmallT && h->fp4_experts) return 2 + 6;   // logits, top-k and ranks; 6 expert-path kernels
     return router + flint::expert_launches(h->s, T);
 }

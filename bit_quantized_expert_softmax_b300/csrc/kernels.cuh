@@ -105,6 +105,7 @@ constexpr int kFuseCombineT = 8;        // combine in the down kernel's last CTA
 
 // router.cu
 cudaError_t prepare_router();   // once per device: shared-memory opt-in of the fused router
+bool router_fused(const Shape& s, int T);   // router, top-k and bucketing in one launch
 int expert_launches(const Shape& s, int T);   // gate/up + down (+ combine) kernels of the mma.sync path
 cudaError_t prepare_experts();  // once per device: shared-memory opt-in of the ring-fed expert kernels
 cudaError_t launch_router(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,

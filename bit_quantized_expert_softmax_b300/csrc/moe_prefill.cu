@@ -13,8 +13,10 @@
 //             tiles of its k routed experts and of the shared expert
 //   gemm1     gate/up: [rows x d] . [2f x d]^T, each 128-column tile holds 64
 //             gate and 64 up columns of the same f range, two such tiles per
-//             item sharing the A k-tiles; epilogue h = silu(g)*u (fp32)
+//             item sharing the A k-tiles; epilogue h = silu(g)*u (fp32,
+//             stored blocked so that a warp's stores are contiguous: h_at)
 //   quant_h   quantise each fp32 h row into swizzled A tiles of the down GEMM
+//             (32 rows per CTA staged in shared memory from coalesced reads)
 //   gemm2     down: [rows x f] . [d x f]^T, each M-tile's A tile held in
 //             shared memory across its 16 N-tiles; epilogue scales by the routing
 //             weight (1 for the shared expert) and stores the contribution in
@@ -373,37 +375,40 @@ __device__ __forceinline__ float4* h_at(float* h, int f, int mt, int chunk, int 
 
 constexpr int kQhRows = 4;                       // rows per warp
 constexpr int kQhCtaRows = 8 * kQhRows;          // rows per CTA (8 warps): 32 consecutive rows of one M-tile
-constexpr int kQhPitch = 512 + 4;                // floats per staged row (f = 512; padded: conflict-free stores)
+// staged row: 32 chunks of 16 floats, each followed by 4 floats of padding,
+// plus 4: the staging stores (32 rows, one 16-byte piece) and the chunk reads
+// (one row, lane l at chunk l) both fall in distinct banks
+constexpr int kQhChunkPitch = 20;
+constexpr int kQhPitch = 32 * kQhChunkPitch + 4;
 constexpr int kQhSmem = kQhCtaRows * kQhPitch * 4;
 
 // Quantise each h row (fp32) into the down GEMM's A tiles and write the down
-// GEMM's per-row epilogue data. A CTA takes 32 consecutive rows: it reads them
-// from the blocked h with every warp load covering 512 contiguous bytes (32
-// rows of one 16-byte piece), stages them row-major in shared memory, then
-// each warp quantises 4 rows (lane l: elements 16 l .. 16 l + 15), resolving
-// the rows' slots and routing weights while the loads are in flight. Padding
-// rows get prow = -1.
+// GEMM's per-row epilogue data. A CTA takes 32 consecutive rows of one
+// M-tile, the last CTA the first rows (the gate/up GEMM wrote the high rows
+// last, so they are the likeliest still in L2). It reads them from the
+// blocked h with every warp load covering 512 contiguous bytes (32 rows of
+// one 16-byte piece), all loads issued before the rows' slot lookups, stages
+// them row-major in shared memory, then each warp quantises 4 rows (lane l:
+// elements 16 l .. 16 l + 15). Padding rows get prow = -1.
 template <int EPL>
 __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
     static_assert(EPL == 16, "a lane's elements are one 16-column chunk of the row");
     extern __shared__ __align__(16) float qhs[];   // [kQhCtaRows][kQhPitch]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KT = c.f / kGK;
-    // last CTA first: the gate/up GEMM wrote the high rows last
     const int rb = (gridDim.x - 1 - blockIdx.x) * kQhCtaRows;
     if (rb >= c.meta[2] * kGM) return;
-    const int mt_b = rb / kGM, rin = rb % kGM;
-    // all of this thread's loads first (thread t: row t % 32, pieces t / 32 + 8 k)
+    const int mt = rb / kGM, rin = rb % kGM;
+    // thread t loads row t % 32 of the CTA's rows, pieces t / 32 + 8 k
     constexpr int kPer = kQhCtaRows * (512 / 4) / 256;
     const int r_t = threadIdx.x % kQhCtaRows, cq0 = threadIdx.x / kQhCtaRows;
     float4 v[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
         const int cq = cq0 + 8 * k;   // chunk * 4 + float4 of the chunk
-        v[k] = *h_at(c.h, c.f, mt_b, cq >> 2, cq & 3, rin + r_t);
+        v[k] = *h_at(c.h, c.f, mt, cq >> 2, cq & 3, rin + r_t);
     }
-    const int row0 = rb + warp * kQhRows;
-    const int mt = row0 / kGM, r0 = row0 % kGM;
+    const int row0 = rb + warp * kQhRows, r0 = row0 % kGM;
     const int slot = c.mt_slot[mt], m = c.mt_m[mt];
     // lane i < kQhRows: position and epilogue scale of row row0 + i (-1: padding)
     int p = -1;
@@ -418,14 +423,18 @@ __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
     }
     uint8_t* blocks = c.a2 + (size_t)mt * KT * kGBlk;
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) *reinterpret_cast<float4*>(qhs + r_t * kQhPitch + (cq0 + 8 * k) * 4) = v[k];
+    for (int k = 0; k < kPer; ++k) {
+        const int cq = cq0 + 8 * k;
+        *reinterpret_cast<float4*>(qhs + r_t * kQhPitch + (cq >> 2) * kQhChunkPitch + (cq & 3) * 4) = v[k];
+    }
     __syncthreads();   // the CTA's rows are staged
     float4 raw[kQhRows][EPL / 4];
 #pragma unroll
     for (int i = 0; i < kQhRows; ++i)
 #pragma unroll
         for (int j = 0; j < EPL / 4; ++j)
-            raw[i][j] = *reinterpret_cast<const float4*>(qhs + (warp * kQhRows + i) * kQhPitch + lane * EPL + 4 * j);
+            raw[i][j] = *reinterpret_cast<const float4*>(qhs + (warp * kQhRows + i) * kQhPitch + lane * kQhChunkPitch +
+                                                         4 * j);
 #pragma unroll
     for (int i = 0; i < kQhRows; ++i) {
         const int pi = __shfl_sync(0xffffffffu, p, i);
@@ -852,7 +861,6 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     fp4_gemm_kernel<Gemm1><<<148, kGThreads, fp4_gemm_smem<Gemm1>(), st>>>(g1, ws.status);
     mark(2);
     static_assert(kGM % (8 * kQhRows) == 0, "a CTA's rows stay inside one M-tile");
-    static_assert(kQhCtaRows * kQhPitch >= kQhCtaRows * (512 + 4), "staging pitch");
     quant_h_kernel<16><<<(unsigned)(rt * kGM / kQhCtaRows), 256, kQhSmem, st>>>(c);
     mark(3);
     static_assert(Gemm2R::kNT * kGN == 2048 && kRKT * kGK == 512, "the Flint shape (d = 2048, f = 512)");

@@ -8,6 +8,8 @@
 // softmax renormalised over the chosen k.
 #include <float.h>
 
+#include <algorithm>
+
 #include "kernels.cuh"
 #include "topk.cuh"
 
@@ -198,6 +200,7 @@ struct RouterArgs {
 // 2*blockIdx + w/4.
 // ---------------------------------------------------------------------------
 constexpr int kTokGroup = 8;   // tokens per CTA (one warp per token)
+constexpr int kRouterExp = 4;  // experts per CTA
 // arrival counters of the token groups of router_small_kernel (after the
 // ones the expert kernels use)
 constexpr int kGroupCounters = kCounters - kSmallT / kTokGroup;
@@ -208,55 +211,63 @@ static_assert(kGroupCounters > 64, "counter ranges overlap");
 // computes both experts' dot products for token w of the group over the full
 // K, with 4 consecutive elements per lane per 128-element chunk.
 __global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouterArgs a) {
-    extern __shared__ __align__(128) uint8_t rsm[];   // [2][d] fp32 router rows, then [8][d] bf16 hidden rows
+    // [kRouterExp][d] fp32 router rows, then [8][d] bf16 hidden rows; the
+    // bucketing CTA reuses the buffer for its tables once its dot products
+    // are done
+    extern __shared__ __align__(128) uint8_t rsm[];
     __shared__ uint64_t rbar;
     __shared__ float red[32];
-    __shared__ int s_cnt[256];
-    __shared__ int s_offs[257];
-    __shared__ int s_wcnt[8 * 256];
     __shared__ int s_last;
+    int* s_wcnt = reinterpret_cast<int*>(rsm);   // [8][256]
+    int* s_cnt = s_wcnt + 8 * 256;               // [256]
+    int* s_offs = s_cnt + 256;                   // [257]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = a.T, d = a.d;
-    const int e0 = blockIdx.x * 2;
+    const int e0 = blockIdx.x * kRouterExp;
     const int t0 = blockIdx.y * kTokGroup;
     const int nt = min(kTokGroup, T - t0);
     const float* wsm = reinterpret_cast<const float*>(rsm);
-    const __nv_bfloat16* xsm = reinterpret_cast<const __nv_bfloat16*>(rsm + (size_t)2 * d * 4);
+    const __nv_bfloat16* xsm = reinterpret_cast<const __nv_bfloat16*>(rsm + (size_t)kRouterExp * d * 4);
     if (threadIdx.x == 0) {
         mbar_init(&rbar, 1);
         mbar_fence_init();
-        mbar_arrive_expect_tx(&rbar, (uint32_t)(2 * d * 4 + nt * d * 2));
-        bulk_g2s(rsm, a.wr + (size_t)e0 * d, (uint32_t)(2 * d * 4), &rbar);
-        bulk_g2s(rsm + (size_t)2 * d * 4, a.x + (size_t)t0 * d, (uint32_t)(nt * d * 2), &rbar);
+        mbar_arrive_expect_tx(&rbar, (uint32_t)(kRouterExp * d * 4 + nt * d * 2));
+        bulk_g2s(rsm, a.wr + (size_t)e0 * d, (uint32_t)(kRouterExp * d * 4), &rbar);
+        bulk_g2s(rsm + (size_t)kRouterExp * d * 4, a.x + (size_t)t0 * d, (uint32_t)(nt * d * 2), &rbar);
     }
-    const float b0 = a.bias[e0], b1 = a.bias[e0 + 1];
+    float bias[kRouterExp];
+#pragma unroll
+    for (int j = 0; j < kRouterExp; ++j) bias[j] = a.bias[e0 + j];
     __syncthreads();
     const bool w_ok = mbar_wait_bounded(&rbar, 0, a.ws.status);
     const bool ok = __syncthreads_and(w_ok ? 1 : 0) != 0;
     if (ok && warp < nt) {
         const __nv_bfloat16* xr = xsm + (size_t)warp * d;
-        float s0 = 0.f, s1 = 0.f;
+        float sj[kRouterExp];
+#pragma unroll
+        for (int j = 0; j < kRouterExp; ++j) sj[j] = 0.f;
         for (int i = lane * 4; i < d; i += 128) {
-            const float4 w0 = *reinterpret_cast<const float4*>(wsm + i);
-            const float4 w1 = *reinterpret_cast<const float4*>(wsm + d + i);
             const uint2 raw = *reinterpret_cast<const uint2*>(xr + i);
             const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
             const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
             const float x0 = __low2float(p0), x1 = __high2float(p0), x2 = __low2float(p1), x3 = __high2float(p1);
-            s0 = fmaf(w0.x, x0, s0);
-            s0 = fmaf(w0.y, x1, s0);
-            s0 = fmaf(w0.z, x2, s0);
-            s0 = fmaf(w0.w, x3, s0);
-            s1 = fmaf(w1.x, x0, s1);
-            s1 = fmaf(w1.y, x1, s1);
-            s1 = fmaf(w1.z, x2, s1);
-            s1 = fmaf(w1.w, x3, s1);
+#pragma unroll
+            for (int j = 0; j < kRouterExp; ++j) {
+                const float4 w = *reinterpret_cast<const float4*>(wsm + (size_t)j * d + i);
+                sj[j] = fmaf(w.x, x0, sj[j]);
+                sj[j] = fmaf(w.y, x1, sj[j]);
+                sj[j] = fmaf(w.z, x2, sj[j]);
+                sj[j] = fmaf(w.w, x3, sj[j]);
+            }
         }
-        s0 = warp_sum(s0);
-        s1 = warp_sum(s1);
-        if (lane == 0) {
-            a.ws.logits[(size_t)(t0 + warp) * a.E + e0] = s0 + b0;
-            a.ws.logits[(size_t)(t0 + warp) * a.E + e0 + 1] = s1 + b1;
+#pragma unroll
+        for (int j = 0; j < kRouterExp; ++j) sj[j] = warp_sum(sj[j]);
+        if (lane < kRouterExp) {
+            float v = sj[0] + bias[0];
+#pragma unroll
+            for (int j = 1; j < kRouterExp; ++j)
+                if (lane == j) v = sj[j] + bias[j];
+            a.ws.logits[(size_t)(t0 + warp) * a.E + e0 + lane] = v;
         }
     }
     // fp16 staging: CTA (p, g) with p < 8 stages token 8g + p
@@ -425,15 +436,50 @@ __global__ void __launch_bounds__(256) bucket_place_kernel(BucketArgs a) {
 // The order of the rows inside an expert is free on that path -- every row is
 // computed on its own and the combine reads rows by assignment -- so the
 // atomics' arrival order changes no result.
+// Top-k of 32 consecutive tokens per CTA (a warp takes 4, one after the
+// other), then every assignment's rank within its expert: ranks inside the
+// CTA from shared-memory counters, and one global atomic per (CTA, expert)
+// for the CTA's base, so a popular expert's counter sees one atomic per CTA
+// instead of one per assignment. Rows of one expert come out in an arbitrary
+// order, which changes no result (every row is computed on its own and the
+// combine finds it through inv).
+constexpr int kRankTokPerWarp = 4;
+
 __global__ void __launch_bounds__(256) token_rank_kernel(RouterArgs a) {
+    __shared__ int s_cnt[256];
+    __shared__ int s_base[256];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + warp;
-    if (t >= a.T) return;
-    topk_warp<false>(a.ws.logits + (size_t)t * a.E, a.E, a.k, a.ws.idx + t * a.k, a.ws.w + t * a.k, a.ws.status);
-    __syncwarp();
-    if (lane < a.k) {
-        const int e = a.ws.idx[t * a.k + lane];
-        a.ws.inv[t * a.k + lane] = atomicAdd(a.ws.ecount + e, 1);
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_cnt[e] = 0;
+    __syncthreads();
+    int eid[kRankTokPerWarp], loc[kRankTokPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRankTokPerWarp; ++i) {
+        const int t = (blockIdx.x * 8 + warp) * kRankTokPerWarp + i;
+        eid[i] = -1;
+        loc[i] = 0;
+        if (t < a.T) {
+            topk_warp<false>(a.ws.logits + (size_t)t * a.E, a.E, a.k, a.ws.idx + t * a.k, a.ws.w + t * a.k,
+                             a.ws.status);
+            __syncwarp();
+            if (lane < a.k) {
+                const int e = a.ws.idx[t * a.k + lane];
+                if (e >= 0 && e < a.E) {
+                    eid[i] = e;
+                    loc[i] = atomicAdd(&s_cnt[e], 1);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+        const int n = s_cnt[e];
+        s_base[e] = n > 0 ? atomicAdd(a.ws.ecount + e, n) : 0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kRankTokPerWarp; ++i) {
+        const int t = (blockIdx.x * 8 + warp) * kRankTokPerWarp + i;
+        if (eid[i] >= 0) a.ws.inv[t * a.k + lane] = s_base[eid[i]] + loc[i];
     }
 }
 
@@ -491,13 +537,22 @@ cudaError_t prepare_router() {
     return e;
 }
 
+namespace {
+// the router rows and hidden rows, or the bucketing tables if larger
+size_t router_small_smem(const Shape& s) {
+    return std::max((size_t)kRouterExp * s.d * 4 + (size_t)kTokGroup * s.d * 2, (size_t)(8 * 256 + 256 + 257) * 4);
+}
+}  // namespace
+
+bool router_fused(const Shape& s, int T) { return T <= kSmallT && router_small_smem(s) <= kRouterDynSmemMax; }
+
 cudaError_t launch_router(const Shape& s, const LayerDev& L, const __nv_bfloat16* x, int T,
                           const Workspace& ws, cudaStream_t st, int* n_launch, bool stage_x16) {
     RouterArgs a = make_args(s, L, x, T, ws);
     a.stage_x16 = stage_x16 ? 1 : 0;
-    const size_t smem = (size_t)2 * s.d * 4 + (size_t)kTokGroup * s.d * 2;
-    if (T <= kSmallT && smem <= kRouterDynSmemMax) {
-        router_small_kernel<<<dim3(s.E / 2, (T + kTokGroup - 1) / kTokGroup), kRouterThreads, smem, st>>>(a);
+    const size_t smem = router_small_smem(s);
+    if (router_fused(s, T)) {
+        router_small_kernel<<<dim3(s.E / kRouterExp, (T + kTokGroup - 1) / kTokGroup), kRouterThreads, smem, st>>>(a);
         *n_launch += 1;
         return cudaGetLastError();
     }
@@ -525,7 +580,7 @@ cudaError_t launch_router_fp4(const Shape& s, const LayerDev& L, const __nv_bflo
         dim3 g1((T + kLTok - 1) / kLTok, (s.E + kLExp - 1) / kLExp);
         router_logits_tiled<<<g1, 256, 0, st>>>(a);
     }
-    token_rank_kernel<<<(T + 7) / 8, 256, 0, st>>>(a);
+    token_rank_kernel<<<(T + 8 * kRankTokPerWarp - 1) / (8 * kRankTokPerWarp), 256, 0, st>>>(a);
     *n_launch += 2;
     return cudaGetLastError();
 }
