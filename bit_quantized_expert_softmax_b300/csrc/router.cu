@@ -200,7 +200,7 @@ struct RouterArgs {
 // 2*blockIdx + w/4.
 // ---------------------------------------------------------------------------
 constexpr int kTokGroup = 8;   // tokens per CTA (one warp per token)
-constexpr int kRouterExp = 4;  // experts per CTA
+constexpr int kRouterExp = 2;  // experts per CTA
 // arrival counters of the token groups of router_small_kernel (after the
 // ones the expert kernels use)
 constexpr int kGroupCounters = kCounters - kSmallT / kTokGroup;
