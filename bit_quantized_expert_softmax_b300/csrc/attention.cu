@@ -157,16 +157,20 @@ __global__ void __launch_bounds__(256, 2) attn_decode_kernel(AttnArgs a) {
 
     // rows past the window's end are zero-filled: their probabilities are 0
     // and 0 * (stale bits) must not make a NaN
+    // one modulo per tile: a tile's 64 rows wrap the ring at most once (cap >= 64
+    // whenever a window is cached: cap >= window; full attention: cap > pos)
     auto load_tile = [&](int tile, int st) {
         const int p0 = first + tile * kATile;
+        const int s0 = p0 % a.cap;
         uint8_t* kd = kbuf(st);
         uint8_t* vd = vbuf(st);
         for (int i = threadIdx.x; i < kATile * 16; i += blockDim.x) {
             const int r = i >> 4, c = i & 15;
             if (p0 + r < pos) {
-                const size_t slot = (size_t)((p0 + r) % a.cap);
-                cp_async16(kd + r * kARow + c * 16, kcg + slot * kAD + c * 8);
-                cp_async16(vd + r * kARow + c * 16, vcg + slot * kAD + c * 8);
+                int slot = s0 + r;
+                while (slot >= a.cap) slot -= a.cap;
+                cp_async16(kd + r * kARow + c * 16, kcg + (size_t)slot * kAD + c * 8);
+                cp_async16(vd + r * kARow + c * 16, vcg + (size_t)slot * kAD + c * 8);
             } else {
                 *reinterpret_cast<uint4*>(kd + r * kARow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4*>(vd + r * kARow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
