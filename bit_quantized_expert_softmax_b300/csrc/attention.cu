@@ -15,6 +15,8 @@
 // weighted sum keep about 16 significant bits per operand. The softmax is
 // online (running max and sum per head, in fp32). The current token's key and
 // value enter unrounded and are then stored, bf16, in its cache slot.
+#include <cmath>
+
 #include "../../include/flint_moe.h"
 #include "kernels.cuh"
 
@@ -40,7 +42,10 @@ struct AttnArgs {
     const float* sinks;        // [H]
     __nv_bfloat16* out;        // [B][H][128]
     int H, KV, window, cap, rope;
-    double log2_theta;
+    // rotary frequency of pair i as a fraction of a turn per position, in
+    // 2^-64 turns: pos * rope_turns[i] (64-bit, wrapping) is the angle
+    // modulo one turn, exactly up to the table's rounding
+    unsigned long long rope_turns[kAD / 2];
     float eps;
 };
 
@@ -64,13 +69,14 @@ __device__ __forceinline__ void norm_rope(float (&v)[4], const float* w, int lan
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int i = lane + 32 * j;   // pair index
-            // the angle in double and reduced modulo 2 pi, so that large
-            // positions keep full precision
-            const double f = exp2(-(double)i / 64.0 * a.log2_theta);
-            double ang = (double)pos * f;
-            ang -= 6.283185307179586476925 * floor(ang / 6.283185307179586476925);
+            // the angle as a fraction of a turn: integer arithmetic keeps
+            // large positions exact; the top 24 bits, in half-turns, go to
+            // sincospif
+            const unsigned long long turns = (unsigned long long)(unsigned)pos * a.rope_turns[i];
+            // rounded to 24 bits (2^24 is a whole turn: sin and cos come out right)
+            const float half_turns = (float)(unsigned)((turns + (1ull << 39)) >> 40) * 0x1p-23f;   // in [0, 2]
             float sn, cs;
-            sincosf((float)ang, &sn, &cs);
+            sincospif(half_turns, &sn, &cs);
             const float x0 = v[j], x1 = v[j + 2];
             v[j] = x0 * cs - x1 * sn;
             v[j + 2] = x0 * sn + x1 * cs;
@@ -367,7 +373,14 @@ extern "C" flint_status flint_moe_attn_decode(const flint_moe_attn_config* cfg, 
     a.window = cfg->window;
     a.cap = cfg->cap;
     a.rope = cfg->rope;
-    a.log2_theta = log2((double)cfg->rope_theta);
+    // frequencies theta^(-i/64) in turns per position, as 64-bit fractions
+    // (long double: 64 significant bits on the host)
+    for (int i = 0; i < kAD / 2; ++i) {
+        const long double f = powl((long double)cfg->rope_theta, -(long double)i / (kAD / 2));
+        const long double t = f / (2.0L * 3.14159265358979323846264338327950288L);   // turns per position
+        const long double frac = t - floorl(t);
+        a.rope_turns[i] = (unsigned long long)(frac * 18446744073709551616.0L);
+    }
     a.eps = cfg->eps;
     static bool opted_in = false;   // the attribute is per device function, set once
     if (!opted_in) {

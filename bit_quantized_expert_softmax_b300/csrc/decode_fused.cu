@@ -638,7 +638,9 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_fused_kernel(FusedArgs a)
 // whatever order the CTAs arrive in and every run gives the same bits. The
 // accumulators and their non-finite flags are zero between launches.
 // ---------------------------------------------------------------------------
-constexpr double kRaccScale = 4294967296.0;   // 2^32 units per logit
+// 2^32 units per logit: a power of two, so the scaling to and from the
+// fixed-point grid is exact in fp32 and each conversion rounds once
+constexpr float kRaccScale = 4294967296.0f;
 
 struct StackArgs {
     FusedArgs f;                     // shape, shared-memory plan, h scratch, status
@@ -667,7 +669,7 @@ __device__ void router_partials(const StackArgs& sa, const float* rslab, const f
         if (!(fabsf(p) <= 1.0e9f)) {   // non-finite, or beyond the fixed-point range
             atomicOr(sa.rnf + o, 1u);
         } else {
-            const long long q = __double2ll_rn((double)p * kRaccScale);
+            const long long q = __float2ll_rn(p * kRaccScale);
             atomicAdd(sa.racc + o, (unsigned long long)q);
         }
     }
@@ -834,7 +836,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
         if (threadIdx.x < n_ts) tss[threadIdx.x] = ts0;
         if (threadIdx.x + kFThreads < n_ts) tss[threadIdx.x + kFThreads] = ts1;
         if (threadIdx.x < T * E) {
-            const float v = (float)((double)qsum * (1.0 / kRaccScale)) + bias_v;
+            const float v = __ll2float_rn(qsum) * (1.0f / kRaccScale) + bias_v;
             lg[(threadIdx.x / E) * 256 + (threadIdx.x % E)] = nf ? __int_as_float(0x7fc00000) : v;
         }
         // the other accumulator is filled by this layer's P2; its last readers
