@@ -436,14 +436,15 @@ __global__ void __launch_bounds__(256) bucket_place_kernel(BucketArgs a) {
 // The order of the rows inside an expert is free on that path -- every row is
 // computed on its own and the combine reads rows by assignment -- so the
 // atomics' arrival order changes no result.
-// Top-k of 32 consecutive tokens per CTA (a warp takes 4, one after the
-// other), then every assignment's rank within its expert: ranks inside the
-// CTA from shared-memory counters, and one global atomic per (CTA, expert)
-// for the CTA's base, so a popular expert's counter sees one atomic per CTA
-// instead of one per assignment. Rows of one expert come out in an arbitrary
+// Top-k of 8 consecutive tokens per CTA (one per warp), then every
+// assignment's rank within its expert: ranks inside the CTA from
+// shared-memory counters, and one global atomic per (CTA, expert) for the
+// CTA's base, so a popular expert's counter sees one atomic per CTA instead
+// of one per assignment (four tokens per warp, one after the other, measured
+// slower: the top-k chains are serial). Rows of one expert come out in an arbitrary
 // order, which changes no result (every row is computed on its own and the
 // combine finds it through inv).
-constexpr int kRankTokPerWarp = 4;
+constexpr int kRankTokPerWarp = 1;
 
 __global__ void __launch_bounds__(256) token_rank_kernel(RouterArgs a) {
     __shared__ int s_cnt[256];
