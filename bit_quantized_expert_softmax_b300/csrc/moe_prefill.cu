@@ -623,50 +623,46 @@ struct Gemm2R {
 // issued before the first add.
 __global__ void __launch_bounds__(256) combine_kernel(PrefillCtx c, __nv_bfloat16* __restrict__ out,
                                                       const __nv_bfloat16* __restrict__ residual) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int t = blockIdx.x * 8 + warp; t < c.T; t += gridDim.x * 8) {
-        const __nv_bfloat16* rows[9];   // fully unrolled below: kept in registers
-        rows[0] = c.y + ((size_t)c.T * c.k + t) * c.d;
+    // one CTA per token, 8 columns per thread: every contribution's load is
+    // issued before the first is used
+    const int t = blockIdx.x, col = threadIdx.x * 8;
+    if (t >= c.T || col >= c.d) return;
+    uint4 r[9];
+    r[0] = __ldcs(reinterpret_cast<const uint4*>(c.y + ((size_t)c.T * c.k + t) * c.d + col));
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            rows[j + 1] = j < c.k ? c.y + (size_t)__ldg(c.inv + t * c.k + j) * c.d : rows[0];
-        for (int col = lane * 16; col < c.d; col += 512) {
-            uint4 r[9][2];
+    for (int j = 0; j < 8; ++j)
+        if (j < c.k) r[j + 1] = __ldcs(reinterpret_cast<const uint4*>(c.y + (size_t)__ldg(c.inv + t * c.k + j) * c.d + col));
+    // shared + slot 0 + ... + slot k-1, in that order, in fp32
+    float acc[8];
+    unpack8(r[0], acc);
 #pragma unroll
-            for (int j = 0; j <= 8; ++j) {
-                if (j <= c.k) {
-                    r[j][0] = __ldcs(reinterpret_cast<const uint4*>(rows[j] + col));
-                    r[j][1] = __ldcs(reinterpret_cast<const uint4*>(rows[j] + col + 8));
-                }
-            }
-            float acc[16];
-            unpack8(r[0][0], acc);
-            unpack8(r[0][1], acc + 8);
+    for (int j = 1; j <= 8; ++j) {
+        if (j <= c.k) {
+            float v[8];
+            unpack8(r[j], v);
 #pragma unroll
-            for (int j = 1; j <= 8; ++j) {
-                if (j <= c.k) {
-                    float v[16];
-                    unpack8(r[j][0], v);
-                    unpack8(r[j][1], v + 8);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[i] += v[i];
-                }
-            }
-            uint32_t o[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                __nv_bfloat16 b0 = __float2bfloat16_rn(acc[2 * u]), b1 = __float2bfloat16_rn(acc[2 * u + 1]);
-                if (residual != nullptr) {
-                    const __nv_bfloat16* rr = residual + (size_t)t * c.d + col + 2 * u;
-                    b0 = __float2bfloat16_rn(__bfloat162float(rr[0]) + __bfloat162float(b0));
-                    b1 = __float2bfloat16_rn(__bfloat162float(rr[1]) + __bfloat162float(b1));
-                }
-                o[u] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
-            }
-            *reinterpret_cast<uint4*>(out + (size_t)t * c.d + col) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(out + (size_t)t * c.d + col + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+            for (int i = 0; i < 8; ++i) acc[i] += v[i];
         }
     }
+    uint32_t o[4];
+    if (residual != nullptr) {
+        float rv[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(residual + (size_t)t * c.d + col)), rv);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const __nv_bfloat16 b0 = __float2bfloat16_rn(rv[2 * u] + __bfloat162float(__float2bfloat16_rn(acc[2 * u])));
+            const __nv_bfloat16 b1 =
+                __float2bfloat16_rn(rv[2 * u + 1] + __bfloat162float(__float2bfloat16_rn(acc[2 * u + 1])));
+            o[u] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const __nv_bfloat16 b0 = __float2bfloat16_rn(acc[2 * u]), b1 = __float2bfloat16_rn(acc[2 * u + 1]);
+            o[u] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
+        }
+    }
+    *reinterpret_cast<uint4*>(out + (size_t)t * c.d + col) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // Gate/up weights -> blocks (swizzled tile + scales) with gate and up
@@ -867,7 +863,7 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     Gemm2R g2{Gemm2{c, s.d / kGN, s.f / kGK}};
     fp4_gemm_resa_kernel<Gemm2R><<<148, kGThreads, fp4_gemm_resa_smem<Gemm2R>(), st>>>(g2, ws.status);
     mark(4);
-    combine_kernel<<<(T + 7) / 8 < 148 * 8 ? (T + 7) / 8 : 148 * 8, 256, 0, st>>>(c, out, residual);
+    combine_kernel<<<T, s.d / 8, 0, st>>>(c, out, residual);   // one CTA per token, 8 columns per thread
     mark(5);
     *n_launch += 6;
     return cudaGetLastError();
