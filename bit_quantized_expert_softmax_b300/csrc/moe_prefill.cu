@@ -359,12 +359,6 @@ __global__ void __launch_bounds__(256, 3) quant_x_kernel(PrefillCtx c) {
     }
 }
 
-// Quantise each h row (fp32, f elements) into the down GEMM's A tiles and
-// write the down GEMM's per-row epilogue data. A warp takes kQhRows
-// consecutive padded rows (one M-tile's): it loads all of their h first (the
-// buffer holds every row the grid covers, so the loads need no lookup), then
-// resolves the rows' slots and routing weights while those loads are in
-// flight. Warps past the actual rows return; padding rows get prow = -1.
 // h between the two GEMMs, fp32, blocked so that a warp of the gate/up
 // epilogue (one accumulator row per lane) stores 512 contiguous bytes: per
 // M-tile, per 16-column chunk, per float4 of the chunk, the M-tile's 128 rows
@@ -374,7 +368,9 @@ __device__ __forceinline__ float4* h_at(float* h, int f, int mt, int chunk, int 
 }
 
 constexpr int kQhRows = 4;                       // rows per warp
-constexpr int kQhCtaRows = 8 * kQhRows;          // rows per CTA (8 warps): 32 consecutive rows of one M-tile
+constexpr int kQhWarps = 4;
+constexpr int kQhThreads = 32 * kQhWarps;
+constexpr int kQhCtaRows = kQhWarps * kQhRows;   // consecutive rows of one M-tile per CTA
 // staged row: 32 chunks of 16 floats, each followed by 4 floats of padding,
 // plus 4: the staging stores (32 rows, one 16-byte piece) and the chunk reads
 // (one row, lane l at chunk l) both fall in distinct banks
@@ -383,15 +379,15 @@ constexpr int kQhPitch = 32 * kQhChunkPitch + 4;
 constexpr int kQhSmem = kQhCtaRows * kQhPitch * 4;
 
 // Quantise each h row (fp32) into the down GEMM's A tiles and write the down
-// GEMM's per-row epilogue data. A CTA takes 32 consecutive rows of one
-// M-tile, the last CTA the first rows (the gate/up GEMM wrote the high rows
+// GEMM's per-row epilogue data. A CTA takes kQhCtaRows consecutive rows of
+// one M-tile, the last CTA the first rows (the gate/up GEMM wrote the high rows
 // last, so they are the likeliest still in L2). It reads them from the
 // blocked h with every warp load covering 512 contiguous bytes (32 rows of
 // one 16-byte piece), all loads issued before the rows' slot lookups, stages
 // them row-major in shared memory, then each warp quantises 4 rows (lane l:
 // elements 16 l .. 16 l + 15). Padding rows get prow = -1.
 template <int EPL>
-__global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
+__global__ void __launch_bounds__(kQhThreads) quant_h_kernel(PrefillCtx c) {
     static_assert(EPL == 16, "a lane's elements are one 16-column chunk of the row");
     extern __shared__ __align__(16) float qhs[];   // [kQhCtaRows][kQhPitch]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -399,8 +395,9 @@ __global__ void __launch_bounds__(256) quant_h_kernel(PrefillCtx c) {
     const int rb = (gridDim.x - 1 - blockIdx.x) * kQhCtaRows;
     if (rb >= c.meta[2] * kGM) return;
     const int mt = rb / kGM, rin = rb % kGM;
-    // thread t loads row t % 32 of the CTA's rows, pieces t / 32 + 8 k
-    constexpr int kPer = kQhCtaRows * (512 / 4) / 256;
+    // thread t loads row t % kQhCtaRows of the CTA's rows, pieces
+    // t / kQhCtaRows + 8 k (kQhThreads / kQhCtaRows = 8)
+    constexpr int kPer = kQhCtaRows * (512 / 4) / kQhThreads;
     const int r_t = threadIdx.x % kQhCtaRows, cq0 = threadIdx.x / kQhCtaRows;
     float4 v[kPer];
 #pragma unroll
@@ -856,8 +853,8 @@ cudaError_t launch_prefill_experts(const Shape& s, const LayerDev& L, const __nv
     Gemm1 g1{c, 2 * s.f / kGN, s.d / kGK};
     fp4_gemm_kernel<Gemm1><<<148, kGThreads, fp4_gemm_smem<Gemm1>(), st>>>(g1, ws.status);
     mark(2);
-    static_assert(kGM % (8 * kQhRows) == 0, "a CTA's rows stay inside one M-tile");
-    quant_h_kernel<16><<<(unsigned)(rt * kGM / kQhCtaRows), 256, kQhSmem, st>>>(c);
+    static_assert(kGM % kQhCtaRows == 0, "a CTA's rows stay inside one M-tile");
+    quant_h_kernel<16><<<(unsigned)(rt * kGM / kQhCtaRows), kQhThreads, kQhSmem, st>>>(c);
     mark(3);
     static_assert(Gemm2R::kNT * kGN == 2048 && kRKT * kGK == 512, "the Flint shape (d = 2048, f = 512)");
     Gemm2R g2{Gemm2{c, s.d / kGN, s.f / kGK}};
