@@ -120,7 +120,7 @@ Workspace carve(const Shape& s, char* base, size_t* total) {
     w.perm = cv.take<int>(Tm * s.k);
     w.inv = cv.take<int>(Tm * s.k);
     w.offsets = cv.take<int>(s.E + 1);
-    w.ecount = cv.take<int>(s.E);
+    w.ecount = cv.take<int>((size_t)s.E * flint::kEcountStride);
     w.slot_expert = cv.take<int>(s.E + 1);
     w.slot_off = cv.take<int>(s.E + 1);
     w.slot_cnt = cv.take<int>(s.E + 1);
@@ -594,7 +594,7 @@ flint_status flint_moe_status(flint_moe* h) {
         if (e == cudaSuccess) e = cudaMemset(h->ws.rnf, 0, nacc * 4);
         if (e == cudaSuccess)
             e = cudaMemset(h->ws.gbar8, 0, (size_t)flint::kGridGroups * flint::kGridGroupStride * 8);
-        if (e == cudaSuccess) e = cudaMemset(h->ws.ecount, 0, (size_t)h->s.E * sizeof(int));
+        if (e == cudaSuccess) e = cudaMemset(h->ws.ecount, 0, (size_t)h->s.E * flint::kEcountStride * sizeof(int));
     }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return FLINT_ECUDA;

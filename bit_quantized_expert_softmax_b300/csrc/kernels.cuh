@@ -69,7 +69,8 @@ struct Workspace {
     int* perm;            // [Tm*k]  sorted position -> assignment t*k+j
     int* inv;             // [Tm*k]  assignment -> sorted position
     int* offsets;         // [E+1]
-    int* ecount;          // [E]    per-expert assignment counters of the FP4 path (zero between forwards)
+    int* ecount;          // [E * kEcountStride] per-expert assignment counters of the FP4 path, one per
+                          //        128-byte line (zero between forwards)
     int* slot_expert;     // [E+1]  active slot -> expert (E = shared)
     int* slot_off;        // [E+1]  first position of the slot
     int* slot_cnt;        // [E+1]  positions of the slot
@@ -99,6 +100,7 @@ struct FusedScratch {
 
 constexpr int kCounters = 1024;
 constexpr int kBucketChunk = 2048;      // assignments per bucketing CTA
+constexpr int kEcountStride = 32;       // ints between two experts' counters in ws.ecount
 constexpr int kRaccCopies = 8;          // copies of the decode stack's router accumulators (atomics spread)
 constexpr int kSmallT = 64;             // fused router (logits + top-k + bucketing) up to this many tokens
 constexpr int kFuseCombineT = 8;        // combine in the down kernel's last CTA up to this many tokens

@@ -221,8 +221,8 @@ __global__ void __launch_bounds__(256) scan_plan_kernel(PrefillCtx c, int* __res
     __shared__ int s_ns, s_total;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = threadIdx.x;
-    const int cnt = e < c.E ? ecount[e] : 0;
-    if (e < c.E) ecount[e] = 0;
+    const int cnt = e < c.E ? ecount[e * kEcountStride] : 0;
+    if (e < c.E) ecount[e * kEcountStride] = 0;
     // exclusive scan of (count | active << 20)
     int x = cnt | ((cnt > 0 ? 1 : 0) << 20);
     const int v = x;

@@ -17,7 +17,7 @@ namespace flint {
 
 namespace {
 
-constexpr int kRouterThreads = 256;   // 8 warps: 2 experts x 4 K-quarters
+constexpr int kRouterThreads = 256;   // 8 warps
 
 // ---------------------------------------------------------------------------
 // fp16 staging of one token: per-token power-of-two scale, fragment order
@@ -196,27 +196,54 @@ struct RouterArgs {
 // ---------------------------------------------------------------------------
 // Fused decode router (T <= 64): logits, fp16 staging, and -- in the last CTA
 // to finish -- top-k, renormalised weights and bucketing.
-// grid = E/2 CTAs; warp w computes a quarter of the dot products of expert
-// 2*blockIdx + w/4.
+//
+// grid = (E/8 expert groups, ceil(T/16) token groups). A CTA bulk-copies its 8
+// fp32 router rows and its (up to) 16 bf16 hidden rows into shared memory and
+// forms the 16 x 8 logit tile on the tensor cores (mma.sync m16n8k16, bf16
+// operands, fp32 accumulation): the hidden states are bf16 and exact as the A
+// operand; each fp32 router weight is split in registers into
+// hi = bf16(w) and lo = bf16(w - hi), and the two products are accumulated,
+// which keeps ~16 significant bits of w (relative error of a logit ~2^-16,
+// inside the router's 1e-4 tolerance). Warp w takes the 16-element K steps
+// w, w + 8, ...; the 8 partial tiles are summed in a fixed order.
 // ---------------------------------------------------------------------------
-constexpr int kTokGroup = 8;   // tokens per CTA (one warp per token)
-constexpr int kRouterExp = 2;  // experts per CTA
+constexpr int kTokGroup = 16;   // tokens per CTA: the M of the tile
+constexpr int kRouterExp = 8;   // experts per CTA: the N of the tile
 // arrival counters of the token groups of router_small_kernel (after the
 // ones the expert kernels use)
 constexpr int kGroupCounters = kCounters - kSmallT / kTokGroup;
 static_assert(kGroupCounters > 64, "counter ranges overlap");
 
-// grid = (E/2 expert pairs, ceil(T/8) token groups). Each CTA bulk-copies its
-// two router rows and its (up to) 8 hidden rows into shared memory; warp w
-// computes both experts' dot products for token w of the group over the full
-// K, with 4 consecutive elements per lane per 128-element chunk.
+// Shared-memory row pitches: 32 bytes past a router row and 16 past a hidden
+// row, so that the fragment loads of 8 rows hit distinct banks.
+__host__ __device__ __forceinline__ size_t rs_wpitch(int d) { return (size_t)d * 4 + 32; }
+__host__ __device__ __forceinline__ size_t rs_xpitch(int d) { return (size_t)d * 2 + 16; }
+
+// bf16 x bf16 -> fp32 m16n8k16 (A row-major 16 x 16, B "col" 16 x 8)
+__device__ __forceinline__ void rmma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// two fp32 weights (consecutive K) -> their bf16 hi pair and lo pair
+__device__ __forceinline__ void split_pair(float2 w, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(w.x, w.y);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(w.x - __low2float(h), w.y - __high2float(h));
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 __global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouterArgs a) {
-    // [kRouterExp][d] fp32 router rows, then [8][d] bf16 hidden rows; the
-    // bucketing CTA reuses the buffer for its tables once its dot products
-    // are done
+    // [8][d] fp32 router rows, then [16][d] bf16 hidden rows (padded pitches);
+    // the bucketing CTA reuses the buffer for its tables once its logits are
+    // done
     extern __shared__ __align__(128) uint8_t rsm[];
     __shared__ uint64_t rbar;
     __shared__ float red[32];
+    __shared__ float part[8][kTokGroup * kRouterExp];
     __shared__ int s_last;
     int* s_wcnt = reinterpret_cast<int*>(rsm);   // [8][256]
     int* s_cnt = s_wcnt + 8 * 256;               // [256]
@@ -226,53 +253,60 @@ __global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouterArgs
     const int e0 = blockIdx.x * kRouterExp;
     const int t0 = blockIdx.y * kTokGroup;
     const int nt = min(kTokGroup, T - t0);
-    const float* wsm = reinterpret_cast<const float*>(rsm);
-    const __nv_bfloat16* xsm = reinterpret_cast<const __nv_bfloat16*>(rsm + (size_t)kRouterExp * d * 4);
+    const size_t wp = rs_wpitch(d), xp = rs_xpitch(d);
+    uint8_t* wsm = rsm;
+    uint8_t* xsm = rsm + kRouterExp * wp;
     if (threadIdx.x == 0) {
         mbar_init(&rbar, 1);
         mbar_fence_init();
         mbar_arrive_expect_tx(&rbar, (uint32_t)(kRouterExp * d * 4 + nt * d * 2));
-        bulk_g2s(rsm, a.wr + (size_t)e0 * d, (uint32_t)(kRouterExp * d * 4), &rbar);
-        bulk_g2s(rsm + (size_t)kRouterExp * d * 4, a.x + (size_t)t0 * d, (uint32_t)(nt * d * 2), &rbar);
+        for (int j = 0; j < kRouterExp; ++j)
+            bulk_g2s(wsm + j * wp, a.wr + (size_t)(e0 + j) * d, (uint32_t)(d * 4), &rbar);
+        for (int r = 0; r < nt; ++r) bulk_g2s(xsm + r * xp, a.x + (size_t)(t0 + r) * d, (uint32_t)(d * 2), &rbar);
     }
-    float bias[kRouterExp];
-#pragma unroll
-    for (int j = 0; j < kRouterExp; ++j) bias[j] = a.bias[e0 + j];
+    // rows of absent tokens are zero (their logits are not stored)
+    for (int r = nt; r < kTokGroup; ++r)
+        for (int i = threadIdx.x; i < d / 8; i += blockDim.x)
+            *reinterpret_cast<uint4*>(xsm + r * xp + i * 16) = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     const bool w_ok = mbar_wait_bounded(&rbar, 0, a.ws.status);
     const bool ok = __syncthreads_and(w_ok ? 1 : 0) != 0;
-    if (ok && warp < nt) {
-        const __nv_bfloat16* xr = xsm + (size_t)warp * d;
-        float sj[kRouterExp];
-#pragma unroll
-        for (int j = 0; j < kRouterExp; ++j) sj[j] = 0.f;
-        for (int i = lane * 4; i < d; i += 128) {
-            const uint2 raw = *reinterpret_cast<const uint2*>(xr + i);
-            const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-            const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-            const float x0 = __low2float(p0), x1 = __high2float(p0), x2 = __low2float(p1), x3 = __high2float(p1);
-#pragma unroll
-            for (int j = 0; j < kRouterExp; ++j) {
-                const float4 w = *reinterpret_cast<const float4*>(wsm + (size_t)j * d + i);
-                sj[j] = fmaf(w.x, x0, sj[j]);
-                sj[j] = fmaf(w.y, x1, sj[j]);
-                sj[j] = fmaf(w.z, x2, sj[j]);
-                sj[j] = fmaf(w.w, x3, sj[j]);
-            }
+    if (ok) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        // A (ldmatrix x4): lanes 0-7 rows 0-7 / 8-15 rows 8-15 at K 0..7,
+        // lanes 16-31 the same rows at K 8..15
+        const uint8_t* arow = xsm + ((lane & 7) + 8 * ((lane >> 3) & 1)) * xp + 16 * (lane >> 4);
+        // B: expert lane/4, K pair 2 (lane % 4) and that pair + 8
+        const float* brow = reinterpret_cast<const float*>(wsm + (lane >> 2) * wp) + 2 * (lane & 3);
+        for (int k0 = warp * 16; k0 < d; k0 += 8 * 16) {
+            uint32_t af[4];
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(af[0]), "=r"(af[1]), "=r"(af[2]), "=r"(af[3])
+                         : "r"(smem_u32(arow + k0 * 2)));
+            uint32_t h0, l0, h1, l1;
+            split_pair(*reinterpret_cast<const float2*>(brow + k0), h0, l0);
+            split_pair(*reinterpret_cast<const float2*>(brow + k0 + 8), h1, l1);
+            rmma_bf16(c, af, h0, h1);
+            rmma_bf16(c, af, l0, l1);
         }
-#pragma unroll
-        for (int j = 0; j < kRouterExp; ++j) sj[j] = warp_sum(sj[j]);
-        if (lane < kRouterExp) {
-            float v = sj[0] + bias[0];
-#pragma unroll
-            for (int j = 1; j < kRouterExp; ++j)
-                if (lane == j) v = sj[j] + bias[j];
-            a.ws.logits[(size_t)(t0 + warp) * a.E + e0 + lane] = v;
-        }
+        // C: rows lane/4 (c0, c1) and lane/4 + 8 (c2, c3), columns 2 (lane % 4) + {0, 1}
+        const int r = lane >> 2, col = 2 * (lane & 3);
+        part[warp][r * kRouterExp + col] = c[0];
+        part[warp][r * kRouterExp + col + 1] = c[1];
+        part[warp][(r + 8) * kRouterExp + col] = c[2];
+        part[warp][(r + 8) * kRouterExp + col + 1] = c[3];
     }
-    // fp16 staging: CTA (p, g) with p < 8 stages token 8g + p
-    if (blockIdx.x < kTokGroup && (int)blockIdx.x < nt) {
-        const int t = t0 + blockIdx.x;
+    __syncthreads();
+    if (ok && threadIdx.x < kTokGroup * kRouterExp) {
+        const int r = threadIdx.x / kRouterExp, col = threadIdx.x % kRouterExp;
+        float s = part[0][threadIdx.x];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) s += part[w][threadIdx.x];
+        if (r < nt) a.ws.logits[(size_t)(t0 + r) * a.E + e0 + col] = s + a.bias[e0 + col];
+    }
+    // fp16 staging: CTA (p, g) stages tokens 16g + p, 16g + p + gridDim.x, ...
+    for (int p = blockIdx.x; p < nt; p += gridDim.x) {
+        const int t = t0 + p;
         stage_token_block(a.x + (size_t)t * d, d, a.ws.x16 + (size_t)t * d, a.ws.xinv + t, red);
     }
 
@@ -287,9 +321,9 @@ __global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouterArgs
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    if (warp < nt)
-        topk_warp<true>(a.ws.logits + (size_t)(t0 + warp) * a.E, a.E, a.k, a.ws.idx + (t0 + warp) * a.k,
-                        a.ws.w + (t0 + warp) * a.k, a.ws.status);
+    for (int r = warp; r < nt; r += 8)
+        topk_warp<true>(a.ws.logits + (size_t)(t0 + r) * a.E, a.E, a.k, a.ws.idx + (t0 + r) * a.k,
+                        a.ws.w + (t0 + r) * a.k, a.ws.status);
     if (threadIdx.x == 0) a.ws.counters[kGroupCounters + blockIdx.y] = 0u;
     // ... and the last token group to finish buckets all of them
     __threadfence();
@@ -459,11 +493,9 @@ __global__ void __launch_bounds__(256) token_rank_kernel(RouterArgs a) {
         eid[i] = -1;
         loc[i] = 0;
         if (t < a.T) {
-            topk_warp<false>(a.ws.logits + (size_t)t * a.E, a.E, a.k, a.ws.idx + t * a.k, a.ws.w + t * a.k,
-                             a.ws.status);
-            __syncwarp();
+            const int e = topk_warp<false>(a.ws.logits + (size_t)t * a.E, a.E, a.k, a.ws.idx + t * a.k,
+                                           a.ws.w + t * a.k, a.ws.status);
             if (lane < a.k) {
-                const int e = a.ws.idx[t * a.k + lane];
                 if (e >= 0 && e < a.E) {
                     eid[i] = e;
                     loc[i] = atomicAdd(&s_cnt[e], 1);
@@ -474,7 +506,7 @@ __global__ void __launch_bounds__(256) token_rank_kernel(RouterArgs a) {
     __syncthreads();
     for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
         const int n = s_cnt[e];
-        s_base[e] = n > 0 ? atomicAdd(a.ws.ecount + e, n) : 0;
+        s_base[e] = n > 0 ? atomicAdd(a.ws.ecount + e * kEcountStride, n) : 0;
     }
     __syncthreads();
 #pragma unroll
@@ -541,7 +573,8 @@ cudaError_t prepare_router() {
 namespace {
 // the router rows and hidden rows, or the bucketing tables if larger
 size_t router_small_smem(const Shape& s) {
-    return std::max((size_t)kRouterExp * s.d * 4 + (size_t)kTokGroup * s.d * 2, (size_t)(8 * 256 + 256 + 257) * 4);
+    return std::max((size_t)kRouterExp * rs_wpitch(s.d) + (size_t)kTokGroup * rs_xpitch(s.d),
+                    (size_t)(8 * 256 + 256 + 257) * 4);
 }
 }  // namespace
 

@@ -10,8 +10,9 @@ namespace flint {
 // ---------------------------------------------------------------------------
 // kCG: read the logits with ld.global.cg (global memory written by other CTAs
 // of the same kernel); otherwise a generic load (shared or global memory).
+// Returns, in lane j < k, the expert of selection j (-1 in the other lanes).
 template <bool kCG>
-__device__ __forceinline__ void topk_warp(const float* __restrict__ Lrow, int E, int k, int* __restrict__ idx_out,
+__device__ __forceinline__ int topk_warp(const float* __restrict__ Lrow, int E, int k, int* __restrict__ idx_out,
                           float* __restrict__ w_out, uint32_t* status) {
     const int lane = threadIdx.x & 31;
     const int n = E >> 5;
@@ -76,6 +77,7 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ Lrow, int E,
         idx_out[lane] = my_i;
         if (w_out != nullptr) w_out[lane] = ex / sum;
     }
+    return lane < k ? my_i : -1;
 }
 
 }  // namespace flint
