@@ -377,6 +377,7 @@ constexpr int kGuRedBytes = kRingWarps * 2 * kNB * 32 * 4 * 4;   // the warps' K
 
 // down task: 16 output rows per warp (two tile rows each), full K
 constexpr int kDnRows = 16 * kRingWarps;
+constexpr int kDnChunk = 4;   // consecutive down tasks (row blocks of one pass) a CTA takes at once
 __host__ __device__ __forceinline__ uint32_t dn_stage_bytes(int KTf, int wfmt) {
     return 2u * kRingWarps * (uint32_t)KTf * (512u + (uint32_t)scale_tile_bytes(wfmt));
 }
@@ -470,15 +471,21 @@ __device__ __forceinline__ int4 ring_decode(const RingHead* hd, int ns, int unit
 }
 
 // Thread 0: fill number `fill` into stage fill % stages. Takes the next task
-// from the counter (unless the counter has run out before); with no task
-// left, records slot -1 and completes the stage's phase with a plain arrival.
+// of the chunk [next, end) it holds, or a new chunk of `chunk` consecutive
+// tasks from the counter (unless the counter has run out before); with no
+// task left, records slot -1 and completes the stage's phase with a plain
+// arrival.
 template <class Issue>
 __device__ __forceinline__ void ring_fill(RingHead* hd, int stages, uint32_t fill, int ns, int units,
-                                          unsigned* ctr, bool& out, Issue issue) {
+                                          unsigned* ctr, int chunk, int& next, int& end, bool& out, Issue issue) {
     const int s = (int)(fill % (uint32_t)stages);
     int t = -1;
     if (!out) {
-        t = (int)atomicAdd(ctr, 1u);
+        if (next >= end) {
+            next = (int)atomicAdd(ctr, (unsigned)chunk);
+            end = next + chunk;
+        }
+        t = next++;
         if (t >= hd->n_tasks) {
             t = -1;
             out = true;
@@ -601,11 +608,12 @@ __global__ void __launch_bounds__(kRingThreads, kRingCtasPerSm) gateup_ring_kern
     const int ns = min(a.ws.meta[0], kRingMaxSlots);
     uint32_t fills = 0;
     bool out = false;
+    int tnext = 0, tend = 0;   // one task per grab
     auto issue = [&](int4 tk, int s) {
         gu_issue<WFMT>(a, tk, KT, ring + s * stage_bytes, &hd->full[s]);
     };
     if (threadIdx.x == 0)
-        for (; (int)fills < stages; ++fills) ring_fill(hd, stages, fills, ns, units, ctr, out, issue);
+        for (; (int)fills < stages; ++fills) ring_fill(hd, stages, fills, ns, units, ctr, 1, tnext, tend, out, issue);
     auto R = [&](int w, int m, int nt, int j) -> float& { return red[(((w * 2 + m) * kNB + nt) * 32 + lane) * 4 + j]; };
     for (int i = 0;; ++i) {
         if (!ring_acquire(hd->full, stages, i, a.ws.status)) break;
@@ -676,7 +684,7 @@ __global__ void __launch_bounds__(kRingThreads, kRingCtasPerSm) gateup_ring_kern
         __syncthreads();   // partials written; every thread is done with the stage's weights
         if (threadIdx.x == 0) {
             fence_proxy_async_smem();
-            ring_fill(hd, stages, fills, ns, units, ctr, out, issue);
+            ring_fill(hd, stages, fills, ns, units, ctr, 1, tnext, tend, out, issue);
             ++fills;
         }
         if (warp < nb) gu_epilogue(a, red, warp, lane, n0, p0, cnt, r16, tsg, tsu);
@@ -721,11 +729,14 @@ __global__ void __launch_bounds__(kRingThreads, kRingCtasPerSm) down_ring_kernel
     const int ns = min(a.ws.meta[0], kRingMaxSlots);
     uint32_t fills = 0;
     bool out = false;
+    int tnext = 0, tend = 0;   // kDnChunk consecutive tasks per grab
     auto issue = [&](int4 tk, int s) {
         dn_issue<WFMT>(a, tk, KTf, ring + s * stage_bytes, &hd->full[s]);
     };
     if (threadIdx.x == 0)
-        for (; (int)fills < stages; ++fills) ring_fill(hd, stages, fills, ns, units, ctr, out, issue);
+        for (; (int)fills < stages; ++fills)
+            ring_fill(hd, stages, fills, ns, units, ctr, kDnChunk, tnext, tend, out, issue);
+    int st_slot = -1, st_pass = -1;   // the (slot, pass) whose h is in hs
     for (int i = 0;; ++i) {
         if (!ring_acquire(hd->full, stages, i, a.ws.status)) break;
         const int4 tk = hd->task[i % stages];
@@ -740,17 +751,35 @@ __global__ void __launch_bounds__(kRingThreads, kRingCtasPerSm) down_ring_kernel
         const uint8_t* ss_ = st + cb;     // their scales
         const int np = min(kDownPos, cnt - n0);
         const int nb = (np + 7) >> 3;
-        if (threadIdx.x < np) hmul[threadIdx.x] = f16_range_mult(__uint_as_float(a.ws.hamax[p0 + n0 + threadIdx.x]));
-        __syncthreads();
-        const int row_f4 = a.f >> 2;
-        for (int q = threadIdx.x; q < np * row_f4; q += kRingThreads) {
-            const int pl = q / row_f4, r = q - pl * row_f4;
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws.hf + (size_t)(p0 + n0 + pl) * a.f) + r);
-            const float m = hmul[pl];
-            *reinterpret_cast<uint2*>(hs + (size_t)pl * a.f + r * 4) =
-                make_uint2(pack_half2(v.x * m, v.y * m), pack_half2(v.z * m, v.w * m));
+        if (slot != st_slot || tk.z != st_pass) {
+            // stage the pass's h once for the consecutive row blocks of one
+            // (slot, pass) this CTA takes: 8 float4 loads in flight per thread
+            if (threadIdx.x < np)
+                hmul[threadIdx.x] = f16_range_mult(__uint_as_float(a.ws.hamax[p0 + n0 + threadIdx.x]));
+            __syncthreads();
+            const int row_f4 = a.f >> 2, total = np * row_f4;
+            const float4* src = reinterpret_cast<const float4*>(a.ws.hf + (size_t)(p0 + n0) * a.f);
+            for (int q0 = threadIdx.x; q0 < total; q0 += 8 * kRingThreads) {
+                float4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int q = q0 + u * kRingThreads;
+                    if (q < total) v[u] = __ldcg(src + q);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int q = q0 + u * kRingThreads;
+                    if (q < total) {
+                        const float m = hmul[q / row_f4];
+                        *reinterpret_cast<uint2*>(hs + (size_t)q * 4) =
+                            make_uint2(pack_half2(v[u].x * m, v[u].y * m), pack_half2(v[u].z * m, v[u].w * m));
+                    }
+                }
+            }
+            __syncthreads();
+            st_slot = slot;
+            st_pass = tk.z;
         }
-        __syncthreads();
         float acc[kNB][4];
 #pragma unroll
         for (int q = 0; q < kNB; ++q)
@@ -790,7 +819,7 @@ __global__ void __launch_bounds__(kRingThreads, kRingCtasPerSm) down_ring_kernel
         __syncthreads();   // every thread is done with the stage's weights and with hs
         if (threadIdx.x == 0) {
             fence_proxy_async_smem();
-            ring_fill(hd, stages, fills, ns, units, ctr, out, issue);
+            ring_fill(hd, stages, fills, ns, units, ctr, kDnChunk, tnext, tend, out, issue);
             ++fills;
         }
         // rows g, g + 8 of this warp's 16; positions 2c, 2c + 1 of each n-tile

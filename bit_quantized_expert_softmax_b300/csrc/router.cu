@@ -305,9 +305,11 @@ __global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouterArgs
         if (r < nt) a.ws.logits[(size_t)(t0 + r) * a.E + e0 + col] = s + a.bias[e0 + col];
     }
     // fp16 staging: CTA (p, g) stages tokens 16g + p, 16g + p + gridDim.x, ...
+    // from its own copy of the hidden rows
     for (int p = blockIdx.x; p < nt; p += gridDim.x) {
         const int t = t0 + p;
-        stage_token_block(a.x + (size_t)t * d, d, a.ws.x16 + (size_t)t * d, a.ws.xinv + t, red);
+        const __nv_bfloat16* xr = ok ? reinterpret_cast<const __nv_bfloat16*>(xsm + p * xp) : a.x + (size_t)t * d;
+        stage_token_block(xr, d, a.ws.x16 + (size_t)t * d, a.ws.xinv + t, red);
     }
 
     // the last CTA of this token group takes the top-k of its tokens (a warp
