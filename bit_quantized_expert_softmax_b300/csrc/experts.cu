@@ -390,7 +390,9 @@ struct RingHead {
     int4 task[kRingMaxStages];        // slot (-1: no task), unit, pass, -
     int wsum[kRingWarps];
     int n_tasks;
-    int pre[kRingMaxSlots + 1];       // slot s owns tasks [pre[s], pre[s + 1])
+    int pre[kRingMaxSlots + 1];       // the slot of rank r owns tasks [pre[r], pre[r + 1])
+    int ord[kRingMaxSlots];           // rank -> slot
+    int cnt[kRingMaxSlots];           // positions of each slot
 };
 constexpr uint32_t kRingHeadBytes = (sizeof(RingHead) + 127) / 128 * 128;
 
@@ -415,11 +417,27 @@ __host__ __forceinline__ RingLayout dn_layout(const Shape& s) {
     return ring_layout(dn_stage_bytes(s.f >> 7, s.wfmt), kRingHeadBytes + kDownPos * 4 + dn_hs_bytes(s.f));
 }
 
-// The task table: every thread takes consecutive slots, one block scan.
+// The task table. Slots are ranked by their number of positions, most first
+// (ties: lower slot first), so that the tasks of full passes -- the shared
+// expert's and the popular experts' -- are handed out before the short ones
+// and the last tasks to start are the cheapest. Every CTA computes the same
+// table. Then every thread takes consecutive ranks, one block scan.
 // units: row units per pass of a slot. Returns the number of tasks.
 __device__ int ring_task_table(const ExpertArgs& a, int units, RingHead* hd) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ns = min(a.ws.meta[0], kRingMaxSlots);
+    for (int sl = threadIdx.x; sl < ns; sl += kRingThreads) hd->cnt[sl] = a.ws.slot_cnt[sl];
+    __syncthreads();
+    for (int sl = threadIdx.x; sl < ns; sl += kRingThreads) {
+        const int c = hd->cnt[sl];
+        int r = 0;
+        for (int j = 0; j < ns; ++j) {
+            const int cj = hd->cnt[j];
+            r += (cj > c || (cj == c && j < sl)) ? 1 : 0;
+        }
+        hd->ord[r] = sl;
+    }
+    __syncthreads();
     const int per = (ns + kRingThreads - 1) / kRingThreads;
     const int s0 = threadIdx.x * per;
     int mine[kRingMaxSlots / kRingThreads];
@@ -427,7 +445,7 @@ __device__ int ring_task_table(const ExpertArgs& a, int units, RingHead* hd) {
 #pragma unroll
     for (int j = 0; j < kRingMaxSlots / kRingThreads; ++j) {
         const int sl = s0 + j;
-        mine[j] = (j < per && sl < ns) ? units * ((a.ws.slot_cnt[sl] + 8 * kNB - 1) / (8 * kNB)) : 0;
+        mine[j] = (j < per && sl < ns) ? units * ((hd->cnt[hd->ord[sl]] + 8 * kNB - 1) / (8 * kNB)) : 0;
         local += mine[j];
     }
     int x = local;
@@ -467,7 +485,7 @@ __device__ __forceinline__ int4 ring_decode(const RingHead* hd, int ns, int unit
         if (hd->pre[mid] <= t) lo = mid; else hi = mid;
     }
     const int r = t - hd->pre[lo];
-    return make_int4(lo, r % units, r / units, 0);
+    return make_int4(hd->ord[lo], r % units, r / units, 0);
 }
 
 // Thread 0: fill number `fill` into stage fill % stages. Takes the next task
