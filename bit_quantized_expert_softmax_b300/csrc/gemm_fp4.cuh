@@ -34,6 +34,7 @@
 // quadrants hold the same data. The MMA is given the first of its 4 columns.
 #pragma once
 
+#include "pdl.cuh"
 #include "umma.cuh"
 
 namespace flint {
@@ -99,6 +100,7 @@ constexpr int fp4_gemm_smem() {
 // description of its next item before it waits on the current one.
 template <class P>
 __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_kernel(const P prob, uint32_t* status) {
+    griddep_wait();
     extern __shared__ uint8_t graw[];
     constexpr int kGStages = P::kStages;
     constexpr int kNB = P::kNB;
@@ -352,6 +354,7 @@ constexpr int fp4_gemm_resa_smem() {
 
 template <class P>
 __global__ void __launch_bounds__(kGThreads, 1) fp4_gemm_resa_kernel(const P prob, uint32_t* status) {
+    griddep_wait();
     extern __shared__ uint8_t graw[];
     constexpr int kS = P::kStages;
     constexpr int kNT = P::kNT;

@@ -17,6 +17,7 @@
 #include <cudaTypedefs.h>
 
 #include "kernels.cuh"
+#include "pdl.cuh"
 #include "umma.cuh"
 
 namespace flint {
@@ -39,6 +40,7 @@ struct RouterUmmaArgs {
 __global__ void __launch_bounds__(kRThreads, 1)
     router_umma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mwh,
                        const __grid_constant__ CUtensorMap mwl, RouterUmmaArgs a) {
+    griddep_wait();
     extern __shared__ uint8_t rsm_raw[];
     __shared__ __align__(8) uint64_t full[kRStages], empty[kRStages], done;
     __shared__ uint32_t tmem_base;
@@ -195,8 +197,7 @@ cudaError_t launch_router_umma(const Shape& s, const LayerDev& L, const __nv_bfl
     if (!make_tmap_bf16(&mx, x, T, s.d)) return cudaErrorInvalidValue;
     RouterUmmaArgs a{logits, L.bias, T, s.E, s.d / kRK, status};
     dim3 grid((T + kRM - 1) / kRM, s.E / kRN);
-    router_umma_kernel<<<grid, kRThreads, kRSmem, st>>>(mx, L.tmap_router_hi, L.tmap_router_lo, a);
-    return cudaGetLastError();
+    return launch_pdl(router_umma_kernel, grid, dim3(kRThreads), kRSmem, st, mx, L.tmap_router_hi, L.tmap_router_lo, a);
 }
 
 }  // namespace flint

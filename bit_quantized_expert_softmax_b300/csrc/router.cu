@@ -11,6 +11,7 @@
 #include <algorithm>
 
 #include "kernels.cuh"
+#include "pdl.cuh"
 #include "topk.cuh"
 
 namespace flint {
@@ -483,6 +484,7 @@ __global__ void __launch_bounds__(256) bucket_place_kernel(BucketArgs a) {
 constexpr int kRankTokPerWarp = 1;
 
 __global__ void __launch_bounds__(256) token_rank_kernel(RouterArgs a) {
+    griddep_wait();
     __shared__ int s_cnt[256];
     __shared__ int s_base[256];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -616,9 +618,10 @@ cudaError_t launch_router_fp4(const Shape& s, const LayerDev& L, const __nv_bflo
         dim3 g1((T + kLTok - 1) / kLTok, (s.E + kLExp - 1) / kLExp);
         router_logits_tiled<<<g1, 256, 0, st>>>(a);
     }
-    token_rank_kernel<<<(T + 8 * kRankTokPerWarp - 1) / (8 * kRankTokPerWarp), 256, 0, st>>>(a);
+    const cudaError_t e = launch_pdl(token_rank_kernel, dim3((T + 8 * kRankTokPerWarp - 1) / (8 * kRankTokPerWarp)),
+                                     dim3(256), 0, st, a);
     *n_launch += 2;
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int* idx, float* w,
