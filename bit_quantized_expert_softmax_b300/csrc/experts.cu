@@ -17,6 +17,7 @@
 #include <cstdlib>
 
 #include "kernels.cuh"
+#include "pdl.cuh"
 #include "tiles.cuh"
 #include "umma.cuh"
 
@@ -50,6 +51,7 @@ __device__ __forceinline__ int token_of(const ExpertArgs& a, int pos) {
 // ---------------------------------------------------------------------------
 template <int WFMT>
 __global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertArgs a) {
+    griddep_wait();
     __shared__ float red[4][2][kNB][32][4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
@@ -221,6 +223,7 @@ static_assert(kDownPos >= kFuseCombineT, "the fused combine counts one arrival p
 
 template <int WFMT>
 __global__ void __launch_bounds__(kThreads) down_kernel(ExpertArgs a) {
+    griddep_wait();
     __shared__ __align__(16) __half hs[kDownPos * kDownKC * 128];   // [position][chunk K], fp16
     __shared__ float hmul[kDownPos];
     __shared__ int s_last;
@@ -607,6 +610,7 @@ __device__ __forceinline__ void gu_issue(const ExpertArgs& a, int4 tk, int KT, u
 // memory.
 template <int WFMT>
 __global__ void __launch_bounds__(kRingThreads, kRingCtasPerSm) gateup_ring_kernel(ExpertArgs a, int stages, uint32_t stage_bytes) {
+    griddep_wait();
     extern __shared__ __align__(128) uint8_t rsm[];
     RingHead* hd = reinterpret_cast<RingHead*>(rsm);
     float* red = reinterpret_cast<float*>(rsm + kRingHeadBytes);    // [warps][2][kNB][32][4]
@@ -727,6 +731,7 @@ __device__ __forceinline__ void dn_issue(const ExpertArgs& a, int4 tk, int KTf, 
 // kernel (every T this kernel serves).
 template <int WFMT>
 __global__ void __launch_bounds__(kRingThreads, kRingCtasPerSm) down_ring_kernel(ExpertArgs a, int stages, uint32_t stage_bytes) {
+    griddep_wait();
     extern __shared__ __align__(128) uint8_t rsm[];
     RingHead* hd = reinterpret_cast<RingHead*>(rsm);
     float* hmul = reinterpret_cast<float*>(rsm + kRingHeadBytes);                       // [kDownPos]
@@ -864,6 +869,7 @@ __global__ void __launch_bounds__(kRingThreads, kRingCtasPerSm) down_ring_kernel
 }
 
 __global__ void __launch_bounds__(256) combine_kernel(ExpertArgs a) {
+    griddep_wait();
     const int rows_per_cta = 256;
     const int nblk = (a.d + rows_per_cta - 1) / rows_per_cta;
     const int t = blockIdx.x / nblk;
@@ -945,31 +951,30 @@ cudaError_t prepare_experts() {
     return cudaSuccess;
 }
 
+// Every kernel of the decode-path chain (router, gate/up, down, combine) is
+// launched with programmatic serialisation and waits for its predecessor at
+// its first statement (pdl.cuh).
 cudaError_t launch_gateup(const Shape& s, const LayerDev& L, int T, const Workspace& ws,
                           cudaStream_t st, int* n_launch) {
     ExpertArgs a = make_args(s, L, T, ws);
     const int max_slots = min(s.E, T * s.k) + s.n_shared;
     const RingLayout rl = gu_layout(s);
+    *n_launch += 1;
     if (T > kFuseCombineT && T <= kSmallT && rl.stages >= 2 && ring_enabled()) {
         int dev = 0, n_sms = 148;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
         const int grid = ring_grid(max_slots * (s.f / 16), kRingCtasPerSm * n_sms);
         if (s.wfmt == 0)
-            gateup_ring_kernel<0><<<grid, kRingThreads, rl.smem, st>>>(a, rl.stages, rl.stage_bytes);
-        else
-            gateup_ring_kernel<1><<<grid, kRingThreads, rl.smem, st>>>(a, rl.stages, rl.stage_bytes);
-        *n_launch += 1;
-        return cudaGetLastError();
+            return launch_pdl(gateup_ring_kernel<0>, dim3(grid), dim3(kRingThreads), rl.smem, st, a, rl.stages,
+                              rl.stage_bytes);
+        return launch_pdl(gateup_ring_kernel<1>, dim3(grid), dim3(kRingThreads), rl.smem, st, a, rl.stages,
+                          rl.stage_bytes);
     }
     const int max_pass = (T + 8 * kNB - 1) / (8 * kNB);
     const int grid = grid_for(max_slots * (s.f / 16) * max_pass);
-    if (s.wfmt == 0)
-        gateup_kernel<0><<<grid, kThreads, 0, st>>>(a);
-    else
-        gateup_kernel<1><<<grid, kThreads, 0, st>>>(a);
-    *n_launch += 1;
-    return cudaGetLastError();
+    if (s.wfmt == 0) return launch_pdl(gateup_kernel<0>, dim3(grid), dim3(kThreads), 0, st, a);
+    return launch_pdl(gateup_kernel<1>, dim3(grid), dim3(kThreads), 0, st, a);
 }
 
 cudaError_t launch_down(const Shape& s, const LayerDev& L, int T, const Workspace& ws,
@@ -981,6 +986,7 @@ cudaError_t launch_down(const Shape& s, const LayerDev& L, int T, const Workspac
     const int max_slots = min(s.E, T * s.k) + s.n_shared;
     const RingLayout rl = dn_layout(s);
     const bool ring = T > kFuseCombineT && T <= kSmallT && rl.stages >= 2 && ring_enabled();
+    cudaError_t e;
     if (ring) {
         a.fuse_combine = 0;   // the ring kernel leaves the combine to its own kernel
         int dev = 0, n_sms = 148;
@@ -988,24 +994,26 @@ cudaError_t launch_down(const Shape& s, const LayerDev& L, int T, const Workspac
         cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
         const int grid = ring_grid(max_slots * (s.d / kDnRows), kRingCtasPerSm * n_sms);
         if (s.wfmt == 0)
-            down_ring_kernel<0><<<grid, kRingThreads, rl.smem, st>>>(a, rl.stages, rl.stage_bytes);
+            e = launch_pdl(down_ring_kernel<0>, dim3(grid), dim3(kRingThreads), rl.smem, st, a, rl.stages,
+                           rl.stage_bytes);
         else
-            down_ring_kernel<1><<<grid, kRingThreads, rl.smem, st>>>(a, rl.stages, rl.stage_bytes);
+            e = launch_pdl(down_ring_kernel<1>, dim3(grid), dim3(kRingThreads), rl.smem, st, a, rl.stages,
+                           rl.stage_bytes);
     } else {
         const int max_pass = (T + kDownPos - 1) / kDownPos;
         const int grid = grid_for(max_slots * (s.d / 64) * max_pass);
         if (s.wfmt == 0)
-            down_kernel<0><<<grid, kThreads, 0, st>>>(a);
+            e = launch_pdl(down_kernel<0>, dim3(grid), dim3(kThreads), 0, st, a);
         else
-            down_kernel<1><<<grid, kThreads, 0, st>>>(a);
+            e = launch_pdl(down_kernel<1>, dim3(grid), dim3(kThreads), 0, st, a);
     }
     *n_launch += 1;
-    if (!a.fuse_combine) {
+    if (e == cudaSuccess && !a.fuse_combine) {
         const int nblk = (s.d + 255) / 256;
-        combine_kernel<<<T * nblk, 256, 0, st>>>(a);
+        e = launch_pdl(combine_kernel, dim3(T * nblk), dim3(256), 0, st, a);
         *n_launch += 1;
     }
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace flint

@@ -238,6 +238,7 @@ __device__ __forceinline__ void split_pair(float2 w, uint32_t& hi, uint32_t& lo)
 }
 
 __global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouterArgs a) {
+    griddep_wait();
     // [8][d] fp32 router rows, then [16][d] bf16 hidden rows (padded pitches);
     // the bucketing CTA reuses the buffer for its tables once its logits are
     // done
@@ -361,6 +362,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_small_kernel(RouterArgs
 constexpr int kLTok = 64, kLExp = 64, kLK = 32;
 
 __global__ void __launch_bounds__(256) router_logits_tiled(RouterArgs a) {
+    griddep_wait();
     __shared__ float xs[kLK][kLTok + 1];
     __shared__ float ws_[kLK][kLExp + 1];
     const int t0 = blockIdx.x * kLTok, e0 = blockIdx.y * kLExp;
@@ -403,6 +405,7 @@ __global__ void __launch_bounds__(256) router_logits_tiled(RouterArgs a) {
 }
 
 __global__ void __launch_bounds__(256) token_prep_kernel(RouterArgs a) {
+    griddep_wait();
     const int warp = threadIdx.x >> 5;
     const int t = blockIdx.x * 8 + warp;
     if (t >= a.T) return;
@@ -419,6 +422,7 @@ struct BucketArgs {
 };
 
 __global__ void __launch_bounds__(256) bucket_hist_kernel(BucketArgs a) {
+    griddep_wait();
     __shared__ int cnt[256];
     for (int i = threadIdx.x; i < a.E; i += blockDim.x) cnt[i] = 0;
     __syncthreads();
@@ -430,6 +434,7 @@ __global__ void __launch_bounds__(256) bucket_hist_kernel(BucketArgs a) {
 }
 
 __global__ void __launch_bounds__(256) bucket_scan_kernel(BucketArgs a, int n_chunks) {
+    griddep_wait();
     __shared__ int cnt[256];
     __shared__ int offs[257];
     for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
@@ -457,6 +462,7 @@ __global__ void __launch_bounds__(256) bucket_scan_kernel(BucketArgs a, int n_ch
 }
 
 __global__ void __launch_bounds__(256) bucket_place_kernel(BucketArgs a) {
+    griddep_wait();
     __shared__ int base[256];
     __shared__ int wcnt[8 * 256];
     for (int i = threadIdx.x; i < a.E; i += blockDim.x) base[i] = a.ws.chunk_hist[blockIdx.x * a.E + i];
@@ -557,11 +563,11 @@ cudaError_t launch_bucket(const Shape& s, const int* idx, int T, const Workspace
     b.n_shared = s.n_shared;
     b.ws = ws;
     const int n_chunks = (b.n + kBucketChunk - 1) / kBucketChunk;
-    bucket_hist_kernel<<<n_chunks, 256, 0, st>>>(b);
-    bucket_scan_kernel<<<1, 256, 0, st>>>(b, n_chunks);
-    bucket_place_kernel<<<n_chunks, 256, 0, st>>>(b);
+    cudaError_t e = launch_pdl(bucket_hist_kernel, dim3(n_chunks), dim3(256), 0, st, b);
+    if (e == cudaSuccess) e = launch_pdl(bucket_scan_kernel, dim3(1), dim3(256), 0, st, b, n_chunks);
+    if (e == cudaSuccess) e = launch_pdl(bucket_place_kernel, dim3(n_chunks), dim3(256), 0, st, b);
     *n_launch += 3;
-    return cudaGetLastError();
+    return e;
 }
 
 // Dynamic shared memory the fused router may use (set once per device).
@@ -590,18 +596,20 @@ cudaError_t launch_router(const Shape& s, const LayerDev& L, const __nv_bfloat16
     a.stage_x16 = stage_x16 ? 1 : 0;
     const size_t smem = router_small_smem(s);
     if (router_fused(s, T)) {
-        router_small_kernel<<<dim3(s.E / kRouterExp, (T + kTokGroup - 1) / kTokGroup), kRouterThreads, smem, st>>>(a);
         *n_launch += 1;
-        return cudaGetLastError();
+        return launch_pdl(router_small_kernel, dim3(s.E / kRouterExp, (T + kTokGroup - 1) / kTokGroup),
+                          dim3(kRouterThreads), smem, st, a);
     }
     if (L.umma_router) {
         const cudaError_t e = launch_router_umma(s, L, x, T, ws.logits, ws.status, st);
         if (e != cudaSuccess) return e;
     } else {
         dim3 g1((T + kLTok - 1) / kLTok, (s.E + kLExp - 1) / kLExp);
-        router_logits_tiled<<<g1, 256, 0, st>>>(a);
+        const cudaError_t e = launch_pdl(router_logits_tiled, g1, dim3(256), 0, st, a);
+        if (e != cudaSuccess) return e;
     }
-    token_prep_kernel<<<(T + 7) / 8, 256, 0, st>>>(a);
+    const cudaError_t e = launch_pdl(token_prep_kernel, dim3((T + 7) / 8), dim3(256), 0, st, a);
+    if (e != cudaSuccess) return e;
     *n_launch += 2;
     // the FP4 expert path (no fp16 staging) does not use the h maxima
     return launch_bucket(s, ws.idx, T, ws, st, n_launch, stage_x16);
@@ -616,7 +624,8 @@ cudaError_t launch_router_fp4(const Shape& s, const LayerDev& L, const __nv_bflo
         if (e != cudaSuccess) return e;
     } else {
         dim3 g1((T + kLTok - 1) / kLTok, (s.E + kLExp - 1) / kLExp);
-        router_logits_tiled<<<g1, 256, 0, st>>>(a);
+        const cudaError_t el = launch_pdl(router_logits_tiled, g1, dim3(256), 0, st, a);
+        if (el != cudaSuccess) return el;
     }
     const cudaError_t e = launch_pdl(token_rank_kernel, dim3((T + 8 * kRankTokPerWarp - 1) / (8 * kRankTokPerWarp)),
                                      dim3(256), 0, st, a);
