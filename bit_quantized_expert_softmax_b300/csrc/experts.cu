@@ -380,7 +380,7 @@ constexpr int kGuRedBytes = kRingWarps * 2 * kNB * 32 * 4 * 4;   // the warps' K
 
 // down task: 16 output rows per warp (two tile rows each), full K
 constexpr int kDnRows = 16 * kRingWarps;
-constexpr int kDnChunk = 4;   // consecutive down tasks (row blocks of one pass) a CTA takes at once
+constexpr int kDnChunk = 2;   // consecutive down tasks (row blocks of one pass) a CTA takes at once
 __host__ __device__ __forceinline__ uint32_t dn_stage_bytes(int KTf, int wfmt) {
     return 2u * kRingWarps * (uint32_t)KTf * (512u + (uint32_t)scale_tile_bytes(wfmt));
 }

@@ -23,6 +23,7 @@
 // the last CTA of a token merges the parts' candidates into the token's top-k
 // and draws (see sample_from_topk).
 #include "kernels.cuh"
+#include "pdl.cuh"
 #include "tiles.cuh"
 
 namespace flint {
@@ -109,6 +110,7 @@ __device__ __forceinline__ void head_store(const HeadArgs& a, int unit, int g, i
 }
 
 __global__ void __launch_bounds__(kHeadThreads, 1) head_gemv_kernel(HeadArgs a) {
+    griddep_wait();
     extern __shared__ __align__(16) uint8_t hsm[];
     __half* x16 = reinterpret_cast<__half*>(hsm);                              // [T][d]
     float* xinv = reinterpret_cast<float*>(hsm + (size_t)a.T * a.d * 2);      // [kHeadMaxT]
@@ -289,6 +291,7 @@ __device__ __forceinline__ int sample_from_topk(float sv, int si, int K, float t
 // grid (parts, T): CTA (p, t) takes the top-K of logits [p*2048, (p+1)*2048)
 // of token t; the last CTA of the token merges the parts' candidates and draws.
 __global__ void __launch_bounds__(kSampleThreads) head_sample_kernel(SampleArgs a) {
+    griddep_wait();
     __shared__ unsigned long long best3[3];
     __shared__ uint32_t sel_key[32], sel_idx[32];
     __shared__ int s_last;
@@ -369,8 +372,7 @@ cudaError_t launch_head_gemv(const uint8_t* codes, const uint8_t* scales, float 
     if (T < 1 || T > kHeadMaxT || d % 128 != 0 || d > kHeadMaxD || V % 8 != 0 || V <= 0)
         return cudaErrorInvalidValue;
     HeadArgs a{codes, scales, tscale, x, logits, T, d, V};
-    head_gemv_kernel<<<n_sms, kHeadThreads, head_smem_bytes(T, d), st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(head_gemv_kernel, dim3(n_sms), dim3(kHeadThreads), head_smem_bytes(T, d), st, a);
 }
 
 int head_sample_parts(int V) { return (V + kSampleSlice - 1) / kSampleSlice; }
@@ -398,8 +400,7 @@ cudaError_t launch_head_sample(const float* logits, int T, int V, float temperat
     a.counters = hs.counters;
     a.status = status;
     a.parts = head_sample_parts(V);
-    head_sample_kernel<<<dim3(a.parts, T), kSampleThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(head_sample_kernel, dim3(a.parts, T), dim3(kSampleThreads), 0, st, a);
 }
 
 }  // namespace flint

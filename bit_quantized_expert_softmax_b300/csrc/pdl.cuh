@@ -1,5 +1,6 @@
 // Programmatic dependent launch for chains of kernels on one stream (the
-// prefill layer's eight kernels): a kernel launched with launch_pdl may be
+// prefill layer's eight kernels, the decode-path router, expert and combine
+// kernels, the output head's GEMV and sampler): a kernel launched with launch_pdl may be
 // launched while the kernel before it in the stream is still finishing, so
 // that its launch overlaps the end of that kernel instead of following it.
 //
