@@ -384,7 +384,11 @@ constexpr int kDnChunk = 2;   // consecutive down tasks (row blocks of one pass)
 __host__ __device__ __forceinline__ uint32_t dn_stage_bytes(int KTf, int wfmt) {
     return 2u * kRingWarps * (uint32_t)KTf * (512u + (uint32_t)scale_tile_bytes(wfmt));
 }
-__host__ __device__ __forceinline__ uint32_t dn_hs_bytes(int f) { return (uint32_t)kDownPos * f * 2; }
+// staged h rows: f fp16 + 8 of padding, so that the fragment reads of the
+// 8 positions of an n-tile (rows otherwise a multiple of 128 bytes apart) fall
+// in distinct banks
+__host__ __device__ __forceinline__ int dn_hs_pitch(int f) { return f + 8; }
+__host__ __device__ __forceinline__ uint32_t dn_hs_bytes(int f) { return (uint32_t)kDownPos * dn_hs_pitch(f) * 2; }
 
 // shared memory in front of the ring: barriers and task records, then the
 // task table, then the kernel's own buffer
@@ -741,6 +745,7 @@ __global__ void __launch_bounds__(kRingThreads, kRingCtasPerSm) down_ring_kernel
     const int g = lane >> 2, c = lane & 3;
     const int KTf = a.f >> 7;
     const int units = a.d / kDnRows;
+    const int hpitch = dn_hs_pitch(a.f);
     unsigned* ctr = a.ws.counters + kRingCtr + 2;
     constexpr int TSB = (WFMT == 0) ? 64 : 128;
     const uint32_t cb = 2u * kRingWarps * KTf * 512u;
@@ -794,7 +799,7 @@ __global__ void __launch_bounds__(kRingThreads, kRingCtasPerSm) down_ring_kernel
                     const int q = q0 + u * kRingThreads;
                     if (q < total) {
                         const float m = hmul[q / row_f4];
-                        *reinterpret_cast<uint2*>(hs + (size_t)q * 4) =
+                        *reinterpret_cast<uint2*>(hs + (size_t)(q / row_f4) * hpitch + (q % row_f4) * 4) =
                             make_uint2(pack_half2(v[u].x * m, v[u].y * m), pack_half2(v[u].z * m, v[u].w * m));
                     }
                 }
@@ -821,7 +826,7 @@ __global__ void __launch_bounds__(kRingThreads, kRingCtasPerSm) down_ring_kernel
                 const int pl = nt * 8 + g;
                 uint32_t b[16];
                 if (pl < np) {
-                    const uint4* hp = reinterpret_cast<const uint4*>(hs + (size_t)pl * a.f + kt * 128 + c * 32);
+                    const uint4* hp = reinterpret_cast<const uint4*>(hs + (size_t)pl * hpitch + kt * 128 + c * 32);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const uint4 v = hp[q];
