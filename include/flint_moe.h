@@ -119,6 +119,12 @@ FLINT_API flint_status flint_moe_load_weights(flint_moe* h, int layer, const fli
 
 /* One MoE layer: out_dev[T][d] = MoE_layer(hidden_dev[T][d]), both bfloat16,
  * 16-byte aligned, not overlapping. T == 0 is a no-op returning FLINT_OK.
+ * The kernels are enqueued on `stream` (a cudaStream_t; NULL: the legacy
+ * default stream) and keep its order: work enqueued before the call completes
+ * before any kernel of the layer reads or writes memory, and work enqueued
+ * after it sees the output. (The multi-kernel paths launch their kernels with
+ * programmatic stream serialisation: a kernel may be scheduled while the one
+ * before it is finishing, but waits for it before touching memory.)
  * Errors: FLINT_EINVAL (NULL, misaligned, T < 0 or T > max_tokens, layer out
  * of range), FLINT_ESTATE (layer not loaded), FLINT_ECUDA (launch). */
 FLINT_API flint_status flint_moe_forward(flint_moe* h, int layer, const void* hidden_dev, int T,
