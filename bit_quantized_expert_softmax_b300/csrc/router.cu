@@ -210,6 +210,9 @@ struct RouterArgs {
 // ---------------------------------------------------------------------------
 constexpr int kTokGroup = 16;   // tokens per CTA: the M of the tile
 constexpr int kRouterExp = 8;   // experts per CTA: the N of the tile
+// the fragment loads read 16 hidden rows and the partial tiles hold 16 x 8
+// values: the staging buffer and the tile must have exactly these sizes
+static_assert(kTokGroup == 16 && kRouterExp == 8, "one m16n8 tile per CTA");
 // arrival counters of the token groups of router_small_kernel (after the
 // ones the expert kernels use)
 constexpr int kGroupCounters = kCounters - kSmallT / kTokGroup;
