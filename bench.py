@@ -700,8 +700,9 @@ def kernel_roofline(cfg, res, peaks, fp4) -> dict:
     else:
         # the stack (per-layer figures: the step's time and bytes over the
         # layers): one single-layer launch per layer, replayed from a CUDA
-        # graph; FLINT_MOE_STACK_KERNEL=1: all layers in one persistent launch
-        one_launch = os.environ.get("FLINT_MOE_STACK_KERNEL", "0") == "1"
+        # graph with FLINT_MOE_STACK_KERNEL=0; by default all layers in one
+        # persistent launch
+        one_launch = os.environ.get("FLINT_MOE_STACK_KERNEL", "1") != "0"
         k_us, k_bytes = res["ms"] * 1e3 / cfg.n_layers, nb["layer_bytes"] / cfg.n_layers
         kkey = "decode_stack_kernel" if one_launch else "decode_fused_kernel"
         kname = (f"{kkey} (per layer, one launch for the whole stack)" if one_launch

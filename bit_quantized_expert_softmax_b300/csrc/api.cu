@@ -265,7 +265,9 @@ flint_status flint_moe_create(const flint_moe_config* cfg, flint_moe** out) {
     if (h->fused && flint::prepare_decode_fused() != cudaSuccess) h->fused = false;
     {
         const char* env = getenv("FLINT_MOE_STACK_KERNEL");
-        h->stack = h->fused && env != nullptr && env[0] == '1';
+        // the one-launch stack kernel unless FLINT_MOE_STACK_KERNEL=0 (then a
+        // stack runs one single-layer launch per layer)
+        h->stack = h->fused && !(env != nullptr && env[0] == '0');
     }
     {
         const char* env = getenv("FLINT_MOE_TCGEN05_PREFILL");

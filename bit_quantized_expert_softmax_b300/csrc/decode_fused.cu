@@ -782,7 +782,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
             }
         }
     }
-    GridSync8 gsync = grid_sync8_init(sa.gbar8, (uint32_t)G);   // includes a __syncthreads
+    GridSync gsync = grid_sync_init(a0.bar_count, (uint32_t)G);   // includes a __syncthreads
     if (down_tile >= 0) {
         if (threadIdx.x < T * 16) {
             const int t = threadIdx.x / 16, r = threadIdx.x % 16;
@@ -791,7 +791,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
         wait_bar(i_rslab);
         if (ok) router_partials<T>(sa, rslab, xr, 0, down_tile % kRaccCopies);
     }
-    if (!grid_sync8(gsync, a0.status)) ok = false;
+    if (!grid_sync(gsync, a0.status)) ok = false;
 
 #pragma unroll 1
     for (int li = 0; li < sa.n && ok; ++li) {
@@ -975,7 +975,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
         // barrier completes, request this CTA's routed down slabs (P2), the
         // next layer's shared half-unit (its slot is free now) and the next
         // layer's router slab (read in P2)
-        if (ok) grid_arrive8(gsync);
+        if (ok) grid_arrive(gsync);
         if (threadIdx.x == 0 && ok) {
             fence_proxy_async_smem();
             if (down_tile >= 0 && na > 0) {
@@ -999,7 +999,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
                 }
             }
         }
-        if (ok && !grid_wait8(gsync, a0.status)) ok = false;
+        if (ok && !grid_wait(gsync, a0.status)) ok = false;
         if (!ok) break;
         // ------------------------------------------------------------ P2
         if (last && b == 0) {   // every reader of this layer's accumulators has passed the barrier
@@ -1105,7 +1105,7 @@ __global__ void __launch_bounds__(kFThreads, 1) decode_stack_kernel(StackArgs sa
                 if (ok) router_partials<T>(sa, rslab, xr, buf ^ 1, down_tile % kRaccCopies);
             }
         }
-        if (!last && ok && !grid_sync8(gsync, a0.status)) ok = false;
+        if (!last && ok && !grid_sync(gsync, a0.status)) ok = false;
         Lc = Ln;
         Ln = Lnn;
     }

@@ -133,14 +133,15 @@ FLINT_API flint_status flint_moe_forward(flint_moe* h, int layer, const void* hi
 /* Decode stack with residual: for l = layer0 .. layer0+n_layers-1,
  *   x <- bf16( x + MoE_layer_l(x) )   (the sum taken in fp32 of the bf16 values)
  * applied in place to hidden_dev[T][d] (bfloat16, 16-byte aligned). Same
- * errors as flint_moe_forward. Each layer runs as one forward (for T <= 2 the
- * single-launch decode kernel, one launch per layer). Setting
- * FLINT_MOE_STACK_KERNEL=1 before flint_moe_create runs, for T <= 2 (with one
- * shared expert), all n_layers layers as ONE kernel launch instead: a
- * persistent cooperative kernel with two grid barriers per layer, which
- * computes each layer's router logits from the previous layer's output rows
- * as they are produced (summed in 64-bit fixed point, 2^-32 units, so the
- * result does not depend on arrival order).
+ * errors as flint_moe_forward. For T <= 2 (with one shared expert) all
+ * n_layers layers run as ONE kernel launch: a persistent cooperative kernel
+ * with two grid barriers per layer, which computes each layer's router logits
+ * from the previous layer's output rows as they are produced (summed in 64-bit
+ * fixed point, 2^-32 units, so the result does not depend on arrival order).
+ * Setting FLINT_MOE_STACK_KERNEL=0 before flint_moe_create runs each layer as
+ * one forward instead (the single-launch decode kernel, one launch per layer;
+ * the same result as chaining flint_moe_forward bit for bit); other T always
+ * run that way.
  * Enqueues only kernels, so the whole call can be captured into a CUDA graph. */
 FLINT_API flint_status flint_moe_forward_stack(flint_moe* h, int layer0, int n_layers, void* hidden_dev,
                                      int T, void* stream);

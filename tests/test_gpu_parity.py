@@ -320,7 +320,7 @@ def test_stack_47_layers_T1(fm, monkeypatch):
     Every layer is checked against the oracle on the oracle's own input x_l
     (full size, per-layer weights): the single-layer forward, and the
     one-launch stack kernel run on that one layer. The per-layer path of the
-    stack (the default) must equal the GPU chain of single-layer
+    stack (FLINT_MOE_STACK_KERNEL=0) must equal the GPU chain of single-layer
     forwards bit for bit; the one-launch stack computes the router logits in
     another summation order (fixed-point partials per 16 rows), so it is held
     to bit-for-bit determinism run to run and to the end-to-end drift bound.
@@ -332,8 +332,9 @@ def test_stack_47_layers_T1(fm, monkeypatch):
     bits = synth.make_hidden(cfg)
     monkeypatch.setenv("FLINT_MOE_STACK_KERNEL", "1")
     m = fm.MoE(cfg, max_tokens=1, n_layers=cfg.n_layers)
-    monkeypatch.delenv("FLINT_MOE_STACK_KERNEL")
+    monkeypatch.setenv("FLINT_MOE_STACK_KERNEL", "0")
     m_chain = fm.MoE(cfg, max_tokens=1, n_layers=cfg.n_layers)
+    monkeypatch.delenv("FLINT_MOE_STACK_KERNEL")
     ref_bits = bits.copy()
     idx = torch.empty((1, cfg.top_k), dtype=torch.int32, device="cuda")
     for i in range(cfg.n_layers):          # one layer in host memory at a time
