@@ -62,3 +62,27 @@ def test_clock_summary_parses_nvidia_smi_lines():
     s = c.summary()
     assert s["sm_mhz"] == pytest.approx(1972.5) and s["sm_max_mhz"] == 2032
     assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 2
+
+
+def _decode_res(e2e_pipe_ms):
+    cfg = synth.CONFIGS[2]
+    return cfg, {
+        "value": 48000.0, "ms": 0.0206, "step_ms": [0.0206, 0.0207], "launches": 2000,
+        "launches_per_forward": 1, "plan": 0, "phase_us": None,
+        "bytes": bench.algorithmic_bytes(cfg, 7, 1), "clocks": {"samples": 0}, "n_active": 7,
+        "e2e_value": 27000.0, "e2e_pipe_ms": e2e_pipe_ms,
+    }
+
+
+def test_record_e2e_serial_and_pipelined():
+    """The e2e figure: the serial per-step form by default; with a pipelined
+    per-step time, that form's value, the serial one kept beside it."""
+    peaks = {"hbm_gbs": 6480.8, "source": "measured"}
+    cfg, res = _decode_res(None)
+    r = bench.record(cfg, res, peaks, None, 1)
+    assert r["e2e"]["value"] == 27000.0 and "serial_value" not in r["e2e"]
+    assert r["e2e"]["h2d_bytes_per_step"] == r["e2e"]["d2h_bytes_per_step"] == cfg.tokens * cfg.d * 2
+    cfg, res = _decode_res(0.04)
+    r = bench.record(cfg, res, peaks, None, 2)
+    assert r["e2e"]["value"] == pytest.approx(2 * cfg.tokens / 0.04e-3)
+    assert r["e2e"]["serial_value"] == 27000.0 and r["e2e"]["method"].startswith("pipelined")
